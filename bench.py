@@ -1,0 +1,394 @@
+"""Benchmark of the GB300 tiled GEMM  C = A·Bᵀ  (TFLOP/s = 2MNK / t).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl tkg|reference]
+
+A step is one batch of independent GEMMs of the chosen workload (default: the
+bf16 M=N=K=4096 problem), run back to back through the C ABI with operands
+resident in HBM.  Operands rotate over several copies whose total size exceeds
+the 129 MB L2, so every GEMM reads its inputs from HBM.  Rank 0 prints one
+JSON line.  Under torchrun each rank runs its own replica (weak scaling, no
+collective on the data path); the time is the maximum over ranks.
+
+--impl reference times the CPU oracle (the plain C reference) on the host
+cores on a bounded sample of the same workload, with the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from tiled_tensor_core_gb300 import synth  # noqa: E402
+
+METRIC = "GEMM TFLOP/s (2MNK/t) bf16/FP8/NVFP4 on 1 GB300; % of dense tensor peak"
+L2_BYTES = 129 * 2 ** 20
+# GEMMs per step, sized so that a step is tens of milliseconds of GPU work
+BATCH = {"bf16_256": 2000, "bf16_4096": 400, "bf16_8192": 60, "bf16_skinny": 100, "fp8_8192": 100,
+         "nvfp4_16384": 30}
+# dense tensor-core peak relative to bf16 (nominal GB300 ratios: bf16 2.25, fp8 4.5, fp4 13.5 PFLOP/s)
+PEAK_RATIO = {"bf16": 1.0, "fp8": 2.0, "nvfp4": 6.0}
+DTYPE = {"bf16": "bf16", "fp8": "e4m3", "nvfp4": "e2m1+e4m3"}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"bf16_tflops": float(d["bf16_tflops"]), "bf16_tflops_sustained": float(d["bf16_tflops_sustained"]),
+                "hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    except Exception:
+        return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="tkg_clocks_", suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), max=float(parts[2]), power=float(parts[3]), active=parts[4],
+                                 hw=parts[5], hw_thermal=parts[6], sw_thermal=parts[7], sw_power=parts[8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(r["power"] for r in rows)}
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "tkg" else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- oracle timing
+
+def oracle_sample(ops, target_s: float):
+    """Time the oracle as it stands on a row sample of the workload sized to
+    about target_s seconds of host work.  Returns (TFLOP/s, seconds, rows, threads)."""
+    import oracle
+    M, N, K = ops.M, ops.N, ops.K
+    threads = oracle.num_threads()
+    wave = np.linspace(0, M - 1, min(M, threads)).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.gemm(ops, rows=wave)
+    t_wave = max(time.perf_counter() - t0, 1e-6)
+    waves = max(1, int(target_s / t_wave))
+    n_rows = int(min(M, len(wave) * waves))
+    rows = np.linspace(0, M - 1, n_rows).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.gemm(ops, rows=rows)
+    dt = time.perf_counter() - t0
+    return 2.0 * n_rows * N * K / dt / 1e12, dt, n_rows, threads
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    w = synth.WORKLOADS[args.workload]
+    ops = synth.workload_operands(args.workload)
+    for _ in range(args.warmup):
+        oracle_sample(ops, 0.1)
+    times = []
+    flops = 0.0
+    n_rows = threads = 0
+    for _ in range(args.steps):
+        _, dt, n_rows, threads = oracle_sample(ops, args.ref_step_s)
+        times.append(dt)
+        flops += 2.0 * n_rows * w.N * w.K
+    value = flops / sum(times) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE[w.kind],
+        "data": "synthetic",
+        "config": {"workload": w.description, "M": w.M, "N": w.N, "K": w.K,
+                   "sample_rows_per_step": n_rows},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{n_rows} of {w.M} output rows (x {w.N} cols x K={w.K}) per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_tkg(args, world, rank, local):
+    import torch
+    from tiled_tensor_core_gb300 import tkg
+    from tiled_tensor_core_gb300.device import DeviceGemm
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if args.variant:
+        tkg.tkg_set_option(tkg.TKG_OPT_VARIANT, args.variant)
+    if args.group_m:
+        tkg.tkg_set_option(tkg.TKG_OPT_GROUP_M, args.group_m)
+    w = synth.WORKLOADS[args.workload]
+    ops = synth.workload_operands(args.workload)
+    base = DeviceGemm(ops, dev)
+    footprint = base.input_bytes() + base.output_bytes()
+    n_sets = 1 if footprint >= 2 * L2_BYTES else min(16, math.ceil(4 * L2_BYTES / footprint))
+    sets = [base]
+    for _ in range(n_sets - 1):
+        g = DeviceGemm.__new__(DeviceGemm)
+        g.__dict__.update(base.__dict__)
+        g.a, g.b = base.a.clone(), base.b.clone()
+        if base.sfa is not None:
+            g.sfa, g.sfb = base.sfa.clone(), base.sfb.clone()
+        if base.scale_a is not None:
+            g.scale_a, g.scale_b = base.scale_a.clone(), base.scale_b.clone()
+        g.c = torch.empty_like(base.c)
+        sets.append(g)
+    batch = args.batch or BATCH[args.workload]
+    stream = torch.cuda.Stream(device=dev)
+    sptr = int(stream.cuda_stream)
+    launches_per_gemm = 2 if w.kind == "nvfp4" else 1
+
+    def step(events=None):
+        for i in range(batch):
+            g = sets[i % n_sets]
+            if events is not None:
+                events[2 * i].record(stream)
+            g.run(stream=sptr)
+            if events is not None:
+                events[2 * i + 1].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    st = tkg.tkg_check_status(sptr)
+    if st != tkg.TKG_OK:
+        raise RuntimeError(f"warm-up failed: {tkg.status_string(st)}")
+
+    # correctness spot check of the last warm-up output against the oracle (cheap: a few rows)
+    spot = None
+    if rank == 0 and not args.no_check:
+        import oracle
+        rows = np.array([0, ops.M // 2, ops.M - 1], dtype=np.int64)
+        acc, c_ref = oracle.gemm(ops, rows=rows)
+        got = sets[(batch - 1) % n_sets].c[torch.from_numpy(rows).to(dev)].view(torch.int16).cpu().numpy()
+        got = (got.view(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        ref = acc.astype(np.float64) * ops.scale_a * ops.scale_b
+        spot = float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * batch)]
+    step_ms, kern_ms = [], []
+    sampler = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)  # let the sampler take its first reading
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(args.steps):
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        step(ev)
+        s1.record(stream)
+        s1.synchronize()
+        step_ms.append(s0.elapsed_time(s1))
+        kern_ms.extend(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(batch))
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    barrier(world)
+    st = tkg.tkg_check_status(sptr)
+    if st != tkg.TKG_OK:
+        raise RuntimeError(f"timed run failed: {tkg.status_string(st)}")
+    total_ms = t_start.elapsed_time(t_end)
+    total_ms = max_over_ranks(total_ms, world, dev)
+    gemms = args.steps * batch
+    value = world * gemms * w.flops / (total_ms * 1e-3) / 1e12
+    kern_avg_ms = sum(kern_ms) / len(kern_ms)
+    achieved = w.flops / (kern_avg_ms * 1e-3) / 1e12
+
+    # end to end through the public API: pinned host inputs -> device, GEMM, result -> host
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(ops, dev, w, args)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, dt, n_rows, threads = oracle_sample(ops, args.cpu_s)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"{n_rows} of {w.M} output rows of the same workload ({dt:.1f} s)"}
+
+    peaks = load_peaks()
+    peak = peaks["bf16_tflops"] * PEAK_RATIO[w.kind]
+    info = tkg.tkg_debug_variant_info({"bf16": 0, "fp8": 1, "nvfp4": 2}[w.kind],
+                                      tkg.tkg_debug_pick_variant({"bf16": 0, "fp8": 1, "nvfp4": 2}[w.kind],
+                                                                 w.M, w.N, w.K))
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": DTYPE[w.kind], "data": "synthetic",
+        "config": {"workload": w.description, "M": w.M, "N": w.N, "K": w.K, "gemms_per_step": batch,
+                   "global_batch": batch * world, "parallelism": f"replicas{world}",
+                   "l2": (f"{n_sets} rotating operand sets, {n_sets * footprint / 2**20:.0f} MiB > 129 MiB L2"
+                          if n_sets > 1 else f"operands {footprint / 2**20:.0f} MiB > 129 MiB L2"),
+                   "kernel": info, "group_m": tkg.tkg_get_option(tkg.TKG_OPT_GROUP_M)},
+        "pct_of_peak": 100.0 * value / world / peak,
+        "median_gemm_ms": statistics.median(kern_ms),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_source": f"{peaks['source']} bf16 burst x {PEAK_RATIO[w.kind]:g} (nominal dtype ratio)"},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": gemms * launches_per_gemm,
+        "clocks": clocks,
+        "spot_check_rel_err": spot,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_e2e(ops, dev, w, args):
+    import torch
+    from tiled_tensor_core_gb300.device import DeviceGemm
+
+    g = DeviceGemm(ops, dev)
+    host = {}
+    for name in ("a", "b", "sfa", "sfb", "scale_a", "scale_b"):
+        t = getattr(g, name)
+        if t is not None:
+            host[name] = t.cpu().pin_memory()
+    c_host = torch.empty(g.c.shape, dtype=g.c.dtype).pin_memory()
+    stream = torch.cuda.Stream(device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = c_host.numel() * c_host.element_size()
+
+    def one():
+        for name, t in host.items():
+            getattr(g, name).copy_(t, non_blocking=True)
+        g.run(stream=int(stream.cuda_stream))
+        c_host.copy_(g.c, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            one()
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        n = args.e2e_steps
+        e0.record(stream)
+        for _ in range(n):
+            one()
+        e1.record(stream)
+        e1.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    return {"value": w.flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": ms}
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["tkg", "reference"], default="tkg")
+    p.add_argument("--workload", choices=sorted(synth.WORKLOADS), default="bf16_4096")
+    p.add_argument("--batch", type=int, default=0, help="GEMMs per step (default: per workload)")
+    p.add_argument("--variant", type=int, default=0)
+    p.add_argument("--group-m", type=int, default=0)
+    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--cpu-s", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
+    p.add_argument("--ref-step-s", type=float, default=3.0, help="seconds of oracle work per reference step")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-check", action="store_true")
+    args = p.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        return run_reference(args, world, rank)
+    world, rank, local = dist_setup(args)
+    return run_tkg(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,141 @@
+/*
+ * tkg.h — C ABI of the GB300 (sm_103a) dense tiled tensor-core GEMM.
+ *
+ *     C = A · Bᵀ        A: [M, K] row-major, B: [N, K] row-major, C: [M, N] row-major bf16
+ *
+ * The operation is the tile contraction the ThunderKittens paper calls
+ * mma_ABt ("att += Q @ K^T" — paper summary "ThunderKittens: Simple, Fast, and
+ * Adorable AI Kernels", section "PyTorch-Like Operations on Tiles"), applied to
+ * whole matrices the way its GEMM kernel does (same page, "Integration: How the
+ * Three Levels Compose", App. B.1 walk-through): bf16 operands, fp32
+ * accumulation ("Warp-Level: Tile Operations"), output written back in bf16.
+ * The FP8 and NVFP4 variants are the 8-bit and block-scaled 4-bit GEMMs of the
+ * Rubin article ("ThunderKittens reaches 22.4 PFLOPS on NVIDIA Rubin", NVFP4
+ * paragraph).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All matrix pointers are DEVICE pointers, owned by the caller, and must
+ *    stay valid until the work queued on `stream` has finished.  The library
+ *    never frees or retains them.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Every GEMM is asynchronous: the call validates, queues one
+ *    kernel launch and returns; it never synchronises.
+ *  - Accumulation is fp32.  The output is rounded to bf16 with
+ *    round-to-nearest-even.  There is no alpha/beta and no accumulate-into-C;
+ *    C is overwritten.
+ *  - M and N are arbitrary (>= 1).  Tiles that run past M, N or K are handled
+ *    by the hardware copy engine (zero fill on load, clipping on store), which
+ *    is exact for a sum.
+ *  - Errors detected before launch are returned and nothing is queued.  Errors
+ *    detected on the device (a pipeline wait that exceeded its time limit) are
+ *    recorded in a device status word and reported by tkg_check_status().
+ *  - The library holds, per device, a small tensor-map cache on the host and a
+ *    4-byte status word in a static device variable; tkg_shutdown() clears the
+ *    host cache.  There is no CPU fallback: on a device that is not
+ *    compute capability 10.3 every GEMM returns TKG_ERR_UNSUPPORTED_DEVICE.
+ *  - Entry points are thread-safe.  Calls on different streams may overlap.
+ */
+#ifndef TKG_H_
+#define TKG_H_
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TKG_API __attribute__((visibility("default")))
+#else
+#define TKG_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum tkg_status {
+    TKG_OK = 0,
+    TKG_ERR_INVALID_ARG = 1,        /* a size or pointer argument is out of range */
+    TKG_ERR_MISALIGNED = 2,         /* a matrix base pointer is not 16-byte aligned */
+    TKG_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not an sm_103 (GB300-class) GPU */
+    TKG_ERR_CUDA = 4,               /* a CUDA runtime / driver call failed */
+    TKG_ERR_TIMEOUT = 5,            /* a device pipeline wait ran out (see tkg_check_status) */
+    TKG_ERR_INTERNAL = 6
+} tkg_status;
+
+/* Scale operands.  All pointers are DEVICE pointers, caller-owned.
+ *  - FP8:   a_scale / b_scale point to one fp32 each: the dequantisation scale
+ *           of A and of B (value = e4m3(code) * scale).  Block-scale pointers
+ *           must be NULL.
+ *  - NVFP4: a_scale / b_scale point to the fp32 per-tensor scales g_A, g_B;
+ *           a_block_scale is e4m3 [M][K/16] row-major (one scale per 16
+ *           consecutive K elements of a row of A), b_block_scale is e4m3
+ *           [N][K/16] row-major.
+ *  - bf16:  pass NULL for the whole struct.
+ * The epilogue applies the per-tensor scales as  bf16((acc * a_scale) * b_scale). */
+typedef struct tkg_scales {
+    const float* a_scale;
+    const float* b_scale;
+    const uint8_t* a_block_scale;
+    const uint8_t* b_block_scale;
+} tkg_scales;
+
+/* bf16 GEMM.  A: bf16 [M][K], B: bf16 [N][K], C: bf16 [M][N].
+ * Requirements: M, N, K >= 1, each <= 2^31-1; K % 8 == 0 (16-byte row pitch);
+ * A, B, C 16-byte aligned.  scales must be NULL.
+ * Returns TKG_OK once the kernel is queued. */
+TKG_API tkg_status tkg_gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* C,
+                         const tkg_scales* scales, void* stream);
+
+/* FP8 GEMM.  A: e4m3 bytes [M][K], B: e4m3 bytes [N][K], C: bf16 [M][N].
+ * C = bf16((sum_k e4m3(A[m][k]) * e4m3(B[n][k])) * a_scale * b_scale).
+ * Requirements: as bf16 but K % 16 == 0; scales, scales->a_scale and
+ * scales->b_scale non-NULL (4-byte aligned device floats). */
+TKG_API tkg_status tkg_gemm_fp8(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* C,
+                        const tkg_scales* scales, void* stream);
+
+/* NVFP4 block-scaled GEMM.  A: packed e2m1 [M][K/2] bytes, element 2j in the
+ * low nibble of byte j; B: packed e2m1 [N][K/2]; C: bf16 [M][N].
+ * C = bf16((sum_k (e2m1(A[m][k]) * e4m3(SFA[m][k/16])) *
+ *                  (e2m1(B[n][k]) * e4m3(SFB[n][k/16]))) * g_A * g_B).
+ * Requirements: as bf16 but K % 32 == 0; all four scale pointers non-NULL;
+ * block-scale arrays 16-byte aligned. */
+TKG_API tkg_status tkg_gemm_nvfp4(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* C,
+                          const tkg_scales* scales, void* stream);
+
+/* Synchronises `stream`, then reads and clears the device status word of the
+ * current device.  Returns TKG_ERR_TIMEOUT if any kernel since the last check
+ * abandoned a pipeline wait (its output is then undefined), TKG_ERR_CUDA if the
+ * stream reported an error, else TKG_OK. */
+TKG_API tkg_status tkg_check_status(void* stream);
+
+/* Static, never-NULL description of a status code. */
+TKG_API const char* tkg_status_string(tkg_status status);
+
+/* Releases host-side caches (tensor maps, per-device launch data).  Device
+ * memory owned by the caller is untouched.  Safe to call more than once; the
+ * next GEMM call re-initialises. */
+TKG_API void tkg_shutdown(void);
+
+/* Tunables (process-wide).  Values persist until changed; 0 restores the
+ * default.  Returns TKG_ERR_INVALID_ARG for an unknown key or bad value.
+ *  TKG_OPT_TIMEOUT_NS  limit for any single pipeline wait on the device (default 2 s)
+ *  TKG_OPT_GROUP_M     super-group height in output tiles for the L2-aware
+ *                      tile order (default 8; the paper's {8, N, M/8} order,
+ *                      "Block Launch Order and L2 Cache Reuse", Table 3)
+ *  TKG_OPT_VARIANT     force a kernel variant: 0 = pick by shape, 1 = 1-SM
+ *                      128x256 tiles, 2 = 2-SM (CTA pair) 256x256 tiles,
+ *                      3 = 2-SM 256x128 tiles
+ *  TKG_OPT_MAX_CTAS    cap the persistent grid size (0 = all SMs)            */
+typedef enum tkg_option {
+    TKG_OPT_TIMEOUT_NS = 1,
+    TKG_OPT_GROUP_M = 2,
+    TKG_OPT_VARIANT = 3,
+    TKG_OPT_MAX_CTAS = 4
+} tkg_option;
+TKG_API tkg_status tkg_set_option(tkg_option key, int64_t value);
+TKG_API int64_t tkg_get_option(tkg_option key);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TKG_H_ */

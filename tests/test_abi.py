@@ -1,0 +1,151 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+the headers declare, rejects bad arguments before touching CUDA, and its
+host-compiled scheduler / swizzle helpers agree with the definitions."""
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+from oracle import swizzle as sw
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def tkg():
+    from tiled_tensor_core_gb300 import build
+    build.build()
+    from tiled_tensor_core_gb300 import tkg as mod
+    return mod
+
+
+def declared_functions():
+    names = []
+    for h in ("tkg.h", "tkg_debug.h"):
+        text = open(os.path.join(ROOT, "include", h)).read()
+        names += re.findall(r"TKG_API\s+[\w\s\*]+?\b(tkg_\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_headers_declare_the_boundary():
+    names = declared_functions()
+    for required in ("tkg_gemm_bf16", "tkg_gemm_fp8", "tkg_gemm_nvfp4", "tkg_check_status",
+                     "tkg_status_string", "tkg_shutdown"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(tkg):
+    out = subprocess.run(["nm", "-D", "--defined-only", tkg.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\bT\s+(tkg_\w+)", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    for n in declared_functions():
+        assert hasattr(tkg.lib, n)
+
+
+def test_library_links_no_torch_and_no_libcuda(tkg):
+    out = subprocess.run(["ldd", tkg.LIB_PATH], capture_output=True, text=True).stdout
+    assert "torch" not in out and "libcuda.so" not in out
+
+
+def test_status_strings(tkg):
+    for s in range(7):
+        assert tkg.status_string(s)
+    assert tkg.status_string(99) == "unknown status"
+
+
+@pytest.mark.parametrize("fn", ["tkg_gemm_bf16", "tkg_gemm_fp8", "tkg_gemm_nvfp4"])
+def test_invalid_sizes_rejected_before_any_cuda_call(tkg, fn):
+    f = getattr(tkg.lib, fn)
+    A = B = C = 1 << 20  # 16-byte aligned fake addresses: never dereferenced
+    for M, N, K in [(0, 8, 256), (8, 0, 256), (8, 8, 0), (-1, 8, 256), (8, 8, 1 << 31)]:
+        assert f(M, N, K, A, B, C, None, None) == tkg.TKG_ERR_INVALID_ARG
+    assert f(8, 8, 256, 0, B, C, None, None) == tkg.TKG_ERR_INVALID_ARG
+
+
+def test_k_alignment_rules(tkg):
+    A = B = C = 1 << 20
+    s = tkg.tkg_scales(1 << 12, 1 << 12, None, None)
+    assert tkg.lib.tkg_gemm_bf16(8, 8, 12, A, B, C, None, None) == tkg.TKG_ERR_INVALID_ARG
+    assert tkg.lib.tkg_gemm_fp8(8, 8, 24, A, B, C, s, None) == tkg.TKG_ERR_INVALID_ARG
+    s4 = tkg.tkg_scales(1 << 12, 1 << 12, 1 << 14, 1 << 14)
+    assert tkg.lib.tkg_gemm_nvfp4(8, 8, 48, A, B, C, s4, None) == tkg.TKG_ERR_INVALID_ARG
+
+
+def test_scale_arguments_checked(tkg):
+    A = B = C = 1 << 20
+    s = tkg.tkg_scales(1 << 12, 1 << 12, None, None)
+    assert tkg.lib.tkg_gemm_bf16(8, 8, 64, A, B, C, s, None) == tkg.TKG_ERR_INVALID_ARG
+    assert tkg.lib.tkg_gemm_fp8(8, 8, 64, A, B, C, None, None) == tkg.TKG_ERR_INVALID_ARG
+    assert tkg.lib.tkg_gemm_fp8(8, 8, 64, A, B, C, tkg.tkg_scales(1 << 12, None, None, None), None) \
+        == tkg.TKG_ERR_INVALID_ARG
+    assert tkg.lib.tkg_gemm_nvfp4(8, 8, 64, A, B, C, s, None) == tkg.TKG_ERR_INVALID_ARG
+
+
+def test_misaligned_pointers_rejected(tkg):
+    A = B = C = 1 << 20
+    assert tkg.lib.tkg_gemm_bf16(8, 8, 64, A + 2, B, C, None, None) == tkg.TKG_ERR_MISALIGNED
+    assert tkg.lib.tkg_gemm_bf16(8, 8, 64, A, B + 8, C, None, None) == tkg.TKG_ERR_MISALIGNED
+    assert tkg.lib.tkg_gemm_bf16(8, 8, 64, A, B, C + 4, None, None) == tkg.TKG_ERR_MISALIGNED
+    s = tkg.tkg_scales((1 << 12) + 2, 1 << 12, None, None)
+    assert tkg.lib.tkg_gemm_fp8(8, 8, 64, A, B, C, s, None) == tkg.TKG_ERR_MISALIGNED
+    s4 = tkg.tkg_scales(1 << 12, 1 << 12, (1 << 14) + 4, 1 << 14)
+    assert tkg.lib.tkg_gemm_nvfp4(8, 8, 64, A, B, C, s4, None) == tkg.TKG_ERR_MISALIGNED
+
+
+def test_options_roundtrip(tkg):
+    assert tkg.tkg_get_option(tkg.TKG_OPT_GROUP_M) == 8
+    tkg.tkg_set_option(tkg.TKG_OPT_GROUP_M, 12)
+    assert tkg.tkg_get_option(tkg.TKG_OPT_GROUP_M) == 12
+    tkg.tkg_set_option(tkg.TKG_OPT_GROUP_M, 0)
+    assert tkg.tkg_get_option(tkg.TKG_OPT_GROUP_M) == 8
+    assert tkg.tkg_get_option(tkg.TKG_OPT_TIMEOUT_NS) == 2_000_000_000
+    with pytest.raises(tkg.TkgError):
+        tkg.tkg_set_option(tkg.TKG_OPT_VARIANT, 99)
+    with pytest.raises(tkg.TkgError):
+        tkg.tkg_set_option(77, 1)
+
+
+@pytest.mark.parametrize("tiles_m,tiles_n,group_m", [(1, 1, 8), (16, 16, 8), (32, 32, 8), (64, 32, 12),
+                                                     (13, 7, 8), (7, 13, 8), (5, 3, 1), (3, 5, 100), (33, 1, 8)])
+def test_tile_order_visits_every_tile_once(tkg, tiles_m, tiles_n, group_m):
+    seen = np.zeros((tiles_m, tiles_n), dtype=np.int32)
+    for t in range(tiles_m * tiles_n):
+        tm, tn = tkg.tkg_debug_tile_coord(t, tiles_m, tiles_n, group_m)
+        assert 0 <= tm < tiles_m and 0 <= tn < tiles_n
+        seen[tm, tn] += 1
+    assert (seen == 1).all()
+
+
+def test_tile_order_is_grouped(tkg):
+    # inside a super-row the M index runs fastest: the first G tiles share tile-column 0
+    G = 8
+    coords = [tkg.tkg_debug_tile_coord(t, 32, 32, G) for t in range(2 * G)]
+    assert [c[0] for c in coords[:G]] == list(range(G))
+    assert all(c[1] == 0 for c in coords[:G]) and all(c[1] == 1 for c in coords[G:2 * G])
+    # a persistent wave of 76 tile pairs touches 8 tile-rows and ~10 tile-columns, not 76 columns
+    wave = {tkg.tkg_debug_tile_coord(t, 32, 32, G) for t in range(76)}
+    assert len({m for m, _ in wave}) == 8 and len({n for _, n in wave}) <= 10
+
+
+@pytest.mark.parametrize("s", [0, 32, 64, 128])
+def test_device_swizzle_functor_matches_definition(tkg, s):
+    for off in range(0, 4096, 4):
+        assert tkg.tkg_debug_swizzle_offset(off, s) == sw.swizzle(off, s)
+
+
+def test_swizzle_selection_matches_definition(tkg):
+    for rb in range(16, 1040, 16):
+        assert tkg.tkg_debug_select_swizzle(rb) == sw.select_swizzle(rb)
+
+
+def test_compiled_variants_fit_the_sm(tkg):
+    for kind in (0, 1):
+        for v in (1, 2, 3):
+            info = tkg.tkg_debug_variant_info(kind, v)
+            assert info["smem_bytes"] <= 232448
+            assert info["threads"] in (192, 320)
+            assert info["cta_group"] in (1, 2)

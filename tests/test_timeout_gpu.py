@@ -1,0 +1,49 @@
+"""Failure detection without a GPU fault: every pipeline wait in the kernels is
+bounded.  Fault injection makes the producer skip the copies of its first ring
+stage (no copy is in flight for it), so the compute role's wait on that stage
+runs out; the kernel records the timeout in the status word, every role stops,
+tensor memory is released, and the context stays usable for the next call."""
+import numpy as np
+import pytest
+
+import oracle
+from tiled_tensor_core_gb300 import synth
+
+from gpu_util import check_against_oracle, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def tkg():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from tiled_tensor_core_gb300 import tkg as mod
+    yield mod
+    mod.tkg_set_option(mod.TKG_OPT_TIMEOUT_NS, 0)
+    mod.tkg_set_option(mod.TKG_OPT_VARIANT, 0)
+
+
+@pytest.mark.parametrize("variant", [1, 2])
+def test_injected_stall_reports_timeout_then_recovers(tkg, variant):
+    from tiled_tensor_core_gb300.device import DeviceGemm
+    ops = synth.make_operands("bf16", 512, 512, 512, "normal_sqrtk", 1, 2)
+    tkg.tkg_set_option(tkg.TKG_OPT_VARIANT, variant)
+    tkg.tkg_set_option(tkg.TKG_OPT_TIMEOUT_NS, 100_000_000)  # 0.1 s per wait
+    try:
+        g = DeviceGemm(ops, "cuda")
+        tkg.tkg_debug_set_fault(1)
+        g.run()
+        assert tkg.tkg_check_status() == tkg.TKG_ERR_TIMEOUT
+        # the status word was cleared by the check, and the next call is healthy
+        assert tkg.tkg_check_status() == tkg.TKG_OK
+        tkg.tkg_set_option(tkg.TKG_OPT_TIMEOUT_NS, 0)
+        g2 = run_gpu(ops)
+        acc, c_ref = oracle.gemm(ops)
+        check_against_oracle("bf16", g2.c_bits(), acc, c_ref)
+    finally:
+        tkg.tkg_debug_set_fault(0)
+        tkg.tkg_set_option(tkg.TKG_OPT_TIMEOUT_NS, 0)
+        tkg.tkg_set_option(tkg.TKG_OPT_VARIANT, 0)

@@ -1,0 +1,455 @@
+// api.cu — the tkg C ABI: argument validation, TMA tensor-map construction and
+// caching, per-device launch data, variant choice and the persistent launch.
+//
+// Tensor maps are the host-side half of the TMA path: they carry the global
+// shape, pitch, tile box and swizzle of each operand so that the copy engine
+// computes every address ("Asynchronous I/O: Unified Interface over cp.async
+// and TMA" — TK builds them from its global layout descriptors).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+#include "gemm_variants.h"
+#include "tkg.h"
+#include "tkg_debug.h"
+
+// Device status word (one per device, lives as long as the module).
+static __device__ unsigned int g_tkg_status;
+
+namespace {
+
+using namespace tkg;
+
+constexpr int64_t kDefaultTimeoutNs = 2000000000LL;
+constexpr int64_t kDefaultGroupM = 8;
+constexpr int kMaxDevices = 64;
+constexpr int kNumKinds = 3;
+
+std::atomic<int64_t> g_opt_timeout{0};
+std::atomic<int64_t> g_opt_group{0};
+std::atomic<int64_t> g_opt_variant{0};
+std::atomic<int64_t> g_opt_max_ctas{0};
+std::atomic<int> g_fault{0};
+
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+struct DevState {
+  bool ready = false;
+  int sm_count = 0;
+  int cc_major = 0, cc_minor = 0;
+  unsigned int* status = nullptr;
+  int max_clusters[kNumKinds][kNumVariants] = {};
+};
+DevState g_dev[kMaxDevices];
+
+struct MapKey {
+  const void* ptr;
+  int dtype;
+  uint64_t d0, d1, pitch;
+  uint32_t b0, b1;
+  int swz;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && dtype == o.dtype && d0 == o.d0 && d1 == o.d1 && pitch == o.pitch && b0 == o.b0 &&
+           b1 == o.b1 && swz == o.swz;
+  }
+};
+struct MapKeyHash {
+  size_t operator()(const MapKey& k) const {
+    uint64_t h = reinterpret_cast<uint64_t>(k.ptr) * 0x9E3779B97F4A7C15ull;
+    auto mix = [&](uint64_t v) { h ^= v + 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2); };
+    mix(static_cast<uint64_t>(k.dtype));
+    mix(k.d0);
+    mix(k.d1);
+    mix(k.pitch);
+    mix((static_cast<uint64_t>(k.b0) << 32) | k.b1);
+    mix(static_cast<uint64_t>(k.swz));
+    return static_cast<size_t>(h);
+  }
+};
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
+constexpr size_t kMaxMaps = 4096;
+
+int64_t opt_or(const std::atomic<int64_t>& v, int64_t dflt) {
+  const int64_t x = v.load(std::memory_order_relaxed);
+  return x == 0 ? dflt : x;
+}
+
+// Caller holds g_mu.
+tkg_status ensure_encode_locked() {
+  if (g_encode) return TKG_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q{};
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || fn == nullptr) {
+    cudaGetLastError();
+    return TKG_ERR_CUDA;
+  }
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return TKG_OK;
+}
+
+// Per-device initialisation (device must be current).  Caller holds g_mu.
+tkg_status device_state_locked(int dev, DevState** out) {
+  if (dev < 0 || dev >= kMaxDevices) return TKG_ERR_UNSUPPORTED_DEVICE;
+  DevState& d = g_dev[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return TKG_ERR_CUDA;
+    }
+    if (!(d.cc_major == 10 && d.cc_minor == 3)) return TKG_ERR_UNSUPPORTED_DEVICE;
+    void* sp = nullptr;
+    if (cudaGetSymbolAddress(&sp, g_tkg_status) != cudaSuccess) {
+      cudaGetLastError();
+      return TKG_ERR_CUDA;
+    }
+    d.status = static_cast<unsigned int*>(sp);
+    for (auto& row : d.max_clusters)
+      for (int& v : row) v = 0;
+    d.ready = true;
+  }
+  *out = &d;
+  return TKG_OK;
+}
+
+tkg_status current_device(DevState** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return TKG_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  tkg_status st = ensure_encode_locked();
+  if (st != TKG_OK) return st;
+  return device_state_locked(dev, out);
+}
+
+// 2-D row-major tensor map: d0 = elements per row (innermost), d1 = rows,
+// pitch in bytes, box b0 x b1 elements, swizzle in bytes (0/32/64/128).
+tkg_status get_map(CUtensorMap* out, const void* ptr, CUtensorMapDataType dtype, uint64_t d0, uint64_t d1,
+                   uint64_t pitch, uint32_t b0, uint32_t b1, int swz) {
+  const MapKey key{ptr, static_cast<int>(dtype), d0, d1, pitch, b0, b1, swz};
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_maps.find(key);
+  if (it != g_maps.end()) {
+    *out = it->second;
+    return TKG_OK;
+  }
+  tkg_status st = ensure_encode_locked();
+  if (st != TKG_OK) return st;
+  CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_NONE;
+  if (swz == 32) sw = CU_TENSOR_MAP_SWIZZLE_32B;
+  if (swz == 64) sw = CU_TENSOR_MAP_SWIZZLE_64B;
+  if (swz == 128) sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  const cuuint64_t dims[2] = {d0, d1};
+  const cuuint64_t strides[1] = {pitch};
+  const cuuint32_t box[2] = {b0, b1};
+  const cuuint32_t estr[2] = {1, 1};
+  CUtensorMap m;
+  std::memset(&m, 0, sizeof(m));
+  CUresult r = g_encode(&m, dtype, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return TKG_ERR_INVALID_ARG;
+  if (g_maps.size() >= kMaxMaps) g_maps.clear();
+  g_maps.emplace(key, m);
+  *out = m;
+  return TKG_OK;
+}
+
+const KernelVariant* variant_of(int kind, int id) {
+  switch (kind) {
+    case 0: return bf16_variant(id);
+    case 1: return fp8_variant(id);
+    case 2: return nvfp4_variant(id);
+    default: return nullptr;
+  }
+}
+
+int pick_variant(int kind, int64_t M, int64_t N, int64_t K) {
+  const int forced = static_cast<int>(g_opt_variant.load(std::memory_order_relaxed));
+  if (forced > 0 && variant_of(kind, forced)) return forced;
+  (void)K;
+  (void)N;
+  (void)M;
+  return kVariant2Sm256x256;
+}
+
+// Occupancy-limited number of co-resident clusters for a variant (cached).
+tkg_status max_clusters(DevState& d, int kind, int id, const KernelVariant& v, int* out) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (d.max_clusters[kind][id] > 0) {
+      *out = d.max_clusters[kind][id];
+      return TKG_OK;
+    }
+  }
+  if (cudaFuncSetAttribute(v.func, cudaFuncAttributeMaxDynamicSharedMemorySize, v.smem_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return TKG_ERR_CUDA;
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(v.cg * d.sm_count), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(v.threads), 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(v.smem_bytes);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(v.cg);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, v.func, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return TKG_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  d.max_clusters[kind][id] = n;
+  *out = n;
+  return TKG_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Common host-only checks (no CUDA call), then device checks and the launch.
+tkg_status gemm_launch(int kind, int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* C,
+                       const tkg_scales* scales, void* stream) {
+  const int64_t kMax = 0x7FFFFFFF;
+  if (M < 1 || N < 1 || K < 1 || M > kMax || N > kMax || K > kMax) return TKG_ERR_INVALID_ARG;
+  const int64_t k_align = kind == 0 ? 8 : kind == 1 ? 16 : 32;
+  if (K % k_align != 0) return TKG_ERR_INVALID_ARG;
+  if (!A || !B || !C) return TKG_ERR_INVALID_ARG;
+  if (kind == 0 && scales != nullptr) return TKG_ERR_INVALID_ARG;
+  if (kind == 1 && (!scales || !scales->a_scale || !scales->b_scale || scales->a_block_scale ||
+                    scales->b_block_scale))
+    return TKG_ERR_INVALID_ARG;
+  if (kind == 2 && (!scales || !scales->a_scale || !scales->b_scale || !scales->a_block_scale ||
+                    !scales->b_block_scale))
+    return TKG_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return TKG_ERR_MISALIGNED;
+  if (kind != 0 && ((reinterpret_cast<uintptr_t>(scales->a_scale) & 3u) ||
+                    (reinterpret_cast<uintptr_t>(scales->b_scale) & 3u)))
+    return TKG_ERR_MISALIGNED;
+  if (kind == 2 && (!aligned16(scales->a_block_scale) || !aligned16(scales->b_block_scale)))
+    return TKG_ERR_MISALIGNED;
+
+  const int id = pick_variant(kind, M, N, K);
+  const KernelVariant* v = variant_of(kind, id);
+  if (!v) return TKG_ERR_INTERNAL;
+  const int64_t tile_m = 128LL * v->cg;
+  const int64_t tiles_m = (M + tile_m - 1) / tile_m;
+  const int64_t tiles_n = (N + v->bn - 1) / v->bn;
+  if (tiles_m * tiles_n > kMax) return TKG_ERR_INVALID_ARG;
+
+  DevState* d = nullptr;
+  tkg_status st = current_device(&d);
+  if (st != TKG_OK) return st;
+
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  // Operand maps: rows of K elements, boxes of 128 bytes x (rows per CTA).
+  const uint32_t b_rows = static_cast<uint32_t>(v->bn / v->cg);
+  if (kind == 0) {
+    st = get_map(&p.tmap_a, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, K * 2, 64, 128, 128);
+    if (st == TKG_OK) st = get_map(&p.tmap_b, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, N, K * 2, 64, b_rows, 128);
+  } else {
+    const int64_t row_bytes = kind == 1 ? K : K / 2;
+    st = get_map(&p.tmap_a, A, CU_TENSOR_MAP_DATA_TYPE_UINT8, row_bytes, M, row_bytes, 128, 128, 128);
+    if (st == TKG_OK)
+      st = get_map(&p.tmap_b, B, CU_TENSOR_MAP_DATA_TYPE_UINT8, row_bytes, N, row_bytes, 128, b_rows, 128);
+  }
+  if (st != TKG_OK) return st;
+  p.c_via_tma = (N % 8 == 0) ? 1 : 0;
+  if (p.c_via_tma) {
+    st = get_map(&p.tmap_c, C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, N * 2, 64, 32, 128);
+    if (st != TKG_OK) return st;
+  }
+  p.c_ptr = C;
+  if (kind != 0) {
+    p.a_scale = scales->a_scale;
+    p.b_scale = scales->b_scale;
+  }
+  p.status = d->status;
+  p.timeout_ns = static_cast<unsigned long long>(opt_or(g_opt_timeout, kDefaultTimeoutNs));
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.tiles_m = static_cast<int>(tiles_m);
+  p.tiles_n = static_cast<int>(tiles_n);
+  const int64_t k_bytes = kind == 0 ? K * 2 : kind == 1 ? K : K / 2;
+  p.num_kb = static_cast<int>((k_bytes + 127) / 128);
+  p.group_m = static_cast<int>(opt_or(g_opt_group, kDefaultGroupM));
+  p.fault_mode = g_fault.exchange(0);
+
+  int clusters = 0;
+  st = max_clusters(*d, kind, id, *v, &clusters);
+  if (st != TKG_OK) return st;
+  int64_t grid_clusters = clusters;
+  const int64_t cap = g_opt_max_ctas.load(std::memory_order_relaxed);
+  if (cap > 0 && cap / v->cg < grid_clusters) grid_clusters = cap / v->cg > 0 ? cap / v->cg : 1;
+  if (tiles_m * tiles_n < grid_clusters) grid_clusters = tiles_m * tiles_n;
+
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid_clusters * v->cg), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(v->threads), 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(v->smem_bytes);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(v->cg);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {&p};
+  if (cudaLaunchKernelExC(&cfg, v->func, args) != cudaSuccess) {
+    cudaGetLastError();
+    return TKG_ERR_CUDA;
+  }
+  return TKG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+tkg_status tkg_gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* C,
+                         const tkg_scales* scales, void* stream) {
+  return gemm_launch(0, M, N, K, A, B, C, scales, stream);
+}
+
+tkg_status tkg_gemm_fp8(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* C,
+                        const tkg_scales* scales, void* stream) {
+  return gemm_launch(1, M, N, K, A, B, C, scales, stream);
+}
+
+tkg_status tkg_gemm_nvfp4(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* C,
+                          const tkg_scales* scales, void* stream) {
+  return gemm_launch(2, M, N, K, A, B, C, scales, stream);
+}
+
+tkg_status tkg_check_status(void* stream) {
+  DevState* d = nullptr;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return TKG_ERR_CUDA;
+  }
+  tkg_status st = current_device(&d);
+  if (st != TKG_OK) return st;
+  unsigned int word = 0;
+  if (cudaMemcpy(&word, d->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return TKG_ERR_CUDA;
+  }
+  if (word != 0) {
+    const unsigned int zero = 0;
+    if (cudaMemcpy(d->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) {
+      cudaGetLastError();
+      return TKG_ERR_CUDA;
+    }
+  }
+  return (word & kStatusTimeout) ? TKG_ERR_TIMEOUT : TKG_OK;
+}
+
+const char* tkg_status_string(tkg_status s) {
+  switch (s) {
+    case TKG_OK: return "ok";
+    case TKG_ERR_INVALID_ARG: return "invalid argument";
+    case TKG_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case TKG_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs compute capability 10.3)";
+    case TKG_ERR_CUDA: return "CUDA runtime or driver error";
+    case TKG_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case TKG_ERR_INTERNAL: return "internal error";
+  }
+  return "unknown status";
+}
+
+void tkg_shutdown(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_maps.clear();
+  for (auto& d : g_dev) d = DevState{};
+}
+
+tkg_status tkg_set_option(tkg_option key, int64_t value) {
+  if (value < 0) return TKG_ERR_INVALID_ARG;
+  switch (key) {
+    case TKG_OPT_TIMEOUT_NS: g_opt_timeout.store(value); return TKG_OK;
+    case TKG_OPT_GROUP_M:
+      if (value > 65536) return TKG_ERR_INVALID_ARG;
+      g_opt_group.store(value);
+      return TKG_OK;
+    case TKG_OPT_VARIANT:
+      if (value >= kNumVariants) return TKG_ERR_INVALID_ARG;
+      g_opt_variant.store(value);
+      return TKG_OK;
+    case TKG_OPT_MAX_CTAS: g_opt_max_ctas.store(value); return TKG_OK;
+  }
+  return TKG_ERR_INVALID_ARG;
+}
+
+int64_t tkg_get_option(tkg_option key) {
+  switch (key) {
+    case TKG_OPT_TIMEOUT_NS: return opt_or(g_opt_timeout, kDefaultTimeoutNs);
+    case TKG_OPT_GROUP_M: return opt_or(g_opt_group, kDefaultGroupM);
+    case TKG_OPT_VARIANT: return g_opt_variant.load();
+    case TKG_OPT_MAX_CTAS: return g_opt_max_ctas.load();
+  }
+  return -1;
+}
+
+// ---------------------------------------------------------------- debug (host)
+
+int tkg_debug_tile_coord(int t, int tiles_m, int tiles_n, int group_m, int* tm, int* tn) {
+  if (tiles_m < 1 || tiles_n < 1 || group_m < 1 || t < 0 || !tm || !tn) return -1;
+  if (static_cast<int64_t>(tiles_m) * tiles_n <= t) return -1;
+  TileOrder{tiles_m, tiles_n, group_m}.coord(t, *tm, *tn);
+  return 0;
+}
+
+uint32_t tkg_debug_swizzle_offset(uint32_t off, uint32_t s_bytes) { return swizzle_offset(off, s_bytes); }
+
+uint32_t tkg_debug_select_swizzle(uint32_t row_bytes) { return select_swizzle(row_bytes); }
+
+tkg_status tkg_debug_variant_info(int kind, int variant, int32_t info[6]) {
+  const KernelVariant* v = variant_of(kind, variant);
+  if (!v || !info) return TKG_ERR_INVALID_ARG;
+  info[0] = v->cg;
+  info[1] = v->bn;
+  info[2] = v->stages;
+  info[3] = v->epi_warps;
+  info[4] = v->threads;
+  info[5] = v->smem_bytes;
+  return TKG_OK;
+}
+
+int tkg_debug_pick_variant(int kind, int64_t M, int64_t N, int64_t K) { return pick_variant(kind, M, N, K); }
+
+tkg_status tkg_debug_set_fault(int mode) {
+  if (mode < 0 || mode > 1) return TKG_ERR_INVALID_ARG;
+  g_fault.store(mode);
+  return TKG_OK;
+}
+
+}  // extern "C"
+
+// Used by the probe translation unit.
+namespace tkg {
+tkg_status debug_encode_map(CUtensorMap* out, const void* ptr, uint64_t d0, uint64_t d1, uint64_t pitch, uint32_t b0,
+                            uint32_t b1, int swz) {
+  return get_map(out, ptr, CU_TENSOR_MAP_DATA_TYPE_UINT8, d0, d1, pitch, b0, b1, swz);
+}
+tkg_status debug_device_ready() {
+  DevState* d = nullptr;
+  return current_device(&d);
+}
+}  // namespace tkg

@@ -1,0 +1,24 @@
+// gemm_bf16.cu — bf16 instantiations of the persistent tcgen05 GEMM.
+#include <cuda_bf16.h>
+
+#include "gemm_variants.h"
+
+namespace tkg {
+
+using Bf16_1Sm_256 = GemmCfg<Kind::BF16, 1, 256, 4, 4>;
+using Bf16_2Sm_256 = GemmCfg<Kind::BF16, 2, 256, 6, 4>;
+using Bf16_2Sm_128 = GemmCfg<Kind::BF16, 2, 128, 8, 4>;
+
+const KernelVariant* bf16_variant(int id) {
+  static const KernelVariant v1 = make_variant<Bf16_1Sm_256>("bf16_1sm_128x256_s4");
+  static const KernelVariant v2 = make_variant<Bf16_2Sm_256>("bf16_2sm_256x256_s6");
+  static const KernelVariant v3 = make_variant<Bf16_2Sm_128>("bf16_2sm_256x128_s8");
+  switch (id) {
+    case kVariant1Sm128x256: return &v1;
+    case kVariant2Sm256x256: return &v2;
+    case kVariant2Sm256x128: return &v3;
+    default: return nullptr;
+  }
+}
+
+}  // namespace tkg

@@ -1,0 +1,26 @@
+// gemm_fp8.cu — FP8 (e4m3 x e4m3, kind::f8f6f4) instantiations of the
+// persistent tcgen05 GEMM.  Same byte geometry as bf16: a stage row is 128
+// bytes = 128 K elements; each MMA consumes 32 of them.
+#include <cuda_bf16.h>
+
+#include "gemm_variants.h"
+
+namespace tkg {
+
+using Fp8_1Sm_256 = GemmCfg<Kind::FP8, 1, 256, 4, 4>;
+using Fp8_2Sm_256 = GemmCfg<Kind::FP8, 2, 256, 6, 4>;
+using Fp8_2Sm_128 = GemmCfg<Kind::FP8, 2, 128, 8, 4>;
+
+const KernelVariant* fp8_variant(int id) {
+  static const KernelVariant v1 = make_variant<Fp8_1Sm_256>("fp8_1sm_128x256_s4");
+  static const KernelVariant v2 = make_variant<Fp8_2Sm_256>("fp8_2sm_256x256_s6");
+  static const KernelVariant v3 = make_variant<Fp8_2Sm_128>("fp8_2sm_256x128_s8");
+  switch (id) {
+    case kVariant1Sm128x256: return &v1;
+    case kVariant2Sm256x256: return &v2;
+    case kVariant2Sm256x128: return &v3;
+    default: return nullptr;
+  }
+}
+
+}  // namespace tkg

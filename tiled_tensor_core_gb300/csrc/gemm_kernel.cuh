@@ -1,0 +1,394 @@
+// gemm_kernel.cuh — persistent load / compute / store-finish GEMM kernel for
+// sm_103a:  C[M,N] (bf16) = A[M,K] · B[N,K]ᵀ with fp32 accumulation in TMEM.
+//
+// Structure (the LCSF template of "ThunderKittens: Simple, Fast, and Adorable
+// AI Kernels", "The Four Functions: Load, Compute, Store, Finish", re-cast for
+// tcgen05):
+//   warp 0, one lane   LOAD     TMA 2-D tile loads of A and B (and the NVFP4
+//                               block scales) into a STAGES-deep shared ring,
+//                               guarded by full/empty mbarriers
+//                               ("Multi-Stage Buffer", Table 1).
+//   warp 1, one lane   COMPUTE  tcgen05.mma into a double-buffered fp32
+//                               accumulator in tensor memory; each stage is
+//                               released by tcgen05.commit on its empty barrier.
+//   warps 2.., all     STORE /  TMEM -> registers (tcgen05.ld), per-tensor
+//                      FINISH   scales, round to bf16, 128-byte-swizzled
+//                               staging tile, TMA store.  The accumulator is
+//                               handed back early so the next tile's MMAs
+//                               overlap this tile's store ("overlapping one
+//                               chunk's load with the previous chunk's finish").
+// Grid: persistent, one CTA (or CTA pair for the 2-SM MMA) per SM, walking the
+// output tiles in the L2-aware grouped order ("Persistent Grid Launch",
+// "Block Launch Order and L2 Cache Reuse").
+//
+// Every wait is bounded (TKG_OPT_TIMEOUT_NS).  A role that gives up records
+// TKG timeout bits in the status word, raises the CTA abort flag so the others
+// stop too, lets its in-flight copies land, and the CTA still frees its TMEM.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "tkg_device.cuh"
+
+namespace tkg {
+
+enum class Kind : int { BF16 = 0, FP8 = 1, NVFP4 = 2 };
+
+// Status word bits written by the device.
+constexpr unsigned int kStatusTimeout = 1u;
+constexpr unsigned int kStatusRoleShift = 8;  // bit (8 + role) names the role that timed out
+constexpr int kRoleProducer = 0, kRoleMma = 1, kRoleEpilogue = 2;
+
+struct GemmParams {
+  CUtensorMap tmap_a;
+  CUtensorMap tmap_b;
+  CUtensorMap tmap_c;
+  CUtensorMap tmap_sfa;
+  CUtensorMap tmap_sfb;
+  void* c_ptr;
+  const float* a_scale;
+  const float* b_scale;
+  unsigned int* status;
+  unsigned long long timeout_ns;
+  int M, N, K;
+  int tiles_m, tiles_n, num_kb;
+  int group_m;
+  int c_via_tma;
+  int fault_mode;  // 0 = none; 1 = the producer skips the loads of its first stage (timeout test)
+};
+
+template <Kind KIND_, int CG_, int BN_, int STAGES_, int EPI_WARPS_>
+struct GemmCfg {
+  static constexpr Kind KIND = KIND_;
+  static constexpr int CG = CG_;                // CTAs per MMA (1, or 2 for the CTA pair)
+  static constexpr int BN = BN_;                // output-tile columns (whole pair)
+  static constexpr int BM = 128;                // output-tile rows per CTA = TMEM lanes
+  static constexpr int STAGES = STAGES_;
+  static constexpr int EPI_WARPS = EPI_WARPS_;  // 4 or 8
+  static constexpr int ROW_BYTES = 128;         // K bytes per operand row per stage
+  static constexpr uint32_t SWZ = select_swizzle(ROW_BYTES);
+  static_assert(SWZ == 128, "operand rows must take the 128-byte swizzle");
+  // K elements per stage / per MMA, in tensor-map x units per stage
+  static constexpr int K_TMAP = (KIND == Kind::BF16) ? 64 : 128;
+  static constexpr int KSTEPS = 4;              // MMAs per stage: 32 bytes of K each
+  static constexpr int B_ROWS = BN / CG;        // B rows staged by each CTA
+  static constexpr int A_STAGE = BM * ROW_BYTES;
+  static constexpr int B_STAGE = B_ROWS * ROW_BYTES;
+  static constexpr int STAGE_TX = A_STAGE + B_STAGE;  // bytes landing per CTA per stage
+  static constexpr int NUM_ACC = 2;
+  static constexpr int TMEM_COLS = (NUM_ACC * BN <= 256) ? 256 : 512;
+  static constexpr int EPI_COLS = 64;           // output columns per epilogue chunk (128 B of bf16)
+  static constexpr int EPI_BUF = 32 * 128;      // one warp's 32-row staging tile
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  static constexpr uint32_t IDESC =
+      (KIND == Kind::BF16) ? idesc_dense(kFmtBF16, BM * CG, BN) : idesc_dense(kFmtE4M3, BM * CG, BN);
+
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
+  static constexpr int OFF_EPI = OFF_B + STAGES * B_STAGE;
+  static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * 2 * EPI_BUF;
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1;
+  static constexpr int OFF_MISC = OFF_BAR + 8 * NUM_BARS;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
+
+  static_assert(B_STAGE % 1024 == 0 && A_STAGE % 1024 == 0, "stages must keep 1024-byte swizzle atoms aligned");
+  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be a multiple of 64 in [64,256]");
+  static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "epilogue is one or two warpgroups");
+  static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB shared-memory limit");
+  static_assert(KIND != Kind::NVFP4, "block-scaled kind uses its own configuration");
+};
+
+__device__ __forceinline__ void record_timeout(unsigned int* status, int role, volatile int* abort_flag) {
+  atomicOr(status, kStatusTimeout | (1u << (kStatusRoleShift + role)));
+  *abort_flag = 1;
+}
+
+// Spin (bounded) so that copies already issued by this CTA can land before it
+// gives up its shared memory.
+__device__ __forceinline__ void settle_inflight_copies() {
+  const uint64_t t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 < 50000ull) {
+  }
+}
+
+template <int CG>
+__device__ __forceinline__ void mma_commit(uint32_t bar, uint16_t mask) {
+  if constexpr (CG == 1) {
+    (void)mask;
+    mma_commit_local(bar);
+  } else {
+    mma_commit_pair(bar, mask);
+  }
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_constant__ GemmParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sA = sbase + C::OFF_A;
+  const uint32_t sB = sbase + C::OFF_B;
+  const uint32_t sEpi = sbase + C::OFF_EPI;
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + C::NUM_ACC + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * C::STAGES + 2 * C::NUM_ACC);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  volatile int* never_abort = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = (C::CG == 2) ? cluster_ctarank() : 0u;
+  const int cluster_id = blockIdx.x / C::CG;
+  const int num_clusters = gridDim.x / C::CG;
+  const int num_tiles = p.tiles_m * p.tiles_n;
+  const TileOrder order{p.tiles_m, p.tiles_n, p.group_m};
+  const uint64_t tmo = p.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < C::NUM_ACC; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), C::CG * C::EPI_WARPS);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    *never_abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&p.tmap_a);
+    tma_prefetch_desc(&p.tmap_b);
+    if (p.c_via_tma) tma_prefetch_desc(&p.tmap_c);
+  }
+  if (warp == 1) {
+    tmem_alloc<C::CG>(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish<C::CG>();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if constexpr (C::CG == 2) {
+    cluster_arrive();
+    cluster_wait();
+  }
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ LOAD
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      bool first = true;
+      for (int t = cluster_id; t < num_tiles && ok; t += num_clusters) {
+        int tm, tn;
+        order.coord(t, tm, tn);
+        const int a_row = tm * (C::BM * C::CG) + static_cast<int>(rank) * C::BM;
+        const int b_row = tn * C::BN + static_cast<int>(rank) * C::B_ROWS;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, tmo, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = (C::CG == 2) ? mapa_shared(full_bar(stage), 0) : full_bar(stage);
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), C::STAGE_TX * C::CG);
+          if (!(first && p.fault_mode == 1)) {
+            tma_load_2d<C::CG>(sA + stage * C::A_STAGE, &p.tmap_a, fb, kb * C::K_TMAP, a_row);
+            tma_load_2d<C::CG>(sB + stage * C::B_STAGE, &p.tmap_b, fb, kb * C::K_TMAP, b_row);
+          }
+          first = false;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        record_timeout(p.status, kRoleProducer, abort_flag);
+        settle_inflight_copies();
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ COMPUTE
+    if (lane == 0 && rank == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int it = 0;
+      for (int t = cluster_id; t < num_tiles && ok; t += num_clusters, ++it) {
+        const int acc = it & 1;
+        const uint32_t acc_phase = (it >> 1) & 1;
+        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, tmo, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::BN);
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, tmo, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = sA + stage * C::A_STAGE;
+          const uint32_t b0 = sB + stage * C::B_STAGE;
+#pragma unroll
+          for (int kk = 0; kk < C::KSTEPS; ++kk) {
+            const uint64_t ad = sdesc_sw128(a0 + 32u * kk);
+            const uint64_t bd = sdesc_sw128(b0 + 32u * kk);
+            const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
+            if constexpr (C::KIND == Kind::BF16)
+              mma_bf16<C::CG>(d_tmem, ad, bd, C::IDESC, accum);
+            else
+              mma_f8f6f4<C::CG>(d_tmem, ad, bd, C::IDESC, accum);
+          }
+          mma_commit<C::CG>(empty_bar(stage), 0x3);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit<C::CG>(tfull_bar(acc), 0x3);
+      }
+      // No MMA may still be writing TMEM when it is released.
+      mma_commit<C::CG>(drain_bar, 0x1);
+      mbar_wait(drain_bar, 0, tmo, never_abort);
+      if (!ok) record_timeout(p.status, kRoleMma, abort_flag);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ STORE / FINISH
+    constexpr int SUBS = C::EPI_WARPS / 4;
+    const int ew = warp - 2;
+    const int quad = warp & 3;  // the TMEM lane quarter this warp may read
+    const int sub = ew / 4;
+    const uint32_t stage0 = sEpi + static_cast<uint32_t>(ew) * 2u * C::EPI_BUF;
+    float sa = 1.0f, sb = 1.0f;
+    if constexpr (C::KIND != Kind::BF16) {
+      sa = *p.a_scale;
+      sb = *p.b_scale;
+    }
+    const uint32_t tempty_leader0 = (C::CG == 2) ? mapa_shared(tempty_bar(0), 0) : tempty_bar(0);
+    int it = 0;
+    int chunk_ctr = 0;
+    for (int t = cluster_id; t < num_tiles; t += num_clusters, ++it) {
+      int tm, tn;
+      order.coord(t, tm, tn);
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      const bool got = __all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), acc_phase, tmo, abort_flag));
+      if (!got) {
+        if (lane == 0) record_timeout(p.status, kRoleEpilogue, abort_flag);
+        break;
+      }
+      tc_fence_after();
+      const int row0 = tm * (C::BM * C::CG) + static_cast<int>(rank) * C::BM + quad * 32;
+      const int col0 = tn * C::BN;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * C::BN);
+      constexpr int NCH = C::BN / C::EPI_COLS;
+      for (int c = sub; c < NCH; c += SUBS, ++chunk_ctr) {
+        uint32_t r0[32], r1[32];
+        __syncwarp();
+        tmem_ld_32x32b_x32(t_row + c * C::EPI_COLS, r0);
+        tmem_ld_32x32b_x32(t_row + c * C::EPI_COLS + 32, r1);
+        tmem_wait_ld();
+        reg_fence(r0);
+        reg_fence(r1);
+        if (c + SUBS >= NCH) {
+          // last TMEM read of this accumulator by this warp: hand it back
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(tempty_leader0 + 8u * acc);
+        }
+        uint32_t pk[32];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          float x0 = __uint_as_float(r0[2 * j]), x1 = __uint_as_float(r0[2 * j + 1]);
+          float y0 = __uint_as_float(r1[2 * j]), y1 = __uint_as_float(r1[2 * j + 1]);
+          if constexpr (C::KIND != Kind::BF16) {
+            x0 = x0 * sa; x0 = x0 * sb;
+            x1 = x1 * sa; x1 = x1 * sb;
+            y0 = y0 * sa; y0 = y0 * sb;
+            y1 = y1 * sa; y1 = y1 * sb;
+          }
+          pk[j] = pack_bf16x2(x0, x1);
+          pk[16 + j] = pack_bf16x2(y0, y1);
+        }
+        if (p.c_via_tma) {
+          const uint32_t buf = stage0 + static_cast<uint32_t>(chunk_ctr & 1) * C::EPI_BUF;
+          if (lane == 0) bulk_wait_group_read<1>();  // the store that last used `buf` has read it
+          __syncwarp();
+          const uint32_t row_addr = buf + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            const uint32_t off = swizzle_offset(static_cast<uint32_t>(lane) * 128u + ch * 16u, C::SWZ) -
+                                 static_cast<uint32_t>(lane) * 128u;
+            st_shared_v4(row_addr + off, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&p.tmap_c, buf, col0 + c * C::EPI_COLS, row0);
+            bulk_commit_group();
+          }
+        } else {
+          // generic path for an output whose row pitch TMA cannot take
+          const int row = row0 + lane;
+          if (row < p.M) {
+            uint16_t* out = static_cast<uint16_t*>(p.c_ptr) + static_cast<size_t>(row) * p.N;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int col = col0 + c * C::EPI_COLS + 2 * j;
+              const uint32_t v = pk[j];
+              if (col < p.N) out[col] = static_cast<uint16_t>(v & 0xFFFFu);
+              if (col + 1 < p.N) out[col + 1] = static_cast<uint16_t>(v >> 16);
+            }
+          }
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if constexpr (C::CG == 2) {
+    cluster_arrive();
+    cluster_wait();
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<C::CG>(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+struct KernelVariant {
+  int kind;
+  int cg;
+  int bn;
+  int stages;
+  int epi_warps;
+  int threads;
+  int smem_bytes;
+  const char* name;
+  const void* func;
+};
+
+template <class C>
+KernelVariant make_variant(const char* name) {
+  return KernelVariant{static_cast<int>(C::KIND), C::CG, C::BN, C::STAGES, C::EPI_WARPS, C::THREADS, C::SMEM_BYTES,
+                       name, reinterpret_cast<const void*>(&tkg_gemm_kernel<C>)};
+}
+
+}  // namespace tkg
