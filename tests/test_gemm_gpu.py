@@ -38,11 +38,13 @@ SMALL_SHAPES = {
     "bf16": [(128, 256, 64), (256, 256, 256), (300, 520, 200), (77, 100, 40), (1, 8, 8), (513, 136, 1032),
              (1000, 1000, 512)],
     "fp8": [(128, 256, 128), (256, 256, 256), (300, 520, 208), (77, 100, 48), (1, 16, 16), (1000, 1000, 512)],
+    "nvfp4": [(128, 256, 256), (256, 256, 512), (300, 520, 416), (77, 100, 96), (1, 16, 32), (1000, 1000, 1024),
+              (520, 300, 288)],
 }
 
 
 @pytest.mark.parametrize("variant", VARIANTS, indirect=True)
-@pytest.mark.parametrize("kind", ["bf16", "fp8"])
+@pytest.mark.parametrize("kind", ["bf16", "fp8", "nvfp4"])
 def test_small_shapes_match_oracle(tkg, variant, kind):
     for i, (M, N, K) in enumerate(SMALL_SHAPES[kind]):
         ops = synth.make_operands(kind, M, N, K, "normal_sqrtk" if kind == "bf16" else "normal", 31 + i, 47 + i)
@@ -52,8 +54,8 @@ def test_small_shapes_match_oracle(tkg, variant, kind):
 
 
 @pytest.mark.parametrize("variant", VARIANTS, indirect=True)
-@pytest.mark.parametrize("kind", ["bf16", "fp8"])
-@pytest.mark.parametrize("shape", [(256, 256, 256), (300, 392, 128), (129, 64, 256)])
+@pytest.mark.parametrize("kind", ["bf16", "fp8", "nvfp4"])
+@pytest.mark.parametrize("shape", [(256, 256, 256), (300, 392, 128), (129, 64, 256), (200, 264, 544)])
 def test_small_integers_bit_exact(tkg, variant, kind, shape):
     M, N, K = shape
     ops = synth.small_int_operands(kind, M, N, K, seed=sum(shape))
@@ -63,7 +65,7 @@ def test_small_integers_bit_exact(tkg, variant, kind, shape):
 
 
 @pytest.mark.parametrize("variant", VARIANTS, indirect=True)
-@pytest.mark.parametrize("kind", ["bf16", "fp8"])
+@pytest.mark.parametrize("kind", ["bf16", "fp8", "nvfp4"])
 @pytest.mark.parametrize("identity", [True, False])
 def test_permutation_exact(tkg, variant, kind, identity):
     ops, perm = synth.permutation_operands(kind, 384, 256, seed=3, identity=identity)
@@ -115,7 +117,7 @@ def test_workload_full_compare(tkg, name):
     check_against_oracle(ops.kind, g.c_bits(), acc, c_ref, ops.scale_a, ops.scale_b)
 
 
-@pytest.mark.parametrize("name", ["bf16_8192", "bf16_skinny", "fp8_8192"])
+@pytest.mark.parametrize("name", ["bf16_8192", "bf16_skinny", "fp8_8192", "nvfp4_16384"])
 def test_workload_sampled_rows(tkg, name):
     ops = synth.workload_operands(name)
     g = run_gpu(ops)
@@ -123,3 +125,22 @@ def test_workload_sampled_rows(tkg, name):
     acc, c_ref = oracle.gemm(ops, rows=rows)
     c = g.c[torch.from_numpy(rows).cuda()].view(torch.int16).cpu().numpy().view(np.uint16)
     check_against_oracle(ops.kind, c, acc, c_ref, ops.scale_a, ops.scale_b)
+
+
+def test_nvfp4_zero_block_scales_give_zero(tkg):
+    # a block whose scale is 0 contributes nothing, whatever its e2m1 codes
+    ops = synth.make_operands("nvfp4", 256, 256, 512, "normal", 21, 22)
+    ops.sfa[:, 1::2] = 0
+    g = run_gpu(ops)
+    acc, c_ref = oracle.gemm(ops)
+    check_against_oracle("nvfp4", g.c_bits(), acc, c_ref, ops.scale_a, ops.scale_b)
+
+
+def test_nvfp4_repeated_calls_reuse_scratch(tkg):
+    # the interleaved-scale scratch is stream-ordered and recycled between calls
+    shapes = [(512, 384, 1024), (256, 256, 256), (768, 1024, 512)]
+    for i, (M, N, K) in enumerate(shapes * 2):
+        ops = synth.make_operands("nvfp4", M, N, K, "normal", 60 + i, 80 + i)
+        g = run_gpu(ops)
+        acc, c_ref = oracle.gemm(ops)
+        check_against_oracle("nvfp4", g.c_bits(), acc, c_ref, ops.scale_a, ops.scale_b)

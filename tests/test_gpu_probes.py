@@ -64,3 +64,36 @@ def test_single_tile_fp8_mma(tkg, oracle_mod, n, ksteps):
     kk = 32 * ksteps
     acc, _ = oracle_mod.gemm_fp8(ops.a[:, :kk], ops.b[:, :kk], 1.0, 1.0)
     assert np.array_equal(out, acc)
+
+
+def _sf_words(sf_rows, quarter_lanes):
+    """TMEM contents [128 lanes][8 columns] holding the 4 scales of each of up
+    to 256 rows: row i at column i // 32, lane (i % 32) + 32 q for every
+    quarter q (B's rule, and a superset of A's: lane i itself)."""
+    words = np.zeros((128, 8), dtype=np.uint32)
+    for i in range(sf_rows.shape[0]):
+        w = int(sf_rows[i, 0]) | (int(sf_rows[i, 1]) << 8) | (int(sf_rows[i, 2]) << 16) | (int(sf_rows[i, 3]) << 24)
+        for q in quarter_lanes:
+            words[(i % 32) + 32 * q, i // 32] = w
+    return words
+
+
+@pytest.mark.parametrize("n", [128, 256])
+def test_single_tile_nvfp4_mma_scale_layout(tkg, oracle_mod, n):
+    # one block-scaled MMA (K = 64): 4 scales per row, slice j in byte j;
+    # A's row m read at lane m, column m // 32; B's row n at lane n % 32, column n // 32
+    ops = synth.small_int_operands("nvfp4", 128, n, 64, seed=n)
+    a_tile = np.zeros((128, 128), np.uint8)
+    b_tile = np.zeros((n, 128), np.uint8)
+    a_tile[:, :32] = ops.a
+    b_tile[:, :32] = ops.b
+    sfa = _sf_words(ops.sfa, [0, 1, 2, 3])
+    sfb = _sf_words(ops.sfb, [0, 1, 2, 3])
+    d_a = torch.from_numpy(a_tile).cuda()
+    d_b = torch.from_numpy(b_tile).cuda()
+    d_sfa = torch.from_numpy(sfa.view(np.int32)).cuda()
+    d_sfb = torch.from_numpy(sfb.view(np.int32)).cuda()
+    d_out = torch.full((128, n), float("nan"), dtype=torch.float32, device="cuda")
+    assert tkg.tkg_debug_mma_probe(2, n, 1, d_a, d_b, d_sfa, d_sfb, [0, 0], d_out) == tkg.TKG_OK
+    acc, _ = oracle_mod.gemm_nvfp4(ops.a, ops.b, ops.sfa, ops.sfb, 1.0, 1.0)
+    assert np.array_equal(d_out.cpu().numpy(), acc)

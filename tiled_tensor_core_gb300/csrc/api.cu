@@ -45,6 +45,7 @@ struct DevState {
   int cc_major = 0, cc_minor = 0;
   unsigned int* status = nullptr;
   int max_clusters[kNumKinds][kNumVariants] = {};
+  cudaMemPool_t pool = nullptr;  // stream-ordered scratch for the NVFP4 scale interleave
 };
 DevState g_dev[kMaxDevices];
 
@@ -114,6 +115,19 @@ tkg_status device_state_locked(int dev, DevState** out) {
     d.status = static_cast<unsigned int*>(sp);
     for (auto& row : d.max_clusters)
       for (int& v : row) v = 0;
+    if (!d.pool) {
+      cudaMemPoolProps props{};
+      props.allocType = cudaMemAllocationTypePinned;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev;
+      if (cudaMemPoolCreate(&d.pool, &props) != cudaSuccess) {
+        cudaGetLastError();
+        d.pool = nullptr;
+        return TKG_ERR_CUDA;
+      }
+      uint64_t keep = UINT64_MAX;  // keep freed blocks for reuse by the next call
+      cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    }
     d.ready = true;
   }
   *out = &d;
@@ -268,10 +282,48 @@ tkg_status gemm_launch(int kind, int64_t M, int64_t N, int64_t K, const void* A,
       st = get_map(&p.tmap_b, B, CU_TENSOR_MAP_DATA_TYPE_UINT8, row_bytes, N, row_bytes, 128, b_rows, 128);
   }
   if (st != TKG_OK) return st;
+  const int64_t k_bytes = kind == 0 ? K * 2 : kind == 1 ? K : K / 2;
+  p.num_kb = static_cast<int>((k_bytes + 127) / 128);
+  uint8_t* scratch = nullptr;
+  if (kind == 2) {
+    // Interleaved block scales (stream-ordered scratch, freed after the GEMM in stream order).
+    p.sf_blocks_a = static_cast<int>(tiles_m * v->cg);
+    p.sf_blocks_b = static_cast<int>(tiles_n * (v->bn / 128));
+    const size_t bytes = nvfp4_scratch_bytes(p.sf_blocks_a, p.sf_blocks_b, p.num_kb);
+    const size_t b_off = static_cast<size_t>(p.sf_blocks_a) * p.num_kb * 2048;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&scratch), bytes, d->pool, cs) != cudaSuccess) {
+      cudaGetLastError();
+      return TKG_ERR_CUDA;
+    }
+    if (nvfp4_interleave_scales(scales->a_block_scale, scales->b_block_scale, static_cast<int>(M),
+                                static_cast<int>(N), static_cast<int>(K), p.sf_blocks_a, p.sf_blocks_b, p.num_kb,
+                                scratch, b_off, cs) != cudaSuccess) {
+      cudaGetLastError();
+      cudaFreeAsync(scratch, cs);
+      return TKG_ERR_CUDA;
+    }
+    st = get_map(&p.tmap_sfa, scratch, CU_TENSOR_MAP_DATA_TYPE_UINT8, 128,
+                 static_cast<uint64_t>(p.sf_blocks_a) * p.num_kb * 16, 128, 128, 16, 0);
+    if (st == TKG_OK)
+      st = get_map(&p.tmap_sfb, scratch + b_off, CU_TENSOR_MAP_DATA_TYPE_UINT8, 128,
+                   static_cast<uint64_t>(p.sf_blocks_b) * p.num_kb * 16, 128, 128,
+                   static_cast<uint32_t>(16 * (v->bn / 128)), 0);
+    if (st != TKG_OK) {
+      cudaFreeAsync(scratch, cs);
+      return st;
+    }
+  }
   p.c_via_tma = (N % 8 == 0) ? 1 : 0;
+  auto release = [&]() {
+    if (scratch) cudaFreeAsync(scratch, static_cast<cudaStream_t>(stream));
+  };
   if (p.c_via_tma) {
     st = get_map(&p.tmap_c, C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, N * 2, 64, 32, 128);
-    if (st != TKG_OK) return st;
+    if (st != TKG_OK) {
+      release();
+      return st;
+    }
   }
   p.c_ptr = C;
   if (kind != 0) {
@@ -285,14 +337,15 @@ tkg_status gemm_launch(int kind, int64_t M, int64_t N, int64_t K, const void* A,
   p.K = static_cast<int>(K);
   p.tiles_m = static_cast<int>(tiles_m);
   p.tiles_n = static_cast<int>(tiles_n);
-  const int64_t k_bytes = kind == 0 ? K * 2 : kind == 1 ? K : K / 2;
-  p.num_kb = static_cast<int>((k_bytes + 127) / 128);
   p.group_m = static_cast<int>(opt_or(g_opt_group, kDefaultGroupM));
   p.fault_mode = g_fault.exchange(0);
 
   int clusters = 0;
   st = max_clusters(*d, kind, id, *v, &clusters);
-  if (st != TKG_OK) return st;
+  if (st != TKG_OK) {
+    release();
+    return st;
+  }
   int64_t grid_clusters = clusters;
   const int64_t cap = g_opt_max_ctas.load(std::memory_order_relaxed);
   if (cap > 0 && cap / v->cg < grid_clusters) grid_clusters = cap / v->cg > 0 ? cap / v->cg : 1;
@@ -313,8 +366,10 @@ tkg_status gemm_launch(int kind, int64_t M, int64_t N, int64_t K, const void* A,
   void* args[] = {&p};
   if (cudaLaunchKernelExC(&cfg, v->func, args) != cudaSuccess) {
     cudaGetLastError();
+    release();
     return TKG_ERR_CUDA;
   }
+  release();
   return TKG_OK;
 }
 
@@ -377,7 +432,12 @@ const char* tkg_status_string(tkg_status s) {
 void tkg_shutdown(void) {
   std::lock_guard<std::mutex> lk(g_mu);
   g_maps.clear();
-  for (auto& d : g_dev) d = DevState{};
+  for (auto& d : g_dev) {
+    cudaMemPool_t pool = d.pool;
+    if (pool) cudaMemPoolTrimTo(pool, 0);  // hand cached scratch back; the pool itself is reused
+    d = DevState{};
+    d.pool = pool;
+  }
 }
 
 tkg_status tkg_set_option(tkg_option key, int64_t value) {

@@ -55,9 +55,11 @@ struct GemmParams {
   int group_m;
   int c_via_tma;
   int fault_mode;  // 0 = none; 1 = the producer skips the loads of its first stage (timeout test)
+  int sf_blocks_a;  // NVFP4: 128-row scale blocks per stage-k in the interleaved A scales
+  int sf_blocks_b;  // same for B
 };
 
-template <Kind KIND_, int CG_, int BN_, int STAGES_, int EPI_WARPS_>
+template <Kind KIND_, int CG_, int BN_, int STAGES_, int EPI_WARPS_, int NUM_ACC_ = 2>
 struct GemmCfg {
   static constexpr Kind KIND = KIND_;
   static constexpr int CG = CG_;                // CTAs per MMA (1, or 2 for the CTA pair)
@@ -65,37 +67,59 @@ struct GemmCfg {
   static constexpr int BM = 128;                // output-tile rows per CTA = TMEM lanes
   static constexpr int STAGES = STAGES_;
   static constexpr int EPI_WARPS = EPI_WARPS_;  // 4 or 8
+  static constexpr int NUM_ACC = NUM_ACC_;      // fp32 accumulators in TMEM (2 = epilogue overlaps next tile)
+  static constexpr bool SCALED = (KIND == Kind::NVFP4);
   static constexpr int ROW_BYTES = 128;         // K bytes per operand row per stage
   static constexpr uint32_t SWZ = select_swizzle(ROW_BYTES);
   static_assert(SWZ == 128, "operand rows must take the 128-byte swizzle");
-  // K elements per stage / per MMA, in tensor-map x units per stage
+  // K per stage in tensor-map x units (bf16 elements, or bytes for e4m3 / packed e2m1)
   static constexpr int K_TMAP = (KIND == Kind::BF16) ? 64 : 128;
   static constexpr int KSTEPS = 4;              // MMAs per stage: 32 bytes of K each
   static constexpr int B_ROWS = BN / CG;        // B rows staged by each CTA
   static constexpr int A_STAGE = BM * ROW_BYTES;
   static constexpr int B_STAGE = B_ROWS * ROW_BYTES;
-  static constexpr int STAGE_TX = A_STAGE + B_STAGE;  // bytes landing per CTA per stage
-  static constexpr int NUM_ACC = 2;
-  static constexpr int TMEM_COLS = (NUM_ACC * BN <= 256) ? 256 : 512;
+  // NVFP4 block scales, per stage: 4 interleaved 512-byte atoms (one per MMA)
+  // for each 128 rows.  Each CTA stages its own 128 rows of A's scales and the
+  // scales of all BN rows of B (every CTA of a pair multiplies by all of B).
+  static constexpr int SF_ATOM = 512;
+  static constexpr int SFA_STAGE = SCALED ? KSTEPS * SF_ATOM : 0;
+  static constexpr int SFB_BLOCKS = BN / 128;   // 128-row blocks of B scales per tile
+  static constexpr int SFB_STAGE = SCALED ? SFB_BLOCKS * KSTEPS * SF_ATOM : 0;
+  static constexpr int STAGE_TX = A_STAGE + B_STAGE + SFA_STAGE + SFB_STAGE;  // bytes landing per CTA per stage
+  static constexpr int ACC_COLS = NUM_ACC * BN;
+  // TMEM columns of one stage's scales: A: 4 per MMA (row m at column m/32);
+  // B: BN/32 per MMA (row n at column n/32).
+  static constexpr int SF_COLS_A = 4 * KSTEPS;
+  static constexpr int SF_COLS_B = (BN / 32) * KSTEPS;
+  static constexpr int SF_COLS_STAGE = SCALED ? SF_COLS_A + SF_COLS_B : 0;
+  static constexpr int TMEM_USED = ACC_COLS + STAGES * SF_COLS_STAGE;
+  static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128
+                                 : TMEM_USED <= 256 ? 256 : 512;
   static constexpr int EPI_COLS = 64;           // output columns per epilogue chunk (128 B of bf16)
   static constexpr int EPI_BUF = 32 * 128;      // one warp's 32-row staging tile
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
-  static constexpr uint32_t IDESC =
-      (KIND == Kind::BF16) ? idesc_dense(kFmtBF16, BM * CG, BN) : idesc_dense(kFmtE4M3, BM * CG, BN);
+  static constexpr uint32_t IDESC = (KIND == Kind::BF16)   ? idesc_dense(kFmtBF16, BM * CG, BN)
+                                    : (KIND == Kind::FP8) ? idesc_dense(kFmtE4M3, BM * CG, BN)
+                                                          : idesc_mxf4nvf4(BM * CG, BN);
 
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
-  static constexpr int OFF_EPI = OFF_B + STAGES * B_STAGE;
+  static constexpr int OFF_SFA = OFF_B + STAGES * B_STAGE;
+  static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
+  static constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_STAGE;
   static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * 2 * EPI_BUF;
   static constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NUM_BARS;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
 
   static_assert(B_STAGE % 1024 == 0 && A_STAGE % 1024 == 0, "stages must keep 1024-byte swizzle atoms aligned");
+  static_assert((OFF_SFA % 1024) == 0 && (OFF_EPI % 1024) == 0, "region alignment");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be a multiple of 64 in [64,256]");
+  static_assert(!SCALED || BN % 128 == 0, "block-scaled tiles cover whole 128-row scale blocks of B");
   static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "epilogue is one or two warpgroups");
+  static_assert(NUM_ACC == 1 || NUM_ACC == 2, "one or two accumulators");
+  static_assert(TMEM_USED <= 512, "tensor memory has 512 columns");
   static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB shared-memory limit");
-  static_assert(KIND != Kind::NVFP4, "block-scaled kind uses its own configuration");
 };
 
 __device__ __forceinline__ void record_timeout(unsigned int* status, int role, volatile int* abort_flag) {
@@ -129,6 +153,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
   const uint32_t sA = sbase + C::OFF_A;
   const uint32_t sB = sbase + C::OFF_B;
   const uint32_t sEpi = sbase + C::OFF_EPI;
+  const uint32_t sSFA = sbase + C::OFF_SFA;
+  const uint32_t sSFB = sbase + C::OFF_SFB;
   const uint32_t bar0 = sbase + C::OFF_BAR;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
@@ -163,6 +189,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
     fence_mbar_init();
     tma_prefetch_desc(&p.tmap_a);
     tma_prefetch_desc(&p.tmap_b);
+    if constexpr (C::SCALED) {
+      tma_prefetch_desc(&p.tmap_sfa);
+      tma_prefetch_desc(&p.tmap_sfb);
+    }
     if (p.c_via_tma) tma_prefetch_desc(&p.tmap_c);
   }
   if (warp == 1) {
@@ -200,6 +230,14 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
           if (!(first && p.fault_mode == 1)) {
             tma_load_2d<C::CG>(sA + stage * C::A_STAGE, &p.tmap_a, fb, kb * C::K_TMAP, a_row);
             tma_load_2d<C::CG>(sB + stage * C::B_STAGE, &p.tmap_b, fb, kb * C::K_TMAP, b_row);
+            if constexpr (C::SCALED) {
+              // interleaved scale atoms: 16 rows of 128 B per (stage-k, 128-row block), blocks of one
+              // stage-k contiguous
+              const int rb_a = a_row / 128;
+              const int rb_b = (tn * C::BN) / 128;
+              tma_load_2d<C::CG>(sSFA + stage * C::SFA_STAGE, &p.tmap_sfa, fb, 0, (kb * p.sf_blocks_a + rb_a) * 16);
+              tma_load_2d<C::CG>(sSFB + stage * C::SFB_STAGE, &p.tmap_sfb, fb, 0, (kb * p.sf_blocks_b + rb_b) * 16);
+            }
           }
           first = false;
           if (++stage == C::STAGES) {
@@ -222,8 +260,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
       bool ok = true;
       int it = 0;
       for (int t = cluster_id; t < num_tiles && ok; t += num_clusters, ++it) {
-        const int acc = it & 1;
-        const uint32_t acc_phase = (it >> 1) & 1;
+        const int acc = it % C::NUM_ACC;
+        const uint32_t acc_phase = (it / C::NUM_ACC) & 1;
         if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, tmo, abort_flag)) {
           ok = false;
           break;
@@ -238,6 +276,20 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
           tc_fence_after();
           const uint32_t a0 = sA + stage * C::A_STAGE;
           const uint32_t b0 = sB + stage * C::B_STAGE;
+          // this stage's scale columns (reused only after the ring stage itself is released)
+          const uint32_t sf_tmem = tmem_base + static_cast<uint32_t>(C::ACC_COLS + stage * C::SF_COLS_STAGE);
+          if constexpr (C::SCALED) {
+            const uint32_t sfa0 = sSFA + stage * C::SFA_STAGE;
+            const uint32_t sfb0 = sSFB + stage * C::SFB_STAGE;
+#pragma unroll
+            for (int kk = 0; kk < C::KSTEPS; ++kk) {
+              tmem_cp_32x128b_warpx4<C::CG>(sf_tmem + 4u * kk, sdesc_plain_rows16(sfa0 + kk * C::SF_ATOM));
+#pragma unroll
+              for (int j = 0; j < C::SFB_BLOCKS; ++j)
+                tmem_cp_32x128b_warpx4<C::CG>(sf_tmem + C::SF_COLS_A + (C::BN / 32) * kk + 4u * j,
+                                              sdesc_plain_rows16(sfb0 + (j * C::KSTEPS + kk) * C::SF_ATOM));
+            }
+          }
 #pragma unroll
           for (int kk = 0; kk < C::KSTEPS; ++kk) {
             const uint64_t ad = sdesc_sw128(a0 + 32u * kk);
@@ -245,8 +297,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
             const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
             if constexpr (C::KIND == Kind::BF16)
               mma_bf16<C::CG>(d_tmem, ad, bd, C::IDESC, accum);
-            else
+            else if constexpr (C::KIND == Kind::FP8)
               mma_f8f6f4<C::CG>(d_tmem, ad, bd, C::IDESC, accum);
+            else
+              mma_mxf4nvf4<C::CG>(d_tmem, ad, bd, C::IDESC, sf_tmem + 4u * kk,
+                                  sf_tmem + C::SF_COLS_A + (C::BN / 32) * kk, accum);
           }
           mma_commit<C::CG>(empty_bar(stage), 0x3);
           if (++stage == C::STAGES) {
@@ -281,8 +336,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
     for (int t = cluster_id; t < num_tiles; t += num_clusters, ++it) {
       int tm, tn;
       order.coord(t, tm, tn);
-      const int acc = it & 1;
-      const uint32_t acc_phase = (it >> 1) & 1;
+      const int acc = it % C::NUM_ACC;
+      const uint32_t acc_phase = (it / C::NUM_ACC) & 1;
       const bool got = __all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), acc_phase, tmo, abort_flag));
       if (!got) {
         if (lane == 0) record_timeout(p.status, kRoleEpilogue, abort_flag);

@@ -1,13 +1,99 @@
-// gemm_nvfp4.cu — NVFP4 block-scaled GEMM variants (kind::mxf4nvf4).
+// gemm_nvfp4.cu — NVFP4 block-scaled GEMM (kind::mxf4nvf4, scale_vec::4X):
+// packed e2m1 operands, one e4m3 scale per 16 consecutive K elements of each
+// row, fp32 per-tensor scales applied in the epilogue (the block-scaled 4-bit
+// GEMM of "ThunderKittens reaches 22.4 PFLOPS on NVIDIA Rubin", NVFP4 and
+// tiling paragraphs).
+//
+// The tensor core reads the scales of one MMA (64 K elements = 4 scales per
+// row) from tensor memory: row m of a 128-row block at lane m, column
+// (base + m/32), byte = 16-element slice.  tcgen05.cp.32x128b.warpx4 produces
+// that from a 512-byte shared "atom" laid out [r = 0..31][q = 0..3][slice 0..3]
+// holding the scales of rows 32q + r.  The caller's row-major [rows][K/16]
+// scales are rewritten into such atoms by interleave_scales_kernel, ordered
+// [stage-k][128-row block][MMA of the stage][atom], so that every ring stage
+// loads one contiguous 2 KB run per 128 rows with a plain 2-D TMA box.
 #include <cuda_bf16.h>
 
 #include "gemm_variants.h"
 
 namespace tkg {
 
+using Nvfp4_1Sm_256 = GemmCfg<Kind::NVFP4, 1, 256, 3, 4, 1>;
+using Nvfp4_2Sm_256 = GemmCfg<Kind::NVFP4, 2, 256, 5, 4, 1>;
+using Nvfp4_2Sm_128 = GemmCfg<Kind::NVFP4, 2, 128, 6, 4, 2>;
+
 const KernelVariant* nvfp4_variant(int id) {
-  (void)id;
-  return nullptr;
+  static const KernelVariant v1 = make_variant<Nvfp4_1Sm_256>("nvfp4_1sm_128x256_s3");
+  static const KernelVariant v2 = make_variant<Nvfp4_2Sm_256>("nvfp4_2sm_256x256_s5");
+  static const KernelVariant v3 = make_variant<Nvfp4_2Sm_128>("nvfp4_2sm_256x128_s6");
+  switch (id) {
+    case kVariant1Sm128x256: return &v1;
+    case kVariant2Sm256x256: return &v2;
+    case kVariant2Sm256x128: return &v3;
+    default: return nullptr;
+  }
+}
+
+namespace {
+
+struct InterleaveArgs {
+  const uint8_t* src;  // row-major [rows][k16] e4m3 scales
+  uint8_t* dst;        // atoms [kstages][blocks][4][512]
+  int rows;            // valid rows
+  int k16;             // scales per row (K / 16)
+  int blocks;          // 128-row blocks in dst (rows padded with zero scales)
+  int kstages;         // 256-element K stages in dst (padded with zero scales)
+};
+
+// One CTA rewrites one 128-row block for two consecutive K stages (32 source
+// bytes per row, i.e. whole 32-byte sectors).  Scales of rows or K positions
+// past the matrix are written as 0.
+__global__ void __launch_bounds__(256) interleave_scales_kernel(InterleaveArgs a, InterleaveArgs b, int blocks_a) {
+  const bool is_a = static_cast<int>(blockIdx.x) < blocks_a;
+  const InterleaveArgs& s = is_a ? a : b;
+  const int local = is_a ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x) - blocks_a;
+  const int rb = local % s.blocks;
+  const int kb0 = 2 * (local / s.blocks);
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const int lin = static_cast<int>(threadIdx.x) + 256 * w;  // 0..1023
+    const int r_in = lin >> 3;                                // row within the block
+    const int word = lin & 7;
+    const int kb = kb0 + (word >> 2);
+    const int t = word & 3;                                   // MMA within the stage
+    if (kb >= s.kstages) continue;
+    const int row = rb * 128 + r_in;
+    const int col = kb * 16 + 4 * t;
+    uint32_t v = 0;
+    if (row < s.rows) {
+      const uint8_t* p = s.src + static_cast<size_t>(row) * s.k16;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (col + j < s.k16) v |= static_cast<uint32_t>(__ldg(p + col + j)) << (8 * j);
+    }
+    const size_t atom = (static_cast<size_t>(kb) * s.blocks + rb) * 4 + t;
+    *reinterpret_cast<uint32_t*>(s.dst + atom * 512 + (r_in & 31) * 16 + (r_in >> 5) * 4) = v;
+  }
+}
+
+}  // namespace
+
+// Rewrites both operands' scales into `scratch` (see the layout above).
+// Returns the byte offset of B's atoms inside `scratch`.
+cudaError_t nvfp4_interleave_scales(const uint8_t* sfa, const uint8_t* sfb, int M, int N, int K, int blocks_a,
+                                    int blocks_b, int kstages, uint8_t* scratch, size_t b_offset,
+                                    cudaStream_t stream) {
+  InterleaveArgs a{sfa, scratch, M, K / 16, blocks_a, kstages};
+  InterleaveArgs b{sfb, scratch + b_offset, N, K / 16, blocks_b, kstages};
+  const int kpairs = (kstages + 1) / 2;
+  const int grid_a = blocks_a * kpairs;
+  const int grid_b = blocks_b * kpairs;
+  interleave_scales_kernel<<<grid_a + grid_b, 256, 0, stream>>>(a, b, grid_a);
+  return cudaGetLastError();
+}
+
+size_t nvfp4_scratch_bytes(int blocks_a, int blocks_b, int kstages) {
+  return (static_cast<size_t>(blocks_a) + blocks_b) * kstages * 2048;
 }
 
 }  // namespace tkg

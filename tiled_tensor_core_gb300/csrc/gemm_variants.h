@@ -19,4 +19,12 @@ const KernelVariant* bf16_variant(int id);
 const KernelVariant* fp8_variant(int id);
 const KernelVariant* nvfp4_variant(int id);
 
+// NVFP4: rewrite row-major [rows][K/16] block scales of A and B into the
+// interleaved per-MMA atoms the GEMM stages (A's atoms at scratch, B's at
+// scratch + b_offset).  One kernel launch on `stream`.
+cudaError_t nvfp4_interleave_scales(const uint8_t* sfa, const uint8_t* sfb, int M, int N, int K, int blocks_a,
+                                    int blocks_b, int kstages, uint8_t* scratch, size_t b_offset,
+                                    cudaStream_t stream);
+size_t nvfp4_scratch_bytes(int blocks_a, int blocks_b, int kstages);
+
 }  // namespace tkg

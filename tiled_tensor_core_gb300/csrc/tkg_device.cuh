@@ -226,6 +226,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   return d;
 }
 
+// Shared-memory descriptor of an unswizzled source of rows of 16 bytes stored
+// back to back (core matrices of 8 rows x 16 B, 128 B apart): the layout of a
+// 32-row x 128-bit tcgen05.cp source.
+__device__ __forceinline__ uint64_t sdesc_plain_rows16(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(128u >> 4) << 16;
+  d |= static_cast<uint64_t>(128u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  return d;
+}
+
 // Instruction descriptor, dense kinds (kind::f16, kind::f8f6f4): D fp32
 // (bits 4-5 = 1), A/B format in bits 7-9 / 10-12, both K-major, N>>3 in bits
 // 17-22, M>>4 in bits 24-28.

@@ -78,14 +78,71 @@ def _encode_nearest_even(x: np.ndarray, table: np.ndarray, sign_bit: int, dtype)
     return (code | (neg.astype(np.int64) << sign_bit)).astype(dtype)
 
 
-def encode_e4m3(x: np.ndarray) -> np.ndarray:
-    """fp values -> e4m3 codes (uint8), RNE, saturating to ±448."""
+def encode_e4m3_table(x: np.ndarray) -> np.ndarray:
+    """fp values -> e4m3 codes by nearest-table-entry search (slow, plain)."""
     return _encode_nearest_even(x, E4M3_POS, 7, np.uint8)
 
 
-def encode_e2m1(x: np.ndarray) -> np.ndarray:
-    """fp values -> e2m1 codes (uint8 in 0..15), RNE, saturating to ±6."""
+def encode_e2m1_table(x: np.ndarray) -> np.ndarray:
     return _encode_nearest_even(x, E2M1_POS, 3, np.uint8)
+
+
+_CHUNK = 1 << 22
+
+
+def encode_e4m3(x: np.ndarray) -> np.ndarray:
+    """fp values -> e4m3 codes (uint8), round to nearest even, saturating to ±448.
+
+    Inside one binade [2^e, 2^(e+1)) the e4m3 grid is uniform with step
+    2^(e-3) (2^-9 below 2^-6, the subnormal range), so rounding |x| / step to
+    the nearest integer with ties to even (np.rint) is round-to-nearest-even on
+    the grid; an integer of 16 is the first value of the next binade."""
+    x = np.asarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    flat_in, flat_out = x.reshape(-1), out.reshape(-1)
+    for s in range(0, flat_in.size, _CHUNK):
+        a = np.abs(flat_in[s:s + _CHUNK])
+        neg = np.signbit(flat_in[s:s + _CHUNK])
+        a = np.minimum(a, np.float32(E4M3_MAX))
+        e = ((a.view(np.int32) >> 23) & 0xFF) - 127
+        e = np.maximum(e, -6)  # subnormals share the step of the first normal binade
+        step_exp = (e - 3).astype(np.int32)
+        r = np.rint(np.ldexp(a, -step_exp)).astype(np.int32)  # exact scaling by a power of two
+        sub = e == -6
+        # normal: r in [8, 16]; r == 16 carries into the next binade
+        carry = r >= 16
+        en = np.where(carry, e + 1, e)
+        rn = np.where(carry, 8, r)
+        code_norm = ((en + 7) << 3) | (rn - 8)
+        code = np.where(sub & (r < 8), r, np.where(sub, 8 + (r - 8), code_norm))
+        code = np.minimum(code, 0x7E)
+        code = np.where(neg & (code != 0), code | 0x80, code)
+        flat_out[s:s + _CHUNK] = code.astype(np.uint8)
+    return out
+
+
+_E2M1_FROM_HALVES = np.full(13, 255, dtype=np.uint8)
+for _c, _v in enumerate([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]):
+    _E2M1_FROM_HALVES[int(_v * 2)] = _c
+
+
+def encode_e2m1(x: np.ndarray) -> np.ndarray:
+    """fp values -> e2m1 codes (uint8 in 0..15), round to nearest even, saturating to ±6.
+
+    Grid steps: 0.5 below 2, 1 in [2, 4), 2 from 4 up; as for e4m3 the rounded
+    multiple of the step is the nearest-even grid value."""
+    x = np.asarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    flat_in, flat_out = x.reshape(-1), out.reshape(-1)
+    for s in range(0, flat_in.size, _CHUNK):
+        v = flat_in[s:s + _CHUNK]
+        a = np.abs(v)
+        step = np.where(a < 2, np.float32(0.5), np.where(a < 4, np.float32(1.0), np.float32(2.0)))
+        q = np.minimum(np.rint(a / step) * step, np.float32(E2M1_MAX))
+        code = _E2M1_FROM_HALVES[(q * 2).astype(np.int32)]
+        code = np.where(np.signbit(v) & (code != 0), code | 0x8, code)
+        flat_out[s:s + _CHUNK] = code.astype(np.uint8)
+    return out
 
 
 def e4m3_value(codes: np.ndarray) -> np.ndarray:
@@ -125,6 +182,22 @@ def unpack_fp4(packed: np.ndarray) -> np.ndarray:
 # --------------------------------------------------------------------------
 
 
+def _rowwise(x: np.ndarray, out_shapes, fn):
+    """Apply fn(rows_in) -> tuple of row blocks to row chunks of x in parallel."""
+    rows, K = x.shape
+    outs = [np.empty(shape, dtype=dt) for shape, dt in out_shapes]
+    ch = _chunk_rows(K)
+
+    def work(c):
+        r0, r1 = c * ch, min(rows, (c + 1) * ch)
+        for o, v in zip(outs, fn(x[r0:r1])):
+            o[r0:r1] = v
+
+    with _pool() as ex:
+        list(ex.map(work, range((rows + ch - 1) // ch)))
+    return outs
+
+
 def quantize_fp8(x: np.ndarray):
     """Per-tensor FP8: scale so max|x| maps to 448, cast to e4m3.
 
@@ -136,8 +209,16 @@ def quantize_fp8(x: np.ndarray):
     if amax == 0.0:
         return encode_e4m3(x), np.float32(1.0)
     sq = np.float32(E4M3_MAX / amax)
-    codes = encode_e4m3(x * sq)
+    (codes,) = _rowwise(x, [(x.shape, np.uint8)], lambda xr: (encode_e4m3(xr * sq),))
     return codes, np.float32(amax / E4M3_MAX)
+
+
+def _block_amax16(xb: np.ndarray) -> np.ndarray:
+    a = np.abs(xb)
+    a = np.maximum(a[..., :8], a[..., 8:])
+    a = np.maximum(a[..., :4], a[..., 4:])
+    a = np.maximum(a[..., :2], a[..., 2:])
+    return np.maximum(a[..., 0], a[..., 1])
 
 
 def quantize_nvfp4(x: np.ndarray):
@@ -152,14 +233,17 @@ def quantize_nvfp4(x: np.ndarray):
     assert K % 16 == 0
     amax = float(np.max(np.abs(x))) if x.size else 0.0
     g = np.float32(amax / (E2M1_MAX * E4M3_MAX)) if amax > 0 else np.float32(1.0)
-    xb = x.reshape(rows, K // 16, 16)
-    bamax = np.max(np.abs(xb), axis=2).astype(np.float64)
-    sb = encode_e4m3(bamax / (E2M1_MAX * float(g)))
-    sbv = e4m3_value(sb) * float(g)  # dequantised block scale
-    with np.errstate(divide="ignore", invalid="ignore"):
-        scaled = np.where(sbv[..., None] > 0, xb / sbv[..., None], 0.0)
-    q = encode_e2m1(scaled).reshape(rows, K)
-    return pack_fp4(q), sb.astype(np.uint8), np.float32(g)
+
+    def block(xr):
+        xb = xr.reshape(-1, K // 16, 16)
+        sb = encode_e4m3(_block_amax16(xb) / np.float32(E2M1_MAX * float(g)))
+        sbv = (e4m3_value(sb) * float(g)).astype(np.float32)[..., None]
+        scaled = np.zeros_like(xb)
+        np.divide(xb, sbv, out=scaled, where=sbv > 0)
+        return pack_fp4(encode_e2m1(scaled).reshape(-1, K)), sb
+
+    packed, sb_all = _rowwise(x, [((rows, K // 2), np.uint8), ((rows, K // 16), np.uint8)], block)
+    return packed, sb_all, np.float32(g)
 
 
 # --------------------------------------------------------------------------
@@ -203,13 +287,38 @@ WORKLOADS = {
 }
 
 
-def _draw(rng: np.random.Generator, rows: int, K: int, dist: str) -> np.ndarray:
-    if dist == "uniform":
-        return rng.uniform(-1.0, 1.0, size=(rows, K)).astype(np.float32)
-    x = rng.standard_normal(size=(rows, K), dtype=np.float32)
-    if dist == "normal_sqrtk":
-        x *= np.float32(1.0 / np.sqrt(K))
-    return x
+def _chunk_rows(K: int) -> int:
+    return max(1, (1 << 20) // max(K, 1))
+
+
+def _pool():
+    import concurrent.futures as cf
+    import os
+    return cf.ThreadPoolExecutor(max_workers=min(32, os.cpu_count() or 1))
+
+
+def _draw(seed: int, rows: int, K: int, dist: str) -> np.ndarray:
+    """Seeded draw of a [rows, K] fp32 matrix.  Row chunk c comes from the
+    PCG64 stream of `seed` advanced by c jumps, so the result does not depend
+    on how many threads fill it."""
+    out = np.empty((rows, K), dtype=np.float32)
+    ch = _chunk_rows(K)
+    base = np.random.PCG64(seed)
+
+    def fill(c):
+        rng = np.random.Generator(base.jumped(c))
+        r0, r1 = c * ch, min(rows, (c + 1) * ch)
+        if dist == "uniform":
+            out[r0:r1] = rng.uniform(-1.0, 1.0, size=(r1 - r0, K)).astype(np.float32)
+        else:
+            rng.standard_normal(size=(r1 - r0, K), dtype=np.float32, out=out[r0:r1])
+            if dist == "normal_sqrtk":
+                out[r0:r1] *= np.float32(1.0 / np.sqrt(K))
+
+    n = (rows + ch - 1) // ch
+    with _pool() as ex:
+        list(ex.map(fill, range(n)))
+    return out
 
 
 @dataclasses.dataclass
@@ -244,7 +353,9 @@ def encode(kind: str, xa: np.ndarray, xb: np.ndarray) -> Operands:
     M, K = xa.shape
     N = xb.shape[0]
     if kind == "bf16":
-        return Operands(kind, M, N, K, encode_bf16(xa), encode_bf16(xb))
+        (a,) = _rowwise(xa, [(xa.shape, np.uint16)], lambda r: (encode_bf16(r),))
+        (b,) = _rowwise(xb, [(xb.shape, np.uint16)], lambda r: (encode_bf16(r),))
+        return Operands(kind, M, N, K, a, b)
     if kind == "fp8":
         a, sa = quantize_fp8(xa)
         b, sb = quantize_fp8(xb)
@@ -257,8 +368,8 @@ def encode(kind: str, xa: np.ndarray, xb: np.ndarray) -> Operands:
 
 
 def make_operands(kind: str, M: int, N: int, K: int, dist: str, seed_a: int, seed_b: int) -> Operands:
-    xa = _draw(np.random.default_rng(seed_a), M, K, dist)
-    xb = _draw(np.random.default_rng(seed_b), N, K, dist)
+    xa = _draw(seed_a, M, K, dist)
+    xb = _draw(seed_b, N, K, dist)
     return encode(kind, xa, xb)
 
 
