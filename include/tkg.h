@@ -101,6 +101,28 @@ TKG_API tkg_status tkg_gemm_fp8(int64_t M, int64_t N, int64_t K, const void* A, 
 TKG_API tkg_status tkg_gemm_nvfp4(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* C,
                           const tkg_scales* scales, void* stream);
 
+/* NVFP4 GEMM that allocates no memory.  The pages have no counterpart: this
+ * entry point exists for callers that cannot allocate device memory during a
+ * call (for example a caller whose allocator is owned by another framework, or
+ * one running under a fixed device-memory budget), because tkg_gemm_nvfp4
+ * takes the scratch for its on-device re-layout of the block scales from a
+ * stream-ordered memory pool.  Same operation, arguments, layouts and result
+ * as tkg_gemm_nvfp4.
+ *  - Scratch: a fixed device array of TKG_NVFP4_NOALLOC_SCRATCH_BYTES inside
+ *    the library, held by every device that loads the library until the
+ *    process exits.  A call needs (Ba + Bb) * ceil(K/256) * 2048 bytes, with
+ *    Ba = ceil(M/256)*2 and Bb = ceil(N/256)*2 for the default kernel; larger
+ *    problems are rejected with TKG_ERR_INVALID_ARG before any GPU work.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress); make that first call before any stream capture.
+ *  - All calls share the one array and each call overwrites the part it uses,
+ *    so calls whose GPU work overlaps (e.g. on two streams) race and give
+ *    wrong results; order them on one stream or with events.
+ *  - It never calls cudaMalloc, cudaFree or any other allocating routine. */
+#define TKG_NVFP4_NOALLOC_SCRATCH_BYTES (32u << 20)
+TKG_API tkg_status tkg_gemm_nvfp4_noalloc(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* C,
+                                          const tkg_scales* scales, void* stream);
+
 /* Synchronises `stream`, then reads and clears the device status word of the
  * current device.  Returns TKG_ERR_TIMEOUT if any kernel since the last check
  * abandoned a pipeline wait (its output is then undefined), TKG_ERR_CUDA if the

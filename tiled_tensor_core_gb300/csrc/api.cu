@@ -513,3 +513,17 @@ tkg_status debug_device_ready() {
   return current_device(&d);
 }
 }  // namespace tkg
+
+// Address of the current device's status word, without any other per-device
+// set-up (used by the entry point that must not allocate).
+namespace tkg {
+tkg_status status_word_address(unsigned int** out) {
+  void* sp = nullptr;
+  if (cudaGetSymbolAddress(&sp, g_tkg_status) != cudaSuccess) {
+    cudaGetLastError();
+    return TKG_ERR_CUDA;
+  }
+  *out = static_cast<unsigned int*>(sp);
+  return TKG_OK;
+}
+}  // namespace tkg

@@ -51,7 +51,7 @@ class TkgError(RuntimeError):
 
 
 _i64, _vp, _i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
-for _name in ("tkg_gemm_bf16", "tkg_gemm_fp8", "tkg_gemm_nvfp4"):
+for _name in ("tkg_gemm_bf16", "tkg_gemm_fp8", "tkg_gemm_nvfp4", "tkg_gemm_nvfp4_noalloc"):
     _f = getattr(lib, _name)
     _f.argtypes = [_i64, _i64, _i64, _vp, _vp, _vp, ctypes.POINTER(tkg_scales), _vp]
     _f.restype = _i32
@@ -135,6 +135,15 @@ def tkg_gemm_fp8(M, N, K, A, B, C, scales, stream=None, check=True) -> int:
 def tkg_gemm_nvfp4(M, N, K, A, B, C, scales, stream=None, check=True) -> int:
     st = lib.tkg_gemm_nvfp4(M, N, K, _addr(A), _addr(B), _addr(C), _scales(scales), _stream(stream))
     return _check(st, "tkg_gemm_nvfp4") if check else st
+
+
+def tkg_gemm_nvfp4_noalloc(M, N, K, A, B, C, scales, stream=None, check=True) -> int:
+    """NVFP4 GEMM whose scale re-layout scratch is a fixed array inside the
+    library instead of a pool allocation, for callers that must not allocate
+    device memory during the call.  Calls that overlap on the GPU share that
+    array and race; the first call on a device must precede any capture."""
+    st = lib.tkg_gemm_nvfp4_noalloc(M, N, K, _addr(A), _addr(B), _addr(C), _scales(scales), _stream(stream))
+    return _check(st, "tkg_gemm_nvfp4_noalloc") if check else st
 
 
 def tkg_check_status(stream=None) -> int:
