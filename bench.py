@@ -42,6 +42,31 @@ PEAK_RATIO = {"bf16": 1.0, "fp8": 2.0, "nvfp4": 6.0}
 DTYPE = {"bf16": "bf16", "fp8": "e4m3", "nvfp4": "e2m1+e4m3"}
 
 
+# DRAM bytes (read + write) per launch of the dominant kernel, from one ncu capture
+# (profiles/), valid only while the kernel sources hash to the value recorded with it.
+TRAFFIC = {
+    "bf16_4096": {"bytes": 97_171_456, "src": "30026a10c7925a73"},        # profiles/gemm_bf16_4096_ncu_full.md
+    "nvfp4_16384": {"bytes": 1_982_171_136, "src": "30026a10c7925a73"},   # profiles/gemm_nvfp4_16384_ncu_full.md
+}
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "tiled_tensor_core_gb300", "csrc")
+    for f in ("tkg_device.cuh", "gemm_kernel.cuh", "gemm_bf16.cu", "gemm_fp8.cu", "gemm_nvfp4.cu"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_bytes(workload: str):
+    rec = TRAFFIC.get(workload)
+    if rec and rec["src"] == kernel_source_hash():
+        return rec["bytes"]
+    return None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -297,7 +322,10 @@ def run_tkg(args, world, rank, local):
                "sample": f"{n_rows} of {w.M} output rows of the same workload ({dt:.1f} s)"}
 
     peaks = load_peaks()
-    peak = peaks["bf16_tflops"] * PEAK_RATIO[w.kind]
+    # The timed region is a long back-to-back run (power-capped regime): the sustained
+    # measured bf16 figure is the matching denominator; the burst one is reported too.
+    peak = peaks["bf16_tflops_sustained"] * PEAK_RATIO[w.kind]
+    peak_burst = peaks["bf16_tflops"] * PEAK_RATIO[w.kind]
     info = tkg.tkg_debug_variant_info({"bf16": 0, "fp8": 1, "nvfp4": 2}[w.kind],
                                       tkg.tkg_debug_pick_variant({"bf16": 0, "fp8": 1, "nvfp4": 2}[w.kind],
                                                                  w.M, w.N, w.K))
@@ -311,10 +339,13 @@ def run_tkg(args, world, rank, local):
                           if n_sets > 1 else f"operands {footprint / 2**20:.0f} MiB > 129 MiB L2"),
                    "kernel": info, "group_m": tkg.tkg_get_option(tkg.TKG_OPT_GROUP_M)},
         "pct_of_peak": 100.0 * value / world / peak,
+        "pct_of_burst_peak": 100.0 * value / world / peak_burst,
         "median_gemm_ms": statistics.median(kern_ms),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None,
-                     "peak_source": f"{peaks['source']} bf16 burst x {PEAK_RATIO[w.kind]:g} (nominal dtype ratio)"},
+                     "frac": achieved / peak, "traffic": traffic_bytes(w.name),
+                     "frac_of_burst_peak": achieved / peak_burst,
+                     "peak_source": (f"{peaks['source']} bf16 sustained (back-to-back cuBLAS) x "
+                                     f"{PEAK_RATIO[w.kind]:g} (nominal dtype ratio)")},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": gemms * launches_per_gemm,

@@ -32,7 +32,7 @@ def variant(tkg, request):
     tkg.tkg_set_option(tkg.TKG_OPT_VARIANT, 0)
 
 
-VARIANTS = [1, 2, 3]
+VARIANTS = [1, 2, 3, 4]
 
 SMALL_SHAPES = {
     "bf16": [(128, 256, 64), (256, 256, 256), (300, 520, 200), (77, 100, 40), (1, 8, 8), (513, 136, 1032),

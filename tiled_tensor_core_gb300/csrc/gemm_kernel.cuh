@@ -77,7 +77,8 @@ struct GemmCfg {
   static constexpr int KSTEPS = 4;              // MMAs per stage: 32 bytes of K each
   static constexpr int B_ROWS = BN / CG;        // B rows staged by each CTA
   static constexpr int A_STAGE = BM * ROW_BYTES;
-  static constexpr int B_STAGE = B_ROWS * ROW_BYTES;
+  static constexpr int B_BOX = B_ROWS * ROW_BYTES;             // bytes of one B tile load
+  static constexpr int B_STAGE = (B_BOX + 1023) / 1024 * 1024;  // keeps every stage 1024-byte aligned
   // NVFP4 block scales, per stage: 4 interleaved 512-byte atoms (one per MMA)
   // for each 128 rows.  Each CTA stages its own 128 rows of A's scales and the
   // scales of all BN rows of B (every CTA of a pair multiplies by all of B).
@@ -85,8 +86,9 @@ struct GemmCfg {
   static constexpr int SFA_STAGE = SCALED ? KSTEPS * SF_ATOM : 0;
   static constexpr int SFB_BLOCKS = BN / 128;   // 128-row blocks of B scales per tile
   static constexpr int SFB_STAGE = SCALED ? SFB_BLOCKS * KSTEPS * SF_ATOM : 0;
-  static constexpr int STAGE_TX = A_STAGE + B_STAGE + SFA_STAGE + SFB_STAGE;  // bytes landing per CTA per stage
-  static constexpr int ACC_COLS = NUM_ACC * BN;
+  static constexpr int STAGE_TX = A_STAGE + B_BOX + SFA_STAGE + SFB_STAGE;  // bytes landing per CTA per stage
+  static constexpr int ACC_STRIDE = BN <= 128 ? 128 : 256;  // accumulators start on aligned columns
+  static constexpr int ACC_COLS = NUM_ACC * ACC_STRIDE;
   // TMEM columns of one stage's scales: A: 4 per MMA (row m at column m/32);
   // B: BN/32 per MMA (row n at column n/32).
   static constexpr int SF_COLS_A = 4 * KSTEPS;
@@ -95,8 +97,11 @@ struct GemmCfg {
   static constexpr int TMEM_USED = ACC_COLS + STAGES * SF_COLS_STAGE;
   static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128
                                  : TMEM_USED <= 256 ? 256 : 512;
-  static constexpr int EPI_COLS = 64;           // output columns per epilogue chunk (128 B of bf16)
-  static constexpr int EPI_BUF = 32 * 128;      // one warp's 32-row staging tile
+  // output columns per epilogue chunk: 64 (rows of 128 B of bf16) when BN allows, else 32 (64 B)
+  static constexpr int EPI_COLS = (BN % 64 == 0) ? 64 : 32;
+  static constexpr int EPI_ROW_BYTES = EPI_COLS * 2;
+  static constexpr uint32_t EPI_SWZ = select_swizzle(EPI_ROW_BYTES);
+  static constexpr int EPI_BUF = 32 * EPI_ROW_BYTES;  // one warp's 32-row staging tile
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   static constexpr uint32_t IDESC = (KIND == Kind::BF16)   ? idesc_dense(kFmtBF16, BM * CG, BN)
                                     : (KIND == Kind::FP8) ? idesc_dense(kFmtE4M3, BM * CG, BN)
@@ -114,7 +119,9 @@ struct GemmCfg {
 
   static_assert(B_STAGE % 1024 == 0 && A_STAGE % 1024 == 0, "stages must keep 1024-byte swizzle atoms aligned");
   static_assert((OFF_SFA % 1024) == 0 && (OFF_EPI % 1024) == 0, "region alignment");
-  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be a multiple of 64 in [64,256]");
+  static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN must be a multiple of 32 in [64,256]");
+  static_assert(B_ROWS % 8 == 0, "B rows per CTA must fill whole 8-row swizzle atoms");
+  static_assert(EPI_BUF % (8 * EPI_SWZ) == 0, "staging tiles must keep swizzle atoms aligned");
   static_assert(!SCALED || BN % 128 == 0, "block-scaled tiles cover whole 128-row scale blocks of B");
   static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "epilogue is one or two warpgroups");
   static_assert(NUM_ACC == 1 || NUM_ACC == 2, "one or two accumulators");
@@ -267,7 +274,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::BN);
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::ACC_STRIDE);
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait(full_bar(stage), phase, tmo, abort_flag)) {
             ok = false;
@@ -346,46 +353,50 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
       tc_fence_after();
       const int row0 = tm * (C::BM * C::CG) + static_cast<int>(rank) * C::BM + quad * 32;
       const int col0 = tn * C::BN;
-      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * C::BN);
+      const uint32_t t_row =
+          tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * C::ACC_STRIDE);
       constexpr int NCH = C::BN / C::EPI_COLS;
+      constexpr int NLD = C::EPI_COLS / 32;  // 32-column TMEM loads per chunk
+      constexpr int NPK = C::EPI_COLS / 2;   // packed bf16 pairs per row
+      constexpr int RB = C::EPI_ROW_BYTES;
       for (int c = sub; c < NCH; c += SUBS, ++chunk_ctr) {
-        uint32_t r0[32], r1[32];
+        uint32_t r[NLD][32];
         __syncwarp();
-        tmem_ld_32x32b_x32(t_row + c * C::EPI_COLS, r0);
-        tmem_ld_32x32b_x32(t_row + c * C::EPI_COLS + 32, r1);
+#pragma unroll
+        for (int l = 0; l < NLD; ++l) tmem_ld_32x32b_x32(t_row + c * C::EPI_COLS + 32 * l, r[l]);
         tmem_wait_ld();
-        reg_fence(r0);
-        reg_fence(r1);
+#pragma unroll
+        for (int l = 0; l < NLD; ++l) reg_fence(r[l]);
         if (c + SUBS >= NCH) {
           // last TMEM read of this accumulator by this warp: hand it back
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(tempty_leader0 + 8u * acc);
         }
-        uint32_t pk[32];
+        uint32_t pk[NPK];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          float x0 = __uint_as_float(r0[2 * j]), x1 = __uint_as_float(r0[2 * j + 1]);
-          float y0 = __uint_as_float(r1[2 * j]), y1 = __uint_as_float(r1[2 * j + 1]);
-          if constexpr (C::KIND != Kind::BF16) {
-            x0 = x0 * sa; x0 = x0 * sb;
-            x1 = x1 * sa; x1 = x1 * sb;
-            y0 = y0 * sa; y0 = y0 * sb;
-            y1 = y1 * sa; y1 = y1 * sb;
+        for (int l = 0; l < NLD; ++l) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            float x0 = __uint_as_float(r[l][2 * j]), x1 = __uint_as_float(r[l][2 * j + 1]);
+            if constexpr (C::KIND != Kind::BF16) {
+              x0 = x0 * sa;
+              x0 = x0 * sb;
+              x1 = x1 * sa;
+              x1 = x1 * sb;
+            }
+            pk[16 * l + j] = pack_bf16x2(x0, x1);
           }
-          pk[j] = pack_bf16x2(x0, x1);
-          pk[16 + j] = pack_bf16x2(y0, y1);
         }
         if (p.c_via_tma) {
           const uint32_t buf = stage0 + static_cast<uint32_t>(chunk_ctr & 1) * C::EPI_BUF;
           if (lane == 0) bulk_wait_group_read<1>();  // the store that last used `buf` has read it
           __syncwarp();
-          const uint32_t row_addr = buf + static_cast<uint32_t>(lane) * 128u;
+          const uint32_t row_off = static_cast<uint32_t>(lane) * RB;
 #pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            const uint32_t off = swizzle_offset(static_cast<uint32_t>(lane) * 128u + ch * 16u, C::SWZ) -
-                                 static_cast<uint32_t>(lane) * 128u;
-            st_shared_v4(row_addr + off, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+          for (int ch = 0; ch < RB / 16; ++ch) {
+            const uint32_t off = swizzle_offset(row_off + ch * 16u, C::EPI_SWZ);
+            st_shared_v4(buf + off, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -399,7 +410,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
           if (row < p.M) {
             uint16_t* out = static_cast<uint16_t*>(p.c_ptr) + static_cast<size_t>(row) * p.N;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
+            for (int j = 0; j < NPK; ++j) {
               const int col = col0 + c * C::EPI_COLS + 2 * j;
               const uint32_t v = pk[j];
               if (col < p.N) out[col] = static_cast<uint16_t>(v & 0xFFFFu);
@@ -432,6 +443,7 @@ struct KernelVariant {
   int kind;
   int cg;
   int bn;
+  int epi_cols;  // columns of one epilogue TMA store box (64: 128-byte swizzle, 32: 64-byte swizzle)
   int stages;
   int epi_warps;
   int threads;
@@ -442,8 +454,9 @@ struct KernelVariant {
 
 template <class C>
 KernelVariant make_variant(const char* name) {
-  return KernelVariant{static_cast<int>(C::KIND), C::CG, C::BN, C::STAGES, C::EPI_WARPS, C::THREADS, C::SMEM_BYTES,
-                       name, reinterpret_cast<const void*>(&tkg_gemm_kernel<C>)};
+  return KernelVariant{static_cast<int>(C::KIND), C::CG,        C::BN,          C::EPI_COLS, C::STAGES,
+                       C::EPI_WARPS,                 C::THREADS, C::SMEM_BYTES, name,
+                       reinterpret_cast<const void*>(&tkg_gemm_kernel<C>)};
 }
 
 }  // namespace tkg

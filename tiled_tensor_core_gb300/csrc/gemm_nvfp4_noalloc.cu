@@ -155,7 +155,8 @@ extern "C" tkg_status tkg_gemm_nvfp4_noalloc(int64_t M, int64_t N, int64_t K, co
                 false);
   p.c_via_tma = (N % 8 == 0) ? 1 : 0;
   if (st == TKG_OK && p.c_via_tma)
-    st = encode(&p.tmap_c, C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, N * 2, 64, 32, true);
+    st = encode(&p.tmap_c, C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, N * 2, static_cast<uint32_t>(v->epi_cols), 32,
+                v->epi_cols == 64);
   if (st != TKG_OK) return st;
   p.c_ptr = C;
   p.a_scale = scales->a_scale;

@@ -11,7 +11,8 @@ enum VariantId : int {
   kVariant1Sm128x256 = 1,  // cta_group::1, 128 x 256 tile per CTA
   kVariant2Sm256x256 = 2,  // cta_group::2, 256 x 256 tile per CTA pair
   kVariant2Sm256x128 = 3,  // cta_group::2, 256 x 128 tile per CTA pair
-  kNumVariants = 4
+  kVariant2Sm256x224 = 4,  // cta_group::2, 256 x 224 tile per CTA pair (bf16 / FP8)
+  kNumVariants = 5
 };
 
 // Each returns the variant for `id`, or nullptr if that kind has no such variant.
