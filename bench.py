@@ -229,6 +229,7 @@ def run_tkg(args, world, rank, local):
         tkg.tkg_set_option(tkg.TKG_OPT_VARIANT, args.variant)
     if args.group_m:
         tkg.tkg_set_option(tkg.TKG_OPT_GROUP_M, args.group_m)
+
     w = synth.WORKLOADS[args.workload]
     ops = synth.workload_operands(args.workload)
     base = DeviceGemm(ops, dev)
@@ -266,6 +267,19 @@ def run_tkg(args, world, rank, local):
     if st != tkg.TKG_OK:
         raise RuntimeError(f"warm-up failed: {tkg.status_string(st)}")
 
+    # Launch-bound workloads replay the step from a CUDA graph (captured after the
+    # warm-up, so every lazy set-up is done); the GEMM launches are unchanged.
+    use_graph = args.graph == "on" or (args.graph == "auto" and w.flops < 1e9 and w.kind != "nvfp4")
+    graph = None
+    if use_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                graph.replay()
+        torch.cuda.synchronize(dev)
+
     # correctness spot check of the last warm-up output against the oracle (cheap: a few rows)
     spot = None
     if rank == 0 and not args.no_check:
@@ -291,11 +305,18 @@ def run_tkg(args, world, rank, local):
         s0 = torch.cuda.Event(enable_timing=True)
         s1 = torch.cuda.Event(enable_timing=True)
         s0.record(stream)
-        step(ev)
+        if graph is not None:
+            with torch.cuda.stream(stream):
+                graph.replay()
+        else:
+            step(ev)
         s1.record(stream)
         s1.synchronize()
         step_ms.append(s0.elapsed_time(s1))
-        kern_ms.extend(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(batch))
+        if graph is not None:  # no per-launch events inside a graph: spread the step over its launches
+            kern_ms.extend([step_ms[-1] / batch] * batch)
+        else:
+            kern_ms.extend(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(batch))
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
@@ -337,7 +358,8 @@ def run_tkg(args, world, rank, local):
                    "global_batch": batch * world, "parallelism": f"replicas{world}",
                    "l2": (f"{n_sets} rotating operand sets, {n_sets * footprint / 2**20:.0f} MiB > 129 MiB L2"
                           if n_sets > 1 else f"operands {footprint / 2**20:.0f} MiB > 129 MiB L2"),
-                   "kernel": info, "group_m": tkg.tkg_get_option(tkg.TKG_OPT_GROUP_M)},
+                   "kernel": info, "group_m": tkg.tkg_get_option(tkg.TKG_OPT_GROUP_M),
+                   "cuda_graph": graph is not None},
         "pct_of_peak": 100.0 * value / world / peak,
         "pct_of_burst_peak": 100.0 * value / world / peak_burst,
         "median_gemm_ms": statistics.median(kern_ms),
@@ -358,41 +380,63 @@ def run_tkg(args, world, rank, local):
 
 
 def run_e2e(ops, dev, w, args):
+    """End to end through the public API with host buffers: every step copies
+    its inputs from pinned host memory to the device, runs the GEMM and copies
+    C back to pinned host memory.  Steps are pipelined over two device buffer
+    sets and three streams (H2D of step i+1 and D2H of step i-1 overlap the
+    GEMM of step i); the timed region spans all copies of all steps."""
     import torch
     from tiled_tensor_core_gb300.device import DeviceGemm
 
-    g = DeviceGemm(ops, dev)
-    host = {}
-    for name in ("a", "b", "sfa", "sfb", "scale_a", "scale_b"):
-        t = getattr(g, name)
-        if t is not None:
-            host[name] = t.cpu().pin_memory()
-    c_host = torch.empty(g.c.shape, dtype=g.c.dtype).pin_memory()
-    stream = torch.cuda.Stream(device=dev)
+    sets = [DeviceGemm(ops, dev), DeviceGemm(ops, dev)]
+    names = [n for n in ("a", "b", "sfa", "sfb", "scale_a", "scale_b") if getattr(sets[0], n) is not None]
+    host = {n: getattr(sets[0], n).cpu().pin_memory() for n in names}
+    c_host = [torch.empty(sets[0].c.shape, dtype=sets[0].c.dtype).pin_memory() for _ in range(2)]
+    h2d_s, gemm_s, d2h_s = (torch.cuda.Stream(device=dev) for _ in range(3))
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = c_host.numel() * c_host.element_size()
+    d2h = c_host[0].numel() * c_host[0].element_size()
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    inputs_free = [ev(), ev()]   # GEMM of the set finished reading its inputs
+    inputs_ready = [ev(), ev()]
+    out_free = [ev(), ev()]      # D2H of the set finished reading C
+    out_ready = [ev(), ev()]
+    for e in inputs_free + out_free:
+        e.record(gemm_s)
 
-    def one():
-        for name, t in host.items():
-            getattr(g, name).copy_(t, non_blocking=True)
-        g.run(stream=int(stream.cuda_stream))
-        c_host.copy_(g.c, non_blocking=True)
+    def one(i):
+        k = i % 2
+        g = sets[k]
+        h2d_s.wait_event(inputs_free[k])
+        with torch.cuda.stream(h2d_s):
+            for n in names:
+                getattr(g, n).copy_(host[n], non_blocking=True)
+        inputs_ready[k].record(h2d_s)
+        gemm_s.wait_event(inputs_ready[k])
+        gemm_s.wait_event(out_free[k])
+        g.run(stream=int(gemm_s.cuda_stream))
+        inputs_free[k].record(gemm_s)
+        out_ready[k].record(gemm_s)
+        d2h_s.wait_event(out_ready[k])
+        with torch.cuda.stream(d2h_s):
+            c_host[k].copy_(g.c, non_blocking=True)
+        out_free[k].record(d2h_s)
 
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            one()
-        stream.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        n = args.e2e_steps
-        e0.record(stream)
-        for _ in range(n):
-            one()
-        e1.record(stream)
-        e1.synchronize()
-    ms = e0.elapsed_time(e1) / n
+    for i in range(4):
+        one(i)
+    torch.cuda.synchronize(dev)
+    n = args.e2e_steps
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(h2d_s)
+    for i in range(n):
+        one(i)
+    d2h_s.wait_stream(h2d_s)
+    d2h_s.wait_stream(gemm_s)
+    t1.record(d2h_s)
+    t1.synchronize()
+    ms = t0.elapsed_time(t1) / n
     return {"value": w.flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "ms_per_step": ms}
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": ms, "pipelined": "2 buffer sets, 3 streams"}
 
 
 def main(argv=None):
@@ -411,6 +455,8 @@ def main(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-check", action="store_true")
+    p.add_argument("--graph", choices=["auto", "on", "off"], default="auto",
+                   help="replay each step from a CUDA graph (auto: launch-bound workloads)")
     args = p.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.impl == "reference":
