@@ -146,7 +146,11 @@ TKG_API void tkg_shutdown(void);
  *  TKG_OPT_VARIANT     force a kernel variant: 0 = pick by shape, 1 = 1-SM
  *                      128x256 tiles, 2 = 2-SM (CTA pair) 256x256 tiles,
  *                      3 = 2-SM 256x128 tiles, 4 = 2-SM 256x224 tiles
- *                      (bf16 and FP8 only)
+ *                      (bf16 and FP8 only), 5 = 2-SM 256x256 tiles whose
+ *                      block scales are written to tensor memory by four
+ *                      scale warps instead of tensor-pipe copies (NVFP4
+ *                      only).  A variant the kind lacks falls back to the
+ *                      shape's pick.
  *  TKG_OPT_MAX_CTAS    cap the persistent grid size (0 = all SMs)            */
 typedef enum tkg_option {
     TKG_OPT_TIMEOUT_NS = 1,

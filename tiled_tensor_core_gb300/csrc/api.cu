@@ -302,11 +302,13 @@ tkg_status gemm_launch(int kind, int64_t M, int64_t N, int64_t K, const void* A,
     }
     if (nvfp4_interleave_scales(scales->a_block_scale, scales->b_block_scale, static_cast<int>(M),
                                 static_cast<int>(N), static_cast<int>(K), p.sf_blocks_a, p.sf_blocks_b, p.num_kb,
-                                scratch, b_off, cs) != cudaSuccess) {
+                                v->sf_mode, scratch, b_off, cs) != cudaSuccess) {
       cudaGetLastError();
       cudaFreeAsync(scratch, cs);
       return TKG_ERR_CUDA;
     }
+    p.sf_a = scratch;
+    p.sf_b = scratch + b_off;
     st = get_map(&p.tmap_sfa, scratch, CU_TENSOR_MAP_DATA_TYPE_UINT8, 128,
                  static_cast<uint64_t>(p.sf_blocks_a) * p.num_kb * 16, 128, 128, 16, 0);
     if (st == TKG_OK)

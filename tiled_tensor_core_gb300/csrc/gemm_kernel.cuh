@@ -55,11 +55,25 @@ struct GemmParams {
   int group_m;
   int c_via_tma;
   int fault_mode;  // 0 = none; 1 = the producer skips the loads of its first stage (timeout test)
-  int sf_blocks_a;  // NVFP4: 128-row scale blocks per stage-k in the interleaved A scales
+  int sf_blocks_a;  // NVFP4: 128-row scale blocks per K stage in the staged A scales
   int sf_blocks_b;  // same for B
+  const uint8_t* sf_a;  // NVFP4 scale-warp mode: staged A scales in global memory
+  const uint8_t* sf_b;  // same for B
 };
 
-template <Kind KIND_, int CG_, int BN_, int STAGES_, int EPI_WARPS_, int NUM_ACC_ = 2>
+// Block-scale staging modes (NVFP4).
+//   kSfCopy: the scales ride the shared-memory ring with the operands and the
+//            MMA thread copies them shared -> TMEM with tcgen05.cp.32x128b.warpx4
+//            (12 copies per 256-K stage of a 256x256 tile).
+//   kSfWarps: scale warps (SF_GROUPS groups of four, one warp per TMEM lane
+//            quarter; group g takes every SF_GROUPS-th stage) read them from
+//            global memory ahead of use and write them with tcgen05.st into a
+//            ring of TMEM slots of their own; the tensor pipe only runs MMAs and
+//            the shared-memory ring only carries operands.
+constexpr int kSfCopy = 0, kSfWarps = 1;
+
+template <Kind KIND_, int CG_, int BN_, int STAGES_, int EPI_WARPS_, int NUM_ACC_ = 2, int SF_MODE_ = kSfCopy,
+          int SF_GROUPS_ = 1>
 struct GemmCfg {
   static constexpr Kind KIND = KIND_;
   static constexpr int CG = CG_;                // CTAs per MMA (1, or 2 for the CTA pair)
@@ -69,6 +83,8 @@ struct GemmCfg {
   static constexpr int EPI_WARPS = EPI_WARPS_;  // 4 or 8
   static constexpr int NUM_ACC = NUM_ACC_;      // fp32 accumulators in TMEM (2 = epilogue overlaps next tile)
   static constexpr bool SCALED = (KIND == Kind::NVFP4);
+  static constexpr int SF_MODE = SF_MODE_;
+  static constexpr bool SF_WARPS_MODE = SCALED && SF_MODE == kSfWarps;
   static constexpr int ROW_BYTES = 128;         // K bytes per operand row per stage
   static constexpr uint32_t SWZ = select_swizzle(ROW_BYTES);
   static_assert(SWZ == 128, "operand rows must take the 128-byte swizzle");
@@ -79,13 +95,17 @@ struct GemmCfg {
   static constexpr int A_STAGE = BM * ROW_BYTES;
   static constexpr int B_BOX = B_ROWS * ROW_BYTES;             // bytes of one B tile load
   static constexpr int B_STAGE = (B_BOX + 1023) / 1024 * 1024;  // keeps every stage 1024-byte aligned
-  // NVFP4 block scales, per stage: 4 interleaved 512-byte atoms (one per MMA)
-  // for each 128 rows.  Each CTA stages its own 128 rows of A's scales and the
-  // scales of all BN rows of B (every CTA of a pair multiplies by all of B).
+  // NVFP4 block scales, copy mode, per stage: 4 interleaved 512-byte atoms
+  // (one per MMA) for each 128 rows.  Each CTA stages its own 128 rows of A's
+  // scales and the scales of all BN rows of B (every CTA of a pair multiplies
+  // by all of B).  Scale-warp mode keeps no scales in shared memory.
+  static constexpr bool SF_IN_SMEM = SCALED && !SF_WARPS_MODE;
   static constexpr int SF_ATOM = 512;
-  static constexpr int SFA_STAGE = SCALED ? KSTEPS * SF_ATOM : 0;
+  static constexpr int SFA_STAGE = SF_IN_SMEM ? KSTEPS * SF_ATOM : 0;
   static constexpr int SFB_BLOCKS = BN / 128;   // 128-row blocks of B scales per tile
-  static constexpr int SFB_STAGE = SCALED ? SFB_BLOCKS * KSTEPS * SF_ATOM : 0;
+  static constexpr int SFB_STAGE = SF_IN_SMEM ? SFB_BLOCKS * KSTEPS * SF_ATOM : 0;
+  static constexpr int SF_GROUPS = SF_WARPS_MODE ? SF_GROUPS_ : 0;
+  static constexpr int SF_WARPS = 4 * SF_GROUPS;
   static constexpr int STAGE_TX = A_STAGE + B_BOX + SFA_STAGE + SFB_STAGE;  // bytes landing per CTA per stage
   static constexpr int ACC_STRIDE = BN <= 128 ? 128 : 256;  // accumulators start on aligned columns
   static constexpr int ACC_COLS = NUM_ACC * ACC_STRIDE;
@@ -94,7 +114,12 @@ struct GemmCfg {
   static constexpr int SF_COLS_A = 4 * KSTEPS;
   static constexpr int SF_COLS_B = (BN / 32) * KSTEPS;
   static constexpr int SF_COLS_STAGE = SCALED ? SF_COLS_A + SF_COLS_B : 0;
-  static constexpr int TMEM_USED = ACC_COLS + STAGES * SF_COLS_STAGE;
+  // TMEM scale slots: one per ring stage in copy mode; in scale-warp mode a ring
+  // of their own, as many as fit beside the accumulators (at most STAGES)
+  static constexpr int SF_SLOTS = !SF_WARPS_MODE ? STAGES
+                                : ((512 - ACC_COLS) / SF_COLS_STAGE < STAGES ? (512 - ACC_COLS) / SF_COLS_STAGE
+                                                                             : STAGES);
+  static constexpr int TMEM_USED = ACC_COLS + (SCALED ? SF_SLOTS * SF_COLS_STAGE : 0);
   static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128
                                  : TMEM_USED <= 256 ? 256 : 512;
   // output columns per epilogue chunk: 64 (rows of 128 B of bf16) when BN allows, else 32 (64 B)
@@ -102,7 +127,7 @@ struct GemmCfg {
   static constexpr int EPI_ROW_BYTES = EPI_COLS * 2;
   static constexpr uint32_t EPI_SWZ = select_swizzle(EPI_ROW_BYTES);
   static constexpr int EPI_BUF = 32 * EPI_ROW_BYTES;  // one warp's 32-row staging tile
-  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  static constexpr int THREADS = 64 + 32 * (EPI_WARPS + SF_WARPS);
   static constexpr uint32_t IDESC = (KIND == Kind::BF16)   ? idesc_dense(kFmtBF16, BM * CG, BN)
                                     : (KIND == Kind::FP8) ? idesc_dense(kFmtE4M3, BM * CG, BN)
                                                           : idesc_mxf4nvf4(BM * CG, BN);
@@ -113,7 +138,7 @@ struct GemmCfg {
   static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
   static constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_STAGE;
   static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * 2 * EPI_BUF;
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1;
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1 + (SF_WARPS_MODE ? 2 * SF_SLOTS : 0);
   static constexpr int OFF_MISC = OFF_BAR + 8 * NUM_BARS;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
 
@@ -126,6 +151,10 @@ struct GemmCfg {
   static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "epilogue is one or two warpgroups");
   static_assert(NUM_ACC == 1 || NUM_ACC == 2, "one or two accumulators");
   static_assert(TMEM_USED <= 512, "tensor memory has 512 columns");
+  static_assert(!SF_WARPS_MODE || (ACC_COLS % 16 == 0 && SF_COLS_STAGE % 16 == 0 && SF_COLS_A == 16),
+                "scale columns are written 16 at a time at 16-column-aligned addresses");
+  static_assert(!SF_WARPS_MODE || SF_SLOTS >= 2, "the scale warps run at least one slot ahead");
+  static_assert(!SF_WARPS_MODE || SF_GROUPS == 1 || SF_GROUPS == 2, "one or two groups of scale warps");
   static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB shared-memory limit");
 };
 
@@ -168,6 +197,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + C::NUM_ACC + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * C::STAGES + 2 * C::NUM_ACC);
+  // scale-warp mode: TMEM scale slot j was written (leader's, one arrival per warp of the scale
+  // group that wrote it, in each CTA of the pair) / was read by its MMAs (every CTA's, one commit)
+  auto sf_ready_bar = [&](int j) { return bar0 + 8u * (2 * C::STAGES + 2 * C::NUM_ACC + 1 + j); };
+  auto sf_empty_bar = [&](int j) { return bar0 + 8u * (2 * C::STAGES + 2 * C::NUM_ACC + 1 + C::SF_SLOTS + j); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* never_abort = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
@@ -191,12 +224,18 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
       mbar_init(tempty_bar(a), C::CG * C::EPI_WARPS);
     }
     mbar_init(drain_bar, 1);
+    if constexpr (C::SF_WARPS_MODE) {
+      for (int j = 0; j < C::SF_SLOTS; ++j) {
+        mbar_init(sf_ready_bar(j), C::CG * 4);  // one group of four scale warps per CTA writes a slot
+        mbar_init(sf_empty_bar(j), 1);
+      }
+    }
     *abort_flag = 0;
     *never_abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&p.tmap_a);
     tma_prefetch_desc(&p.tmap_b);
-    if constexpr (C::SCALED) {
+    if constexpr (C::SF_IN_SMEM) {
       tma_prefetch_desc(&p.tmap_sfa);
       tma_prefetch_desc(&p.tmap_sfb);
     }
@@ -237,9 +276,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
           if (!(first && p.fault_mode == 1)) {
             tma_load_2d<C::CG>(sA + stage * C::A_STAGE, &p.tmap_a, fb, kb * C::K_TMAP, a_row);
             tma_load_2d<C::CG>(sB + stage * C::B_STAGE, &p.tmap_b, fb, kb * C::K_TMAP, b_row);
-            if constexpr (C::SCALED) {
-              // interleaved scale atoms: 16 rows of 128 B per (stage-k, 128-row block), blocks of one
-              // stage-k contiguous
+            if constexpr (C::SF_IN_SMEM) {
+              // interleaved scale atoms: 2 KB (16 rows of 128 B) per (K stage, 128-row block), the
+              // blocks of one K stage contiguous
               const int rb_a = a_row / 128;
               const int rb_b = (tn * C::BN) / 128;
               tma_load_2d<C::CG>(sSFA + stage * C::SFA_STAGE, &p.tmap_sfa, fb, 0, (kb * p.sf_blocks_a + rb_a) * 16);
@@ -264,6 +303,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
     if (lane == 0 && rank == 0) {
       int stage = 0;
       uint32_t phase = 0;
+      int slot = 0;  // scale-warp mode: TMEM scale slot
+      uint32_t slot_phase = 0;
       bool ok = true;
       int it = 0;
       for (int t = cluster_id; t < num_tiles && ok; t += num_clusters, ++it) {
@@ -283,9 +324,17 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
           tc_fence_after();
           const uint32_t a0 = sA + stage * C::A_STAGE;
           const uint32_t b0 = sB + stage * C::B_STAGE;
-          // this stage's scale columns (reused only after the ring stage itself is released)
-          const uint32_t sf_tmem = tmem_base + static_cast<uint32_t>(C::ACC_COLS + stage * C::SF_COLS_STAGE);
-          if constexpr (C::SCALED) {
+          // this stage's scale columns: copy mode reuses them only after the ring stage itself is
+          // released; scale-warp mode has a slot ring of its own
+          const uint32_t sf_tmem =
+              tmem_base + static_cast<uint32_t>(C::ACC_COLS + (C::SF_WARPS_MODE ? slot : stage) * C::SF_COLS_STAGE);
+          if constexpr (C::SF_WARPS_MODE) {
+            if (!mbar_wait(sf_ready_bar(slot), slot_phase, tmo, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          } else if constexpr (C::SCALED) {
             const uint32_t sfa0 = sSFA + stage * C::SFA_STAGE;
             const uint32_t sfb0 = sSFB + stage * C::SFB_STAGE;
 #pragma unroll
@@ -311,6 +360,13 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
                                   sf_tmem + C::SF_COLS_A + (C::BN / 32) * kk, accum);
           }
           mma_commit<C::CG>(empty_bar(stage), 0x3);
+          if constexpr (C::SF_WARPS_MODE) {
+            mma_commit<C::CG>(sf_empty_bar(slot), 0x3);
+            if (++slot == C::SF_SLOTS) {
+              slot = 0;
+              slot_phase ^= 1u;
+            }
+          }
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -325,7 +381,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
       if (!ok) record_timeout(p.status, kRoleMma, abort_flag);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 2 + C::EPI_WARPS) {
     // ------------------------------------------------------------ STORE / FINISH
     constexpr int SUBS = C::EPI_WARPS / 4;
     const int ew = warp - 2;
@@ -422,6 +478,97 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
     }
     if (lane == 0) bulk_wait_group<0>();
     __syncwarp();
+  } else {
+    // ------------------------------------------------------------ SCALES (scale-warp mode)
+    // One warp per TMEM lane quarter q.  For each (tile, K stage) of the CTA it
+    // reads the staged scales ([K stage][128-row block][row][16 scales] in
+    // global memory, two steps ahead of use) and writes them into the next TMEM
+    // scale slot with tcgen05.st: A's row 32q+lane to lane 32q+lane, column
+    // 4t+q of the slot's A columns (one word = the 4 scales of MMA t); B's rows
+    // 32g+lane (g < BN/32) to lane 32q+lane, column (BN/32)t+g of the slot's B
+    // columns, in every quarter (each quarter's rows read all of B's scales).
+    if constexpr (C::SF_WARPS_MODE) {
+      constexpr int G = C::BN / 32;
+      const int quad = warp & 3;
+      const int sgroup = (warp - 2 - C::EPI_WARPS) / 4;  // this warp takes steps sgroup, sgroup + SF_GROUPS, ...
+      const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+      const uint32_t ready_leader0 = (C::CG == 2) ? mapa_shared(sf_ready_bar(0), 0) : sf_ready_bar(0);
+      const int my_tiles = cluster_id < num_tiles ? (num_tiles - 1 - cluster_id) / num_clusters + 1 : 0;
+      const int steps = my_tiles * p.num_kb;
+      const uint4* sfa = reinterpret_cast<const uint4*>(p.sf_a);
+      const uint4* sfb = reinterpret_cast<const uint4*>(p.sf_b);
+      // scales of step s: [0] = this lane's A row, [1 + g] = B row 32g + lane
+      auto fetch = [&](int s_, uint4 (&v)[1 + G]) {
+        const int i = s_ / p.num_kb;
+        const int kb = s_ - i * p.num_kb;
+        int tm, tn;
+        order.coord(cluster_id + i * num_clusters, tm, tn);
+        const size_t ra = (static_cast<size_t>(kb) * p.sf_blocks_a + tm * C::CG + rank) * 128 + quad * 32 + lane;
+        const size_t rb = static_cast<size_t>(kb) * p.sf_blocks_b * 128 + static_cast<size_t>(tn) * C::BN + lane;
+        v[0] = __ldg(sfa + ra);
+#pragma unroll
+        for (int g = 0; g < G; ++g) v[1 + g] = __ldg(sfb + rb + 32 * g);
+      };
+      bool ok = true;
+      // step s into slot s % SF_SLOTS once the MMAs of step s - SF_SLOTS have read it
+      auto put = [&](int s_, const uint4 (&v)[1 + G]) -> bool {
+        const int j = s_ % C::SF_SLOTS;
+        const uint32_t ph = static_cast<uint32_t>(s_ / C::SF_SLOTS) & 1u;
+        if (!__all_sync(0xffffffffu, mbar_wait(sf_empty_bar(j), ph ^ 1u, tmo, abort_flag))) return false;
+        tc_fence_after();
+        const uint32_t cols = lane_base + static_cast<uint32_t>(C::ACC_COLS + j * C::SF_COLS_STAGE);
+        uint32_t ra[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const uint32_t w = (c >> 2) == 0 ? v[0].x : (c >> 2) == 1 ? v[0].y : (c >> 2) == 2 ? v[0].z : v[0].w;
+          ra[c] = ((c & 3) == quad) ? w : 0u;
+        }
+        tmem_st_32x32b_x16(cols, ra);
+        uint32_t rbw[G * C::KSTEPS];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          rbw[0 * G + g] = v[1 + g].x;
+          rbw[1 * G + g] = v[1 + g].y;
+          rbw[2 * G + g] = v[1 + g].z;
+          rbw[3 * G + g] = v[1 + g].w;
+        }
+#pragma unroll
+        for (int h = 0; h < (G * C::KSTEPS) / 16; ++h)
+          tmem_st_32x32b_x16(cols + C::SF_COLS_A + 16u * h, *reinterpret_cast<uint32_t(*)[16]>(rbw + 16 * h));
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(ready_leader0 + 8u * j);
+        return true;
+      };
+      if constexpr (C::SF_GROUPS == 1) {
+        // two register sets, so that the loads of step s + 2 fly while step s waits for its slot
+        uint4 v0[1 + G], v1[1 + G];
+        if (steps > 0) fetch(0, v0);
+        if (steps > 1) fetch(1, v1);
+        for (int s_ = 0; s_ < steps && ok; s_ += 2) {
+          ok = put(s_, v0);
+          if (!ok) break;
+          if (s_ + 2 < steps) fetch(s_ + 2, v0);
+          if (s_ + 1 < steps) {
+            ok = put(s_ + 1, v1);
+            if (!ok) break;
+            if (s_ + 3 < steps) fetch(s_ + 3, v1);
+          }
+        }
+      } else {
+        // one register set: the loads of this group's next step fly while the other group works
+        uint4 v0[1 + G];
+        if (sgroup < steps) fetch(sgroup, v0);
+        for (int s_ = sgroup; s_ < steps && ok; s_ += C::SF_GROUPS) {
+          ok = put(s_, v0);
+          if (!ok) break;
+          if (s_ + C::SF_GROUPS < steps) fetch(s_ + C::SF_GROUPS, v0);
+        }
+      }
+      if (!ok && lane == 0) record_timeout(p.status, kRoleProducer, abort_flag);
+      __syncwarp();
+    }
   }
 
   // ------------------------------------------------------------ teardown
@@ -444,6 +591,7 @@ struct KernelVariant {
   int cg;
   int bn;
   int epi_cols;  // columns of one epilogue TMA store box (64: 128-byte swizzle, 32: 64-byte swizzle)
+  int sf_mode;   // NVFP4 block-scale staging mode (kSfCopy / kSfWarps)
   int stages;
   int epi_warps;
   int threads;
@@ -454,9 +602,9 @@ struct KernelVariant {
 
 template <class C>
 KernelVariant make_variant(const char* name) {
-  return KernelVariant{static_cast<int>(C::KIND), C::CG,        C::BN,          C::EPI_COLS, C::STAGES,
-                       C::EPI_WARPS,                 C::THREADS, C::SMEM_BYTES, name,
-                       reinterpret_cast<const void*>(&tkg_gemm_kernel<C>)};
+  return KernelVariant{static_cast<int>(C::KIND), C::CG,         C::BN,         C::EPI_COLS,
+                       C::SF_MODE,                   C::STAGES,     C::EPI_WARPS,  C::THREADS,
+                       C::SMEM_BYTES,                name,          reinterpret_cast<const void*>(&tkg_gemm_kernel<C>)};
 }
 
 }  // namespace tkg

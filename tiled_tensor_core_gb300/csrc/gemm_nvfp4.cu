@@ -12,6 +12,12 @@
 // scales are rewritten into such atoms by interleave_scales_kernel, ordered
 // [stage-k][128-row block][MMA of the stage][atom], so that every ring stage
 // loads one contiguous 2 KB run per 128 rows with a plain 2-D TMA box.
+//
+// The scale-warp variants take the same 2 KB runs in plain row order,
+// [stage-k][128-row block][row][16 scales]: their scale warps read one row's
+// 16 bytes straight from global memory and write them to the row's own TMEM
+// lane with tcgen05.st, so the shared-memory ring only holds operands (six
+// 32 KB stages instead of five of 38 KB).
 #include <cuda_bf16.h>
 
 #include "gemm_variants.h"
@@ -21,15 +27,18 @@ namespace tkg {
 using Nvfp4_1Sm_256 = GemmCfg<Kind::NVFP4, 1, 256, 3, 4, 1>;
 using Nvfp4_2Sm_256 = GemmCfg<Kind::NVFP4, 2, 256, 5, 4, 1>;
 using Nvfp4_2Sm_128 = GemmCfg<Kind::NVFP4, 2, 128, 6, 4, 2>;
+using Nvfp4_2Sm_256_Sfw = GemmCfg<Kind::NVFP4, 2, 256, 6, 4, 1, kSfWarps, 2>;
 
 const KernelVariant* nvfp4_variant(int id) {
   static const KernelVariant v1 = make_variant<Nvfp4_1Sm_256>("nvfp4_1sm_128x256_s3");
   static const KernelVariant v2 = make_variant<Nvfp4_2Sm_256>("nvfp4_2sm_256x256_s5");
   static const KernelVariant v3 = make_variant<Nvfp4_2Sm_128>("nvfp4_2sm_256x128_s6");
+  static const KernelVariant v5 = make_variant<Nvfp4_2Sm_256_Sfw>("nvfp4_2sm_256x256_s6_sfw8");
   switch (id) {
     case kVariant1Sm128x256: return &v1;
     case kVariant2Sm256x256: return &v2;
     case kVariant2Sm256x128: return &v3;
+    case kVariant2Sm256x256Sfw: return &v5;
     default: return nullptr;
   }
 }
@@ -43,11 +52,13 @@ struct InterleaveArgs {
   int k16;             // scales per row (K / 16)
   int blocks;          // 128-row blocks in dst (rows padded with zero scales)
   int kstages;         // 256-element K stages in dst (padded with zero scales)
+  int row_layout;      // 0: per-MMA atoms; 1: [row][16 scales] runs
 };
 
 // One CTA rewrites one 128-row block for two consecutive K stages (32 source
 // bytes per row, i.e. whole 32-byte sectors).  Scales of rows or K positions
-// past the matrix are written as 0.
+// past the matrix are written as 0.  Either layout keeps each (K stage, block)
+// in its own 2 KB run.
 __global__ void __launch_bounds__(256) interleave_scales_kernel(InterleaveArgs a, InterleaveArgs b, int blocks_a) {
   const bool is_a = static_cast<int>(blockIdx.x) < blocks_a;
   const InterleaveArgs& s = is_a ? a : b;
@@ -71,8 +82,10 @@ __global__ void __launch_bounds__(256) interleave_scales_kernel(InterleaveArgs a
       for (int j = 0; j < 4; ++j)
         if (col + j < s.k16) v |= static_cast<uint32_t>(__ldg(p + col + j)) << (8 * j);
     }
-    const size_t atom = (static_cast<size_t>(kb) * s.blocks + rb) * 4 + t;
-    *reinterpret_cast<uint32_t*>(s.dst + atom * 512 + (r_in & 31) * 16 + (r_in >> 5) * 4) = v;
+    const size_t run = static_cast<size_t>(kb) * s.blocks + rb;
+    const size_t off = s.row_layout ? run * 2048 + r_in * 16 + t * 4
+                                    : (run * 4 + t) * 512 + (r_in & 31) * 16 + (r_in >> 5) * 4;
+    *reinterpret_cast<uint32_t*>(s.dst + off) = v;
   }
 }
 
@@ -81,10 +94,11 @@ __global__ void __launch_bounds__(256) interleave_scales_kernel(InterleaveArgs a
 // Rewrites both operands' scales into `scratch` (see the layout above).
 // Returns the byte offset of B's atoms inside `scratch`.
 cudaError_t nvfp4_interleave_scales(const uint8_t* sfa, const uint8_t* sfb, int M, int N, int K, int blocks_a,
-                                    int blocks_b, int kstages, uint8_t* scratch, size_t b_offset,
+                                    int blocks_b, int kstages, int sf_mode, uint8_t* scratch, size_t b_offset,
                                     cudaStream_t stream) {
-  InterleaveArgs a{sfa, scratch, M, K / 16, blocks_a, kstages};
-  InterleaveArgs b{sfb, scratch + b_offset, N, K / 16, blocks_b, kstages};
+  const int rows = sf_mode == kSfWarps ? 1 : 0;
+  InterleaveArgs a{sfa, scratch, M, K / 16, blocks_a, kstages, rows};
+  InterleaveArgs b{sfb, scratch + b_offset, N, K / 16, blocks_b, kstages, rows};
   const int kpairs = (kstages + 1) / 2;
   const int grid_a = blocks_a * kpairs;
   const int grid_b = blocks_b * kpairs;

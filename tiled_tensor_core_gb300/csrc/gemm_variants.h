@@ -12,7 +12,8 @@ enum VariantId : int {
   kVariant2Sm256x256 = 2,  // cta_group::2, 256 x 256 tile per CTA pair
   kVariant2Sm256x128 = 3,  // cta_group::2, 256 x 128 tile per CTA pair
   kVariant2Sm256x224 = 4,  // cta_group::2, 256 x 224 tile per CTA pair (bf16 / FP8)
-  kNumVariants = 5
+  kVariant2Sm256x256Sfw = 5,  // cta_group::2, 256 x 256, block scales written by scale warps (NVFP4)
+  kNumVariants = 6
 };
 
 // Each returns the variant for `id`, or nullptr if that kind has no such variant.
@@ -21,10 +22,11 @@ const KernelVariant* fp8_variant(int id);
 const KernelVariant* nvfp4_variant(int id);
 
 // NVFP4: rewrite row-major [rows][K/16] block scales of A and B into the
-// interleaved per-MMA atoms the GEMM stages (A's atoms at scratch, B's at
-// scratch + b_offset).  One kernel launch on `stream`.
+// 2 KB per (K stage, 128-row block) runs the GEMM stages (A's at scratch, B's
+// at scratch + b_offset), laid out for the variant's `sf_mode`.  One kernel
+// launch on `stream`.
 cudaError_t nvfp4_interleave_scales(const uint8_t* sfa, const uint8_t* sfb, int M, int N, int K, int blocks_a,
-                                    int blocks_b, int kstages, uint8_t* scratch, size_t b_offset,
+                                    int blocks_b, int kstages, int sf_mode, uint8_t* scratch, size_t b_offset,
                                     cudaStream_t stream);
 size_t nvfp4_scratch_bytes(int blocks_a, int blocks_b, int kstages);
 
