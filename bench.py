@@ -45,8 +45,8 @@ DTYPE = {"bf16": "bf16", "fp8": "e4m3", "nvfp4": "e2m1+e4m3"}
 # DRAM bytes (read + write) per launch of the dominant kernel, from one ncu capture
 # (profiles/), valid only while the kernel sources hash to the value recorded with it.
 TRAFFIC = {
-    "bf16_4096": {"bytes": 97_171_456, "src": "30026a10c7925a73"},        # profiles/gemm_bf16_4096_ncu_full.md
-    "nvfp4_16384": {"bytes": 1_982_171_136, "src": "30026a10c7925a73"},   # profiles/gemm_nvfp4_16384_ncu_full.md
+    "bf16_4096": {"bytes": 97_307_904, "src": "bfb42ea12c47cef7"},        # profiles/gemm_bf16_4096_ncu_full.md
+    "nvfp4_16384": {"bytes": 1_960_812_032, "src": "bfb42ea12c47cef7"},   # profiles/gemm_nvfp4_16384_ncu_full.md
 }
 
 

@@ -143,14 +143,16 @@ TKG_API void tkg_shutdown(void);
  *  TKG_OPT_GROUP_M     super-group height in output tiles for the L2-aware
  *                      tile order (default 8; the paper's {8, N, M/8} order,
  *                      "Block Launch Order and L2 Cache Reuse", Table 3)
- *  TKG_OPT_VARIANT     force a kernel variant: 0 = pick by shape, 1 = 1-SM
- *                      128x256 tiles, 2 = 2-SM (CTA pair) 256x256 tiles,
- *                      3 = 2-SM 256x128 tiles, 4 = 2-SM 256x224 tiles
- *                      (bf16 and FP8 only), 5 = 2-SM 256x256 tiles whose
- *                      block scales are written to tensor memory by four
- *                      scale warps instead of tensor-pipe copies (NVFP4
- *                      only).  A variant the kind lacks falls back to the
- *                      shape's pick.
+ *  TKG_OPT_VARIANT     force a kernel variant: 0 = the default (5 for
+ *                      NVFP4, else 2), 1 = 1-SM 128x256 tiles, 2 = 2-SM
+ *                      (CTA pair) 256x256 tiles, 3 = 2-SM 256x128 tiles,
+ *                      4 = 2-SM 256x224 tiles (bf16 and FP8 only),
+ *                      5 = 2-SM 256x256 tiles whose block scales are
+ *                      written to tensor memory by eight scale warps with
+ *                      tcgen05.st instead of tensor-pipe copies (NVFP4
+ *                      only; NVFP4 variants 1-3 copy them with
+ *                      tcgen05.cp).  A variant the kind lacks falls back
+ *                      to the default.
  *  TKG_OPT_MAX_CTAS    cap the persistent grid size (0 = all SMs)            */
 typedef enum tkg_option {
     TKG_OPT_TIMEOUT_NS = 1,
