@@ -151,8 +151,10 @@ TKG_API void tkg_shutdown(void);
  *                      written to tensor memory by eight scale warps with
  *                      tcgen05.st instead of tensor-pipe copies (NVFP4
  *                      only; NVFP4 variants 1-3 copy them with
- *                      tcgen05.cp).  A variant the kind lacks falls back
- *                      to the default.
+ *                      tcgen05.cp), 6 = 2-SM 256x256 tiles whose A scales
+ *                      are written by four scale warps and B scales copied
+ *                      by a copy warp (NVFP4 only).  A variant the kind
+ *                      lacks falls back to the default.
  *  TKG_OPT_MAX_CTAS    cap the persistent grid size (0 = all SMs)            */
 typedef enum tkg_option {
     TKG_OPT_TIMEOUT_NS = 1,

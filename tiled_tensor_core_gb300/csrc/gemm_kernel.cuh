@@ -70,7 +70,12 @@ struct GemmParams {
 //            global memory ahead of use and write them with tcgen05.st into a
 //            ring of TMEM slots of their own; the tensor pipe only runs MMAs and
 //            the shared-memory ring only carries operands.
-constexpr int kSfCopy = 0, kSfWarps = 1;
+//   kSfHybrid: B's scales ride the operand ring and a copy warp (not the MMA
+//            thread) copies them with tcgen05.cp.32x128b.warpx4, whose
+//            four-quarter broadcast is the replication B's layout needs; four
+//            scale warps write A's scales (one 16-byte row each) with
+//            tcgen05.st.  TMEM scale slots follow the ring stages.
+constexpr int kSfCopy = 0, kSfWarps = 1, kSfHybrid = 2;
 
 template <Kind KIND_, int CG_, int BN_, int STAGES_, int EPI_WARPS_, int NUM_ACC_ = 2, int SF_MODE_ = kSfCopy,
           int SF_GROUPS_ = 1>
@@ -85,6 +90,8 @@ struct GemmCfg {
   static constexpr bool SCALED = (KIND == Kind::NVFP4);
   static constexpr int SF_MODE = SF_MODE_;
   static constexpr bool SF_WARPS_MODE = SCALED && SF_MODE == kSfWarps;
+  static constexpr bool SF_HYBRID = SCALED && SF_MODE == kSfHybrid;
+  static constexpr bool SF_ST = SF_WARPS_MODE || SF_HYBRID;  // scale warps write scales with tcgen05.st
   static constexpr int ROW_BYTES = 128;         // K bytes per operand row per stage
   static constexpr uint32_t SWZ = select_swizzle(ROW_BYTES);
   static_assert(SWZ == 128, "operand rows must take the 128-byte swizzle");
@@ -99,13 +106,15 @@ struct GemmCfg {
   // (one per MMA) for each 128 rows.  Each CTA stages its own 128 rows of A's
   // scales and the scales of all BN rows of B (every CTA of a pair multiplies
   // by all of B).  Scale-warp mode keeps no scales in shared memory.
-  static constexpr bool SF_IN_SMEM = SCALED && !SF_WARPS_MODE;
+  static constexpr bool SFA_IN_SMEM = SCALED && SF_MODE == kSfCopy;
+  static constexpr bool SFB_IN_SMEM = SCALED && SF_MODE != kSfWarps;
   static constexpr int SF_ATOM = 512;
-  static constexpr int SFA_STAGE = SF_IN_SMEM ? KSTEPS * SF_ATOM : 0;
+  static constexpr int SFA_STAGE = SFA_IN_SMEM ? KSTEPS * SF_ATOM : 0;
   static constexpr int SFB_BLOCKS = BN / 128;   // 128-row blocks of B scales per tile
-  static constexpr int SFB_STAGE = SF_IN_SMEM ? SFB_BLOCKS * KSTEPS * SF_ATOM : 0;
-  static constexpr int SF_GROUPS = SF_WARPS_MODE ? SF_GROUPS_ : 0;
+  static constexpr int SFB_STAGE = SFB_IN_SMEM ? SFB_BLOCKS * KSTEPS * SF_ATOM : 0;
+  static constexpr int SF_GROUPS = SF_ST ? SF_GROUPS_ : 0;
   static constexpr int SF_WARPS = 4 * SF_GROUPS;
+  static constexpr int CP_WARPS = SF_HYBRID ? 1 : 0;
   static constexpr int STAGE_TX = A_STAGE + B_BOX + SFA_STAGE + SFB_STAGE;  // bytes landing per CTA per stage
   static constexpr int ACC_STRIDE = BN <= 128 ? 128 : 256;  // accumulators start on aligned columns
   static constexpr int ACC_COLS = NUM_ACC * ACC_STRIDE;
@@ -127,7 +136,7 @@ struct GemmCfg {
   static constexpr int EPI_ROW_BYTES = EPI_COLS * 2;
   static constexpr uint32_t EPI_SWZ = select_swizzle(EPI_ROW_BYTES);
   static constexpr int EPI_BUF = 32 * EPI_ROW_BYTES;  // one warp's 32-row staging tile
-  static constexpr int THREADS = 64 + 32 * (EPI_WARPS + SF_WARPS);
+  static constexpr int THREADS = 64 + 32 * (EPI_WARPS + SF_WARPS + CP_WARPS);
   static constexpr uint32_t IDESC = (KIND == Kind::BF16)   ? idesc_dense(kFmtBF16, BM * CG, BN)
                                     : (KIND == Kind::FP8) ? idesc_dense(kFmtE4M3, BM * CG, BN)
                                                           : idesc_mxf4nvf4(BM * CG, BN);
@@ -138,7 +147,8 @@ struct GemmCfg {
   static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
   static constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_STAGE;
   static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * 2 * EPI_BUF;
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1 + (SF_WARPS_MODE ? 2 * SF_SLOTS : 0);
+  static constexpr int NUM_BARS =
+      2 * STAGES + 2 * NUM_ACC + 1 + (SF_WARPS_MODE ? 2 * SF_SLOTS : SF_HYBRID ? SF_SLOTS : 0);
   static constexpr int OFF_MISC = OFF_BAR + 8 * NUM_BARS;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
 
@@ -151,10 +161,11 @@ struct GemmCfg {
   static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "epilogue is one or two warpgroups");
   static_assert(NUM_ACC == 1 || NUM_ACC == 2, "one or two accumulators");
   static_assert(TMEM_USED <= 512, "tensor memory has 512 columns");
-  static_assert(!SF_WARPS_MODE || (ACC_COLS % 16 == 0 && SF_COLS_STAGE % 16 == 0 && SF_COLS_A == 16),
+  static_assert(!SF_ST || (ACC_COLS % 16 == 0 && SF_COLS_STAGE % 16 == 0 && SF_COLS_A == 16),
                 "scale columns are written 16 at a time at 16-column-aligned addresses");
-  static_assert(!SF_WARPS_MODE || SF_SLOTS >= 2, "the scale warps run at least one slot ahead");
-  static_assert(!SF_WARPS_MODE || SF_GROUPS == 1 || SF_GROUPS == 2, "one or two groups of scale warps");
+  static_assert(!SF_ST || SF_SLOTS >= 2, "the scale warps run at least one slot ahead");
+  static_assert(!SF_ST || SF_GROUPS == 1 || SF_GROUPS == 2, "one or two groups of scale warps");
+  static_assert(!SF_HYBRID || SF_GROUPS == 1, "the hybrid mode's A scales need one group");
   static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB shared-memory limit");
 };
 
@@ -197,8 +208,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + C::NUM_ACC + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * C::STAGES + 2 * C::NUM_ACC);
-  // scale-warp mode: TMEM scale slot j was written (leader's, one arrival per warp of the scale
-  // group that wrote it, in each CTA of the pair) / was read by its MMAs (every CTA's, one commit)
+  // scale-warp and hybrid modes: TMEM scale slot j was written (leader's; one arrival per warp of
+  // the scale group that wrote it in each CTA of the pair, plus, hybrid, the copy warp's commit) /
+  // scale-warp mode: was read by its MMAs (every CTA's, one commit; the hybrid mode's slots follow
+  // the ring stages, so the stage's empty barrier says it)
   auto sf_ready_bar = [&](int j) { return bar0 + 8u * (2 * C::STAGES + 2 * C::NUM_ACC + 1 + j); };
   auto sf_empty_bar = [&](int j) { return bar0 + 8u * (2 * C::STAGES + 2 * C::NUM_ACC + 1 + C::SF_SLOTS + j); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
@@ -229,16 +242,16 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
         mbar_init(sf_ready_bar(j), C::CG * 4);  // one group of four scale warps per CTA writes a slot
         mbar_init(sf_empty_bar(j), 1);
       }
+    } else if constexpr (C::SF_HYBRID) {
+      for (int j = 0; j < C::SF_SLOTS; ++j) mbar_init(sf_ready_bar(j), C::CG * 4 + 1);
     }
     *abort_flag = 0;
     *never_abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&p.tmap_a);
     tma_prefetch_desc(&p.tmap_b);
-    if constexpr (C::SF_IN_SMEM) {
-      tma_prefetch_desc(&p.tmap_sfa);
-      tma_prefetch_desc(&p.tmap_sfb);
-    }
+    if constexpr (C::SFA_IN_SMEM) tma_prefetch_desc(&p.tmap_sfa);
+    if constexpr (C::SFB_IN_SMEM) tma_prefetch_desc(&p.tmap_sfb);
     if (p.c_via_tma) tma_prefetch_desc(&p.tmap_c);
   }
   if (warp == 1) {
@@ -276,14 +289,13 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
           if (!(first && p.fault_mode == 1)) {
             tma_load_2d<C::CG>(sA + stage * C::A_STAGE, &p.tmap_a, fb, kb * C::K_TMAP, a_row);
             tma_load_2d<C::CG>(sB + stage * C::B_STAGE, &p.tmap_b, fb, kb * C::K_TMAP, b_row);
-            if constexpr (C::SF_IN_SMEM) {
-              // interleaved scale atoms: 2 KB (16 rows of 128 B) per (K stage, 128-row block), the
-              // blocks of one K stage contiguous
-              const int rb_a = a_row / 128;
-              const int rb_b = (tn * C::BN) / 128;
-              tma_load_2d<C::CG>(sSFA + stage * C::SFA_STAGE, &p.tmap_sfa, fb, 0, (kb * p.sf_blocks_a + rb_a) * 16);
-              tma_load_2d<C::CG>(sSFB + stage * C::SFB_STAGE, &p.tmap_sfb, fb, 0, (kb * p.sf_blocks_b + rb_b) * 16);
-            }
+            // interleaved scale atoms: 2 KB (16 rows of 128 B) per (K stage, 128-row block), the
+            // blocks of one K stage contiguous
+            if constexpr (C::SFA_IN_SMEM)
+              tma_load_2d<C::CG>(sSFA + stage * C::SFA_STAGE, &p.tmap_sfa, fb, 0, (kb * p.sf_blocks_a + a_row / 128) * 16);
+            if constexpr (C::SFB_IN_SMEM)
+              tma_load_2d<C::CG>(sSFB + stage * C::SFB_STAGE, &p.tmap_sfb, fb, 0,
+                                 (kb * p.sf_blocks_b + (tn * C::BN) / 128) * 16);
           }
           first = false;
           if (++stage == C::STAGES) {
@@ -328,8 +340,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
           // released; scale-warp mode has a slot ring of its own
           const uint32_t sf_tmem =
               tmem_base + static_cast<uint32_t>(C::ACC_COLS + (C::SF_WARPS_MODE ? slot : stage) * C::SF_COLS_STAGE);
-          if constexpr (C::SF_WARPS_MODE) {
-            if (!mbar_wait(sf_ready_bar(slot), slot_phase, tmo, abort_flag)) {
+          if constexpr (C::SF_ST) {
+            const bool ready = C::SF_WARPS_MODE ? mbar_wait(sf_ready_bar(slot), slot_phase, tmo, abort_flag)
+                                                : mbar_wait(sf_ready_bar(stage), phase, tmo, abort_flag);
+            if (!ready) {
               ok = false;
               break;
             }
@@ -478,17 +492,18 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
     }
     if (lane == 0) bulk_wait_group<0>();
     __syncwarp();
-  } else {
-    // ------------------------------------------------------------ SCALES (scale-warp mode)
+  } else if (warp < 2 + C::EPI_WARPS + C::SF_WARPS) {
+    // ------------------------------------------------------------ SCALES (scale-warp and hybrid modes)
     // One warp per TMEM lane quarter q.  For each (tile, K stage) of the CTA it
     // reads the staged scales ([K stage][128-row block][row][16 scales] in
-    // global memory, two steps ahead of use) and writes them into the next TMEM
-    // scale slot with tcgen05.st: A's row 32q+lane to lane 32q+lane, column
-    // 4t+q of the slot's A columns (one word = the 4 scales of MMA t); B's rows
-    // 32g+lane (g < BN/32) to lane 32q+lane, column (BN/32)t+g of the slot's B
-    // columns, in every quarter (each quarter's rows read all of B's scales).
-    if constexpr (C::SF_WARPS_MODE) {
-      constexpr int G = C::BN / 32;
+    // global memory, ahead of use) and writes them into the step's TMEM scale
+    // slot with tcgen05.st: A's row 32q+lane to lane 32q+lane, column 4t+q of
+    // the slot's A columns (one word = the 4 scales of MMA t); in scale-warp
+    // mode also B's rows 32g+lane (g < BN/32) to lane 32q+lane, column
+    // (BN/32)t+g of the slot's B columns, in every quarter (each quarter's rows
+    // read all of B's scales).
+    if constexpr (C::SF_ST) {
+      constexpr int G = C::SF_WARPS_MODE ? C::BN / 32 : 0;  // B rows per lane this warp loads and stores
       const int quad = warp & 3;
       const int sgroup = (warp - 2 - C::EPI_WARPS) / 4;  // this warp takes steps sgroup, sgroup + SF_GROUPS, ...
       const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
@@ -497,7 +512,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
       const int steps = my_tiles * p.num_kb;
       const uint4* sfa = reinterpret_cast<const uint4*>(p.sf_a);
       const uint4* sfb = reinterpret_cast<const uint4*>(p.sf_b);
-      // scales of step s: [0] = this lane's A row, [1 + g] = B row 32g + lane
+      // scales of step s: [0] = this lane's A row, [1 + g] = B row 32g + lane (scale-warp mode)
       auto fetch = [&](int s_, uint4 (&v)[1 + G]) {
         const int i = s_ / p.num_kb;
         const int kb = s_ - i * p.num_kb;
@@ -508,13 +523,16 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
         v[0] = __ldg(sfa + ra);
 #pragma unroll
         for (int g = 0; g < G; ++g) v[1 + g] = __ldg(sfb + rb + 32 * g);
+        (void)rb;
+        (void)sfb;
       };
       bool ok = true;
       // step s into slot s % SF_SLOTS once the MMAs of step s - SF_SLOTS have read it
       auto put = [&](int s_, const uint4 (&v)[1 + G]) -> bool {
         const int j = s_ % C::SF_SLOTS;
         const uint32_t ph = static_cast<uint32_t>(s_ / C::SF_SLOTS) & 1u;
-        if (!__all_sync(0xffffffffu, mbar_wait(sf_empty_bar(j), ph ^ 1u, tmo, abort_flag))) return false;
+        const uint32_t freed = C::SF_WARPS_MODE ? sf_empty_bar(j) : empty_bar(j);
+        if (!__all_sync(0xffffffffu, mbar_wait(freed, ph ^ 1u, tmo, abort_flag))) return false;
         tc_fence_after();
         const uint32_t cols = lane_base + static_cast<uint32_t>(C::ACC_COLS + j * C::SF_COLS_STAGE);
         uint32_t ra[16];
@@ -524,17 +542,19 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
           ra[c] = ((c & 3) == quad) ? w : 0u;
         }
         tmem_st_32x32b_x16(cols, ra);
-        uint32_t rbw[G * C::KSTEPS];
+        if constexpr (G > 0) {
+          uint32_t rbw[G * C::KSTEPS];
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          rbw[0 * G + g] = v[1 + g].x;
-          rbw[1 * G + g] = v[1 + g].y;
-          rbw[2 * G + g] = v[1 + g].z;
-          rbw[3 * G + g] = v[1 + g].w;
+          for (int g = 0; g < G; ++g) {
+            rbw[0 * G + g] = v[1 + g].x;
+            rbw[1 * G + g] = v[1 + g].y;
+            rbw[2 * G + g] = v[1 + g].z;
+            rbw[3 * G + g] = v[1 + g].w;
+          }
+#pragma unroll
+          for (int h = 0; h < (G * C::KSTEPS) / 16; ++h)
+            tmem_st_32x32b_x16(cols + C::SF_COLS_A + 16u * h, *reinterpret_cast<uint32_t(*)[16]>(rbw + 16 * h));
         }
-#pragma unroll
-        for (int h = 0; h < (G * C::KSTEPS) / 16; ++h)
-          tmem_st_32x32b_x16(cols + C::SF_COLS_A + 16u * h, *reinterpret_cast<uint32_t(*)[16]>(rbw + 16 * h));
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -567,6 +587,44 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
         }
       }
       if (!ok && lane == 0) record_timeout(p.status, kRoleProducer, abort_flag);
+      __syncwarp();
+    }
+  } else {
+    // ------------------------------------------------------------ B SCALE COPIES (hybrid mode)
+    // One lane of the leader CTA copies each stage's B scale atoms shared -> TMEM (in both CTAs
+    // of a pair) and commits the copies to the stage's sf_ready barrier.  The stage's full barrier
+    // says the atoms landed in both CTAs; it also implies the slot is free, since the producer
+    // refilled the stage only after the MMAs that read the slot had completed.
+    if constexpr (C::SF_HYBRID) {
+      if (lane == 0 && rank == 0) {
+        const int my_tiles = cluster_id < num_tiles ? (num_tiles - 1 - cluster_id) / num_clusters + 1 : 0;
+        const int steps = my_tiles * p.num_kb;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int s_ = 0; s_ < steps; ++s_) {
+          if (!mbar_wait(full_bar(stage), phase, tmo, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sf_tmem = tmem_base + static_cast<uint32_t>(C::ACC_COLS + stage * C::SF_COLS_STAGE);
+          const uint32_t sfb0 = sSFB + stage * C::SFB_STAGE;
+#pragma unroll
+          for (int kk = 0; kk < C::KSTEPS; ++kk) {
+#pragma unroll
+            for (int j = 0; j < C::SFB_BLOCKS; ++j)
+              tmem_cp_32x128b_warpx4<C::CG>(sf_tmem + C::SF_COLS_A + (C::BN / 32) * kk + 4u * j,
+                                            sdesc_plain_rows16(sfb0 + (j * C::KSTEPS + kk) * C::SF_ATOM));
+          }
+          mma_commit<C::CG>(sf_ready_bar(stage), 0x1);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) record_timeout(p.status, kRoleMma, abort_flag);
+      }
       __syncwarp();
     }
   }

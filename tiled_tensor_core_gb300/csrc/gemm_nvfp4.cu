@@ -28,17 +28,20 @@ using Nvfp4_1Sm_256 = GemmCfg<Kind::NVFP4, 1, 256, 3, 4, 1>;
 using Nvfp4_2Sm_256 = GemmCfg<Kind::NVFP4, 2, 256, 5, 4, 1>;
 using Nvfp4_2Sm_128 = GemmCfg<Kind::NVFP4, 2, 128, 6, 4, 2>;
 using Nvfp4_2Sm_256_Sfw = GemmCfg<Kind::NVFP4, 2, 256, 6, 4, 1, kSfWarps, 2>;
+using Nvfp4_2Sm_256_Hyb = GemmCfg<Kind::NVFP4, 2, 256, 5, 4, 1, kSfHybrid, 1>;
 
 const KernelVariant* nvfp4_variant(int id) {
   static const KernelVariant v1 = make_variant<Nvfp4_1Sm_256>("nvfp4_1sm_128x256_s3");
   static const KernelVariant v2 = make_variant<Nvfp4_2Sm_256>("nvfp4_2sm_256x256_s5");
   static const KernelVariant v3 = make_variant<Nvfp4_2Sm_128>("nvfp4_2sm_256x128_s6");
   static const KernelVariant v5 = make_variant<Nvfp4_2Sm_256_Sfw>("nvfp4_2sm_256x256_s6_sfw8");
+  static const KernelVariant v6 = make_variant<Nvfp4_2Sm_256_Hyb>("nvfp4_2sm_256x256_s5_hybrid");
   switch (id) {
     case kVariant1Sm128x256: return &v1;
     case kVariant2Sm256x256: return &v2;
     case kVariant2Sm256x128: return &v3;
     case kVariant2Sm256x256Sfw: return &v5;
+    case kVariant2Sm256x256Hybrid: return &v6;
     default: return nullptr;
   }
 }
@@ -96,9 +99,10 @@ __global__ void __launch_bounds__(256) interleave_scales_kernel(InterleaveArgs a
 cudaError_t nvfp4_interleave_scales(const uint8_t* sfa, const uint8_t* sfb, int M, int N, int K, int blocks_a,
                                     int blocks_b, int kstages, int sf_mode, uint8_t* scratch, size_t b_offset,
                                     cudaStream_t stream) {
-  const int rows = sf_mode == kSfWarps ? 1 : 0;
-  InterleaveArgs a{sfa, scratch, M, K / 16, blocks_a, kstages, rows};
-  InterleaveArgs b{sfb, scratch + b_offset, N, K / 16, blocks_b, kstages, rows};
+  const int rows_a = sf_mode == kSfWarps || sf_mode == kSfHybrid ? 1 : 0;
+  const int rows_b = sf_mode == kSfWarps ? 1 : 0;
+  InterleaveArgs a{sfa, scratch, M, K / 16, blocks_a, kstages, rows_a};
+  InterleaveArgs b{sfb, scratch + b_offset, N, K / 16, blocks_b, kstages, rows_b};
   const int kpairs = (kstages + 1) / 2;
   const int grid_a = blocks_a * kpairs;
   const int grid_b = blocks_b * kpairs;

@@ -13,7 +13,8 @@ enum VariantId : int {
   kVariant2Sm256x128 = 3,  // cta_group::2, 256 x 128 tile per CTA pair
   kVariant2Sm256x224 = 4,  // cta_group::2, 256 x 224 tile per CTA pair (bf16 / FP8)
   kVariant2Sm256x256Sfw = 5,  // cta_group::2, 256 x 256, block scales written by scale warps (NVFP4)
-  kNumVariants = 6
+  kVariant2Sm256x256Hybrid = 6,  // cta_group::2, 256 x 256, A scales by scale warps, B by a copy warp (NVFP4)
+  kNumVariants = 7
 };
 
 // Each returns the variant for `id`, or nullptr if that kind has no such variant.
