@@ -71,6 +71,17 @@ TKG_API tkg_status tkg_debug_mma_probe(int kind, int n, int ksteps, const void* 
                                const uint32_t* sfa_words, const uint32_t* sfb_words, const int32_t* sf_cols,
                                float* d_out, void* stream);
 
+/* Device: tensor-core issue rate.  One thread issues `count` MMAs of one
+ * kind (0 bf16 K=16, 1 e4m3 K=32, 2 nvfp4 block-scaled K=64: 32 bytes of K
+ * per row each) and shape (128*cta_group) x n back to back, cta_group 1 (one
+ * CTA) or 2 (a CTA pair, cta_group::2), operands rotating over shared-memory
+ * stages; *cycles (host) receives the SM cycles from the first issue until
+ * their commit lands.  The difference of two counts divided by the
+ * difference in MMAs is the per-MMA cost.  n in {128, 256}, count in
+ * 1..65536.  Synchronous on `stream`. */
+TKG_API tkg_status tkg_debug_mma_rate(int kind, int cta_group, int n, int count, unsigned long long* cycles,
+                                      void* stream);
+
 #ifdef __cplusplus
 }
 #endif

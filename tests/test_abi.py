@@ -1,6 +1,7 @@
 """C-ABI checks that need no GPU: the library loads, exports every function
 the headers declare, rejects bad arguments before touching CUDA, and its
 host-compiled scheduler / swizzle helpers agree with the definitions."""
+import ctypes
 import os
 import re
 import subprocess
@@ -153,3 +154,10 @@ def test_compiled_variants_fit_the_sm(tkg):
             assert info["smem_bytes"] <= 232448
             assert info["threads"] in (192, 352, 448)
             assert info["cta_group"] in (1, 2)
+
+
+def test_mma_rate_probe_arguments_checked(tkg):
+    c = ctypes.c_ulonglong(0)
+    for args in [(3, 1, 256, 64), (0, 3, 256, 64), (0, 1, 192, 64), (0, 1, 256, 0), (0, 1, 256, 65537)]:
+        assert tkg.lib.tkg_debug_mma_rate(*args, ctypes.byref(c), None) == tkg.TKG_ERR_INVALID_ARG
+    assert tkg.lib.tkg_debug_mma_rate(0, 1, 256, 64, None, None) == tkg.TKG_ERR_INVALID_ARG

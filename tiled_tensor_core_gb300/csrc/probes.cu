@@ -1,8 +1,8 @@
 // probes.cu — diagnostic kernels behind tkg_debug.h: a TMA swizzled load whose
-// raw shared-memory image is copied out, and a one-tile tensor-core MMA with
+// raw shared-memory image is copied out, a one-tile tensor-core MMA with
 // caller-chosen operands and (for the block-scaled kind) caller-chosen
-// tensor-memory contents of the scale regions.  Each checks one building block
-// of the GEMM in isolation.
+// tensor-memory contents of the scale regions, and an MMA issue-rate timer.
+// Each checks or measures one building block of the GEMM in isolation.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -181,6 +181,104 @@ unsigned int* probe_err_word() {
   return w;
 }
 
+// MMA issue rate: one thread issues `count` tcgen05.mma back to back (1-SM:
+// one CTA; 2-SM: a cluster of two, the leader issuing cta_group::2) and the
+// elapsed SM cycles until their commit lands are recorded.  Operands rotate
+// over 4 stages x 4 K steps of 48 KB shared stages (A 16 KB, B up to 32 KB)
+// filled with 0x38 bytes; for the block-scaled kind both scale regions hold
+// e4m3 1.0 (0x38) in every lane.  TMEM: accumulator at columns 0..255, scales
+// at 256 (A) and 272 (B).
+constexpr int kRateStages = 4;
+constexpr int kRateStageBytes = 49152;
+constexpr int kRateSmem = kRateStages * kRateStageBytes + 1024;
+
+__device__ unsigned long long g_rate_cycles;
+
+template <int CG>
+__global__ void __launch_bounds__(128, 1) mma_rate_kernel(int kind, int n, int count, unsigned int* err) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t slot;
+  __shared__ int no_abort;
+  const int warp = threadIdx.x >> 5;
+  const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
+  for (int i = threadIdx.x; i < kRateStages * kRateStageBytes / 4; i += 128)
+    reinterpret_cast<uint32_t*>(smem)[i] = 0x38383838u;
+  if (threadIdx.x == 0) {
+    no_abort = 0;
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  if (warp == 0) {
+    tmem_alloc<CG>(smem_u32(&slot), 512);
+    tmem_relinquish<CG>();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  if constexpr (CG == 2) {
+    cluster_arrive();
+    cluster_wait();
+  }
+  tc_fence_after();
+  const uint32_t tmem = slot;
+  {
+    uint32_t r[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) r[c] = 0x38383838u;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    tmem_st_32x32b_x16(lane_base + 256u, r);
+    tmem_st_32x32b_x16(lane_base + 272u, r);
+    tmem_wait_st();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if constexpr (CG == 2) {
+    cluster_arrive();
+    cluster_wait();
+  }
+  tc_fence_after();
+  if (threadIdx.x == 0 && rank == 0) {
+    const uint32_t s0 = smem_u32(smem);
+    const uint32_t id_f4 = idesc_mxf4nvf4(128 * CG, n);
+    const uint32_t id_bf = idesc_dense(kFmtBF16, 128 * CG, n);
+    const uint32_t id_f8 = idesc_dense(kFmtE4M3, 128 * CG, n);
+    const unsigned long long t0 = clock64();
+    for (int i = 0; i < count; ++i) {
+      const uint32_t base = s0 + static_cast<uint32_t>(((i >> 2) % kRateStages) * kRateStageBytes) + 32u * (i & 3);
+      const uint64_t ad = sdesc_sw128(base);
+      const uint64_t bd = sdesc_sw128(base + 16384u);
+      const uint32_t acc = i > 0 ? 1u : 0u;
+      if (kind == 0)
+        mma_bf16<CG>(tmem, ad, bd, id_bf, acc);
+      else if (kind == 1)
+        mma_f8f6f4<CG>(tmem, ad, bd, id_f8, acc);
+      else
+        mma_mxf4nvf4<CG>(tmem, ad, bd, id_f4, tmem + 256u, tmem + 272u, acc);
+    }
+    if constexpr (CG == 2)
+      mma_commit_pair(smem_u32(&bar), 0x1);
+    else
+      mma_commit_local(smem_u32(&bar));
+    if (mbar_wait(smem_u32(&bar), 0, kProbeTimeoutNs, &no_abort))
+      g_rate_cycles = clock64() - t0;
+    else
+      atomicOr(err, 1u);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if constexpr (CG == 2) {
+    cluster_arrive();
+    cluster_wait();
+  }
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc<CG>(tmem, 512);
+  }
+}
+
 }  // namespace
 
 extern "C" {
@@ -257,6 +355,52 @@ tkg_status tkg_debug_mma_probe(int kind, int n, int ksteps, const void* a_tile, 
     return TKG_ERR_CUDA;
   }
   return err ? TKG_ERR_TIMEOUT : TKG_OK;
+}
+
+tkg_status tkg_debug_mma_rate(int kind, int cta_group, int n, int count, unsigned long long* cycles, void* stream) {
+  if (kind < 0 || kind > 2 || (cta_group != 1 && cta_group != 2) || (n != 128 && n != 256) || count < 1 ||
+      count > 65536 || !cycles)
+    return TKG_ERR_INVALID_ARG;
+  tkg_status st = debug_device_ready();
+  if (st != TKG_OK) return st;
+  unsigned int* err = probe_err_word();
+  if (!err) return TKG_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(err, 0, sizeof(unsigned int), s) != cudaSuccess) return TKG_ERR_CUDA;
+  const void* fn = cta_group == 2 ? reinterpret_cast<const void*>(&mma_rate_kernel<2>)
+                                  : reinterpret_cast<const void*>(&mma_rate_kernel<1>);
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kRateSmem) != cudaSuccess) {
+    cudaGetLastError();
+    return TKG_ERR_CUDA;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(static_cast<unsigned>(cta_group), 1, 1);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = kRateSmem;
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cta_group);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {&kind, &n, &count, &err};
+  if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) {
+    cudaGetLastError();
+    return TKG_ERR_CUDA;
+  }
+  unsigned int e = 0;
+  unsigned long long c = 0;
+  if (cudaMemcpyAsync(&e, err, sizeof(e), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemcpyFromSymbolAsync(&c, g_rate_cycles, sizeof(c), 0, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return TKG_ERR_CUDA;
+  }
+  if (e) return TKG_ERR_TIMEOUT;
+  *cycles = c;
+  return TKG_OK;
 }
 
 }  // extern "C"

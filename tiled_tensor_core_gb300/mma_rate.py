@@ -1,0 +1,42 @@
+"""Print the tensor-core issue rate of each MMA kind this library uses.
+
+    python -m tiled_tensor_core_gb300.mma_rate
+
+For every kind (bf16 K=16, e4m3 K=32, block-scaled e2m1 K=64; 32 bytes of K
+per operand row each), CTA-group form (one CTA, or a CTA pair with
+cta_group::2) and N, one thread issues 128 and then 1024 MMAs back to back
+(tkg_debug_mma_rate); the difference gives the cost of one MMA in SM cycles,
+and from it the dense rate per SM and, at a given clock, per GPU.
+"""
+from __future__ import annotations
+
+import argparse
+
+KINDS = {0: ("bf16", 16), 1: ("e4m3", 32), 2: ("nvfp4", 64)}
+
+
+def main(argv=None) -> None:
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--clock-mhz", type=float, default=2070.0, help="SM clock for the per-GPU figure")
+    args = ap.parse_args(argv)
+    import torch
+
+    from . import tkg
+
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    print(f"{sms} SMs, per-GPU figures at {args.clock_mhz:.0f} MHz")
+    print("| kind | CTA group | MMA (M x N x K) | cycles per MMA | FMA per cycle per SM | TFLOP/s per GPU |")
+    print("|---|---|---|---|---|---|")
+    for kind, (name, k) in KINDS.items():
+        for cg in (1, 2):
+            for n in (256, 128):
+                c0 = tkg.tkg_debug_mma_rate(kind, cg, n, 128)
+                c1 = tkg.tkg_debug_mma_rate(kind, cg, n, 1024)
+                per = (c1 - c0) / (1024 - 128)
+                fma_sm = 128 * n * k / per  # each SM computes 128 rows of the (128*cg) x n tile
+                tflops = 2 * fma_sm * sms * args.clock_mhz * 1e6 / 1e12
+                print(f"| {name} | {cg} | {128 * cg} x {n} x {k} | {per:.1f} | {fma_sm:.0f} | {tflops:.0f} |")
+
+
+if __name__ == "__main__":
+    main()

@@ -81,6 +81,8 @@ lib.tkg_debug_tma_swizzle_probe.argtypes = [_i32, _vp, _vp, _vp]
 lib.tkg_debug_tma_swizzle_probe.restype = _i32
 lib.tkg_debug_mma_probe.argtypes = [_i32, _i32, _i32, _vp, _vp, _vp, _vp, ctypes.POINTER(ctypes.c_int32), _vp, _vp]
 lib.tkg_debug_mma_probe.restype = _i32
+lib.tkg_debug_mma_rate.argtypes = [_i32, _i32, _i32, _i32, ctypes.POINTER(ctypes.c_ulonglong), _vp]
+lib.tkg_debug_mma_rate.restype = _i32
 
 
 def _addr(x) -> int | None:
@@ -205,3 +207,10 @@ def tkg_debug_mma_probe(kind, n, ksteps, a_tile, b_tile, sfa=None, sfb=None, sf_
         cols = (ctypes.c_int32 * len(sf_cols))(*[int(c) for c in sf_cols])
     return lib.tkg_debug_mma_probe(kind, n, ksteps, _addr(a_tile), _addr(b_tile), _addr(sfa), _addr(sfb), cols,
                                    _addr(d_out), _stream(stream))
+
+
+def tkg_debug_mma_rate(kind, cta_group, n, count, stream=None) -> int:
+    """SM cycles for `count` back-to-back MMAs (see tkg_debug.h)."""
+    c = ctypes.c_ulonglong(0)
+    _check(lib.tkg_debug_mma_rate(kind, cta_group, n, count, ctypes.byref(c), _stream(stream)), "tkg_debug_mma_rate")
+    return int(c.value)
