@@ -19,6 +19,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
+_SRCS = [_SRC, os.path.join(_HERE, "quantize.c")]
 _LIB_PATH = os.path.join(_HERE, "_oracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -28,10 +29,11 @@ CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off"
 
 
 def build(force: bool = False) -> str:
-    """Compile oracle.c into _oracle.so (gcc, a second or two)."""
-    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+    """Compile oracle.c and quantize.c into _oracle.so (gcc, a second or two)."""
+    newest = max(os.path.getmtime(p) for p in _SRCS)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < newest:
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.run(["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"], check=True)
+        subprocess.run(["gcc", *CFLAGS, "-o", tmp, *_SRCS, "-lm"], check=True)
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -61,6 +63,14 @@ def _load():
             lib.oracle_gemm_fp8_rows.restype = ctypes.c_int
             lib.oracle_gemm_nvfp4_rows.argtypes = [i64, i64, i64, vp, vp, vp, vp, f32, f32, vp, i64, vp, vp]
             lib.oracle_gemm_nvfp4_rows.restype = ctypes.c_int
+            lib.oracle_e4m3_rne_sat.argtypes = [f32]
+            lib.oracle_e4m3_rne_sat.restype = ctypes.c_uint8
+            lib.oracle_e2m1_rne_sat.argtypes = [f32]
+            lib.oracle_e2m1_rne_sat.restype = ctypes.c_uint8
+            lib.oracle_quantize_fp8.argtypes = [i64, i64, vp, vp, vp]
+            lib.oracle_quantize_fp8.restype = None
+            lib.oracle_quantize_nvfp4.argtypes = [i64, i64, vp, vp, vp, vp]
+            lib.oracle_quantize_nvfp4.restype = None
             lib.oracle_num_threads.restype = ctypes.c_int
             lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
             lib.oracle_init()
@@ -190,3 +200,45 @@ def gemm(ops, rows=None):
     if ops.kind == "nvfp4":
         return gemm_nvfp4(ops.a, ops.b, ops.sfa, ops.sfb, ops.scale_a, ops.scale_b, rows)
     raise ValueError(ops.kind)
+
+
+# ---- input encodings (quantize.c) -------------------------------------------
+
+
+def e4m3_rne_sat(x: np.ndarray) -> np.ndarray:
+    """fp32 -> e4m3 code, round to nearest even, saturating at 448 (elementwise)."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.float32).ravel()
+    return np.fromiter((lib.oracle_e4m3_rne_sat(float(v)) for v in x), dtype=np.uint8, count=x.size)
+
+
+def e2m1_rne_sat(x: np.ndarray) -> np.ndarray:
+    """fp32 -> e2m1 code (0..15), round to nearest even, saturating at 6 (elementwise)."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.float32).ravel()
+    return np.fromiter((lib.oracle_e2m1_rne_sat(float(v)) for v in x), dtype=np.uint8, count=x.size)
+
+
+def quantize_fp8(x: np.ndarray):
+    """Per-tensor FP8 encoding of fp32 [rows][cols]: (codes uint8, dequantisation scale float32)."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    rows, cols = x.shape
+    q = np.empty((rows, cols), dtype=np.uint8)
+    s = np.zeros(1, dtype=np.float32)
+    lib.oracle_quantize_fp8(rows, cols, _ptr(x), _ptr(q), _ptr(s))
+    return q, np.float32(s[0])
+
+
+def quantize_nvfp4(x: np.ndarray):
+    """NVFP4 encoding of fp32 [rows][cols] (cols % 16 == 0): (packed uint8 [rows][cols/2],
+    block scales uint8 [rows][cols/16], global scale float32)."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    rows, cols = x.shape
+    assert cols % 16 == 0
+    q = np.empty((rows, cols // 2), dtype=np.uint8)
+    sf = np.empty((rows, cols // 16), dtype=np.uint8)
+    g = np.zeros(1, dtype=np.float32)
+    lib.oracle_quantize_nvfp4(rows, cols, _ptr(x), _ptr(q), _ptr(sf), _ptr(g))
+    return q, sf, np.float32(g[0])

@@ -321,6 +321,12 @@ def _draw(seed: int, rows: int, K: int, dist: str) -> np.ndarray:
     return out
 
 
+def draw_fp32(seed: int, rows: int, cols: int, dist: str = "normal") -> np.ndarray:
+    """Seeded fp32 [rows, cols] matrix ("uniform" U[-1,1], "normal" N(0,1) or
+    "normal_sqrtk" N(0,1)/sqrt(cols)): the input of the FP8 / NVFP4 encoders."""
+    return _draw(seed, rows, cols, dist)
+
+
 @dataclasses.dataclass
 class Operands:
     """Raw operand bytes for one GEMM.  a/b are [rows, K] (bf16 bits as uint16,
