@@ -186,9 +186,41 @@ def oracle_sample(ops, target_s: float):
 
 # ---------------------------------------------------------------- reference arm
 
+def run_reference_encoder(args):
+    """The oracle's encoder, as it stands, on a row sample of the same tensor per step."""
+    import oracle
+
+    kind, rows, cols, seed = ENCODERS[args.workload]
+    r = max(16, min(rows, int(rows * min(1.0, args.ref_step_s / 10.0))))
+    xs = synth.draw_fp32(seed, r, cols, "normal")
+    fn = oracle.quantize_fp8 if kind == "fp8" else oracle.quantize_nvfp4
+    nb = 2 * 4 * r * cols + (r * cols if kind == "fp8" else r * cols // 2 + r * cols // 16)
+    for _ in range(args.warmup):
+        fn(xs[:16])
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        fn(xs)
+        times.append(time.perf_counter() - t)
+    value = nb * args.steps / sum(times) / 1e9
+    line = {"metric": "encoder GB/s (algorithmic bytes: 2 reads of fp32 x + encoded output, / time)",
+            "value": value, "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * sum(times) / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic", "impl": "reference",
+            "config": {"workload": f"{kind} encoder of an fp32 [{rows}][{cols}] N(0,1) tensor", "rows": rows,
+                       "cols": cols},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{r} of {rows} rows per step"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return 0
+    if args.workload in ENCODERS:
+        return run_reference_encoder(args)
     w = synth.WORKLOADS[args.workload]
     ops = synth.workload_operands(args.workload)
     for _ in range(args.warmup):
@@ -379,6 +411,129 @@ def run_tkg(args, world, rank, local):
     return 0
 
 
+# ---------------------------------------------------------------- input encoders
+
+ENCODERS = {
+    # name: (kind, rows, cols, seed) — the fp32 data the FP8 8192^3 and NVFP4 16384^3 workloads encode
+    "encode_fp8_8192": ("fp8", 8192, 8192, 1004),
+    "encode_nvfp4_16384": ("nvfp4", 16384, 16384, 1005),
+}
+
+
+def run_encoder(args, world, rank, local):
+    """One step = one on-device encoding (tkg_quantize_fp8 / tkg_quantize_nvfp4)
+    of an fp32 [rows][cols] tensor resident in HBM.  HBM-bound: the algorithmic
+    bytes are two reads of x (the tensor amax must be known before any element
+    is encoded) plus the encoded output."""
+    import torch
+    from tiled_tensor_core_gb300 import tkg
+
+    import oracle
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    kind, rows, cols, seed = ENCODERS[args.workload]
+    x_host = synth.draw_fp32(seed, rows, cols, "normal")
+    x = torch.from_numpy(x_host).to(dev)
+    n = rows * cols
+    if kind == "fp8":
+        outs = [torch.empty((rows, cols), dtype=torch.uint8, device=dev), torch.empty(1, dtype=torch.float32, device=dev)]
+        call = lambda st: tkg.tkg_quantize_fp8(rows, cols, x, outs[0], outs[1], stream=st)  # noqa: E731
+        out_bytes = n + 4
+    else:
+        outs = [torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev),
+                torch.empty((rows, cols // 16), dtype=torch.uint8, device=dev),
+                torch.empty(1, dtype=torch.float32, device=dev)]
+        call = lambda st: tkg.tkg_quantize_nvfp4(rows, cols, x, outs[0], outs[1], outs[2], stream=st)  # noqa: E731
+        out_bytes = n // 2 + n // 16 + 4
+    alg_bytes = 2 * 4 * n + out_bytes
+    stream = torch.cuda.Stream(device=dev)
+    sptr = int(stream.cuda_stream)
+    for _ in range(args.warmup):
+        call(sptr)
+    if tkg.tkg_check_status(sptr) != tkg.TKG_OK:
+        raise RuntimeError("encoder warm-up failed")
+    spot = None
+    if rank == 0 and not args.no_check:  # full bit-exact comparison with the oracle's encoder
+        if kind == "fp8":
+            q_ref, s_ref = oracle.quantize_fp8(x_host)
+            spot = bool(np.array_equal(outs[0].cpu().numpy(), q_ref) and outs[1].item() == s_ref)
+        else:
+            q_ref, sf_ref, g_ref = oracle.quantize_nvfp4(x_host)
+            spot = bool(np.array_equal(outs[0].cpu().numpy(), q_ref) and np.array_equal(outs[1].cpu().numpy(), sf_ref)
+                        and outs[2].item() == g_ref)
+        if not spot:
+            raise RuntimeError("encoder output differs from the oracle")
+    sampler = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+    for i in range(args.steps):
+        ev[2 * i].record(stream)
+        call(sptr)
+        ev[2 * i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    barrier(world)
+    if tkg.tkg_check_status(sptr) != tkg.TKG_OK:
+        raise RuntimeError("encoder timed run failed")
+    step_ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)]
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
+    value = world * args.steps * alg_bytes / (total_ms * 1e-3) / 1e9
+    achieved = alg_bytes / (statistics.mean(step_ms) * 1e-3) / 1e9
+
+    e2e = None
+    if not args.no_e2e:  # pinned host x -> device, encode, encoded operand -> host
+        xh = torch.from_numpy(x_host).pin_memory()
+        oh = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+        torch.cuda.synchronize(dev)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        k = max(1, args.e2e_steps)
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for _ in range(k):
+                x.copy_(xh, non_blocking=True)
+                call(sptr)
+                for o, h in zip(outs, oh):
+                    h.copy_(o, non_blocking=True)
+            t1.record(stream)
+        t1.synchronize()
+        ms = t0.elapsed_time(t1) / k
+        e2e = {"value": alg_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": 4 * n,
+               "d2h_bytes_per_step": out_bytes, "ms_per_step": ms}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r = max(1, min(rows, int(rows * min(1.0, args.cpu_s / 10.0))))
+        xs = np.ascontiguousarray(x_host[:r])
+        t = time.perf_counter()
+        (oracle.quantize_fp8 if kind == "fp8" else oracle.quantize_nvfp4)(xs)
+        dt = time.perf_counter() - t
+        nb = 2 * 4 * r * cols + (r * cols if kind == "fp8" else r * cols // 2 + r * cols // 16)
+        cpu = {"value": nb / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{r} of {rows} rows of the same tensor ({dt:.1f} s)"}
+
+    peaks = load_peaks()
+    line = {
+        "metric": "encoder GB/s (algorithmic bytes: 2 reads of fp32 x + encoded output, / time)",
+        "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{kind} encoder of an fp32 [{rows}][{cols}] N(0,1) tensor", "rows": rows, "cols": cols,
+                   "l2": f"input {4 * n / 2**20:.0f} MiB > 129 MiB L2"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "peak_source": f"{peaks['source']} copy bandwidth"},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 3 * args.steps, "clocks": clocks,
+        "bit_exact_vs_oracle": spot,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_e2e(ops, dev, w, args):
     """End to end through the public API with host buffers: every step copies
     its inputs from pinned host memory to the device, runs the GEMM and copies
@@ -445,7 +600,7 @@ def main(argv=None):
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["tkg", "reference"], default="tkg")
-    p.add_argument("--workload", choices=sorted(synth.WORKLOADS), default="bf16_4096")
+    p.add_argument("--workload", choices=sorted(synth.WORKLOADS) + sorted(ENCODERS), default="bf16_4096")
     p.add_argument("--batch", type=int, default=0, help="GEMMs per step (default: per workload)")
     p.add_argument("--variant", type=int, default=0)
     p.add_argument("--group-m", type=int, default=0)
@@ -464,6 +619,8 @@ def main(argv=None):
         rank = int(os.environ.get("RANK", "0"))
         return run_reference(args, world, rank)
     world, rank, local = dist_setup(args)
+    if args.workload in ENCODERS:
+        return run_encoder(args, world, rank, local)
     return run_tkg(args, world, rank, local)
 
 

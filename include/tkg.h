@@ -123,6 +123,32 @@ TKG_API tkg_status tkg_gemm_nvfp4(int64_t M, int64_t N, int64_t K, const void* A
 TKG_API tkg_status tkg_gemm_nvfp4_noalloc(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* C,
                                           const tkg_scales* scales, void* stream);
 
+/* On-device input encoders: fp32 data -> the operands of tkg_gemm_fp8 and
+ * tkg_gemm_nvfp4 (the 8-bit and block-scaled 4-bit formats of "ThunderKittens
+ * reaches 22.4 PFLOPS on NVIDIA Rubin", NVFP4 and FP8 paragraphs; the pages
+ * give the formats, the scale recipe is this library's reading):
+ *   FP8:   amax = max|x| over the tensor, q = e4m3(x * (448 / amax)),
+ *          *dequant_scale = amax / 448 (1 and q = 0 for an all-zero tensor);
+ *          pass q and the scale to tkg_gemm_fp8 as an operand and its scale.
+ *   NVFP4: g = amax / (6 * 448); for every row and 16 consecutive elements,
+ *          b = max|x| over the block, sb = e4m3(b / (6 g)),
+ *          q = e2m1(x / (e4m3(sb) * g)) (q = 0 when that divisor is 0);
+ *          q packed two per byte (element 2j in the low nibble of byte j),
+ *          block scales [rows][cols/16] e4m3, *global_scale = g; pass them to
+ *          tkg_gemm_nvfp4 as an operand, its block scales and its scale.
+ * Every multiply and divide is one fp32 IEEE operation; e4m3 / e2m1 rounding
+ * is to nearest, ties to even, saturating at 448 / 6, keeping the sign.
+ * x: fp32 [rows][cols] row-major; cols % 16 == 0; x and q 16-byte aligned,
+ * the scale 4-byte aligned; all device pointers, caller-owned.  The scale
+ * output doubles as the amax accumulator while the call runs.  Asynchronous
+ * on `stream`: four stream-ordered operations (a 4-byte memset and three
+ * kernels), no allocation.  Returns TKG_ERR_INVALID_ARG / TKG_ERR_MISALIGNED
+ * before any GPU work for bad arguments. */
+TKG_API tkg_status tkg_quantize_fp8(int64_t rows, int64_t cols, const float* x, uint8_t* q, float* dequant_scale,
+                                    void* stream);
+TKG_API tkg_status tkg_quantize_nvfp4(int64_t rows, int64_t cols, const float* x, uint8_t* q_packed,
+                                      uint8_t* block_scales, float* global_scale, void* stream);
+
 /* Synchronises `stream`, then reads and clears the device status word of the
  * current device.  Returns TKG_ERR_TIMEOUT if any kernel since the last check
  * abandoned a pipeline wait (its output is then undefined), TKG_ERR_CUDA if the

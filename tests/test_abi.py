@@ -161,3 +161,15 @@ def test_mma_rate_probe_arguments_checked(tkg):
     for args in [(3, 1, 256, 64), (0, 3, 256, 64), (0, 1, 192, 64), (0, 1, 256, 0), (0, 1, 256, 65537)]:
         assert tkg.lib.tkg_debug_mma_rate(*args, ctypes.byref(c), None) == tkg.TKG_ERR_INVALID_ARG
     assert tkg.lib.tkg_debug_mma_rate(0, 1, 256, 64, None, None) == tkg.TKG_ERR_INVALID_ARG
+
+
+def test_quantize_arguments_checked_before_any_gpu_work(tkg):
+    x, q, sf, s = 4096, 8192, 12288, 16384  # never dereferenced: every call below fails validation
+    for rows, cols in [(0, 16), (4, 0), (4, 24), (-1, 16)]:
+        assert tkg.lib.tkg_quantize_fp8(rows, cols, x, q, s, None) == tkg.TKG_ERR_INVALID_ARG
+        assert tkg.lib.tkg_quantize_nvfp4(rows, cols, x, q, sf, s, None) == tkg.TKG_ERR_INVALID_ARG
+    assert tkg.lib.tkg_quantize_fp8(4, 16, None, q, s, None) == tkg.TKG_ERR_INVALID_ARG
+    assert tkg.lib.tkg_quantize_nvfp4(4, 16, x, q, None, s, None) == tkg.TKG_ERR_INVALID_ARG
+    assert tkg.lib.tkg_quantize_fp8(4, 16, x + 4, q, s, None) == tkg.TKG_ERR_MISALIGNED
+    assert tkg.lib.tkg_quantize_nvfp4(4, 16, x, q + 8, sf, s, None) == tkg.TKG_ERR_MISALIGNED
+    assert tkg.lib.tkg_quantize_fp8(4, 16, x, q, s + 2, None) == tkg.TKG_ERR_MISALIGNED

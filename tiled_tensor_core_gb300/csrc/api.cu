@@ -521,6 +521,13 @@ tkg_status debug_device_ready() {
   DevState* d = nullptr;
   return current_device(&d);
 }
+
+tkg_status device_sm_count(int* out) {
+  DevState* d = nullptr;
+  const tkg_status st = current_device(&d);
+  if (st == TKG_OK) *out = d->sm_count;
+  return st;
+}
 }  // namespace tkg
 
 // Address of the current device's status word, without any other per-device

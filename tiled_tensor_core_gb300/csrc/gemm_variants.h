@@ -2,6 +2,7 @@
 #pragma once
 
 #include "gemm_kernel.cuh"
+#include "tkg.h"
 
 namespace tkg {
 
@@ -30,5 +31,8 @@ cudaError_t nvfp4_interleave_scales(const uint8_t* sfa, const uint8_t* sfb, int 
                                     int blocks_b, int kstages, int sf_mode, uint8_t* scratch, size_t b_offset,
                                     cudaStream_t stream);
 size_t nvfp4_scratch_bytes(int blocks_a, int blocks_b, int kstages);
+
+// The current device's SM count, after the library's device check (api.cu).
+tkg_status device_sm_count(int* out);
 
 }  // namespace tkg

@@ -81,6 +81,10 @@ lib.tkg_debug_tma_swizzle_probe.argtypes = [_i32, _vp, _vp, _vp]
 lib.tkg_debug_tma_swizzle_probe.restype = _i32
 lib.tkg_debug_mma_probe.argtypes = [_i32, _i32, _i32, _vp, _vp, _vp, _vp, ctypes.POINTER(ctypes.c_int32), _vp, _vp]
 lib.tkg_debug_mma_probe.restype = _i32
+lib.tkg_quantize_fp8.argtypes = [_i64, _i64, _vp, _vp, _vp, _vp]
+lib.tkg_quantize_fp8.restype = _i32
+lib.tkg_quantize_nvfp4.argtypes = [_i64, _i64, _vp, _vp, _vp, _vp, _vp]
+lib.tkg_quantize_nvfp4.restype = _i32
 lib.tkg_debug_mma_rate.argtypes = [_i32, _i32, _i32, _i32, ctypes.POINTER(ctypes.c_ulonglong), _vp]
 lib.tkg_debug_mma_rate.restype = _i32
 
@@ -207,6 +211,17 @@ def tkg_debug_mma_probe(kind, n, ksteps, a_tile, b_tile, sfa=None, sfb=None, sf_
         cols = (ctypes.c_int32 * len(sf_cols))(*[int(c) for c in sf_cols])
     return lib.tkg_debug_mma_probe(kind, n, ksteps, _addr(a_tile), _addr(b_tile), _addr(sfa), _addr(sfb), cols,
                                    _addr(d_out), _stream(stream))
+
+
+def tkg_quantize_fp8(rows, cols, x, q, dequant_scale, stream=None, check=True) -> int:
+    st = lib.tkg_quantize_fp8(rows, cols, _addr(x), _addr(q), _addr(dequant_scale), _stream(stream))
+    return _check(st, "tkg_quantize_fp8") if check else st
+
+
+def tkg_quantize_nvfp4(rows, cols, x, q_packed, block_scales, global_scale, stream=None, check=True) -> int:
+    st = lib.tkg_quantize_nvfp4(rows, cols, _addr(x), _addr(q_packed), _addr(block_scales), _addr(global_scale),
+                                _stream(stream))
+    return _check(st, "tkg_quantize_nvfp4") if check else st
 
 
 def tkg_debug_mma_rate(kind, cta_group, n, count, stream=None) -> int:
