@@ -76,11 +76,22 @@ TKG_API tkg_status tkg_debug_mma_probe(int kind, int n, int ksteps, const void* 
  * per row each) and shape (128*cta_group) x n back to back, cta_group 1 (one
  * CTA) or 2 (a CTA pair, cta_group::2), operands rotating over shared-memory
  * stages; *cycles (host) receives the SM cycles from the first issue until
- * their commit lands.  The difference of two counts divided by the
- * difference in MMAs is the per-MMA cost.  n in {128, 256}, count in
- * 1..65536.  Synchronous on `stream`. */
-TKG_API tkg_status tkg_debug_mma_rate(int kind, int cta_group, int n, int count, unsigned long long* cycles,
-                                      void* stream);
+ * their commit lands.  pattern 0: one accumulator; 1: consecutive pairs of
+ * MMAs share A and accumulate into two accumulators (a 2x1 tile); 2: as 1,
+ * the pair's first MMA filling the A collector buffer and the second reusing
+ * it (collector::a::fill / ::lastuse); 3 (kind 2 only): one accumulator with
+ * the scale-factor addresses moving per MMA and per 4-MMA stage as in the
+ * GEMM; 4: one accumulator, and after every 4 MMAs the GEMM's per-stage
+ * synchronisation work (two completed mbarrier waits with
+ * tcgen05.fence::after_thread_sync, two tcgen05.commit); 5, 6, 7: only the
+ * commits, only the waits, only the fences; 8: only the waits, with acquire
+ * at CTA instead of cluster scope; 9: as 0 with varied operand bits instead
+ * of one repeated byte.  The difference of two counts divided
+ * by the difference in MMAs is the per-MMA cost.  n in {128, 256} (128 for
+ * kind 2 with pattern 1 or 2), count in 1..65536 (at least 2 for patterns 1
+ * and 2, which issue count/2 whole pairs).  Synchronous on `stream`. */
+TKG_API tkg_status tkg_debug_mma_rate(int kind, int cta_group, int n, int count, int pattern,
+                                      unsigned long long* cycles, void* stream);
 
 #ifdef __cplusplus
 }

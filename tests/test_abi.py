@@ -145,8 +145,8 @@ def test_swizzle_selection_matches_definition(tkg):
 
 def test_compiled_variants_fit_the_sm(tkg):
     for kind in (0, 1, 2):
-        for v in (1, 2, 3, 4, 5, 6):
-            if (kind == 2 and v == 4) or (kind != 2 and v in (5, 6)):
+        for v in (1, 2, 3, 4, 5, 6, 7):
+            if (kind == 2 and v == 4) or (kind != 2 and v in (5, 6, 7)):
                 with pytest.raises(tkg.TkgError):
                     tkg.tkg_debug_variant_info(kind, v)
                 continue
@@ -158,9 +158,10 @@ def test_compiled_variants_fit_the_sm(tkg):
 
 def test_mma_rate_probe_arguments_checked(tkg):
     c = ctypes.c_ulonglong(0)
-    for args in [(3, 1, 256, 64), (0, 3, 256, 64), (0, 1, 192, 64), (0, 1, 256, 0), (0, 1, 256, 65537)]:
+    for args in [(3, 1, 256, 64, 0), (0, 3, 256, 64, 0), (0, 1, 192, 64, 0), (0, 1, 256, 0, 0),
+                 (0, 1, 256, 65537, 0), (0, 1, 256, 64, 3), (2, 1, 256, 64, 1), (0, 1, 256, 1, 1), (0, 1, 256, 64, 3), (2, 1, 256, 64, 10)]:
         assert tkg.lib.tkg_debug_mma_rate(*args, ctypes.byref(c), None) == tkg.TKG_ERR_INVALID_ARG
-    assert tkg.lib.tkg_debug_mma_rate(0, 1, 256, 64, None, None) == tkg.TKG_ERR_INVALID_ARG
+    assert tkg.lib.tkg_debug_mma_rate(0, 1, 256, 64, 0, None, None) == tkg.TKG_ERR_INVALID_ARG
 
 
 def test_quantize_arguments_checked_before_any_gpu_work(tkg):

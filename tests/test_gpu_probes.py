@@ -105,8 +105,10 @@ def test_single_tile_nvfp4_mma_scale_layout(tkg, oracle_mod, n):
 def test_mma_rate_probe_times_back_to_back_mmas(tkg, kind, cta_group):
     """The issue-rate timer runs every kind and CTA-group form to completion,
     and more MMAs take longer: a per-MMA cost between 32 and 4096 cycles."""
-    short = tkg.tkg_debug_mma_rate(kind, cta_group, 256, 128)
-    long = tkg.tkg_debug_mma_rate(kind, cta_group, 256, 1024)
-    per = (long - short) / (1024 - 128)
-    assert 0 < short < long
-    assert 32 <= per <= 4096
+    for pattern in (0, 1, 2, 3, 4, 5, 6, 7, 8, 9) if kind == 2 else (0, 1, 2, 4, 5, 6, 7, 8, 9):
+        n = 128 if (kind == 2 and pattern) else 256
+        short = tkg.tkg_debug_mma_rate(kind, cta_group, n, 128, pattern)
+        long = tkg.tkg_debug_mma_rate(kind, cta_group, n, 1024, pattern)
+        per = (long - short) / (1024 - 128)
+        assert 0 < short < long
+        assert 32 <= per <= 4096

@@ -191,16 +191,18 @@ const KernelVariant* variant_of(int kind, int id) {
 // Tile choice: the 2-SM 256 x 256 tile.  (A 256 x 224 tile would balance the
 // persistent rounds of some shapes, e.g. 4096^2 -> 304 tiles = 4 x 76, but on
 // sm_103a an N = 224 MMA takes as long as N = 256, so it gains nothing; it is
-// kept as an explicit variant.)  NVFP4 takes the scale-warp form of that tile:
-// copying the block scales with tcgen05.cp costs the tensor pipe about 60
-// cycles per copy, twelve copies per 256-deep K stage.
+// kept as an explicit variant.)  NVFP4 takes the scale-warp form of that tile
+// with one scale slot per ring stage: copying the block scales with
+// tcgen05.cp costs the tensor pipe about 60 cycles per copy, twelve copies per
+// 256-deep K stage, and coupling the slots to the stages saves the MMA thread
+// a second wait per stage.
 int pick_variant(int kind, int64_t M, int64_t N, int64_t K) {
   (void)K;
   (void)M;
   (void)N;
   const int forced = static_cast<int>(g_opt_variant.load(std::memory_order_relaxed));
   if (forced > 0 && variant_of(kind, forced)) return forced;
-  return kind == 2 ? kVariant2Sm256x256Sfw : kVariant2Sm256x256;
+  return kind == 2 ? kVariant2Sm256x256Coupled : kVariant2Sm256x256;
 }
 
 // Occupancy-limited number of co-resident clusters for a variant (cached).

@@ -78,7 +78,7 @@ struct GemmParams {
 constexpr int kSfCopy = 0, kSfWarps = 1, kSfHybrid = 2;
 
 template <Kind KIND_, int CG_, int BN_, int STAGES_, int EPI_WARPS_, int NUM_ACC_ = 2, int SF_MODE_ = kSfCopy,
-          int SF_GROUPS_ = 1>
+          int SF_GROUPS_ = 1, bool SF_COUPLED_ = false>
 struct GemmCfg {
   static constexpr Kind KIND = KIND_;
   static constexpr int CG = CG_;                // CTAs per MMA (1, or 2 for the CTA pair)
@@ -92,6 +92,9 @@ struct GemmCfg {
   static constexpr bool SF_WARPS_MODE = SCALED && SF_MODE == kSfWarps;
   static constexpr bool SF_HYBRID = SCALED && SF_MODE == kSfHybrid;
   static constexpr bool SF_ST = SF_WARPS_MODE || SF_HYBRID;  // scale warps write scales with tcgen05.st
+  // scale-warp mode with one TMEM scale slot per ring stage: the scale warps wait on the stage's
+  // empty barrier and arrive on its full barrier, so the MMA thread waits once per stage
+  static constexpr bool SF_COUPLED = SF_WARPS_MODE && SF_COUPLED_;
   static constexpr int ROW_BYTES = 128;         // K bytes per operand row per stage
   static constexpr uint32_t SWZ = select_swizzle(ROW_BYTES);
   static_assert(SWZ == 128, "operand rows must take the 128-byte swizzle");
@@ -125,7 +128,7 @@ struct GemmCfg {
   static constexpr int SF_COLS_STAGE = SCALED ? SF_COLS_A + SF_COLS_B : 0;
   // TMEM scale slots: one per ring stage in copy mode; in scale-warp mode a ring
   // of their own, as many as fit beside the accumulators (at most STAGES)
-  static constexpr int SF_SLOTS = !SF_WARPS_MODE ? STAGES
+  static constexpr int SF_SLOTS = (!SF_WARPS_MODE || SF_COUPLED) ? STAGES
                                 : ((512 - ACC_COLS) / SF_COLS_STAGE < STAGES ? (512 - ACC_COLS) / SF_COLS_STAGE
                                                                              : STAGES);
   static constexpr int TMEM_USED = ACC_COLS + (SCALED ? SF_SLOTS * SF_COLS_STAGE : 0);
@@ -148,7 +151,7 @@ struct GemmCfg {
   static constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_STAGE;
   static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * 2 * EPI_BUF;
   static constexpr int NUM_BARS =
-      2 * STAGES + 2 * NUM_ACC + 1 + (SF_WARPS_MODE ? 2 * SF_SLOTS : SF_HYBRID ? SF_SLOTS : 0);
+      2 * STAGES + 2 * NUM_ACC + 1 + ((SF_WARPS_MODE && !SF_COUPLED) ? 2 * SF_SLOTS : SF_HYBRID ? SF_SLOTS : 0);
   static constexpr int OFF_MISC = OFF_BAR + 8 * NUM_BARS;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
 
@@ -229,7 +232,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
+      mbar_init(full_bar(s), C::SF_COUPLED ? 1 + C::CG * 4 : 1);  // + one arrival per scale warp of the group
       mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < C::NUM_ACC; ++a) {
@@ -237,7 +240,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
       mbar_init(tempty_bar(a), C::CG * C::EPI_WARPS);
     }
     mbar_init(drain_bar, 1);
-    if constexpr (C::SF_WARPS_MODE) {
+    if constexpr (C::SF_WARPS_MODE && !C::SF_COUPLED) {
       for (int j = 0; j < C::SF_SLOTS; ++j) {
         mbar_init(sf_ready_bar(j), C::CG * 4);  // one group of four scale warps per CTA writes a slot
         mbar_init(sf_empty_bar(j), 1);
@@ -338,9 +341,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
           const uint32_t b0 = sB + stage * C::B_STAGE;
           // this stage's scale columns: copy mode reuses them only after the ring stage itself is
           // released; scale-warp mode has a slot ring of its own
-          const uint32_t sf_tmem =
-              tmem_base + static_cast<uint32_t>(C::ACC_COLS + (C::SF_WARPS_MODE ? slot : stage) * C::SF_COLS_STAGE);
-          if constexpr (C::SF_ST) {
+          const uint32_t sf_tmem = tmem_base + static_cast<uint32_t>(
+                                                   C::ACC_COLS + ((C::SF_WARPS_MODE && !C::SF_COUPLED) ? slot : stage) *
+                                                                     C::SF_COLS_STAGE);
+          if constexpr (C::SF_ST && !C::SF_COUPLED) {
             const bool ready = C::SF_WARPS_MODE ? mbar_wait(sf_ready_bar(slot), slot_phase, tmo, abort_flag)
                                                 : mbar_wait(sf_ready_bar(stage), phase, tmo, abort_flag);
             if (!ready) {
@@ -348,7 +352,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
               break;
             }
             tc_fence_after();
-          } else if constexpr (C::SCALED) {
+          } else if constexpr (C::SCALED && !C::SF_ST) {
             const uint32_t sfa0 = sSFA + stage * C::SFA_STAGE;
             const uint32_t sfb0 = sSFB + stage * C::SFB_STAGE;
 #pragma unroll
@@ -374,7 +378,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
                                   sf_tmem + C::SF_COLS_A + (C::BN / 32) * kk, accum);
           }
           mma_commit<C::CG>(empty_bar(stage), 0x3);
-          if constexpr (C::SF_WARPS_MODE) {
+          if constexpr (C::SF_WARPS_MODE && !C::SF_COUPLED) {
             mma_commit<C::CG>(sf_empty_bar(slot), 0x3);
             if (++slot == C::SF_SLOTS) {
               slot = 0;
@@ -415,7 +419,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
       order.coord(t, tm, tn);
       const int acc = it % C::NUM_ACC;
       const uint32_t acc_phase = (it / C::NUM_ACC) & 1;
-      const bool got = __all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), acc_phase, tmo, abort_flag));
+      const bool got = __all_sync(0xffffffffu, mbar_wait<true>(tfull_bar(acc), acc_phase, tmo, abort_flag));
       if (!got) {
         if (lane == 0) record_timeout(p.status, kRoleEpilogue, abort_flag);
         break;
@@ -507,7 +511,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
       const int quad = warp & 3;
       const int sgroup = (warp - 2 - C::EPI_WARPS) / 4;  // this warp takes steps sgroup, sgroup + SF_GROUPS, ...
       const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
-      const uint32_t ready_leader0 = (C::CG == 2) ? mapa_shared(sf_ready_bar(0), 0) : sf_ready_bar(0);
+      // where a written slot is announced: the stage's full barrier (coupled) or the slot's ready barrier
+      const uint32_t ready0 = C::SF_COUPLED ? full_bar(0) : sf_ready_bar(0);
+      const uint32_t ready_leader0 = (C::CG == 2) ? mapa_shared(ready0, 0) : ready0;
       const int my_tiles = cluster_id < num_tiles ? (num_tiles - 1 - cluster_id) / num_clusters + 1 : 0;
       const int steps = my_tiles * p.num_kb;
       const uint4* sfa = reinterpret_cast<const uint4*>(p.sf_a);
@@ -531,17 +537,15 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
       auto put = [&](int s_, const uint4 (&v)[1 + G]) -> bool {
         const int j = s_ % C::SF_SLOTS;
         const uint32_t ph = static_cast<uint32_t>(s_ / C::SF_SLOTS) & 1u;
-        const uint32_t freed = C::SF_WARPS_MODE ? sf_empty_bar(j) : empty_bar(j);
+        const uint32_t freed = (C::SF_WARPS_MODE && !C::SF_COUPLED) ? sf_empty_bar(j) : empty_bar(j);
         if (!__all_sync(0xffffffffu, mbar_wait(freed, ph ^ 1u, tmo, abort_flag))) return false;
         tc_fence_after();
         const uint32_t cols = lane_base + static_cast<uint32_t>(C::ACC_COLS + j * C::SF_COLS_STAGE);
-        uint32_t ra[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const uint32_t w = (c >> 2) == 0 ? v[0].x : (c >> 2) == 1 ? v[0].y : (c >> 2) == 2 ? v[0].z : v[0].w;
-          ra[c] = ((c & 3) == quad) ? w : 0u;
-        }
-        tmem_st_32x32b_x16(cols, ra);
+        // A: only column 4t + q of MMA t is read by this quarter's rows
+        tmem_st_32x32b_x1(cols + static_cast<uint32_t>(quad), v[0].x);
+        tmem_st_32x32b_x1(cols + 4u + static_cast<uint32_t>(quad), v[0].y);
+        tmem_st_32x32b_x1(cols + 8u + static_cast<uint32_t>(quad), v[0].z);
+        tmem_st_32x32b_x1(cols + 12u + static_cast<uint32_t>(quad), v[0].w);
         if constexpr (G > 0) {
           uint32_t rbw[G * C::KSTEPS];
 #pragma unroll

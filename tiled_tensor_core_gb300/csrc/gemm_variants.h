@@ -15,7 +15,8 @@ enum VariantId : int {
   kVariant2Sm256x224 = 4,  // cta_group::2, 256 x 224 tile per CTA pair (bf16 / FP8)
   kVariant2Sm256x256Sfw = 5,  // cta_group::2, 256 x 256, block scales written by scale warps (NVFP4)
   kVariant2Sm256x256Hybrid = 6,  // cta_group::2, 256 x 256, A scales by scale warps, B by a copy warp (NVFP4)
-  kNumVariants = 7
+  kVariant2Sm256x256Coupled = 7,  // as 5, with one TMEM scale slot per ring stage (NVFP4)
+  kNumVariants = 8
 };
 
 // Each returns the variant for `id`, or nullptr if that kind has no such variant.

@@ -106,11 +106,33 @@ __device__ __forceinline__ void mbar_arrive_local(uint32_t bar) {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
+// Acquire at CTA scope (the instruction's default).  What the pipeline's
+// waits order is tensor-core and TMA (async-proxy) work, which the tcgen05
+// fences and the transaction counts already order; a cluster-scope acquire
+// would add nothing, and on sm_103a it costs ~290 cycles per call even on a
+// completed phase, stalling the MMA-issuing thread (measured with
+// tkg_debug_mma_rate, patterns 6 and 8).
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// The same test, letting the hardware suspend the thread for up to 20 us while
+// the phase is incomplete (it resumes when the phase completes): for waits
+// that usually last long, so that the waiting warps stop competing with the
+// MMA-issuing warp for issue slots and barrier accesses.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 20000;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
@@ -121,13 +143,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Bounded wait for the phase with parity `parity` to complete.  Every wait of
 // the pipeline goes through here: after `timeout_ns` of waiting (or once some
 // other role has raised the CTA's abort flag) it gives up and returns false.
+// kSuspend: use the suspending test (long waits of non-critical roles).
+template <bool kSuspend = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
                                           const volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto test = [&]() { return kSuspend ? mbar_try_wait_suspend(bar, parity) : mbar_try_wait(bar, parity); };
+  if (test()) return true;
   uint64_t t0 = 0;
   for (uint32_t n = 1;; ++n) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((n & 255u) == 0) {
+    if (test()) return true;
+    if ((n & (kSuspend ? 15u : 255u)) == 0) {
       const uint64_t now = globaltimer_ns();
       if (t0 == 0) t0 = now;
       if (now - t0 > timeout_ns || *abort_flag) return false;
@@ -367,6 +392,11 @@ __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
       "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
+}
+
+// 32 lanes x 1 32-bit column from a register into TMEM.
+__device__ __forceinline__ void tmem_st_32x32b_x1(uint32_t taddr, uint32_t r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(r) : "memory");
 }
 
 // 32 lanes x 8 consecutive 32-bit columns from registers into TMEM.

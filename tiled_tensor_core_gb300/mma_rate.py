@@ -6,7 +6,9 @@ For every kind (bf16 K=16, e4m3 K=32, block-scaled e2m1 K=64; 32 bytes of K
 per operand row each), CTA-group form (one CTA, or a CTA pair with
 cta_group::2) and N, one thread issues 128 and then 1024 MMAs back to back
 (tkg_debug_mma_rate); the difference gives the cost of one MMA in SM cycles,
-and from it the dense rate per SM and, at a given clock, per GPU.
+and from it the dense rate per SM and, at a given clock, per GPU.  A second
+table compares one accumulator with the 2x1 tile (pairs of MMAs sharing A,
+two accumulators), with and without reuse of the A collector buffer.
 """
 from __future__ import annotations
 
@@ -36,6 +38,34 @@ def main(argv=None) -> None:
                 fma_sm = 128 * n * k / per  # each SM computes 128 rows of the (128*cg) x n tile
                 tflops = 2 * fma_sm * sms * args.clock_mhz * 1e6 / 1e12
                 print(f"| {name} | {cg} | {128 * cg} x {n} x {k} | {per:.1f} | {fma_sm:.0f} | {tflops:.0f} |")
+
+    print()
+    print("| kind | MMA (M x N x K), one CTA | one accumulator | 2x1: pairs sharing A | 2x1 + collector::a reuse |")
+    print("|---|---|---|---|---|")
+    for kind, (name, k) in KINDS.items():
+        n = 128 if kind == 2 else 256
+        cells = []
+        for pattern in (0, 1, 2):
+            c0 = tkg.tkg_debug_mma_rate(kind, 1, n, 128, pattern)
+            c1 = tkg.tkg_debug_mma_rate(kind, 1, n, 1024, pattern)
+            cells.append(f"{(c1 - c0) / (1024 - 128):.1f}")
+        print(f"| {name} | 128 x {n} x {k} | " + " | ".join(cells) + " |")
+
+    print()
+    print("| kind | CTA group | MMA (M x N x K) | MMAs only | + per-stage sync work | commits only | waits only "
+          "| fences only | waits, CTA-scope acquire | scale columns moving as in the GEMM | varied operand bits |")
+    print("|---|---|---|---|---|---|---|---|---|---|---|")
+    for kind, (name, k) in KINDS.items():
+        for cg in (1, 2):
+            cells = []
+            for pattern in (0, 4, 5, 6, 7, 8, 3, 9):
+                if pattern == 3 and kind != 2:
+                    cells.append("—")
+                    continue
+                c0 = tkg.tkg_debug_mma_rate(kind, cg, 256, 128, pattern)
+                c1 = tkg.tkg_debug_mma_rate(kind, cg, 256, 1024, pattern)
+                cells.append(f"{(c1 - c0) / (1024 - 128):.1f}")
+            print(f"| {name} | {cg} | {128 * cg} x 256 x {k} | " + " | ".join(cells) + " |")
 
 
 if __name__ == "__main__":

@@ -85,7 +85,7 @@ lib.tkg_quantize_fp8.argtypes = [_i64, _i64, _vp, _vp, _vp, _vp]
 lib.tkg_quantize_fp8.restype = _i32
 lib.tkg_quantize_nvfp4.argtypes = [_i64, _i64, _vp, _vp, _vp, _vp, _vp]
 lib.tkg_quantize_nvfp4.restype = _i32
-lib.tkg_debug_mma_rate.argtypes = [_i32, _i32, _i32, _i32, ctypes.POINTER(ctypes.c_ulonglong), _vp]
+lib.tkg_debug_mma_rate.argtypes = [_i32, _i32, _i32, _i32, _i32, ctypes.POINTER(ctypes.c_ulonglong), _vp]
 lib.tkg_debug_mma_rate.restype = _i32
 
 
@@ -224,8 +224,9 @@ def tkg_quantize_nvfp4(rows, cols, x, q_packed, block_scales, global_scale, stre
     return _check(st, "tkg_quantize_nvfp4") if check else st
 
 
-def tkg_debug_mma_rate(kind, cta_group, n, count, stream=None) -> int:
+def tkg_debug_mma_rate(kind, cta_group, n, count, pattern=0, stream=None) -> int:
     """SM cycles for `count` back-to-back MMAs (see tkg_debug.h)."""
     c = ctypes.c_ulonglong(0)
-    _check(lib.tkg_debug_mma_rate(kind, cta_group, n, count, ctypes.byref(c), _stream(stream)), "tkg_debug_mma_rate")
+    _check(lib.tkg_debug_mma_rate(kind, cta_group, n, count, pattern, ctypes.byref(c), _stream(stream)),
+           "tkg_debug_mma_rate")
     return int(c.value)
