@@ -169,7 +169,7 @@ TKG_API void tkg_shutdown(void);
  *  TKG_OPT_GROUP_M     super-group height in output tiles for the L2-aware
  *                      tile order (default 8; the paper's {8, N, M/8} order,
  *                      "Block Launch Order and L2 Cache Reuse", Table 3)
- *  TKG_OPT_VARIANT     force a kernel variant: 0 = the default (7 for
+ *  TKG_OPT_VARIANT     force a kernel variant: 0 = the default (8 for
  *                      NVFP4, else 2), 1 = 1-SM 128x256 tiles, 2 = 2-SM
  *                      (CTA pair) 256x256 tiles, 3 = 2-SM 256x128 tiles,
  *                      4 = 2-SM 256x224 tiles (bf16 and FP8 only),
@@ -182,8 +182,9 @@ TKG_API void tkg_shutdown(void);
  *                      by a copy warp (NVFP4 only), 7 = variant 5 with one
  *                      TMEM scale slot per ring stage, the scale warps
  *                      signalling through the stage's own barriers (NVFP4
- *                      only).  A variant the kind lacks falls back to the
- *                      default.
+ *                      only), 8 = variant 7 with the scales brought into
+ *                      shared memory by the ring's TMA (NVFP4 only).  A
+ *                      variant the kind lacks falls back to the default.
  *  TKG_OPT_MAX_CTAS    cap the persistent grid size (0 = all SMs)            */
 typedef enum tkg_option {
     TKG_OPT_TIMEOUT_NS = 1,

@@ -145,8 +145,8 @@ def test_swizzle_selection_matches_definition(tkg):
 
 def test_compiled_variants_fit_the_sm(tkg):
     for kind in (0, 1, 2):
-        for v in (1, 2, 3, 4, 5, 6, 7):
-            if (kind == 2 and v == 4) or (kind != 2 and v in (5, 6, 7)):
+        for v in (1, 2, 3, 4, 5, 6, 7, 8):
+            if (kind == 2 and v == 4) or (kind != 2 and v in (5, 6, 7, 8)):
                 with pytest.raises(tkg.TkgError):
                     tkg.tkg_debug_variant_info(kind, v)
                 continue

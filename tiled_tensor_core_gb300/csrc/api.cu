@@ -192,17 +192,19 @@ const KernelVariant* variant_of(int kind, int id) {
 // persistent rounds of some shapes, e.g. 4096^2 -> 304 tiles = 4 x 76, but on
 // sm_103a an N = 224 MMA takes as long as N = 256, so it gains nothing; it is
 // kept as an explicit variant.)  NVFP4 takes the scale-warp form of that tile
-// with one scale slot per ring stage: copying the block scales with
-// tcgen05.cp costs the tensor pipe about 60 cycles per copy, twelve copies per
-// 256-deep K stage, and coupling the slots to the stages saves the MMA thread
-// a second wait per stage.
+// with one scale slot per ring stage and the scales riding the ring: copying
+// the block scales with tcgen05.cp costs the tensor pipe about 60 cycles per
+// copy, twelve copies per 256-deep K stage; coupling the slots to the stages
+// saves the MMA thread a second wait per stage; and reading the scales from
+// shared memory, where the ring's TMA put them stages ahead, keeps global-load
+// latency off the scale warps' critical path.
 int pick_variant(int kind, int64_t M, int64_t N, int64_t K) {
   (void)K;
   (void)M;
   (void)N;
   const int forced = static_cast<int>(g_opt_variant.load(std::memory_order_relaxed));
   if (forced > 0 && variant_of(kind, forced)) return forced;
-  return kind == 2 ? kVariant2Sm256x256Coupled : kVariant2Sm256x256;
+  return kind == 2 ? kVariant2Sm256x256SfSmem : kVariant2Sm256x256;
 }
 
 // Occupancy-limited number of co-resident clusters for a variant (cached).

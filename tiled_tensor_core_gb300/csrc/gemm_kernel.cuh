@@ -78,7 +78,7 @@ struct GemmParams {
 constexpr int kSfCopy = 0, kSfWarps = 1, kSfHybrid = 2;
 
 template <Kind KIND_, int CG_, int BN_, int STAGES_, int EPI_WARPS_, int NUM_ACC_ = 2, int SF_MODE_ = kSfCopy,
-          int SF_GROUPS_ = 1, bool SF_COUPLED_ = false>
+          int SF_GROUPS_ = 1, bool SF_COUPLED_ = false, bool SF_SMEM_ = false>
 struct GemmCfg {
   static constexpr Kind KIND = KIND_;
   static constexpr int CG = CG_;                // CTAs per MMA (1, or 2 for the CTA pair)
@@ -95,6 +95,10 @@ struct GemmCfg {
   // scale-warp mode with one TMEM scale slot per ring stage: the scale warps wait on the stage's
   // empty barrier and arrive on its full barrier, so the MMA thread waits once per stage
   static constexpr bool SF_COUPLED = SF_WARPS_MODE && SF_COUPLED_;
+  // coupled scale-warp mode whose scales ride the operand ring: the producer's TMA brings each
+  // stage's scales (row layout) into shared memory, landing on the CTA's own sf_full barrier, and
+  // the scale warps read them from there instead of from global memory
+  static constexpr bool SF_SMEM = SF_COUPLED && SF_SMEM_;
   static constexpr int ROW_BYTES = 128;         // K bytes per operand row per stage
   static constexpr uint32_t SWZ = select_swizzle(ROW_BYTES);
   static_assert(SWZ == 128, "operand rows must take the 128-byte swizzle");
@@ -109,8 +113,8 @@ struct GemmCfg {
   // (one per MMA) for each 128 rows.  Each CTA stages its own 128 rows of A's
   // scales and the scales of all BN rows of B (every CTA of a pair multiplies
   // by all of B).  Scale-warp mode keeps no scales in shared memory.
-  static constexpr bool SFA_IN_SMEM = SCALED && SF_MODE == kSfCopy;
-  static constexpr bool SFB_IN_SMEM = SCALED && SF_MODE != kSfWarps;
+  static constexpr bool SFA_IN_SMEM = SCALED && (SF_MODE == kSfCopy || SF_SMEM_);
+  static constexpr bool SFB_IN_SMEM = SCALED && (SF_MODE != kSfWarps || SF_SMEM_);
   static constexpr int SF_ATOM = 512;
   static constexpr int SFA_STAGE = SFA_IN_SMEM ? KSTEPS * SF_ATOM : 0;
   static constexpr int SFB_BLOCKS = BN / 128;   // 128-row blocks of B scales per tile
@@ -118,7 +122,10 @@ struct GemmCfg {
   static constexpr int SF_GROUPS = SF_ST ? SF_GROUPS_ : 0;
   static constexpr int SF_WARPS = 4 * SF_GROUPS;
   static constexpr int CP_WARPS = SF_HYBRID ? 1 : 0;
-  static constexpr int STAGE_TX = A_STAGE + B_BOX + SFA_STAGE + SFB_STAGE;  // bytes landing per CTA per stage
+  // bytes landing per CTA per stage on the (leader's) full barrier; in SF_SMEM mode the scales
+  // land on the CTA's own sf_full barrier instead
+  static constexpr int STAGE_TX = A_STAGE + B_BOX + (SF_SMEM_ ? 0 : SFA_STAGE + SFB_STAGE);
+  static constexpr int SF_TX = SFA_STAGE + SFB_STAGE;
   static constexpr int ACC_STRIDE = BN <= 128 ? 128 : 256;  // accumulators start on aligned columns
   static constexpr int ACC_COLS = NUM_ACC * ACC_STRIDE;
   // TMEM columns of one stage's scales: A: 4 per MMA (row m at column m/32);
@@ -151,7 +158,8 @@ struct GemmCfg {
   static constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_STAGE;
   static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * 2 * EPI_BUF;
   static constexpr int NUM_BARS =
-      2 * STAGES + 2 * NUM_ACC + 1 + ((SF_WARPS_MODE && !SF_COUPLED) ? 2 * SF_SLOTS : SF_HYBRID ? SF_SLOTS : 0);
+      2 * STAGES + 2 * NUM_ACC + 1 + ((SF_WARPS_MODE && !SF_COUPLED) ? 2 * SF_SLOTS : SF_HYBRID ? SF_SLOTS : 0) +
+      (SF_SMEM ? STAGES : 0);
   static constexpr int OFF_MISC = OFF_BAR + 8 * NUM_BARS;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
 
@@ -169,6 +177,7 @@ struct GemmCfg {
   static_assert(!SF_ST || SF_SLOTS >= 2, "the scale warps run at least one slot ahead");
   static_assert(!SF_ST || SF_GROUPS == 1 || SF_GROUPS == 2, "one or two groups of scale warps");
   static_assert(!SF_HYBRID || SF_GROUPS == 1, "the hybrid mode's A scales need one group");
+  static_assert(SF_SMEM == SF_SMEM_, "shared-memory scale staging is a form of the coupled scale-warp mode");
   static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB shared-memory limit");
 };
 
@@ -217,6 +226,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
   // the ring stages, so the stage's empty barrier says it)
   auto sf_ready_bar = [&](int j) { return bar0 + 8u * (2 * C::STAGES + 2 * C::NUM_ACC + 1 + j); };
   auto sf_empty_bar = [&](int j) { return bar0 + 8u * (2 * C::STAGES + 2 * C::NUM_ACC + 1 + C::SF_SLOTS + j); };
+  // SF_SMEM: stage s's scales landed in this CTA's shared memory (the coupled mode has no slot barriers)
+  auto sf_full_bar = [&](int st) { return bar0 + 8u * (2 * C::STAGES + 2 * C::NUM_ACC + 1 + st); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* never_abort = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
@@ -247,6 +258,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
       }
     } else if constexpr (C::SF_HYBRID) {
       for (int j = 0; j < C::SF_SLOTS; ++j) mbar_init(sf_ready_bar(j), C::CG * 4 + 1);
+    }
+    if constexpr (C::SF_SMEM) {
+      for (int st = 0; st < C::STAGES; ++st) mbar_init(sf_full_bar(st), 1);
     }
     *abort_flag = 0;
     *never_abort = 0;
@@ -292,13 +306,19 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
           if (!(first && p.fault_mode == 1)) {
             tma_load_2d<C::CG>(sA + stage * C::A_STAGE, &p.tmap_a, fb, kb * C::K_TMAP, a_row);
             tma_load_2d<C::CG>(sB + stage * C::B_STAGE, &p.tmap_b, fb, kb * C::K_TMAP, b_row);
-            // interleaved scale atoms: 2 KB (16 rows of 128 B) per (K stage, 128-row block), the
-            // blocks of one K stage contiguous
-            if constexpr (C::SFA_IN_SMEM)
-              tma_load_2d<C::CG>(sSFA + stage * C::SFA_STAGE, &p.tmap_sfa, fb, 0, (kb * p.sf_blocks_a + a_row / 128) * 16);
-            if constexpr (C::SFB_IN_SMEM)
-              tma_load_2d<C::CG>(sSFB + stage * C::SFB_STAGE, &p.tmap_sfb, fb, 0,
-                                 (kb * p.sf_blocks_b + (tn * C::BN) / 128) * 16);
+            // staged scales: 2 KB (16 rows of 128 B) per (K stage, 128-row block), the blocks of one
+            // K stage contiguous
+            const int ya = (kb * p.sf_blocks_a + a_row / 128) * 16;
+            const int yb = (kb * p.sf_blocks_b + (tn * C::BN) / 128) * 16;
+            if constexpr (C::SF_SMEM) {
+              const uint32_t sfb_bar = sf_full_bar(stage);
+              mbar_arrive_expect_tx(sfb_bar, C::SF_TX);
+              tma_load_2d<1>(sSFA + stage * C::SFA_STAGE, &p.tmap_sfa, sfb_bar, 0, ya);
+              tma_load_2d<1>(sSFB + stage * C::SFB_STAGE, &p.tmap_sfb, sfb_bar, 0, yb);
+            } else {
+              if constexpr (C::SFA_IN_SMEM) tma_load_2d<C::CG>(sSFA + stage * C::SFA_STAGE, &p.tmap_sfa, fb, 0, ya);
+              if constexpr (C::SFB_IN_SMEM) tma_load_2d<C::CG>(sSFB + stage * C::SFB_STAGE, &p.tmap_sfb, fb, 0, yb);
+            }
           }
           first = false;
           if (++stage == C::STAGES) {
@@ -519,6 +539,17 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
       const uint4* sfa = reinterpret_cast<const uint4*>(p.sf_a);
       const uint4* sfb = reinterpret_cast<const uint4*>(p.sf_b);
       // scales of step s: [0] = this lane's A row, [1 + g] = B row 32g + lane (scale-warp mode)
+      // SF_SMEM: read them from the stage's shared-memory copy once it has landed
+      auto fetch_smem = [&](int s_, uint4 (&v)[1 + G]) -> bool {
+        const int j = s_ % C::STAGES;
+        const uint32_t ph = static_cast<uint32_t>(s_ / C::STAGES) & 1u;
+        if (!__all_sync(0xffffffffu, mbar_wait(sf_full_bar(j), ph, tmo, abort_flag))) return false;
+        v[0] = ld_shared_v4(sSFA + j * C::SFA_STAGE + static_cast<uint32_t>(quad * 32 + lane) * 16u);
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+          v[1 + g] = ld_shared_v4(sSFB + j * C::SFB_STAGE + static_cast<uint32_t>(g * 32 + lane) * 16u);
+        return true;
+      };
       auto fetch = [&](int s_, uint4 (&v)[1 + G]) {
         const int i = s_ / p.num_kb;
         const int kb = s_ - i * p.num_kb;
@@ -537,8 +568,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
       auto put = [&](int s_, const uint4 (&v)[1 + G]) -> bool {
         const int j = s_ % C::SF_SLOTS;
         const uint32_t ph = static_cast<uint32_t>(s_ / C::SF_SLOTS) & 1u;
-        const uint32_t freed = (C::SF_WARPS_MODE && !C::SF_COUPLED) ? sf_empty_bar(j) : empty_bar(j);
-        if (!__all_sync(0xffffffffu, mbar_wait(freed, ph ^ 1u, tmo, abort_flag))) return false;
+        if constexpr (!C::SF_SMEM) {  // SF_SMEM: the slot is free once the stage's scales have landed
+          const uint32_t freed = (C::SF_WARPS_MODE && !C::SF_COUPLED) ? sf_empty_bar(j) : empty_bar(j);
+          if (!__all_sync(0xffffffffu, mbar_wait(freed, ph ^ 1u, tmo, abort_flag))) return false;
+        }
         tc_fence_after();
         const uint32_t cols = lane_base + static_cast<uint32_t>(C::ACC_COLS + j * C::SF_COLS_STAGE);
         // A: only column 4t + q of MMA t is read by this quarter's rows
@@ -565,7 +598,15 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
         if (lane == 0) mbar_arrive_cluster(ready_leader0 + 8u * j);
         return true;
       };
-      if constexpr (C::SF_GROUPS == 1) {
+      if constexpr (C::SF_SMEM) {
+        // the scales are already on chip: read each step's just before writing it
+        uint4 v0[1 + G];
+        for (int s_ = sgroup; s_ < steps && ok; s_ += C::SF_GROUPS) {
+          ok = fetch_smem(s_, v0);
+          if (!ok) break;
+          ok = put(s_, v0);
+        }
+      } else if constexpr (C::SF_GROUPS == 1) {
         // two register sets, so that the loads of step s + 2 fly while step s waits for its slot
         uint4 v0[1 + G], v1[1 + G];
         if (steps > 0) fetch(0, v0);

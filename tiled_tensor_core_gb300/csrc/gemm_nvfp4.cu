@@ -30,6 +30,7 @@ using Nvfp4_2Sm_128 = GemmCfg<Kind::NVFP4, 2, 128, 6, 4, 2>;
 using Nvfp4_2Sm_256_Sfw = GemmCfg<Kind::NVFP4, 2, 256, 6, 4, 1, kSfWarps, 2>;
 using Nvfp4_2Sm_256_Hyb = GemmCfg<Kind::NVFP4, 2, 256, 5, 4, 1, kSfHybrid, 1>;
 using Nvfp4_2Sm_256_Sfc = GemmCfg<Kind::NVFP4, 2, 256, 5, 4, 1, kSfWarps, 2, true>;
+using Nvfp4_2Sm_256_Sfs = GemmCfg<Kind::NVFP4, 2, 256, 5, 4, 1, kSfWarps, 2, true, true>;
 
 const KernelVariant* nvfp4_variant(int id) {
   static const KernelVariant v1 = make_variant<Nvfp4_1Sm_256>("nvfp4_1sm_128x256_s3");
@@ -38,6 +39,7 @@ const KernelVariant* nvfp4_variant(int id) {
   static const KernelVariant v5 = make_variant<Nvfp4_2Sm_256_Sfw>("nvfp4_2sm_256x256_s6_sfw8");
   static const KernelVariant v6 = make_variant<Nvfp4_2Sm_256_Hyb>("nvfp4_2sm_256x256_s5_hybrid");
   static const KernelVariant v7 = make_variant<Nvfp4_2Sm_256_Sfc>("nvfp4_2sm_256x256_s5_sfw8_coupled");
+  static const KernelVariant v8 = make_variant<Nvfp4_2Sm_256_Sfs>("nvfp4_2sm_256x256_s5_sfw8_smem");
   switch (id) {
     case kVariant1Sm128x256: return &v1;
     case kVariant2Sm256x256: return &v2;
@@ -45,6 +47,7 @@ const KernelVariant* nvfp4_variant(int id) {
     case kVariant2Sm256x256Sfw: return &v5;
     case kVariant2Sm256x256Hybrid: return &v6;
     case kVariant2Sm256x256Coupled: return &v7;
+    case kVariant2Sm256x256SfSmem: return &v8;
     default: return nullptr;
   }
 }

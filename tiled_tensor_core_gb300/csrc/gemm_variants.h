@@ -16,7 +16,8 @@ enum VariantId : int {
   kVariant2Sm256x256Sfw = 5,  // cta_group::2, 256 x 256, block scales written by scale warps (NVFP4)
   kVariant2Sm256x256Hybrid = 6,  // cta_group::2, 256 x 256, A scales by scale warps, B by a copy warp (NVFP4)
   kVariant2Sm256x256Coupled = 7,  // as 5, with one TMEM scale slot per ring stage (NVFP4)
-  kNumVariants = 8
+  kVariant2Sm256x256SfSmem = 8,   // as 7, the scales brought into shared memory by the ring's TMA (NVFP4)
+  kNumVariants = 9
 };
 
 // Each returns the variant for `id`, or nullptr if that kind has no such variant.
