@@ -109,9 +109,8 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
 // Acquire at CTA scope (the instruction's default).  What the pipeline's
 // waits order is tensor-core and TMA (async-proxy) work, which the tcgen05
 // fences and the transaction counts already order; a cluster-scope acquire
-// would add nothing, and on sm_103a it costs ~290 cycles per call even on a
-// completed phase, stalling the MMA-issuing thread (measured with
-// tkg_debug_mma_rate, patterns 6 and 8).
+// would add nothing and costs the MMA-issuing thread more per wait
+// (tkg_debug_mma_rate patterns 6 and 8).
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
