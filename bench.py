@@ -36,7 +36,9 @@ METRIC = "GEMM TFLOP/s (2MNK/t) bf16/FP8/NVFP4 on 1 GB300; % of dense tensor pea
 L2_BYTES = 129 * 2 ** 20
 # GEMMs per step, sized so that a step is tens of milliseconds of GPU work
 BATCH = {"bf16_256": 2000, "bf16_4096": 400, "bf16_8192": 60, "bf16_skinny": 100, "fp8_8192": 100,
-         "nvfp4_16384": 30}
+         "nvfp4_16384": 30, "bf16_4096_k64": 4000, "bf16_4096_k128": 3000, "bf16_4096_k256": 2000,
+         "bf16_4096_k512": 1500, "bf16_4096_k1024": 1000}
+SCHEDULE = {"static": 1, "dynamic": 2, "single": 3}
 # dense tensor-core peak relative to bf16 (nominal GB300 ratios: bf16 2.25, fp8 4.5, fp4 13.5 PFLOP/s)
 PEAK_RATIO = {"bf16": 1.0, "fp8": 2.0, "nvfp4": 6.0}
 DTYPE = {"bf16": "bf16", "fp8": "e4m3", "nvfp4": "e2m1+e4m3"}
@@ -268,6 +270,9 @@ def run_tkg(args, world, rank, local):
         tkg.tkg_set_option(tkg.TKG_OPT_VARIANT, args.variant)
     if args.group_m:
         tkg.tkg_set_option(tkg.TKG_OPT_GROUP_M, args.group_m)
+    tkg.tkg_set_option(tkg.TKG_OPT_SCHEDULE, SCHEDULE[args.schedule])
+    tkg.tkg_set_option(tkg.TKG_OPT_LAUNCH_OVERLAP,
+                       tkg.TKG_OVERLAP_ON if args.overlap == "on" else tkg.TKG_OVERLAP_OFF)
 
     w = synth.WORKLOADS[args.workload]
     ops = synth.workload_operands(args.workload)
@@ -308,7 +313,7 @@ def run_tkg(args, world, rank, local):
 
     # Launch-bound workloads replay the step from a CUDA graph (captured after the
     # warm-up, so every lazy set-up is done); the GEMM launches are unchanged.
-    use_graph = args.graph == "on" or (args.graph == "auto" and w.flops < 1e9 and w.kind != "nvfp4")
+    use_graph = args.graph == "on" or (args.graph == "auto" and w.flops < 5e10 and w.kind != "nvfp4")
     graph = None
     if use_graph:
         graph = torch.cuda.CUDAGraph()
@@ -331,7 +336,7 @@ def run_tkg(args, world, rank, local):
         spot = float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
 
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * batch)]
-    step_ms, kern_ms = [], []
+    step_ms, kern_ms, host_ms = [], [], []
     sampler = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize(dev)
@@ -344,15 +349,20 @@ def run_tkg(args, world, rank, local):
         s0 = torch.cuda.Event(enable_timing=True)
         s1 = torch.cuda.Event(enable_timing=True)
         s0.record(stream)
+        h0 = time.perf_counter()
         if graph is not None:
             with torch.cuda.stream(stream):
                 graph.replay()
         else:
-            step(ev)
+            # an event between two launches would end their overlap: with it on, the step is timed whole
+            step(ev if args.overlap == "off" else None)
+        host_ms.append((time.perf_counter() - h0) * 1e3)
         s1.record(stream)
         s1.synchronize()
         step_ms.append(s0.elapsed_time(s1))
-        if graph is not None:  # no per-launch events inside a graph: spread the step over its launches
+        if graph is not None or args.overlap == "on":
+            # no per-launch events (inside a graph, or between overlapped launches): the step is
+            # nothing but GEMM launches, so spread its time over them
             kern_ms.extend([step_ms[-1] / batch] * batch)
         else:
             kern_ms.extend(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(batch))
@@ -398,10 +408,13 @@ def run_tkg(args, world, rank, local):
                    "l2": (f"{n_sets} rotating operand sets, {n_sets * footprint / 2**20:.0f} MiB > 129 MiB L2"
                           if n_sets > 1 else f"operands {footprint / 2**20:.0f} MiB > 129 MiB L2"),
                    "kernel": info, "group_m": tkg.tkg_get_option(tkg.TKG_OPT_GROUP_M),
+                   "schedule": args.schedule,
+                   "launch_overlap": "programmatic dependent launch" if args.overlap == "on" else "off",
                    "cuda_graph": graph is not None},
         "pct_of_peak": 100.0 * value / world / peak,
         "pct_of_burst_peak": 100.0 * value / world / peak_burst,
         "median_gemm_ms": statistics.median(kern_ms),
+        "host_enqueue_ms_per_step": statistics.median(host_ms),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic_bytes(w.name),
                      "frac_of_burst_peak": achieved / peak_burst,
@@ -619,6 +632,10 @@ def main(argv=None):
     p.add_argument("--no-check", action="store_true")
     p.add_argument("--graph", choices=["auto", "on", "off"], default="auto",
                    help="replay each step from a CUDA graph (auto: launch-bound workloads)")
+    p.add_argument("--schedule", choices=sorted(SCHEDULE), default="static",
+                   help="tile schedule: persistent static grid, dynamic (cluster launch control), one cluster per tile")
+    p.add_argument("--overlap", choices=["on", "off"], default="on",
+                   help="launch GEMMs as programmatic dependents of the previous kernel (on) or plainly (off)")
     args = p.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.impl == "reference":

@@ -185,13 +185,43 @@ TKG_API void tkg_shutdown(void);
  *                      only), 8 = variant 7 with the scales brought into
  *                      shared memory by the ring's TMA (NVFP4 only).  A
  *                      variant the kind lacks falls back to the default.
- *  TKG_OPT_MAX_CTAS    cap the persistent grid size (0 = all SMs)            */
+ *  TKG_OPT_MAX_CTAS    cap the persistent grid size (0 = all SMs)
+ *  TKG_OPT_LAUNCH_OVERLAP
+ *                      TKG_OVERLAP_ON (default): GEMMs are launched as
+ *                      programmatic dependents of the previous kernel on the
+ *                      stream, so their CTAs set up shared and tensor memory
+ *                      on SMs the previous kernel has left while it finishes;
+ *                      each CTA still waits for that kernel to complete (and
+ *                      its writes to be visible) before it reads A, B or the
+ *                      scales or writes C, so stream order is kept.
+ *                      TKG_OVERLAP_OFF: plain stream-ordered launches.
+ *  TKG_OPT_SCHEDULE    how CTA pairs get output tiles ("Persistent Grid
+ *                      Launch", Table 2; Cluster Launch Control):
+ *                      TKG_SCHEDULE_STATIC (default) = persistent grid, one
+ *                      CTA (pair) per SM, pair c takes tiles c, c + pairs,
+ *                      ... in the grouped order;
+ *                      TKG_SCHEDULE_DYNAMIC = one cluster per tile is
+ *                      launched and running clusters cancel the launch of
+ *                      clusters that have not started and take their tiles
+ *                      (not available with NVFP4 variants 5-7, which return
+ *                      TKG_ERR_INVALID_ARG);
+ *                      TKG_SCHEDULE_SINGLE = one cluster per tile, each
+ *                      computes its own tile only (non-persistent launch). */
 typedef enum tkg_option {
     TKG_OPT_TIMEOUT_NS = 1,
     TKG_OPT_GROUP_M = 2,
     TKG_OPT_VARIANT = 3,
-    TKG_OPT_MAX_CTAS = 4
+    TKG_OPT_MAX_CTAS = 4,
+    TKG_OPT_LAUNCH_OVERLAP = 5,
+    TKG_OPT_SCHEDULE = 6
 } tkg_option;
+
+/* Values of TKG_OPT_LAUNCH_OVERLAP and TKG_OPT_SCHEDULE. */
+#define TKG_OVERLAP_ON 1
+#define TKG_OVERLAP_OFF 2
+#define TKG_SCHEDULE_STATIC 1
+#define TKG_SCHEDULE_DYNAMIC 2
+#define TKG_SCHEDULE_SINGLE 3
 TKG_API tkg_status tkg_set_option(tkg_option key, int64_t value);
 TKG_API int64_t tkg_get_option(tkg_option key);
 

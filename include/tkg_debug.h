@@ -50,6 +50,13 @@ TKG_API int tkg_debug_pick_variant(int kind, int64_t M, int64_t N, int64_t K);
  * next GEMM launch only. */
 TKG_API tkg_status tkg_debug_set_fault(int mode);
 
+/* Tile-visit count for the scheduler check: the next GEMM launch adds 1 to
+ * counts[t] (a device array of at least tiles_m * tiles_n zeroed words,
+ * caller-owned) each time a CTA (pair) stores output tile t, t being the
+ * linear tile id before the grouped reordering.  Every schedule must leave
+ * every count at exactly 1.  NULL disables; applies to the next launch only. */
+TKG_API tkg_status tkg_debug_set_visit_counter(unsigned int* counts);
+
 /* Device: TMA-load a [64 rows][S bytes] uint8 tile (row pitch S bytes) from
  * `src` with the S-byte swizzle (S in {32, 64, 128}) and copy the raw shared
  * memory image (64*S bytes) to `dst`.  Synchronous on `stream`. */

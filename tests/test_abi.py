@@ -110,6 +110,38 @@ def test_options_roundtrip(tkg):
         tkg.tkg_set_option(77, 1)
 
 
+def test_schedule_and_overlap_options(tkg):
+    assert tkg.tkg_get_option(tkg.TKG_OPT_SCHEDULE) == tkg.TKG_SCHEDULE_STATIC
+    assert tkg.tkg_get_option(tkg.TKG_OPT_LAUNCH_OVERLAP) == tkg.TKG_OVERLAP_ON
+    for v in (tkg.TKG_SCHEDULE_STATIC, tkg.TKG_SCHEDULE_DYNAMIC, tkg.TKG_SCHEDULE_SINGLE):
+        tkg.tkg_set_option(tkg.TKG_OPT_SCHEDULE, v)
+        assert tkg.tkg_get_option(tkg.TKG_OPT_SCHEDULE) == v
+    tkg.tkg_set_option(tkg.TKG_OPT_LAUNCH_OVERLAP, tkg.TKG_OVERLAP_OFF)
+    assert tkg.tkg_get_option(tkg.TKG_OPT_LAUNCH_OVERLAP) == tkg.TKG_OVERLAP_OFF
+    for key, bad in ((tkg.TKG_OPT_SCHEDULE, 4), (tkg.TKG_OPT_LAUNCH_OVERLAP, 3), (tkg.TKG_OPT_SCHEDULE, -1)):
+        with pytest.raises(tkg.TkgError):
+            tkg.tkg_set_option(key, bad)
+    tkg.tkg_set_option(tkg.TKG_OPT_SCHEDULE, 0)
+    tkg.tkg_set_option(tkg.TKG_OPT_LAUNCH_OVERLAP, 0)
+    assert tkg.tkg_get_option(tkg.TKG_OPT_SCHEDULE) == tkg.TKG_SCHEDULE_STATIC
+    assert tkg.tkg_get_option(tkg.TKG_OPT_LAUNCH_OVERLAP) == tkg.TKG_OVERLAP_ON
+
+
+def test_dynamic_schedule_rejects_static_scale_warp_variants(tkg):
+    # NVFP4 variants 5-7 walk a precomputed tile sequence in their scale warps:
+    # the dynamic schedule is refused for them before any CUDA call
+    A, B, C = 1 << 12, 1 << 13, 1 << 14
+    s4 = tkg.tkg_scales(1 << 12, 1 << 12, 1 << 14, 1 << 14)
+    tkg.tkg_set_option(tkg.TKG_OPT_SCHEDULE, tkg.TKG_SCHEDULE_DYNAMIC)
+    try:
+        for v in (5, 6, 7):
+            tkg.tkg_set_option(tkg.TKG_OPT_VARIANT, v)
+            assert tkg.lib.tkg_gemm_nvfp4(256, 256, 256, A, B, C, s4, None) == tkg.TKG_ERR_INVALID_ARG
+    finally:
+        tkg.tkg_set_option(tkg.TKG_OPT_VARIANT, 0)
+        tkg.tkg_set_option(tkg.TKG_OPT_SCHEDULE, 0)
+
+
 @pytest.mark.parametrize("tiles_m,tiles_n,group_m", [(1, 1, 8), (16, 16, 8), (32, 32, 8), (64, 32, 12),
                                                      (13, 7, 8), (7, 13, 8), (5, 3, 1), (3, 5, 100), (33, 1, 8)])
 def test_tile_order_visits_every_tile_once(tkg, tiles_m, tiles_n, group_m):

@@ -34,7 +34,10 @@ std::atomic<int64_t> g_opt_timeout{0};
 std::atomic<int64_t> g_opt_group{0};
 std::atomic<int64_t> g_opt_variant{0};
 std::atomic<int64_t> g_opt_max_ctas{0};
+std::atomic<int64_t> g_opt_overlap{0};
+std::atomic<int64_t> g_opt_schedule{0};
 std::atomic<int> g_fault{0};
+std::atomic<unsigned int*> g_visits{nullptr};
 
 std::mutex g_mu;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -269,6 +272,11 @@ tkg_status gemm_launch(int kind, int64_t M, int64_t N, int64_t K, const void* A,
   const int id = pick_variant(kind, M, N, K);
   const KernelVariant* v = variant_of(kind, id);
   if (!v) return TKG_ERR_INTERNAL;
+  // the dynamic schedule reaches every role through the answer ring; the
+  // scale warps of these NVFP4 variants walk a precomputed static sequence
+  if (opt_or(g_opt_schedule, TKG_SCHEDULE_STATIC) == TKG_SCHEDULE_DYNAMIC &&
+      (id == kVariant2Sm256x256Sfw || id == kVariant2Sm256x256Hybrid || id == kVariant2Sm256x256Coupled))
+    return TKG_ERR_INVALID_ARG;
   const int64_t tile_m = 128LL * v->cg;
   const int64_t tiles_m = (M + tile_m - 1) / tile_m;
   const int64_t tiles_n = (N + v->bn - 1) / v->bn;
@@ -352,6 +360,9 @@ tkg_status gemm_launch(int kind, int64_t M, int64_t N, int64_t K, const void* A,
   p.tiles_n = static_cast<int>(tiles_n);
   p.group_m = static_cast<int>(opt_or(g_opt_group, kDefaultGroupM));
   p.fault_mode = g_fault.exchange(0);
+  p.visits = g_visits.exchange(nullptr);
+  const int64_t sched = opt_or(g_opt_schedule, TKG_SCHEDULE_STATIC);
+  p.sched = sched == TKG_SCHEDULE_DYNAMIC ? kSchedDynamic : sched == TKG_SCHEDULE_SINGLE ? kSchedSingle : kSchedStatic;
 
   int clusters = 0;
   st = max_clusters(*d, kind, id, *v, &clusters);
@@ -363,19 +374,27 @@ tkg_status gemm_launch(int kind, int64_t M, int64_t N, int64_t K, const void* A,
   const int64_t cap = g_opt_max_ctas.load(std::memory_order_relaxed);
   if (cap > 0 && cap / v->cg < grid_clusters) grid_clusters = cap / v->cg > 0 ? cap / v->cg : 1;
   if (tiles_m * tiles_n < grid_clusters) grid_clusters = tiles_m * tiles_n;
+  // one cluster per tile: the hardware places them as SMs free up (and, in the
+  // dynamic schedule, running clusters cancel and take over those not started)
+  if (p.sched != kSchedStatic) grid_clusters = tiles_m * tiles_n;
 
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(grid_clusters * v->cg), 1, 1);
   cfg.blockDim = dim3(static_cast<unsigned>(v->threads), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(v->smem_bytes);
   cfg.stream = static_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(v->cg);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // programmatic dependent launch: this grid's CTAs may start (and run their
+  // set-up) before the previous kernel on the stream has finished; the kernel
+  // waits for it before touching global memory
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = opt_or(g_opt_overlap, TKG_OVERLAP_ON) == TKG_OVERLAP_ON ? 2 : 1;
   void* args[] = {&p};
   if (cudaLaunchKernelExC(&cfg, v->func, args) != cudaSuccess) {
     cudaGetLastError();
@@ -466,6 +485,14 @@ tkg_status tkg_set_option(tkg_option key, int64_t value) {
       g_opt_variant.store(value);
       return TKG_OK;
     case TKG_OPT_MAX_CTAS: g_opt_max_ctas.store(value); return TKG_OK;
+    case TKG_OPT_LAUNCH_OVERLAP:
+      if (value > TKG_OVERLAP_OFF) return TKG_ERR_INVALID_ARG;
+      g_opt_overlap.store(value);
+      return TKG_OK;
+    case TKG_OPT_SCHEDULE:
+      if (value > TKG_SCHEDULE_SINGLE) return TKG_ERR_INVALID_ARG;
+      g_opt_schedule.store(value);
+      return TKG_OK;
   }
   return TKG_ERR_INVALID_ARG;
 }
@@ -476,6 +503,8 @@ int64_t tkg_get_option(tkg_option key) {
     case TKG_OPT_GROUP_M: return opt_or(g_opt_group, kDefaultGroupM);
     case TKG_OPT_VARIANT: return g_opt_variant.load();
     case TKG_OPT_MAX_CTAS: return g_opt_max_ctas.load();
+    case TKG_OPT_LAUNCH_OVERLAP: return opt_or(g_opt_overlap, TKG_OVERLAP_ON);
+    case TKG_OPT_SCHEDULE: return opt_or(g_opt_schedule, TKG_SCHEDULE_STATIC);
   }
   return -1;
 }
@@ -506,6 +535,11 @@ tkg_status tkg_debug_variant_info(int kind, int variant, int32_t info[6]) {
 }
 
 int tkg_debug_pick_variant(int kind, int64_t M, int64_t N, int64_t K) { return pick_variant(kind, M, N, K); }
+
+tkg_status tkg_debug_set_visit_counter(unsigned int* counts) {
+  g_visits.store(counts);
+  return TKG_OK;
+}
 
 tkg_status tkg_debug_set_fault(int mode) {
   if (mode < 0 || mode > 1) return TKG_ERR_INVALID_ARG;

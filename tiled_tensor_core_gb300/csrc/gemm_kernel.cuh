@@ -59,7 +59,23 @@ struct GemmParams {
   int sf_blocks_b;  // same for B
   const uint8_t* sf_a;  // NVFP4 scale-warp mode: staged A scales in global memory
   const uint8_t* sf_b;  // same for B
+  int sched;            // tile schedule (kSchedStatic / kSchedDynamic / kSchedSingle)
+  unsigned int* visits;  // debug: if set, one increment per tile each time a CTA (pair) stores it
 };
+
+// Tile schedules ("Persistent Grid Launch"; Cluster Launch Control for the
+// dynamic form):
+//   kSchedStatic:  persistent grid, one CTA (pair) per SM; cluster c takes
+//                  tiles c, c + clusters, c + 2 clusters, ...
+//   kSchedDynamic: one cluster per tile is launched; a running cluster takes
+//                  its own tile, then asks the hardware to cancel the launch
+//                  of a cluster that has not started and takes that one's tile
+//                  instead, until nothing is left to cancel.  One lane of the
+//                  leader CTA asks one tile ahead; the answers reach every
+//                  role of both CTAs through a ring of SCHED_SLOTS slots.
+//   kSchedSingle:  one cluster per tile, each does its own tile only (the
+//                  non-persistent launch).
+constexpr int kSchedStatic = 0, kSchedDynamic = 1, kSchedSingle = 2;
 
 // Block-scale staging modes (NVFP4).
 //   kSfCopy: the scales ride the shared-memory ring with the operands and the
@@ -160,8 +176,17 @@ struct GemmCfg {
   static constexpr int NUM_BARS =
       2 * STAGES + 2 * NUM_ACC + 1 + ((SF_WARPS_MODE && !SF_COUPLED) ? 2 * SF_SLOTS : SF_HYBRID ? SF_SLOTS : 0) +
       (SF_SMEM ? STAGES : 0);
-  static constexpr int OFF_MISC = OFF_BAR + 8 * NUM_BARS;
-  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
+  // dynamic schedule: ring of cancellation answers (16 bytes each) with a full
+  // barrier per slot in every CTA and an empty barrier per slot in the leader,
+  // after the barriers above
+  static constexpr int SCHED_SLOTS = 8;
+  static constexpr int SCHED_BAR0 = NUM_BARS;
+  static constexpr int OFF_MISC = OFF_BAR + 8 * (NUM_BARS + 2 * SCHED_SLOTS);
+  static constexpr int OFF_SCHED = (OFF_MISC + 16 + 15) / 16 * 16;
+  // readers of every answer: each CTA's producer lane, epilogue warps and scale
+  // warps, and the leader's MMA lane
+  static constexpr int SCHED_READERS = CG * (1 + EPI_WARPS + SF_WARPS) + 1;
+  static constexpr int SMEM_BYTES = OFF_SCHED + 16 * SCHED_SLOTS + 1024;  // + slack to align the base to 1024
 
   static_assert(B_STAGE % 1024 == 0 && A_STAGE % 1024 == 0, "stages must keep 1024-byte swizzle atoms aligned");
   static_assert((OFF_SFA % 1024) == 0 && (OFF_EPI % 1024) == 0, "region alignment");
@@ -228,6 +253,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
   auto sf_empty_bar = [&](int j) { return bar0 + 8u * (2 * C::STAGES + 2 * C::NUM_ACC + 1 + C::SF_SLOTS + j); };
   // SF_SMEM: stage s's scales landed in this CTA's shared memory (the coupled mode has no slot barriers)
   auto sf_full_bar = [&](int st) { return bar0 + 8u * (2 * C::STAGES + 2 * C::NUM_ACC + 1 + st); };
+  auto sched_full_bar = [&](int j) { return bar0 + 8u * (C::SCHED_BAR0 + j); };
+  auto sched_empty_bar = [&](int j) { return bar0 + 8u * (C::SCHED_BAR0 + C::SCHED_SLOTS + j); };
+  const uint32_t sResp = sbase + C::OFF_SCHED;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* never_abort = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
@@ -262,6 +290,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
     if constexpr (C::SF_SMEM) {
       for (int st = 0; st < C::STAGES; ++st) mbar_init(sf_full_bar(st), 1);
     }
+    for (int j = 0; j < C::SCHED_SLOTS; ++j) {
+      mbar_init(sched_full_bar(j), 1);  // the leader's expect_tx arrival + the 16-byte answer
+      mbar_init(sched_empty_bar(j), C::SCHED_READERS);
+    }
     *abort_flag = 0;
     *never_abort = 0;
     fence_mbar_init();
@@ -283,6 +315,61 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
   }
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Up to here the CTA touched only its own shared and tensor memory.  From
+  // here on it reads A, B and the scales and writes C, which the grid before
+  // it on the stream may still be producing or reading: wait for that grid
+  // (no-op without a programmatic dependency), then let the next grid's CTAs
+  // start their own set-up wherever an SM becomes free.
+  griddep_wait();
+  griddep_launch_dependents();
+
+  // ---------------------------------------------------------------- tile sequence
+  const int first_tile = cluster_id < num_tiles ? cluster_id : -1;
+  const uint32_t sched_empty_leader0 = (C::CG == 2) ? mapa_shared(sched_empty_bar(0), 0) : sched_empty_bar(0);
+  // The tile after tile t, the k-th (k = 0, 1, ...) of this CTA's sequence, or
+  // -1 when there is none.  Called by one thread of each role, in order k.
+  auto next_tile = [&](int t, int k, bool& ok) -> int {
+    if (!ok) return -1;
+    if (p.sched == kSchedStatic) {
+      const int n = t + num_clusters;
+      return n < num_tiles ? n : -1;
+    }
+    if (p.sched == kSchedSingle) return -1;
+    const int j = k % C::SCHED_SLOTS;
+    const uint32_t ph = static_cast<uint32_t>(k / C::SCHED_SLOTS) & 1u;
+    if (!mbar_wait(sched_full_bar(j), ph, tmo, abort_flag)) {
+      ok = false;
+      return -1;
+    }
+    // decoded into a register before the slot is handed back for the next answer
+    const int x = clc_first_ctaid_x(ld_shared_v4(sResp + 16u * static_cast<uint32_t>(j)));
+    mbar_arrive_cluster(sched_empty_leader0 + 8u * static_cast<uint32_t>(j));
+    return x < 0 ? -1 : x / C::CG;
+  };
+  // Dynamic schedule, the leader's producer lane at the start of its k-th tile:
+  // ask for the tile after it, answered into slot k % SCHED_SLOTS of every CTA
+  // once all readers of that slot's previous answer are done with it.
+  auto request_tile = [&](int k) -> bool {
+    const int j = k % C::SCHED_SLOTS;
+    const uint32_t ph = static_cast<uint32_t>(k / C::SCHED_SLOTS) & 1u;
+    if (!mbar_wait(sched_empty_bar(j), ph ^ 1u, tmo, abort_flag)) return false;
+#pragma unroll
+    for (int r = 0; r < C::CG; ++r)
+      mbar_arrive_expect_tx_cluster(C::CG == 2 ? mapa_shared(sched_full_bar(j), static_cast<uint32_t>(r))
+                                               : sched_full_bar(j),
+                                    16u);
+    clc_try_cancel_multicast(sResp + 16u * static_cast<uint32_t>(j), sched_full_bar(j));
+    return true;
+  };
+  // The same for a whole warp: lane 0 reads the ring, the others follow.
+  auto next_tile_warp = [&](int t, int k, bool& ok) -> int {
+    bool okl = ok;
+    int n = -1;
+    if (lane == 0) n = next_tile(t, k, okl);
+    n = __shfl_sync(0xffffffffu, n, 0);
+    ok = __shfl_sync(0xffffffffu, okl ? 1 : 0, 0) != 0;
+    return n;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ LOAD
@@ -291,7 +378,12 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
       uint32_t phase = 0;
       bool ok = true;
       bool first = true;
-      for (int t = cluster_id; t < num_tiles && ok; t += num_clusters) {
+      int k = 0;
+      for (int t = first_tile; t >= 0 && ok; t = next_tile(t, k, ok), ++k) {
+        if (p.sched == kSchedDynamic && rank == 0 && !request_tile(k)) {
+          ok = false;
+          break;
+        }
         int tm, tn;
         order.coord(t, tm, tn);
         const int a_row = tm * (C::BM * C::CG) + static_cast<int>(rank) * C::BM;
@@ -342,7 +434,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
       uint32_t slot_phase = 0;
       bool ok = true;
       int it = 0;
-      for (int t = cluster_id; t < num_tiles && ok; t += num_clusters, ++it) {
+      for (int t = first_tile; t >= 0 && ok; t = next_tile(t, it, ok), ++it) {
         const int acc = it % C::NUM_ACC;
         const uint32_t acc_phase = (it / C::NUM_ACC) & 1;
         if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, tmo, abort_flag)) {
@@ -434,7 +526,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
     const uint32_t tempty_leader0 = (C::CG == 2) ? mapa_shared(tempty_bar(0), 0) : tempty_bar(0);
     int it = 0;
     int chunk_ctr = 0;
-    for (int t = cluster_id; t < num_tiles; t += num_clusters, ++it) {
+    bool seq_ok = true;
+    for (int t = first_tile; t >= 0; t = next_tile_warp(t, it, seq_ok), ++it) {
       int tm, tn;
       order.coord(t, tm, tn);
       const int acc = it % C::NUM_ACC;
@@ -445,6 +538,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
         break;
       }
       tc_fence_after();
+      if (p.visits != nullptr && ew == 0 && lane == 0 && rank == 0) atomicAdd(p.visits + t, 1u);
       const int row0 = tm * (C::BM * C::CG) + static_cast<int>(rank) * C::BM + quad * 32;
       const int col0 = tn * C::BN;
       const uint32_t t_row =
@@ -514,6 +608,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
         }
       }
     }
+    if (!seq_ok && lane == 0) record_timeout(p.status, kRoleEpilogue, abort_flag);
     if (lane == 0) bulk_wait_group<0>();
     __syncwarp();
   } else if (warp < 2 + C::EPI_WARPS + C::SF_WARPS) {
@@ -599,13 +694,21 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
         return true;
       };
       if constexpr (C::SF_SMEM) {
-        // the scales are already on chip: read each step's just before writing it
+        // the scales are already on chip: read each step's just before writing it.  Step s is
+        // K stage kb of the k-th tile of the sequence, s = k * num_kb + kb; this group takes the
+        // steps with s % SF_GROUPS == sgroup.
         uint4 v0[1 + G];
-        for (int s_ = sgroup; s_ < steps && ok; s_ += C::SF_GROUPS) {
-          ok = fetch_smem(s_, v0);
-          if (!ok) break;
-          ok = put(s_, v0);
+        int k = 0;
+        for (int t = first_tile; t >= 0 && ok; t = next_tile_warp(t, k, ok), ++k) {
+          for (int kb = 0; kb < p.num_kb && ok; ++kb) {
+            const int s_ = k * p.num_kb + kb;
+            if (s_ % C::SF_GROUPS != sgroup) continue;
+            ok = fetch_smem(s_, v0);
+            if (!ok) break;
+            ok = put(s_, v0);
+          }
         }
+        (void)steps;
       } else if constexpr (C::SF_GROUPS == 1) {
         // two register sets, so that the loads of step s + 2 fly while step s waits for its slot
         uint4 v0[1 + G], v1[1 + G];

@@ -159,10 +159,60 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
   }
 }
 
+// Arrive on a barrier at a shared::cluster address (own or peer CTA) and add
+// `bytes` to the transactions its current phase waits for.
+__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t cluster_bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_bar), "r"(bytes)
+               : "memory");
+}
+
 // ---------------------------------------------------------------- proxies / fences
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- launch overlap and tile scheduling
+
+// Programmatic dependent launch.  `griddep_wait` returns once every grid this
+// one was made dependent on has completed and its memory operations are
+// visible (immediately when there is none); `griddep_launch_dependents` lets
+// the grid launched after this one start its CTAs (and their prologue) on
+// SMs this grid no longer occupies, once every CTA of this grid has said so.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Cluster launch control: ask the hardware to cancel the launch of a cluster
+// of this grid that has not started yet.  The 16-byte answer is written to the
+// shared-memory address `resp` of every CTA of the issuing cluster and
+// completes 16 transaction bytes on the barrier at offset `bar` of each.
+__device__ __forceinline__ void clc_try_cancel_multicast(uint32_t resp, uint32_t bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.multicast::cluster::all.b128 "
+      "[%0], [%1];" ::"r"(resp),
+      "r"(bar)
+      : "memory");
+}
+
+// Decode an answer: the x index of the first CTA of the cancelled cluster, or
+// -1 if the request cancelled nothing (every cluster has started).
+__device__ __forceinline__ int clc_first_ctaid_x(uint4 r) {
+  const uint64_t lo = static_cast<uint64_t>(r.x) | (static_cast<uint64_t>(r.y) << 32);
+  const uint64_t hi = static_cast<uint64_t>(r.z) | (static_cast<uint64_t>(r.w) << 32);
+  uint32_t ok, x;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b128 q;\n\t"
+      "mov.b128 q, {%2, %3};\n\t"
+      "mov.u32 %1, 0;\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, q;\n\t}"
+      : "=r"(ok), "=r"(x)
+      : "l"(lo), "l"(hi)
+      : "memory");
+  return ok ? static_cast<int>(x) : -1;
 }
 
 // ---------------------------------------------------------------- TMA

@@ -283,6 +283,11 @@ WORKLOADS = {
                  "FP8 e4m3 GEMM M=N=K=8192, per-tensor scale to amax=448, bf16 out"),
         Workload("nvfp4_16384", "nvfp4", 16384, 16384, 16384, "normal", 1005, 2005,
                  "NVFP4 GEMM M=N=K=16384, e2m1 + e4m3 per-16 scale + fp32 global, bf16 out"),
+    ] + [
+        # the K sweep of the persistent-grid study ("Persistent Grid Launch", Table 2): M = N = 4096
+        Workload(f"bf16_4096_k{k}", "bf16", 4096, 4096, k, "normal_sqrtk", 1020 + i, 2020 + i,
+                 f"bf16 GEMM M=N=4096 K={k}, N(0,1)/sqrt(K) entries, fp32 accumulate, bf16 out")
+        for i, k in enumerate((64, 128, 256, 512, 1024))
     ]
 }
 

@@ -31,6 +31,14 @@ TKG_OPT_TIMEOUT_NS = 1
 TKG_OPT_GROUP_M = 2
 TKG_OPT_VARIANT = 3
 TKG_OPT_MAX_CTAS = 4
+TKG_OPT_LAUNCH_OVERLAP = 5
+TKG_OPT_SCHEDULE = 6
+
+TKG_OVERLAP_ON = 1
+TKG_OVERLAP_OFF = 2
+TKG_SCHEDULE_STATIC = 1
+TKG_SCHEDULE_DYNAMIC = 2
+TKG_SCHEDULE_SINGLE = 3
 
 KIND_BF16, KIND_FP8, KIND_NVFP4 = 0, 1, 2
 
@@ -77,6 +85,8 @@ lib.tkg_debug_pick_variant.argtypes = [_i32, _i64, _i64, _i64]
 lib.tkg_debug_pick_variant.restype = _i32
 lib.tkg_debug_set_fault.argtypes = [_i32]
 lib.tkg_debug_set_fault.restype = _i32
+lib.tkg_debug_set_visit_counter.argtypes = [_vp]
+lib.tkg_debug_set_visit_counter.restype = _i32
 lib.tkg_debug_tma_swizzle_probe.argtypes = [_i32, _vp, _vp, _vp]
 lib.tkg_debug_tma_swizzle_probe.restype = _i32
 lib.tkg_debug_mma_probe.argtypes = [_i32, _i32, _i32, _vp, _vp, _vp, _vp, ctypes.POINTER(ctypes.c_int32), _vp, _vp]
@@ -198,6 +208,12 @@ def tkg_debug_pick_variant(kind, M, N, K) -> int:
 
 def tkg_debug_set_fault(mode: int) -> None:
     _check(lib.tkg_debug_set_fault(mode), "tkg_debug_set_fault")
+
+
+def tkg_debug_set_visit_counter(counts) -> None:
+    """Count tile visits of the next GEMM launch into `counts` (zeroed
+    uint32/int32 device array, one word per output tile); None disables."""
+    _check(lib.tkg_debug_set_visit_counter(_addr(counts)), "tkg_debug_set_visit_counter")
 
 
 def tkg_debug_tma_swizzle_probe(s_bytes, src, dst, stream=None) -> int:
