@@ -316,7 +316,8 @@ tkg_status gemm_launch(int kind, int64_t M, int64_t N, int64_t K, const void* A,
     }
     if (nvfp4_interleave_scales(scales->a_block_scale, scales->b_block_scale, static_cast<int>(M),
                                 static_cast<int>(N), static_cast<int>(K), p.sf_blocks_a, p.sf_blocks_b, p.num_kb,
-                                v->sf_mode, scratch, b_off, cs) != cudaSuccess) {
+                                v->sf_mode, scratch, b_off, cs,
+                                opt_or(g_opt_overlap, TKG_OVERLAP_ON) == TKG_OVERLAP_ON) != cudaSuccess) {
       cudaGetLastError();
       cudaFreeAsync(scratch, cs);
       return TKG_ERR_CUDA;

@@ -69,6 +69,10 @@ struct InterleaveArgs {
 // past the matrix are written as 0.  Either layout keeps each (K stage, block)
 // in its own 2 KB run.
 __global__ void __launch_bounds__(256) interleave_scales_kernel(InterleaveArgs a, InterleaveArgs b, int blocks_a) {
+  // launched as a programmatic dependent: the previous GEMM may still read the
+  // scratch this kernel rewrites, or a previous kernel still write the scales
+  griddep_wait();
+  griddep_launch_dependents();
   const bool is_a = static_cast<int>(blockIdx.x) < blocks_a;
   const InterleaveArgs& s = is_a ? a : b;
   const int local = is_a ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x) - blocks_a;
@@ -104,7 +108,7 @@ __global__ void __launch_bounds__(256) interleave_scales_kernel(InterleaveArgs a
 // Returns the byte offset of B's atoms inside `scratch`.
 cudaError_t nvfp4_interleave_scales(const uint8_t* sfa, const uint8_t* sfb, int M, int N, int K, int blocks_a,
                                     int blocks_b, int kstages, int sf_mode, uint8_t* scratch, size_t b_offset,
-                                    cudaStream_t stream) {
+                                    cudaStream_t stream, bool overlap) {
   const int rows_a = sf_mode == kSfWarps || sf_mode == kSfHybrid ? 1 : 0;
   const int rows_b = sf_mode == kSfWarps ? 1 : 0;
   InterleaveArgs a{sfa, scratch, M, K / 16, blocks_a, kstages, rows_a};
@@ -112,8 +116,16 @@ cudaError_t nvfp4_interleave_scales(const uint8_t* sfa, const uint8_t* sfb, int 
   const int kpairs = (kstages + 1) / 2;
   const int grid_a = blocks_a * kpairs;
   const int grid_b = blocks_b * kpairs;
-  interleave_scales_kernel<<<grid_a + grid_b, 256, 0, stream>>>(a, b, grid_a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid_a + grid_b), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, interleave_scales_kernel, a, b, grid_a);
 }
 
 size_t nvfp4_scratch_bytes(int blocks_a, int blocks_b, int kstages) {

@@ -176,7 +176,7 @@ extern "C" tkg_status tkg_gemm_nvfp4_noalloc(int64_t M, int64_t N, int64_t K, co
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (nvfp4_interleave_scales(scales->a_block_scale, scales->b_block_scale, static_cast<int>(M), static_cast<int>(N),
                               static_cast<int>(K), p.sf_blocks_a, p.sf_blocks_b, p.num_kb, v->sf_mode, scratch,
-                              b_off, cs) != cudaSuccess) {
+                              b_off, cs, false) != cudaSuccess) {
     cudaGetLastError();
     return TKG_ERR_CUDA;
   }

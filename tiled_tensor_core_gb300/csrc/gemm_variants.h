@@ -28,10 +28,11 @@ const KernelVariant* nvfp4_variant(int id);
 // NVFP4: rewrite row-major [rows][K/16] block scales of A and B into the
 // 2 KB per (K stage, 128-row block) runs the GEMM stages (A's at scratch, B's
 // at scratch + b_offset), laid out for the variant's `sf_mode`.  One kernel
-// launch on `stream`.
+// launch on `stream`, as a programmatic dependent of the previous kernel if
+// `overlap` (it waits for that kernel before touching memory either way).
 cudaError_t nvfp4_interleave_scales(const uint8_t* sfa, const uint8_t* sfb, int M, int N, int K, int blocks_a,
                                     int blocks_b, int kstages, int sf_mode, uint8_t* scratch, size_t b_offset,
-                                    cudaStream_t stream);
+                                    cudaStream_t stream, bool overlap);
 size_t nvfp4_scratch_bytes(int blocks_a, int blocks_b, int kstages);
 
 // The current device's SM count, after the library's device check (api.cu).

@@ -436,3 +436,66 @@ def permutation_operands(kind: str, M: int, K: int, seed: int, identity: bool = 
         return Operands(kind, M, N, K, pack_fp4(encode_e2m1(xa)), pack_fp4(encode_e2m1(xb)),
                         sfa, sfb, 1.0, 1.0), perm
     raise ValueError(kind)
+
+
+# ---------------------------------------------------------------- attention forward inputs
+
+@dataclasses.dataclass(frozen=True)
+class AttnWorkload:
+    """Non-causal attention forward: Q [B, H, Nq, D], K and V [B, H, Nkv, D],
+    bf16 N(0,1) entries (seeded), O [B, H, Nq, D] bf16."""
+    name: str
+    B: int
+    H: int
+    Nq: int
+    Nkv: int
+    D: int
+    seed: int
+    description: str
+
+    @property
+    def flops(self) -> float:
+        # two matrix products (Q·Kᵀ and P·V), 2 flops per multiply-add
+        return 4.0 * self.B * self.H * self.Nq * self.Nkv * self.D
+
+
+# Shapes of the pages' attention study (batch 16, 16 heads, head dim 64 / 128,
+# sequence lengths from about a thousand to several thousand).
+ATTN_WORKLOADS = {
+    w.name: w
+    for w in [
+        AttnWorkload("attn_n1024_d128", 16, 16, 1024, 1024, 128, 3001,
+                     "non-causal attention forward B=16 H=16 N=1024 D=128, bf16 N(0,1) Q/K/V, bf16 O"),
+        AttnWorkload("attn_n4096_d128", 16, 16, 4096, 4096, 128, 3002,
+                     "non-causal attention forward B=16 H=16 N=4096 D=128, bf16 N(0,1) Q/K/V, bf16 O"),
+        AttnWorkload("attn_n4096_d64", 16, 16, 4096, 4096, 64, 3003,
+                     "non-causal attention forward B=16 H=16 N=4096 D=64, bf16 N(0,1) Q/K/V, bf16 O"),
+    ]
+}
+
+
+@dataclasses.dataclass
+class AttnInputs:
+    """bf16 bit patterns (uint16) of Q [B, H, Nq, D], K and V [B, H, Nkv, D]."""
+    q: np.ndarray
+    k: np.ndarray
+    v: np.ndarray
+
+    @property
+    def shape(self):
+        B, H, Nq, D = self.q.shape
+        return B, H, Nq, self.k.shape[2], D
+
+
+def attention_inputs(B: int, H: int, Nq: int, Nkv: int, D: int, seed: int, dist: str = "normal") -> AttnInputs:
+    """Seeded bf16 Q, K, V (N(0,1) entries by default, rounded to bf16)."""
+    def one(s, n):
+        x = _draw(s, B * H * n, D, dist)
+        (bits,) = _rowwise(x, [(x.shape, np.uint16)], lambda r: (encode_bf16(r),))
+        return bits.reshape(B, H, n, D)
+    return AttnInputs(one(seed, Nq), one(seed + 1, Nkv), one(seed + 2, Nkv))
+
+
+def attn_workload_inputs(name: str) -> AttnInputs:
+    w = ATTN_WORKLOADS[name]
+    return attention_inputs(w.B, w.H, w.Nq, w.Nkv, w.D, w.seed)
