@@ -614,13 +614,190 @@ def run_e2e(ops, dev, w, args):
             "d2h_bytes_per_step": int(d2h), "ms_per_step": ms, "pipelined": "2 buffer sets, 3 streams"}
 
 
+# ---------------------------------------------------------------- attention forward
+
+ATTN_METRIC = "attention forward TFLOP/s (4·B·H·Nq·Nkv·D / t), bf16, non-causal, 1 GB300"
+ATTN_BATCH = {"attn_n1024_d128": 40, "attn_n4096_d128": 6, "attn_n4096_d64": 8}
+
+
+def attn_oracle_sample(x, w, target_s: float):
+    """The attention oracle, as it stands, on a sample of query rows of a few heads
+    (about target_s seconds).  Returns (TFLOP/s, seconds, rows, heads)."""
+    from oracle import attention as oa
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)][:: max(1, (w.B * w.H) // 8)][:8]
+    probe = np.arange(0, w.Nq, max(1, w.Nq // 16))
+    t0 = time.perf_counter()
+    oa.attention_forward(x.q, x.k, x.v, heads=heads[:1], rows=probe)
+    per_row = max(time.perf_counter() - t0, 1e-6) / len(probe)
+    n_rows = int(max(16, min(w.Nq, target_s / per_row / len(heads))))
+    rows = np.linspace(0, w.Nq - 1, n_rows).astype(np.int64)
+    t0 = time.perf_counter()
+    oa.attention_forward(x.q, x.k, x.v, heads=heads, rows=rows)
+    dt = time.perf_counter() - t0
+    flops = 4.0 * len(heads) * n_rows * w.Nkv * w.D
+    return flops / dt / 1e12, dt, n_rows, len(heads)
+
+
+def run_reference_attention(args):
+    w = synth.ATTN_WORKLOADS[args.workload]
+    x = synth.attn_workload_inputs(args.workload)
+    for _ in range(args.warmup):
+        attn_oracle_sample(x, w, 0.05)
+    times, flops = [], 0.0
+    n_rows = n_heads = 0
+    for _ in range(args.steps):
+        _, dt, n_rows, n_heads = attn_oracle_sample(x, w, args.ref_step_s)
+        times.append(dt)
+        flops += 4.0 * n_heads * n_rows * w.Nkv * w.D
+    value = flops / sum(times) / 1e12
+    line = {"impl": "reference", "metric": ATTN_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.description, "B": w.B, "H": w.H, "Nq": w.Nq, "Nkv": w.Nkv, "D": w.D},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"{n_rows} query rows x {n_heads} heads per step (numpy float64, "
+                                       "BLAS threads on all host cores)"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_attention(args, world, rank, local):
+    import torch
+    from tiled_tensor_core_gb300 import tkg
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    tkg.tkg_set_option(tkg.TKG_OPT_LAUNCH_OVERLAP,
+                       tkg.TKG_OVERLAP_ON if args.overlap == "on" else tkg.TKG_OVERLAP_OFF)
+    w = synth.ATTN_WORKLOADS[args.workload]
+    x = synth.attn_workload_inputs(args.workload)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)  # noqa: E731
+    base = {"q": t(x.q), "k": t(x.k), "v": t(x.v)}
+    per_set = sum(v.numel() * 2 for v in base.values()) + base["q"].numel() * 2
+    n_sets = 1 if per_set >= 2 * L2_BYTES else min(8, math.ceil(4 * L2_BYTES / per_set))
+    sets = []
+    for i in range(n_sets):
+        d = {k: (v if i == 0 else v.clone()) for k, v in base.items()}
+        d["o"] = torch.empty_like(d["q"])
+        d["lse"] = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
+        sets.append(d)
+    batch = args.batch or ATTN_BATCH[args.workload]
+    stream = torch.cuda.Stream(device=dev)
+    sptr = int(stream.cuda_stream)
+
+    def call(d, s):
+        tkg.tkg_attention_fwd(w.B, w.H, w.Nq, w.Nkv, w.D, d["q"], d["k"], d["v"], d["o"], d["lse"], stream=s)
+
+    def step():
+        for i in range(batch):
+            call(sets[i % n_sets], sptr)
+
+    for _ in range(args.warmup):
+        step()
+    st = tkg.tkg_check_status(sptr)
+    if st != tkg.TKG_OK:
+        raise RuntimeError(f"warm-up failed: {tkg.status_string(st)}")
+
+    spot = None
+    if rank == 0 and not args.no_check:
+        from oracle import attention as oa
+        rows = np.array([0, w.Nq // 2, w.Nq - 1])
+        ref = oa.attention_forward(x.q, x.k, x.v, heads=[(0, 0)], rows=rows)
+        d = sets[(batch - 1) % n_sets]
+        got = d["o"][0, 0][torch.from_numpy(rows).to(dev)].cpu().numpy().view(np.uint16)
+        g = oa.bf16_decode(got)
+        spot = float(np.linalg.norm(g - ref["o"][0]) / np.linalg.norm(ref["o"][0]))
+
+    sampler = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    step_ms = []
+    t0.record(stream)
+    for _ in range(args.steps):
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        step()
+        s1.record(stream)
+        s1.synchronize()
+        step_ms.append(s0.elapsed_time(s1))
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    barrier(world)
+    st = tkg.tkg_check_status(sptr)
+    if st != tkg.TKG_OK:
+        raise RuntimeError(f"timed run failed: {tkg.status_string(st)}")
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    calls = args.steps * batch
+    value = world * calls * w.flops / (total_ms * 1e-3) / 1e12
+    per_call_ms = statistics.median(step_ms) / batch
+    achieved = w.flops / (per_call_ms * 1e-3) / 1e12
+
+    e2e = None
+    if not args.no_e2e:
+        host = {k: base[k].cpu().pin_memory() for k in ("q", "k", "v")}
+        o_host = torch.empty(base["q"].shape, dtype=torch.int16).pin_memory()
+        d = sets[0]
+        h2d = sum(v.numel() * 2 for v in host.values())
+        ea = torch.cuda.Event(enable_timing=True)
+        eb = torch.cuda.Event(enable_timing=True)
+        n = max(2, args.e2e_steps // 2)
+        with torch.cuda.stream(stream):
+            ea.record(stream)
+            for _ in range(n):
+                for k in ("q", "k", "v"):
+                    d[k].copy_(host[k], non_blocking=True)
+                call(d, sptr)
+                o_host.copy_(d["o"], non_blocking=True)
+            eb.record(stream)
+        eb.synchronize()
+        ms = ea.elapsed_time(eb) / n
+        e2e = {"value": w.flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(o_host.numel() * 2), "ms_per_step": ms, "pipelined": "no (one stream)"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, dt, n_rows, n_heads = attn_oracle_sample(x, w, args.cpu_s)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{n_rows} query rows x {n_heads} heads of the same workload ({dt:.1f} s, numpy float64, "
+                         "BLAS threads on all host cores)"}
+
+    peaks = load_peaks()
+    peak = peaks["bf16_tflops_sustained"]
+    line = {
+        "metric": ATTN_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.description, "B": w.B, "H": w.H, "Nq": w.Nq, "Nkv": w.Nkv, "D": w.D,
+                   "calls_per_step": batch, "parallelism": f"replicas{world}",
+                   "l2": f"{n_sets} rotating input sets, {n_sets * per_set / 2**20:.0f} MiB > 129 MiB L2",
+                   "launch_overlap": "programmatic dependent launch" if args.overlap == "on" else "off"},
+        "median_call_ms": per_call_ms,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "frac_of_burst_peak": achieved / peaks["bf16_tflops"],
+                     "peak_source": f"{peaks['source']} bf16 sustained (back-to-back cuBLAS)"},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": calls, "clocks": clocks, "spot_check_rel_err": spot,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["tkg", "reference"], default="tkg")
-    p.add_argument("--workload", choices=sorted(synth.WORKLOADS) + sorted(ENCODERS), default="bf16_4096")
+    p.add_argument("--workload", choices=sorted(synth.WORKLOADS) + sorted(ENCODERS) + sorted(synth.ATTN_WORKLOADS),
+                   default="bf16_4096")
     p.add_argument("--batch", type=int, default=0, help="GEMMs per step (default: per workload)")
     p.add_argument("--variant", type=int, default=0)
     p.add_argument("--group-m", type=int, default=0)
@@ -641,10 +818,14 @@ def main(argv=None):
     if args.impl == "reference":
         world = int(os.environ.get("WORLD_SIZE", "1"))
         rank = int(os.environ.get("RANK", "0"))
+        if args.workload in synth.ATTN_WORKLOADS:
+            return run_reference_attention(args) if rank == 0 else 0
         return run_reference(args, world, rank)
     world, rank, local = dist_setup(args)
     if args.workload in ENCODERS:
         return run_encoder(args, world, rank, local)
+    if args.workload in synth.ATTN_WORKLOADS:
+        return run_attention(args, world, rank, local)
     return run_tkg(args, world, rank, local)
 
 

@@ -149,6 +149,25 @@ TKG_API tkg_status tkg_quantize_fp8(int64_t rows, int64_t cols, const float* x, 
 TKG_API tkg_status tkg_quantize_nvfp4(int64_t rows, int64_t cols, const float* x, uint8_t* q_packed,
                                       uint8_t* block_scales, float* global_scale, void* stream);
 
+/* Non-causal attention forward (the attention example of "ThunderKittens:
+ * Simple, Fast, and Adorable AI Kernels", "The Four Functions: Load, Compute,
+ * Store, Finish", and the attention prefill of the ThunderKittens DSL page):
+ * for every batch b < B and head h < H,
+ *   O[b,h] = softmax(Q[b,h] · K[b,h]ᵀ / sqrt(D)) · V[b,h],
+ *   lse[b,h,i] = ln Σ_j exp(Q[b,h,i]·K[b,h,j] / sqrt(D))   (if lse != NULL).
+ * Q: bf16 [B][H][Nq][D], K and V: bf16 [B][H][Nkv][D], O: bf16 [B][H][Nq][D],
+ * all contiguous row-major, 16-byte aligned device pointers; lse: fp32
+ * [B][H][Nq], 4-byte aligned, or NULL.  D = 64 or 128; Nq, Nkv >= 1 (any
+ * length); B * H <= 65535.  Scores, softmax statistics and the P·V
+ * accumulation are fp32; the probabilities enter P·V rounded to bf16; O is
+ * rounded to bf16 once.  Buffers are caller-owned; the call allocates nothing
+ * and is asynchronous on `stream` (one kernel; with TKG_OPT_LAUNCH_OVERLAP on,
+ * a programmatic dependent of the previous kernel).  Bad arguments return
+ * TKG_ERR_INVALID_ARG / TKG_ERR_MISALIGNED before any GPU work; device-side
+ * wait timeouts surface through tkg_check_status. */
+TKG_API tkg_status tkg_attention_fwd(int64_t B, int64_t H, int64_t Nq, int64_t Nkv, int64_t D, const void* Q,
+                                     const void* K, const void* V, void* O, float* lse, void* stream);
+
 /* Synchronises `stream`, then reads and clears the device status word of the
  * current device.  Returns TKG_ERR_TIMEOUT if any kernel since the last check
  * abandoned a pipeline wait (its output is then undefined), TKG_ERR_CUDA if the

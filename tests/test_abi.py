@@ -206,3 +206,16 @@ def test_quantize_arguments_checked_before_any_gpu_work(tkg):
     assert tkg.lib.tkg_quantize_fp8(4, 16, x + 4, q, s, None) == tkg.TKG_ERR_MISALIGNED
     assert tkg.lib.tkg_quantize_nvfp4(4, 16, x, q + 8, sf, s, None) == tkg.TKG_ERR_MISALIGNED
     assert tkg.lib.tkg_quantize_fp8(4, 16, x, q, s + 2, None) == tkg.TKG_ERR_MISALIGNED
+
+
+def test_attention_arguments_checked_before_any_gpu_work(tkg):
+    f = tkg.lib.tkg_attention_fwd
+    A = 1 << 12
+    assert f(1, 1, 128, 128, 96, A, A, A, A, None, None) == tkg.TKG_ERR_INVALID_ARG    # head dim
+    assert f(0, 1, 128, 128, 128, A, A, A, A, None, None) == tkg.TKG_ERR_INVALID_ARG   # empty batch
+    assert f(1, 1, 0, 128, 128, A, A, A, A, None, None) == tkg.TKG_ERR_INVALID_ARG     # no queries
+    assert f(1, 1, 128, 0, 128, A, A, A, A, None, None) == tkg.TKG_ERR_INVALID_ARG     # no keys
+    assert f(256, 256, 128, 128, 64, A, A, A, A, None, None) == tkg.TKG_ERR_INVALID_ARG  # B*H > 65535
+    assert f(1, 1, 128, 128, 64, None, A, A, A, None, None) == tkg.TKG_ERR_INVALID_ARG
+    assert f(1, 1, 128, 128, 64, A + 8, A, A, A, None, None) == tkg.TKG_ERR_MISALIGNED
+    assert f(1, 1, 128, 128, 64, A, A, A, A, A + 2, None) == tkg.TKG_ERR_MISALIGNED   # lse alignment

@@ -567,6 +567,39 @@ tkg_status device_sm_count(int* out) {
   if (st == TKG_OK) *out = d->sm_count;
   return st;
 }
+
+tkg_status device_status_word(unsigned int** out) {
+  DevState* d = nullptr;
+  const tkg_status st = current_device(&d);
+  if (st == TKG_OK) *out = d->status;
+  return st;
+}
+
+tkg_status encode_tiled_map(CUtensorMap* out, CUtensorMapDataType dtype, int rank, const void* ptr,
+                            const uint64_t* dims, const uint64_t* strides, const uint32_t* box, int swz) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    const tkg_status st = ensure_encode_locked();
+    if (st != TKG_OK) return st;
+  }
+  CUtensorMapSwizzle sw = swz == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                          : swz == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                          : swz == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                      : CU_TENSOR_MAP_SWIZZLE_NONE;
+  cuuint64_t d[5], st[4];
+  cuuint32_t b[5], e[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    e[i] = 1;
+    if (i + 1 < rank) st[i] = strides[i];
+  }
+  std::memset(out, 0, sizeof(*out));
+  const CUresult r = g_encode(out, dtype, static_cast<cuuint32_t>(rank), const_cast<void*>(ptr), d, st, b, e,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? TKG_OK : TKG_ERR_INVALID_ARG;
+}
 }  // namespace tkg
 
 // Address of the current device's status word, without any other per-device

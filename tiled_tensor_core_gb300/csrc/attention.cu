@@ -1,0 +1,464 @@
+// attention.cu — non-causal attention forward on sm_103a:
+//   O[b,h] = softmax(Q[b,h] · K[b,h]ᵀ / √D) · V[b,h],  bf16 in and out, fp32
+//   scores, softmax statistics and accumulation, plus the log-sum-exp of every
+//   score row.
+//
+// The attention example of "ThunderKittens: Simple, Fast, and Adorable AI
+// Kernels" ("The Four Functions: Load, Compute, Store, Finish"; Figure 5) and
+// the attention prefill of the ThunderKittens DSL page ("Реальный пример:
+// attention prefill") use the same template as the GEMM: one warp loads K and
+// V tiles through a shared-memory ring while compute workers run Q·Kᵀ, an
+// online softmax (subtract the running row maximum, exponentiate, keep the
+// running row sum), a conversion of the probabilities to bf16 and P·V; the
+// finish step divides by the row sum and stores O.  Q stays in shared memory
+// for the whole task.  Re-cast for tcgen05:
+//   warp 0, one lane   LOAD     TMA (3-D maps over [B·H][N][D]) of the Q tile
+//                               once and of K_j, V_j into two STAGES-deep rings
+//   warp 1, one lane   COMPUTE  S_j = Q·K_jᵀ into one of two TMEM score
+//                               buffers; O += P_j·V_j into a TMEM accumulator
+//                               (V read as an MN-major operand)
+//   warps 2-5          SOFTMAX  one thread per query row (its TMEM lane): scores
+//                      / FINISH from TMEM, running max and sum, P_j (bf16) into
+//                               a 128-byte-swizzled shared tile, rescale of the
+//                               row's O when its maximum grew; at the end
+//                               O / l to bf16 and a TMA store, and the log-sum-exp
+// Order of the tensor-core work: S_0, S_1, PV_0, S_2, PV_1, ...: the next score
+// tile is computed while the softmax warps work on the current one.  Every wait
+// is bounded (TKG_OPT_TIMEOUT_NS) and reported through the status word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "gemm_variants.h"
+#include "tkg.h"
+
+namespace tkg {
+namespace {
+
+struct AttnParams {
+  CUtensorMap tmap_q;  // [B·H][Nq][D] bf16, box 64 x 128 x 1, 128-byte swizzle
+  CUtensorMap tmap_k;  // [B·H][Nkv][D]
+  CUtensorMap tmap_v;
+  CUtensorMap tmap_o;  // [B·H][Nq][D], box 64 x 32 x 1
+  float* lse;          // [B·H][Nq] fp32 or null
+  unsigned int* status;
+  unsigned long long timeout_ns;
+  int Nq, Nkv;
+  float scale_log2;  // log2(e) / sqrt(D): scores enter exp2 pre-multiplied by it
+  float scale;       // 1 / sqrt(D)
+};
+
+template <int D>
+struct AttnCfg {
+  static constexpr int BQ = 128;             // query rows per CTA (TMEM lanes)
+  static constexpr int BKV = 128;            // keys per tile
+  static constexpr int DC = D / 64;          // 128-byte column chunks of a Q/K/V row
+  static constexpr int CHUNK = 128 * 128;    // [128 rows][128 B] swizzled tile
+  static constexpr int STAGES = D == 128 ? 2 : 3;
+  static constexpr int KV_STAGE = DC * CHUNK;
+  static constexpr int Q_BYTES = DC * CHUNK;
+  static constexpr int P_BYTES = (BKV / 64) * CHUNK;  // bf16 P tile, K-major
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + STAGES * KV_STAGE;
+  static constexpr int OFF_Q = OFF_V + STAGES * KV_STAGE;
+  static constexpr int OFF_P = OFF_Q + Q_BYTES;  // also the output staging at the end
+  static constexpr int OFF_BAR = OFF_P + P_BYTES;
+  static constexpr int NUM_BARS = 1 + 4 * STAGES + 2 + 2 + 1 + 1 + 1;
+  static constexpr int OFF_MISC = OFF_BAR + 8 * NUM_BARS;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  static constexpr int THREADS = 192;
+  // TMEM columns: two score buffers, then the output accumulator
+  static constexpr uint32_t T_S0 = 0, T_S1 = 128, T_O = 256;
+  static constexpr uint32_t TMEM_COLS = 512;
+  // S = Q·Kᵀ: M = 128, N = BKV, both K-major;  O += P·V: M = 128, N = D, V MN-major (bit 16)
+  static constexpr uint32_t IDESC_S = idesc_dense(kFmtBF16, BQ, BKV);
+  static constexpr uint32_t IDESC_PV = idesc_dense(kFmtBF16, BQ, D) | (1u << 16);
+  static_assert(D == 64 || D == 128, "head dimension 64 or 128");
+  static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB shared-memory limit");
+  // more than half of the SM's shared memory: one CTA per SM, so the 512-column
+  // TMEM allocation never waits for another CTA of this kernel
+  static_assert(SMEM_BYTES > 116 * 1024, "one CTA per SM");
+};
+
+constexpr int kRoleLoad = 0, kRoleMma = 1, kRoleSoftmax = 2;
+
+__device__ __forceinline__ void attn_timeout(unsigned int* status, int role, volatile int* abort_flag) {
+  atomicOr(status, 1u | (1u << (8 + role)));
+  *abort_flag = 1;
+}
+
+template <int D>
+__global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
+  using C = AttnCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sQ = sbase + C::OFF_Q, sP = sbase + C::OFF_P;
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  const uint32_t q_full = bar0;
+  auto k_full = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto k_empty = [&](int s) { return bar0 + 8u * (1 + C::STAGES + s); };
+  auto v_full = [&](int s) { return bar0 + 8u * (1 + 2 * C::STAGES + s); };
+  auto v_empty = [&](int s) { return bar0 + 8u * (1 + 3 * C::STAGES + s); };
+  auto s_full = [&](int b) { return bar0 + 8u * (1 + 4 * C::STAGES + b); };
+  auto s_empty = [&](int b) { return bar0 + 8u * (3 + 4 * C::STAGES + b); };
+  const uint32_t p_full = bar0 + 8u * (5 + 4 * C::STAGES);
+  const uint32_t o_ready = bar0 + 8u * (6 + 4 * C::STAGES);
+  const uint32_t drain = bar0 + 8u * (7 + 4 * C::STAGES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  volatile int* never_abort = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int q0 = static_cast<int>(blockIdx.x) * C::BQ;
+  const int bh = static_cast<int>(blockIdx.y);
+  const int nkv = (p.Nkv + C::BKV - 1) / C::BKV;
+  const uint64_t tmo = p.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(k_full(s), 1);
+      mbar_init(k_empty(s), 1);
+      mbar_init(v_full(s), 1);
+      mbar_init(v_empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s_full(b), 1);
+      mbar_init(s_empty(b), 4);  // one arrival per softmax warp
+    }
+    mbar_init(p_full, 4);
+    mbar_init(o_ready, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    *never_abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&p.tmap_q);
+    tma_prefetch_desc(&p.tmap_k);
+    tma_prefetch_desc(&p.tmap_v);
+    tma_prefetch_desc(&p.tmap_o);
+  }
+  if (warp == 1) {
+    tmem_alloc<1>(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish<1>();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  // the previous kernel on the stream may still be writing Q, K, V or reading O
+  griddep_wait();
+  griddep_launch_dependents();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ LOAD
+    if (lane == 0) {
+      bool ok = true;
+      mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+#pragma unroll
+      for (int c = 0; c < C::DC; ++c) tma_load_3d(sQ + c * C::CHUNK, &p.tmap_q, q_full, 64 * c, q0, bh);
+      for (int j = 0; j < nkv && ok; ++j) {
+        const int st = j % C::STAGES;
+        const uint32_t ph = static_cast<uint32_t>(j / C::STAGES) & 1u;
+        if (!mbar_wait(k_empty(st), ph ^ 1u, tmo, abort_flag)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(k_full(st), C::KV_STAGE);
+#pragma unroll
+        for (int c = 0; c < C::DC; ++c)
+          tma_load_3d(sK + st * C::KV_STAGE + c * C::CHUNK, &p.tmap_k, k_full(st), 64 * c, j * C::BKV, bh);
+        if (!mbar_wait(v_empty(st), ph ^ 1u, tmo, abort_flag)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(v_full(st), C::KV_STAGE);
+#pragma unroll
+        for (int c = 0; c < C::DC; ++c)
+          tma_load_3d(sV + st * C::KV_STAGE + c * C::CHUNK, &p.tmap_v, v_full(st), 64 * c, j * C::BKV, bh);
+      }
+      if (!ok) {
+        attn_timeout(p.status, kRoleLoad, abort_flag);
+        const uint64_t t0 = globaltimer_ns();  // let issued copies land before the CTA leaves
+        while (globaltimer_ns() - t0 < 50000ull) {
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ COMPUTE
+    if (lane == 0) {
+      bool ok = mbar_wait(q_full, 0, tmo, abort_flag);
+      tc_fence_after();
+      // O += P_i · V_i once the softmax warps have written P_i (and rescaled O)
+      auto pv = [&](int i) -> bool {
+        if (!mbar_wait(p_full, static_cast<uint32_t>(i) & 1u, tmo, abort_flag)) return false;
+        const int st = i % C::STAGES;
+        if (!mbar_wait(v_full(st), static_cast<uint32_t>(i / C::STAGES) & 1u, tmo, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t v0 = sV + st * C::KV_STAGE;
+#pragma unroll
+        for (int kk = 0; kk < C::BKV / 16; ++kk) {
+          // A: P rows, 16 keys = 32 bytes of a 128-byte swizzled row; B: 16 rows of V (keys), D columns
+          const uint64_t ad = sdesc_sw128(sP + (kk / 4) * C::CHUNK + 32u * (kk % 4));
+          const uint64_t bd = sdesc_sw128_mn(v0 + 2048u * kk, C::CHUNK);
+          mma_bf16<1>(tmem_base + C::T_O, ad, bd, C::IDESC_PV, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit_local(o_ready);
+        mma_commit_local(v_empty(st));
+        return true;
+      };
+      for (int j = 0; j < nkv && ok; ++j) {
+        const int st = j % C::STAGES;
+        const int sb = j & 1;
+        if (!mbar_wait(k_full(st), static_cast<uint32_t>(j / C::STAGES) & 1u, tmo, abort_flag) ||
+            !mbar_wait(s_empty(sb), (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, tmo, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t k0 = sK + st * C::KV_STAGE;
+        const uint32_t t_s = tmem_base + (sb ? C::T_S1 : C::T_S0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t ad = sdesc_sw128(sQ + (kk / 4) * C::CHUNK + 32u * (kk % 4));
+          const uint64_t bd = sdesc_sw128(k0 + (kk / 4) * C::CHUNK + 32u * (kk % 4));
+          mma_bf16<1>(t_s, ad, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
+        }
+        mma_commit_local(s_full(sb));
+        mma_commit_local(k_empty(st));
+        if (j >= 1 && !pv(j - 1)) {
+          ok = false;
+          break;
+        }
+      }
+      if (ok && nkv > 0) ok = pv(nkv - 1);
+      // no MMA may still be writing TMEM when it is released
+      mma_commit_local(drain);
+      mbar_wait(drain, 0, tmo, never_abort);
+      if (!ok) attn_timeout(p.status, kRoleMma, abort_flag);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ SOFTMAX / FINISH
+    const int quad = warp & 3;  // TMEM lane quarter this warp may access
+    const int r = quad * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const float c2 = p.scale_log2;
+    float m = -INFINITY;  // running maximum of the raw scores of this row
+    float l = 0.0f;       // running sum of exp2((s - m) * c2)
+    bool ok = true;
+    for (int j = 0; j < nkv; ++j) {
+      const int sb = j & 1;
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait<true>(s_full(sb), static_cast<uint32_t>(j >> 1) & 1u, tmo, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t s[4][32];
+      const uint32_t t_s = tmem_base + lane_off + (sb ? C::T_S1 : C::T_S0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tmem_ld_32x32b_x32(t_s + 32u * q, s[q]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int q = 0; q < 4; ++q) reg_fence(s[q]);
+      // the scores are in registers: the buffer can take S_{j+2}
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_local(s_empty(sb));
+
+      const int valid = p.Nkv - j * C::BKV;  // keys of this tile inside the sequence (>= 1)
+      float mt = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (32 * q + i < valid) mt = fmaxf(mt, __uint_as_float(s[q][i]));
+      const float m_new = fmaxf(m, mt);
+      const float neg = -m_new * c2;
+      const float alpha = ex2_approx((m - m_new) * c2);  // 0 on the first tile (m = -inf)
+      float lt = 0.0f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int c = 32 * q + 2 * i;
+          const float x0 = c < valid ? ex2_approx(fmaf(__uint_as_float(s[q][2 * i]), c2, neg)) : 0.0f;
+          const float x1 = c + 1 < valid ? ex2_approx(fmaf(__uint_as_float(s[q][2 * i + 1]), c2, neg)) : 0.0f;
+          lt += x0;
+          lt += x1;
+          pk[16 * q + i] = pack_bf16x2(x0, x1);
+        }
+      l = l * alpha + lt;
+      m = m_new;
+
+      if (j >= 1) {
+        // P_{j-1} · V_{j-1} has finished: the P tile may be overwritten and O rescaled
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait<true>(o_ready, static_cast<uint32_t>(j - 1) & 1u, tmo, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+#pragma unroll
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t o[32];
+            const uint32_t t_o = tmem_base + lane_off + C::T_O + 32u * q;
+            tmem_ld_32x32b_x32(t_o, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st_32x32b_x32(t_o, o);
+          }
+          tmem_wait_st();
+        }
+      }
+      // P row r: 128 bf16 = two 128-byte rows of the two swizzled K-major chunks
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t off = swizzle_offset(static_cast<uint32_t>(r) * 128u + 16u * u, 128u);
+          const int w = 32 * ch + 4 * u;
+          st_shared_v4(sP + ch * C::CHUNK + off, pk[w], pk[w + 1], pk[w + 2], pk[w + 3]);
+        }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_local(p_full);
+    }
+    if (ok && nkv > 0 &&
+        !__all_sync(0xffffffffu,
+                    mbar_wait<true>(o_ready, static_cast<uint32_t>(nkv - 1) & 1u, tmo, abort_flag)))
+      ok = false;
+    if (ok) {
+      // FINISH: O / l to bf16, staged per warp ([32 rows][128 B] per 64 columns) in the P tile
+      tc_fence_after();
+      const float inv = 1.0f / l;
+      const uint32_t stg = sP + static_cast<uint32_t>(quad * C::DC * 4096);
+#pragma unroll
+      for (int q = 0; q < D / 32; ++q) {
+        uint32_t o[32];
+        tmem_ld_32x32b_x32(tmem_base + lane_off + C::T_O + 32u * q, o);
+        tmem_wait_ld();
+        uint32_t ob[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) ob[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+        const uint32_t chunk = stg + static_cast<uint32_t>(q / 2) * 4096u;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t off = swizzle_offset(static_cast<uint32_t>(lane) * 128u + 16u * (4 * (q % 2) + u), 128u);
+          st_shared_v4(chunk + off, ob[4 * u], ob[4 * u + 1], ob[4 * u + 2], ob[4 * u + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+#pragma unroll
+        for (int c = 0; c < C::DC; ++c) tma_store_3d(&p.tmap_o, stg + c * 4096u, 64 * c, q0 + quad * 32, bh);
+        bulk_commit_group();
+        bulk_wait_group<0>();
+      }
+      if (p.lse != nullptr && q0 + r < p.Nq)
+        p.lse[static_cast<size_t>(bh) * p.Nq + q0 + r] = m * p.scale + logf(l);
+    } else if (lane == 0) {
+      attn_timeout(p.status, kRoleSoftmax, abort_flag);
+    }
+    __syncwarp();
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<1>(tmem_base, C::TMEM_COLS);
+  }
+}
+
+template <int D>
+tkg_status attn_launch(int64_t BH, int64_t Nq, int64_t Nkv, const void* Q, const void* K, const void* V, void* O,
+                       float* lse, cudaStream_t stream, unsigned long long timeout_ns, bool overlap) {
+  using C = AttnCfg<D>;
+  AttnParams p;
+  std::memset(&p, 0, sizeof(p));
+  const uint64_t row_bytes = static_cast<uint64_t>(D) * 2;
+  const uint64_t dq[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(Nq), static_cast<uint64_t>(BH)};
+  const uint64_t dk[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(Nkv), static_cast<uint64_t>(BH)};
+  const uint64_t sq[2] = {row_bytes, row_bytes * static_cast<uint64_t>(Nq)};
+  const uint64_t sk[2] = {row_bytes, row_bytes * static_cast<uint64_t>(Nkv)};
+  const uint32_t box_in[3] = {64, 128, 1};
+  const uint32_t box_out[3] = {64, 32, 1};
+  tkg_status st = encode_tiled_map(&p.tmap_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, Q, dq, sq, box_in, 128);
+  if (st == TKG_OK) st = encode_tiled_map(&p.tmap_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, K, dk, sk, box_in, 128);
+  if (st == TKG_OK) st = encode_tiled_map(&p.tmap_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, V, dk, sk, box_in, 128);
+  if (st == TKG_OK) st = encode_tiled_map(&p.tmap_o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, O, dq, sq, box_out, 128);
+  if (st != TKG_OK) return st;
+  st = device_status_word(&p.status);
+  if (st != TKG_OK) return st;
+  p.lse = lse;
+  p.timeout_ns = timeout_ns;
+  p.Nq = static_cast<int>(Nq);
+  p.Nkv = static_cast<int>(Nkv);
+  p.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
+  p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+
+  // the shared-memory opt-in is per device: set it once on each
+  static std::atomic<uint64_t> attr_set{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return TKG_ERR_CUDA;
+  }
+  if (!(attr_set.load() & (1ull << dev))) {
+    if (cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return TKG_ERR_CUDA;
+    }
+    attr_set.fetch_or(1ull << dev);
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>((Nq + C::BQ - 1) / C::BQ), static_cast<unsigned>(BH), 1);
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, attn_fwd_kernel<D>, p) != cudaSuccess) {
+    cudaGetLastError();
+    return TKG_ERR_CUDA;
+  }
+  return TKG_OK;
+}
+
+}  // namespace
+}  // namespace tkg
+
+extern "C" tkg_status tkg_attention_fwd(int64_t B, int64_t H, int64_t Nq, int64_t Nkv, int64_t D, const void* Q,
+                                        const void* K, const void* V, void* O, float* lse, void* stream) {
+  using namespace tkg;
+  const int64_t kMax = 0x7FFFFFFF;
+  if (B < 1 || H < 1 || Nq < 1 || Nkv < 1 || Nq > kMax || Nkv > kMax) return TKG_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return TKG_ERR_INVALID_ARG;
+  if (B * H > 65535 || (Nq + 127) / 128 > kMax) return TKG_ERR_INVALID_ARG;  // grid y limit
+  if (!Q || !K || !V || !O) return TKG_ERR_INVALID_ARG;
+  auto a16 = [](const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; };
+  if (!a16(Q) || !a16(K) || !a16(V) || !a16(O) || (reinterpret_cast<uintptr_t>(lse) & 3u)) return TKG_ERR_MISALIGNED;
+  const unsigned long long tmo = static_cast<unsigned long long>(tkg_get_option(TKG_OPT_TIMEOUT_NS));
+  const bool overlap = tkg_get_option(TKG_OPT_LAUNCH_OVERLAP) == TKG_OVERLAP_ON;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return D == 128 ? attn_launch<128>(B * H, Nq, Nkv, Q, K, V, O, lse, s, tmo, overlap)
+                  : attn_launch<64>(B * H, Nq, Nkv, Q, K, V, O, lse, s, tmo, overlap);
+}

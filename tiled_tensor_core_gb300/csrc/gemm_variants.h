@@ -37,5 +37,12 @@ size_t nvfp4_scratch_bytes(int blocks_a, int blocks_b, int kstages);
 
 // The current device's SM count, after the library's device check (api.cu).
 tkg_status device_sm_count(int* out);
+// The current device's status word (device address), after the same check.
+tkg_status device_status_word(unsigned int** out);
+// A tiled TMA tensor map of `rank` dimensions (innermost first): element
+// counts `dims`, byte strides of dimensions 1.. in `strides`, box `box`,
+// swizzle 0/32/64/128 bytes; zero fill out of bounds.
+tkg_status encode_tiled_map(CUtensorMap* out, CUtensorMapDataType dtype, int rank, const void* ptr,
+                            const uint64_t* dims, const uint64_t* strides, const uint32_t* box, int swz);
 
 }  // namespace tkg

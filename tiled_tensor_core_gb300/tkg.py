@@ -63,6 +63,8 @@ for _name in ("tkg_gemm_bf16", "tkg_gemm_fp8", "tkg_gemm_nvfp4", "tkg_gemm_nvfp4
     _f = getattr(lib, _name)
     _f.argtypes = [_i64, _i64, _i64, _vp, _vp, _vp, ctypes.POINTER(tkg_scales), _vp]
     _f.restype = _i32
+lib.tkg_attention_fwd.argtypes = [_i64, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp]
+lib.tkg_attention_fwd.restype = _i32
 lib.tkg_check_status.argtypes = [_vp]
 lib.tkg_check_status.restype = _i32
 lib.tkg_status_string.argtypes = [_i32]
@@ -160,6 +162,14 @@ def tkg_gemm_nvfp4_noalloc(M, N, K, A, B, C, scales, stream=None, check=True) ->
     array and race; the first call on a device must precede any capture."""
     st = lib.tkg_gemm_nvfp4_noalloc(M, N, K, _addr(A), _addr(B), _addr(C), _scales(scales), _stream(stream))
     return _check(st, "tkg_gemm_nvfp4_noalloc") if check else st
+
+
+def tkg_attention_fwd(B, H, Nq, Nkv, D, Q, K, V, O, lse=None, stream=None, check=True) -> int:
+    """O = softmax(Q·Kᵀ/√D)·V per (batch, head); Q/O bf16 [B,H,Nq,D], K/V bf16
+    [B,H,Nkv,D]; lse (optional) fp32 [B,H,Nq] receives each row's log-sum-exp."""
+    st = lib.tkg_attention_fwd(B, H, Nq, Nkv, D, _addr(Q), _addr(K), _addr(V), _addr(O), _addr(lse),
+                               _stream(stream))
+    return _check(st, "tkg_attention_fwd") if check else st
 
 
 def tkg_check_status(stream=None) -> int:
