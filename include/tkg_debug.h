@@ -93,7 +93,10 @@ TKG_API tkg_status tkg_debug_mma_probe(int kind, int n, int ksteps, const void* 
  * tcgen05.fence::after_thread_sync, two tcgen05.commit); 5, 6, 7: only the
  * commits, only the waits, only the fences; 8: only the waits, with acquire
  * at CTA instead of cluster scope; 9: as 0 with varied operand bits instead
- * of one repeated byte.  The difference of two counts divided
+ * of one repeated byte; 10-12 (kind 0, cta_group 1 only): as 0 with the
+ * operand forms of the attention kernel's P·V product: 10 B MN-major, 11 A
+ * read from tensor memory, 12 both; 13 (n = 128): groups of 8 MMAs alternating
+ * between the forms of 0 and 12, into two accumulators.  The difference of two counts divided
  * by the difference in MMAs is the per-MMA cost.  n in {128, 256} (128 for
  * kind 2 with pattern 1 or 2), count in 1..65536 (at least 2 for patterns 1
  * and 2, which issue count/2 whole pairs).  Synchronous on `stream`. */

@@ -201,8 +201,14 @@ unsigned int* probe_err_word() {
 // followed by tcgen05.fence::after_thread_sync, and two tcgen05.commit (to
 // every CTA of a pair) to a barrier nobody waits on; 5: the two commits only;
 // 6: the two waits only; 7: the two fences only; 8: the two waits with
-// acquire at CTA scope only.  Scales otherwise at TMEM columns 256
-// (A) and 272 (B); columns 256..511 all hold e4m3 1.0.
+// acquire at CTA scope only; 10..12 (bf16, one CTA only) = one accumulator
+// with the operand forms of an attention P·V product — 10: B MN-major (16 K
+// rows of 128 bytes per MMA, N in 64-element blocks 16 KB apart); 11: A read
+// from tensor memory (8 columns per MMA from column 256); 12: both; 13 (n =
+// 128): groups of 8 alternating between the form of 0 (D at column 0) and
+// that of 12 (D at column 128), as the attention kernel issues S and P·V.  Scales
+// otherwise at TMEM columns 256 (A) and 272 (B); columns 256..511 all hold
+// e4m3 1.0 (bf16 pairs of 0x3838 for the A-from-TMEM patterns).
 constexpr int kRateStages = 2;
 constexpr int kRateStageBytes = 81920;
 constexpr int kRateSmem = kRateStages * kRateStageBytes + 1024;
@@ -373,6 +379,36 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int n, int count, unsi
           }
         }
       }
+    } else if constexpr (pattern == 13) {
+      // groups of 8 alternate: S-like (A, B K-major in shared memory, D at column 0) and
+      // P·V-like (A from tensor memory at column 256, B MN-major, D at column 128)
+      static_assert(CG == 1 && kind == 0, "attention operand forms: bf16, one CTA");
+      for (int i = 0; i < count; ++i) {
+        const uint32_t stage = s0 + static_cast<uint32_t>(((i >> 3) % kRateStages) * kRateStageBytes);
+        const uint32_t acc = i >= 16 ? 1u : 0u;
+        if (((i >> 3) & 1) == 0) {
+          rate_mma<CG, kind, 0>(tmem, sdesc_sw128(stage + 32u * (i & 3)), sdesc_sw128(stage + 16384u + 32u * (i & 3)),
+                                id, 0u, 0u, acc);
+        } else {
+          mma_bf16_ts(tmem + 128u, tmem + 256u + 8u * static_cast<uint32_t>(i & 7),
+                      sdesc_sw128_mn(stage + 16384u + 2048u * (i & 7), 16384u), id | (1u << 16), acc);
+        }
+      }
+    } else if constexpr (pattern >= 10) {
+      static_assert(CG == 1 && kind == 0, "attention operand forms: bf16, one CTA");
+      const uint32_t id_mn = id | (pattern == 11 ? 0u : (1u << 16));
+      for (int i = 0; i < count; ++i) {
+        const uint32_t stage = s0 + static_cast<uint32_t>(((i >> 3) % kRateStages) * kRateStageBytes);
+        const uint64_t bd = pattern == 11 ? sdesc_sw128(stage + 16384u + 32u * (i & 3))
+                                          : sdesc_sw128_mn(stage + 16384u + 2048u * (i & 7), 16384u);
+        if constexpr (pattern == 10) {
+          rate_mma<CG, kind, 0>(tmem, sdesc_sw128(stage + 32u * (i & 3)), bd, id_mn, 0u, 0u, i > 0 ? 1u : 0u);
+        } else {
+          const uint32_t a_t = tmem + 256u + 8u * static_cast<uint32_t>(i & 7);
+          const uint32_t acc = i > 0 ? 1u : 0u;
+          mma_bf16_ts(tmem, a_t, bd, id_mn, acc);
+        }
+      }
     } else if constexpr (pattern == 3) {
       int slot = 0;
       for (int i = 0; i < count; ++i) {
@@ -503,8 +539,10 @@ tkg_status tkg_debug_mma_probe(int kind, int n, int ksteps, const void* a_tile, 
 tkg_status tkg_debug_mma_rate(int kind, int cta_group, int n, int count, int pattern, unsigned long long* cycles,
                               void* stream) {
   if (kind < 0 || kind > 2 || (cta_group != 1 && cta_group != 2) || (n != 128 && n != 256) || count < 1 ||
-      count > 65536 || pattern < 0 || pattern > 9 || !cycles)
+      count > 65536 || pattern < 0 || pattern > 13 || !cycles)
     return TKG_ERR_INVALID_ARG;
+  if (pattern >= 10 && (kind != 0 || cta_group != 1)) return TKG_ERR_INVALID_ARG;
+  if (pattern == 13 && n != 128) return TKG_ERR_INVALID_ARG;
   // two accumulators must fit beside the scale columns (256..287) for the block-scaled kind
   if ((pattern == 1 || pattern == 2) && kind == 2 && n != 128) return TKG_ERR_INVALID_ARG;
   if ((pattern == 1 || pattern == 2) && count < 2) return TKG_ERR_INVALID_ARG;  // at least one whole pair
@@ -515,43 +553,45 @@ tkg_status tkg_debug_mma_rate(int kind, int cta_group, int n, int count, int pat
   if (!err) return TKG_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(err, 0, sizeof(unsigned int), s) != cudaSuccess) return TKG_ERR_CUDA;
-  static const void* const kFns[2][3][10] = {
+  static const void* const kFns[2][3][14] = {
       {{reinterpret_cast<const void*>(&mma_rate_kernel<1, 0, 0>), reinterpret_cast<const void*>(&mma_rate_kernel<1, 0, 1>),
         reinterpret_cast<const void*>(&mma_rate_kernel<1, 0, 2>), nullptr,
         reinterpret_cast<const void*>(&mma_rate_kernel<1, 0, 4>),
         reinterpret_cast<const void*>(&mma_rate_kernel<1, 0, 5>), reinterpret_cast<const void*>(&mma_rate_kernel<1, 0, 6>),
         reinterpret_cast<const void*>(&mma_rate_kernel<1, 0, 7>), reinterpret_cast<const void*>(&mma_rate_kernel<1, 0, 8>),
-        reinterpret_cast<const void*>(&mma_rate_kernel<1, 0, 9>)},
+        reinterpret_cast<const void*>(&mma_rate_kernel<1, 0, 9>),
+        reinterpret_cast<const void*>(&mma_rate_kernel<1, 0, 10>), reinterpret_cast<const void*>(&mma_rate_kernel<1, 0, 11>),
+        reinterpret_cast<const void*>(&mma_rate_kernel<1, 0, 12>), reinterpret_cast<const void*>(&mma_rate_kernel<1, 0, 13>)},
        {reinterpret_cast<const void*>(&mma_rate_kernel<1, 1, 0>), reinterpret_cast<const void*>(&mma_rate_kernel<1, 1, 1>),
         reinterpret_cast<const void*>(&mma_rate_kernel<1, 1, 2>), nullptr,
         reinterpret_cast<const void*>(&mma_rate_kernel<1, 1, 4>),
         reinterpret_cast<const void*>(&mma_rate_kernel<1, 1, 5>), reinterpret_cast<const void*>(&mma_rate_kernel<1, 1, 6>),
         reinterpret_cast<const void*>(&mma_rate_kernel<1, 1, 7>), reinterpret_cast<const void*>(&mma_rate_kernel<1, 1, 8>),
-        reinterpret_cast<const void*>(&mma_rate_kernel<1, 1, 9>)},
+        reinterpret_cast<const void*>(&mma_rate_kernel<1, 1, 9>), nullptr, nullptr, nullptr, nullptr},
        {reinterpret_cast<const void*>(&mma_rate_kernel<1, 2, 0>), reinterpret_cast<const void*>(&mma_rate_kernel<1, 2, 1>),
         reinterpret_cast<const void*>(&mma_rate_kernel<1, 2, 2>), reinterpret_cast<const void*>(&mma_rate_kernel<1, 2, 3>),
         reinterpret_cast<const void*>(&mma_rate_kernel<1, 2, 4>),
         reinterpret_cast<const void*>(&mma_rate_kernel<1, 2, 5>), reinterpret_cast<const void*>(&mma_rate_kernel<1, 2, 6>),
         reinterpret_cast<const void*>(&mma_rate_kernel<1, 2, 7>), reinterpret_cast<const void*>(&mma_rate_kernel<1, 2, 8>),
-        reinterpret_cast<const void*>(&mma_rate_kernel<1, 2, 9>)}},
+        reinterpret_cast<const void*>(&mma_rate_kernel<1, 2, 9>), nullptr, nullptr, nullptr, nullptr}},
       {{reinterpret_cast<const void*>(&mma_rate_kernel<2, 0, 0>), reinterpret_cast<const void*>(&mma_rate_kernel<2, 0, 1>),
         reinterpret_cast<const void*>(&mma_rate_kernel<2, 0, 2>), nullptr,
         reinterpret_cast<const void*>(&mma_rate_kernel<2, 0, 4>),
         reinterpret_cast<const void*>(&mma_rate_kernel<2, 0, 5>), reinterpret_cast<const void*>(&mma_rate_kernel<2, 0, 6>),
         reinterpret_cast<const void*>(&mma_rate_kernel<2, 0, 7>), reinterpret_cast<const void*>(&mma_rate_kernel<2, 0, 8>),
-        reinterpret_cast<const void*>(&mma_rate_kernel<2, 0, 9>)},
+        reinterpret_cast<const void*>(&mma_rate_kernel<2, 0, 9>), nullptr, nullptr, nullptr, nullptr},
        {reinterpret_cast<const void*>(&mma_rate_kernel<2, 1, 0>), reinterpret_cast<const void*>(&mma_rate_kernel<2, 1, 1>),
         reinterpret_cast<const void*>(&mma_rate_kernel<2, 1, 2>), nullptr,
         reinterpret_cast<const void*>(&mma_rate_kernel<2, 1, 4>),
         reinterpret_cast<const void*>(&mma_rate_kernel<2, 1, 5>), reinterpret_cast<const void*>(&mma_rate_kernel<2, 1, 6>),
         reinterpret_cast<const void*>(&mma_rate_kernel<2, 1, 7>), reinterpret_cast<const void*>(&mma_rate_kernel<2, 1, 8>),
-        reinterpret_cast<const void*>(&mma_rate_kernel<2, 1, 9>)},
+        reinterpret_cast<const void*>(&mma_rate_kernel<2, 1, 9>), nullptr, nullptr, nullptr, nullptr},
        {reinterpret_cast<const void*>(&mma_rate_kernel<2, 2, 0>), reinterpret_cast<const void*>(&mma_rate_kernel<2, 2, 1>),
         reinterpret_cast<const void*>(&mma_rate_kernel<2, 2, 2>), reinterpret_cast<const void*>(&mma_rate_kernel<2, 2, 3>),
         reinterpret_cast<const void*>(&mma_rate_kernel<2, 2, 4>),
         reinterpret_cast<const void*>(&mma_rate_kernel<2, 2, 5>), reinterpret_cast<const void*>(&mma_rate_kernel<2, 2, 6>),
         reinterpret_cast<const void*>(&mma_rate_kernel<2, 2, 7>), reinterpret_cast<const void*>(&mma_rate_kernel<2, 2, 8>),
-        reinterpret_cast<const void*>(&mma_rate_kernel<2, 2, 9>)}}};
+        reinterpret_cast<const void*>(&mma_rate_kernel<2, 2, 9>), nullptr, nullptr, nullptr, nullptr}}};
   const void* fn = kFns[cta_group - 1][kind][pattern];
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kRateSmem) != cudaSuccess) {
     cudaGetLastError();

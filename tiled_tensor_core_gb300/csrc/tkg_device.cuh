@@ -418,6 +418,18 @@ __device__ __forceinline__ void mma_mxf4nvf4(uint32_t d_tmem, uint64_t adesc, ui
         : "memory");
 }
 
+// bf16 MMA with A read from tensor memory (M rows at lanes 0..M-1, two K
+// elements per 32-bit column, the even one in the low half) and B from shared
+// memory; one CTA.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Make `bar` (own CTA) track completion of all prior tcgen05 async ops of this thread.
 __device__ __forceinline__ void mma_commit_local(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");

@@ -8,7 +8,9 @@ cta_group::2) and N, one thread issues 128 and then 1024 MMAs back to back
 (tkg_debug_mma_rate); the difference gives the cost of one MMA in SM cycles,
 and from it the dense rate per SM and, at a given clock, per GPU.  A second
 table compares one accumulator with the 2x1 tile (pairs of MMAs sharing A,
-two accumulators), with and without reuse of the A collector buffer.
+two accumulators), with and without reuse of the A collector buffer; the last
+compares the operand forms of the attention kernel's P·V product (B MN-major,
+A read from tensor memory) with the GEMM's K-major shared operands.
 """
 from __future__ import annotations
 
@@ -66,6 +68,23 @@ def main(argv=None) -> None:
                 c1 = tkg.tkg_debug_mma_rate(kind, cg, 256, 1024, pattern)
                 cells.append(f"{(c1 - c0) / (1024 - 128):.1f}")
             print(f"| {name} | {cg} | {128 * cg} x 256 x {k} | " + " | ".join(cells) + " |")
+
+    print()
+    print("| bf16, one CTA, MMA (M x N x K) | A, B K-major in shared memory | B MN-major | A from tensor memory "
+          "| both (attention P·V) |")
+    print("|---|---|---|---|---|")
+    for n in (128, 256):
+        cells = []
+        for pattern in (0, 10, 11, 12):
+            c0 = tkg.tkg_debug_mma_rate(0, 1, n, 128, pattern)
+            c1 = tkg.tkg_debug_mma_rate(0, 1, n, 1024, pattern)
+            cells.append(f"{(c1 - c0) / (1024 - 128):.1f}")
+        print(f"| 128 x {n} x 16 | " + " | ".join(cells) + " |")
+    c0 = tkg.tkg_debug_mma_rate(0, 1, 128, 128, 13)
+    c1 = tkg.tkg_debug_mma_rate(0, 1, 128, 1024, 13)
+    print()
+    print(f"bf16 128 x 128 x 16, groups of 8 alternating between the two forms (as attention issues S and P·V): "
+          f"{(c1 - c0) / (1024 - 128):.1f} cycles per MMA")
 
 
 if __name__ == "__main__":
