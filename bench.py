@@ -47,19 +47,22 @@ DTYPE = {"bf16": "bf16", "fp8": "e4m3", "nvfp4": "e2m1+e4m3"}
 # DRAM bytes (read + write) per launch of the dominant kernel, from one ncu capture
 # (profiles/), valid only while the kernel sources hash to the value recorded with it.
 TRAFFIC = {
-    "bf16_4096": {"bytes": 97_573_120, "src": "ce7d21312c388726"},        # profiles/gemm_bf16_4096_ncu_full.md
-    "nvfp4_16384": {"bytes": 1_965_084_928, "src": "ce7d21312c388726"},   # profiles/gemm_nvfp4_16384_ncu_full.md
+    "bf16_4096": {"bytes": 97_275_648, "src": "6928c1ef80dfef9a"},        # profiles/gemm_bf16_4096_ncu_full.md
+    "nvfp4_16384": {"bytes": 1_979_353_152, "src": "6928c1ef80dfef9a"},   # profiles/gemm_nvfp4_16384_ncu_full.md
+    "attn_n4096_d128": {"bytes": 1_061_274_368, "src": "3ca7e41bb4d0e2c1"},           # profiles/attention_fwd_4096_d128_ncu_full.md
 }
+GEMM_SOURCES = ("tkg_device.cuh", "gemm_kernel.cuh", "gemm_bf16.cu", "gemm_fp8.cu", "gemm_nvfp4.cu")
+ATTN_SOURCES = ("tkg_device.cuh", "attention.cu")
 
 
-def kernel_source_hash() -> str:
-    """Hash of the GEMM kernel sources with comments and blank lines removed, so that a
+def kernel_source_hash(files=GEMM_SOURCES) -> str:
+    """Hash of kernel sources with comments and blank lines removed, so that a
     comment edit does not invalidate a recorded capture but any code change does."""
     import hashlib
     import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "tiled_tensor_core_gb300", "csrc")
-    for f in ("tkg_device.cuh", "gemm_kernel.cuh", "gemm_bf16.cu", "gemm_fp8.cu", "gemm_nvfp4.cu"):
+    for f in files:
         with open(os.path.join(csrc, f)) as fh:
             text = re.sub(r"/\*.*?\*/", "", fh.read(), flags=re.S)
         for line in text.splitlines():
@@ -71,7 +74,8 @@ def kernel_source_hash() -> str:
 
 def traffic_bytes(workload: str):
     rec = TRAFFIC.get(workload)
-    if rec and rec["src"] == kernel_source_hash():
+    files = ATTN_SOURCES if workload.startswith("attn_") else GEMM_SOURCES
+    if rec and rec["src"] == kernel_source_hash(files):
         return rec["bytes"]
     return None
 
@@ -780,7 +784,7 @@ def run_attention(args, world, rank, local):
                    "launch_overlap": "programmatic dependent launch" if args.overlap == "on" else "off"},
         "median_call_ms": per_call_ms,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak, "traffic": traffic_bytes(args.workload),
                      "frac_of_burst_peak": achieved / peaks["bf16_tflops"],
                      "peak_source": f"{peaks['source']} bf16 sustained (back-to-back cuBLAS)"},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": calls, "clocks": clocks, "spot_check_rel_err": spot,
