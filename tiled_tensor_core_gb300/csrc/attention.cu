@@ -11,24 +11,23 @@
 // online softmax (subtract the running row maximum, exponentiate, keep the
 // running row sum), a conversion of the probabilities to bf16 and P·V; the
 // finish step divides by the row sum and stores O.  Q stays in shared memory
-// for the whole task.  Re-cast for tcgen05:
-//   warp 0, one lane   LOAD     TMA (3-D maps over [B·H][N][D]) of the Q tile
+// for the whole task.  Re-cast for tcgen05, two 128-row query tiles (A, B)
+// per CTA sharing the K and V tiles:
+//   warp 0, one lane   LOAD     TMA (3-D maps over [B·H][N][D]) of both Q tiles
 //                               once and of K_j, V_j into two rings
-//   warp 1, one lane   COMPUTE  S_j = Q·K_jᵀ into one of three TMEM score
-//                               buffers; O += P_j·V_j into a TMEM accumulator,
-//                               P_j read from tensor memory, V as an MN-major
-//                               shared operand
-//   warps 2-9          SOFTMAX  two threads per query row (its TMEM lane), one per
-//                      / FINISH half of the key columns: scores from TMEM, running
-//                               max (combined through shared memory) and sum, P_j
-//                               (bf16) written back over its own score buffer,
-//                               rescale of the row's O when its maximum grew; at
-//                               the end O / l to bf16, a TMA store, the log-sum-exp
-// P never touches shared memory, which the tensor core's operand reads and the
-// TMA writes of K and V already keep busy.  Order of the tensor-core work:
-// S_0, S_1, S_2, PV_0, S_3, PV_1, S_4, ...: score tiles are computed up to
-// three ahead of the softmax.  Every wait is bounded (TKG_OPT_TIMEOUT_NS) and
-// reported through the status word.
+//   warp 1, one lane   COMPUTE  per query tile t: S_t(j) = Q_t·K_jᵀ into the
+//                               tile's TMEM score buffer, O_t += P_t(j)·V_j into
+//                               its TMEM accumulator (P read from tensor memory,
+//                               V as an MN-major shared operand)
+//   warps 2-5 (A),     SOFTMAX  one thread per query row (its TMEM lane): scores
+//   warps 6-9 (B)      / FINISH from TMEM, running max and sum, P_t(j) (bf16)
+//                               written back over the score buffer, rescale of
+//                               the row's O when its maximum grew; at the end
+//                               O / l to bf16, a TMA store, the log-sum-exp
+// The two tiles' softmax phases alternate: the tensor core computes one tile's
+// P·V and next scores while the other tile's softmax runs.  P never touches
+// shared memory.  Every wait is bounded (TKG_OPT_TIMEOUT_NS) and reported
+// through the status word.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -58,36 +57,33 @@ struct AttnParams {
 
 template <int D>
 struct AttnCfg {
-  static constexpr int BQ = 128;             // query rows per CTA (TMEM lanes)
+  static constexpr int BQ = 128;             // query rows per tile (TMEM lanes)
+  static constexpr int NT = 2;               // query tiles per CTA
   static constexpr int BKV = 128;            // keys per tile
   static constexpr int DC = D / 64;          // 128-byte column chunks of a Q/K/V row
   static constexpr int CHUNK = 128 * 128;    // [128 rows][128 B] swizzled tile
-  static constexpr int KST = D == 128 ? 2 : 3;  // K ring depth (K_j is consumed by S_j, early)
-  static constexpr int VST = D == 128 ? 3 : 4;  // V ring depth (V_j waits for the softmax of tile j)
+  static constexpr int KST = D == 128 ? 2 : 3;  // K ring depth
+  static constexpr int VST = D == 128 ? 2 : 3;  // V ring depth
   static constexpr int KV_STAGE = DC * CHUNK;
-  static constexpr int Q_BYTES = DC * CHUNK;
+  static constexpr int Q_TILE = DC * CHUNK;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KST * KV_STAGE;
-  static constexpr int OFF_Q = OFF_V + VST * KV_STAGE;  // also the output staging at the end
-  static constexpr int OFF_X = OFF_Q + Q_BYTES;         // row max / row sum exchange between column halves
-  static constexpr int X_BYTES = (2 * 2 + 2) * BQ * 4;
-  static constexpr int OFF_BAR = OFF_X + X_BYTES;
-  static constexpr int NSB = 3;  // TMEM score buffers
-  static constexpr int NUM_BARS = 1 + 2 * KST + 2 * VST + 3 * NSB + 2;
+  static constexpr int OFF_Q = OFF_V + VST * KV_STAGE;  // tile t at OFF_Q + t * Q_TILE; the output staging at the end
+  static constexpr int OFF_BAR = OFF_Q + NT * Q_TILE;
+  static constexpr int NUM_BARS = 1 + 2 * KST + 2 * VST + 3 * NT + 2;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NUM_BARS;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
-  static constexpr int SOFTMAX_WARPS = 8;  // two per TMEM lane quarter: one per half of the key columns
-  static constexpr int THREADS = 64 + 32 * SOFTMAX_WARPS;
-  // TMEM columns: three score buffers (S_j in buffer j % 3; the softmax writes
-  // P_j, bf16, over the first 64 columns of the same buffer), then O
-  static constexpr uint32_t T_O = 128 * NSB;
+  static constexpr int THREADS = 64 + 32 * 4 * NT;  // producer, MMA, one softmax warpgroup per query tile
+  // TMEM columns: tile t's scores at 128 t (its P, bf16, written over the first
+  // 64 of them), its output accumulator at 256 + D t
+  static constexpr uint32_t T_S = 0, T_O = 128 * NT;
   static constexpr uint32_t TMEM_COLS = 512;
   // S = Q·Kᵀ: M = 128, N = BKV, both K-major;  O += P·V: M = 128, N = D, P from
   // tensor memory, V an MN-major shared operand (bit 16)
   static constexpr uint32_t IDESC_S = idesc_dense(kFmtBF16, BQ, BKV);
   static constexpr uint32_t IDESC_PV = idesc_dense(kFmtBF16, BQ, D) | (1u << 16);
   static_assert(D == 64 || D == 128, "head dimension 64 or 128");
-  static_assert(T_O + D <= TMEM_COLS, "tensor memory has 512 columns");
+  static_assert(T_O + NT * D <= TMEM_COLS, "tensor memory has 512 columns");
   static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB shared-memory limit");
   // more than half of the SM's shared memory: one CTA per SM, so the 512-column
   // TMEM allocation never waits for another CTA of this kernel
@@ -101,11 +97,6 @@ __device__ __forceinline__ void attn_timeout(unsigned int* status, int role, vol
   *abort_flag = 1;
 }
 
-// Barrier among the 64 threads of the two softmax warps that share a lane quarter.
-__device__ __forceinline__ void pair_sync(int quad) {
-  asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
-}
-
 template <int D>
 __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
   using C = AttnCfg<D>;
@@ -113,8 +104,6 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sQ = sbase + C::OFF_Q;
-  float* xmax = reinterpret_cast<float*>(smem + C::OFF_X);  // [tile parity][half][row]
-  float* xsum = xmax + 2 * 2 * C::BQ;                        // [half][row]
   const uint32_t bar0 = sbase + C::OFF_BAR;
   const uint32_t q_full = bar0;
   auto k_full = [&](int s) { return bar0 + 8u * (1 + s); };
@@ -122,20 +111,20 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
   auto v_full = [&](int s) { return bar0 + 8u * (1 + 2 * C::KST + s); };
   auto v_empty = [&](int s) { return bar0 + 8u * (1 + 2 * C::KST + C::VST + s); };
   constexpr int B1 = 1 + 2 * C::KST + 2 * C::VST;
-  // score buffer b (tiles j with j % 3 == b): S_j is in it / P_j was written over it
-  // (and O rescaled) / P_j·V_j has finished, so O holds tiles 0..j and b is free
-  auto s_full = [&](int b) { return bar0 + 8u * (B1 + b); };
-  auto p_full = [&](int b) { return bar0 + 8u * (B1 + C::NSB + b); };
-  auto pv_done = [&](int b) { return bar0 + 8u * (B1 + 2 * C::NSB + b); };
-  const uint32_t o_final = bar0 + 8u * (B1 + 3 * C::NSB);  // the last P·V finished
-  const uint32_t drain = bar0 + 8u * (B1 + 3 * C::NSB + 1);
+  // query tile t: S_t(j) is in its score buffer / P_t(j) was written over it (and O_t
+  // rescaled) / P_t(j)·V_j has finished (the buffer is free, O_t holds key tiles 0..j)
+  auto s_full = [&](int t) { return bar0 + 8u * (B1 + t); };
+  auto p_full = [&](int t) { return bar0 + 8u * (B1 + C::NT + t); };
+  auto pv_done = [&](int t) { return bar0 + 8u * (B1 + 2 * C::NT + t); };
+  const uint32_t o_final = bar0 + 8u * (B1 + 3 * C::NT);  // the last P·V finished
+  const uint32_t drain = bar0 + 8u * (B1 + 3 * C::NT + 1);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* never_abort = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int q0 = static_cast<int>(blockIdx.x) * C::BQ;
+  const int q0 = static_cast<int>(blockIdx.x) * C::BQ * C::NT;
   const int bh = static_cast<int>(blockIdx.y);
   const int nkv = (p.Nkv + C::BKV - 1) / C::BKV;
   const uint64_t tmo = p.timeout_ns;
@@ -150,10 +139,10 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
       mbar_init(v_full(s), 1);
       mbar_init(v_empty(s), 1);
     }
-    for (int b = 0; b < C::NSB; ++b) {
-      mbar_init(s_full(b), 1);
-      mbar_init(p_full(b), C::SOFTMAX_WARPS);  // one arrival per softmax warp
-      mbar_init(pv_done(b), 1);
+    for (int t = 0; t < C::NT; ++t) {
+      mbar_init(s_full(t), 1);
+      mbar_init(p_full(t), 4);  // one arrival per warp of the tile's softmax warpgroup
+      mbar_init(pv_done(t), 1);
     }
     mbar_init(o_final, 1);
     mbar_init(drain, 1);
@@ -181,9 +170,12 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
     // ------------------------------------------------------------ LOAD
     if (lane == 0) {
       bool ok = true;
-      mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+      mbar_arrive_expect_tx(q_full, C::NT * C::Q_TILE);
 #pragma unroll
-      for (int c = 0; c < C::DC; ++c) tma_load_3d(sQ + c * C::CHUNK, &p.tmap_q, q_full, 64 * c, q0, bh);
+      for (int t = 0; t < C::NT; ++t)
+#pragma unroll
+        for (int c = 0; c < C::DC; ++c)
+          tma_load_3d(sQ + t * C::Q_TILE + c * C::CHUNK, &p.tmap_q, q_full, 64 * c, q0 + t * C::BQ, bh);
       for (int j = 0; j < nkv && ok; ++j) {
         const int ks = j % C::KST, vs = j % C::VST;
         if (!mbar_wait(k_empty(ks), (static_cast<uint32_t>(j / C::KST) & 1u) ^ 1u, tmo, abort_flag)) {
@@ -213,59 +205,68 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ COMPUTE
-    // Score tiles run up to three ahead of the softmax: S_0, S_1, S_2, then
-    // PV_0, S_3, PV_1, S_4, ...; S_{i+3} goes into the buffer of tile i as soon
-    // as PV_i has read P_i from it.  So the softmax warps find S_j ready when
-    // they finish tile j-1, and the tensor core works on S and P·V while they
-    // compute.  Each buffer has its own barriers, used once per three tiles in
-    // order, so no parity wait can see a phase two completions away.
+    // Per key tile j, for query tile A then B: P_t(j)·V_j once the tile's softmax
+    // has written P_t(j), then, once that MMA has read P_t(j), S_t(j+1) into the
+    // same buffer.  So the tensor core works on one tile's products while the
+    // other tile's softmax runs, and S_t(j+1) being complete implies that
+    // P_t(j)·V_j is: the softmax never waits to rescale O.  Each tile's
+    // barriers complete once per key tile, waited on in order.
     if (lane == 0) {
       bool ok = mbar_wait(q_full, 0, tmo, abort_flag);
       tc_fence_after();
-      auto issue_s = [&](int j) -> bool {
-        const int ks = j % C::KST;
-        const int b = j % C::NSB;
-        if (!mbar_wait(k_full(ks), static_cast<uint32_t>(j / C::KST) & 1u, tmo, abort_flag)) return false;
-        // buffer b last held P_{j-3}: its P·V must have read it
-        if (j >= C::NSB &&
-            !mbar_wait(pv_done(b), static_cast<uint32_t>(j / C::NSB - 1) & 1u, tmo, abort_flag))
-          return false;
-        tc_fence_after();
-        const uint32_t k0 = sK + ks * C::KV_STAGE;
-        const uint32_t t_s = tmem_base + 128u * static_cast<uint32_t>(b);
+      auto issue_s = [&](int t, int j) {
+        const uint32_t k0 = sK + (j % C::KST) * C::KV_STAGE;
+        const uint32_t q_t = sQ + t * C::Q_TILE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(sQ + (kk / 4) * C::CHUNK + 32u * (kk % 4));
+          const uint64_t ad = sdesc_sw128(q_t + (kk / 4) * C::CHUNK + 32u * (kk % 4));
           const uint64_t bd = sdesc_sw128(k0 + (kk / 4) * C::CHUNK + 32u * (kk % 4));
-          mma_bf16<1>(t_s, ad, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
+          mma_bf16<1>(tmem_base + C::T_S + 128u * t, ad, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
         }
-        mma_commit_local(s_full(b));
-        mma_commit_local(k_empty(ks));
-        return true;
+        mma_commit_local(s_full(t));
+        if (t == C::NT - 1) mma_commit_local(k_empty(j % C::KST));  // the last reader of K_j
       };
-      // O += P_i · V_i once the softmax warps have written P_i (and rescaled O)
-      auto issue_pv = [&](int i) -> bool {
-        const int b = i % C::NSB;
-        if (!mbar_wait(p_full(b), static_cast<uint32_t>(i / C::NSB) & 1u, tmo, abort_flag)) return false;
-        const int vs = i % C::VST;
-        if (!mbar_wait(v_full(vs), static_cast<uint32_t>(i / C::VST) & 1u, tmo, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t v0 = sV + vs * C::KV_STAGE;
-        const uint32_t a0 = tmem_base + 128u * static_cast<uint32_t>(b);
+      auto issue_pv = [&](int t, int j) {
+        const uint32_t v0 = sV + (j % C::VST) * C::KV_STAGE;
+        const uint32_t a0 = tmem_base + C::T_S + 128u * t;
 #pragma unroll
         for (int kk = 0; kk < C::BKV / 16; ++kk) {
-          // A: 16 keys of P = 8 columns of its score buffer; B: 16 rows of V (keys), D columns
+          // A: 16 keys of P = 8 columns of the tile's score buffer; B: 16 rows of V (keys), D columns
           const uint64_t bd = sdesc_sw128_mn(v0 + 2048u * kk, C::CHUNK);
-          mma_bf16_ts(tmem_base + C::T_O, a0 + 8u * kk, bd, C::IDESC_PV, (i > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem_base + C::T_O + static_cast<uint32_t>(D * t), a0 + 8u * kk, bd, C::IDESC_PV,
+                      (j > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit_local(v_empty(vs));
-        mma_commit_local(pv_done(b));
-        return true;
+        mma_commit_local(pv_done(t));
+        if (t == C::NT - 1) mma_commit_local(v_empty(j % C::VST));  // the last reader of V_j
       };
-      for (int j = 0; j < C::NSB && j < nkv && ok; ++j) ok = issue_s(j);
-      for (int i = 0; i < nkv && ok; ++i) {
-        ok = issue_pv(i);
-        if (ok && i + C::NSB < nkv) ok = issue_s(i + C::NSB);
+      if (ok) ok = mbar_wait(k_full(0), 0, tmo, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < C::NT; ++t) issue_s(t, 0);
+      }
+      for (int j = 0; j < nkv && ok; ++j) {
+        const uint32_t ph = static_cast<uint32_t>(j) & 1u;
+        for (int t = 0; t < C::NT && ok; ++t) {
+          if (!mbar_wait(p_full(t), ph, tmo, abort_flag) ||
+              (t == 0 && !mbar_wait(v_full(j % C::VST), static_cast<uint32_t>(j / C::VST) & 1u, tmo, abort_flag))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_pv(t, j);
+          if (j + 1 < nkv) {
+            // S_t(j+1) overwrites the buffer P_t(j)·V_j reads
+            if (!mbar_wait(pv_done(t), ph, tmo, abort_flag) ||
+                (t == 0 &&
+                 !mbar_wait(k_full((j + 1) % C::KST), static_cast<uint32_t>((j + 1) / C::KST) & 1u, tmo,
+                            abort_flag))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(t, j + 1);
+          }
+        }
       }
       if (ok) mma_commit_local(o_final);
       // no MMA may still be writing TMEM when it is released
@@ -276,71 +277,54 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
     __syncwarp();
   } else {
     // ------------------------------------------------------------ SOFTMAX / FINISH
-    // Two warps per TMEM lane quarter: warp half h takes key columns [64h, 64h+64)
-    // of the rows of its quarter (and O columns [h·D/2, (h+1)·D/2)).  The two
-    // threads of a row combine their maxima through shared memory every tile
-    // (so both make the same reference-maximum decision) and their sums at the end.
-    const int quad = warp & 3;  // TMEM lane quarter this warp may access
-    const int half = (warp - 2) / 4;
-    const int r = quad * 32 + lane;
+    // Warpgroup t (warps 2+4t .. 5+4t) owns query tile t, one thread per row
+    // (its TMEM lane).
+    const int t = (warp - 2) / 4;
+    const int quad = warp & 3;  // TMEM lane quarter this warp may access (rows 32 quad ..)
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t t_s = tmem_base + lane_off + C::T_S + 128u * static_cast<uint32_t>(t);
+    const uint32_t t_o = tmem_base + lane_off + C::T_O + static_cast<uint32_t>(D * t);
     const float c2 = p.scale_log2;
     float m = -INFINITY;  // reference maximum of the raw scores of this row (lazily raised)
-    float l = 0.0f;       // this half's running sum of exp2((s - m) * c2)
+    float l = 0.0f;       // running sum of exp2((s - m) * c2)
     bool ok = true;
-    // Every pair_sync is reached by both warps of the pair the same number of
-    // times whatever fails: a failed wait only clears `ok`, and the pair leaves
-    // the loop together at the next exchange, where a NaN flag tells the partner.
-    const float kFail = __int_as_float(0x7fc00001);
     for (int j = 0; j < nkv; ++j) {
-      const int b = j % C::NSB;
-      if (ok && !__all_sync(0xffffffffu, mbar_wait<true>(s_full(b), static_cast<uint32_t>(j / C::NSB) & 1u, tmo,
-                                                          abort_flag)))
-        ok = false;
-      uint32_t s[2][32];
-      const uint32_t t_s = tmem_base + lane_off + 128u * static_cast<uint32_t>(b);
-      float own = kFail;
-      if (ok) {
-        tc_fence_after();
-#pragma unroll
-        for (int q = 0; q < 2; ++q) tmem_ld_32x32b_x32(t_s + 64u * half + 32u * q, s[q]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int q = 0; q < 2; ++q) reg_fence(s[q]);
-        // keys of this tile past the end of the sequence score -inf (only the last tile has any)
-        const int valid = p.Nkv - j * C::BKV - 64 * half;
-        if (valid < 64) {
-#pragma unroll
-          for (int q = 0; q < 2; ++q)
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (32 * q + i >= valid) s[q][i] = __float_as_uint(-INFINITY);
-        }
-        // this half's maximum: eight independent chains, then a tree
-        float mx[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) mx[e] = __uint_as_float(s[0][e]);
-#pragma unroll
-        for (int e = 8; e < 64; ++e) mx[e % 8] = fmaxf(mx[e % 8], __uint_as_float(s[e / 32][e % 32]));
-#pragma unroll
-        for (int w = 4; w >= 1; w /= 2)
-#pragma unroll
-          for (int e = 0; e < w; ++e) mx[e] = fmaxf(mx[e], mx[e + w]);
-        own = mx[0];
-      }
-      xmax[((j & 1) * 2 + half) * C::BQ + r] = own;
-      pair_sync(quad);
-      const float other = xmax[((j & 1) * 2 + (1 - half)) * C::BQ + r];
-      if (!__all_sync(0xffffffffu, ok && !isnan(other))) {
+      if (!__all_sync(0xffffffffu, mbar_wait<true>(s_full(t), static_cast<uint32_t>(j) & 1u, tmo, abort_flag))) {
         ok = false;
         break;
       }
-      const float mt = fmaxf(own, other);
+      tc_fence_after();
+      uint32_t s[4][32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tmem_ld_32x32b_x32(t_s + 32u * q, s[q]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int q = 0; q < 4; ++q) reg_fence(s[q]);
+      // keys of this tile past the end of the sequence score -inf (only the last tile has any)
+      const int valid = p.Nkv - j * C::BKV;
+      if (valid < C::BKV) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (32 * q + i >= valid) s[q][i] = __float_as_uint(-INFINITY);
+      }
+      // tile row maximum: eight independent chains, then a tree
+      float mx[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) mx[e] = __uint_as_float(s[0][e]);
+#pragma unroll
+      for (int e = 8; e < 128; ++e) mx[e % 8] = fmaxf(mx[e % 8], __uint_as_float(s[e / 32][e % 32]));
+#pragma unroll
+      for (int w = 4; w >= 1; w /= 2)
+#pragma unroll
+        for (int e = 0; e < w; ++e) mx[e] = fmaxf(mx[e], mx[e + w]);
+      const float mt = mx[0];
       // Lazy reference maximum: the row keeps m (and so its O and l) until a
       // tile's maximum exceeds it by more than 8 in exp2 units, so that every
       // probability stays <= 2^8; only then is m raised and O, l rescaled.  The
       // result is the same softmax: m cancels between O and l.  The first tile
-      // always sets m (m = -inf, alpha = 0).  Both halves see the same mt.
+      // always sets m (m = -inf, alpha = 0).
       float alpha = 1.0f;
       if ((mt - m) * c2 > 8.0f) {
         alpha = ex2_approx((m - mt) * c2);
@@ -348,9 +332,9 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
       }
       const float neg = -m * c2;
       float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[32];
+      uint32_t pk[64];
 #pragma unroll
-      for (int q = 0; q < 2; ++q)
+      for (int q = 0; q < 4; ++q)
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float x0 = ex2_approx(fmaf(__uint_as_float(s[q][2 * i]), c2, neg));
@@ -364,78 +348,59 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
 #pragma unroll
         for (int e = 0; e < w; ++e) ls[e] += ls[e + w];
       l = l * alpha + ls[0];
-
       if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-        // rescale this half's columns of O once P_{j-1}·V_{j-1} has finished.  (S_j
-        // went into a buffer that P_{j-3}·V_{j-3} had released, so the barrier of
-        // tile j-1's buffer is at most one completion behind.)
-        if (!__all_sync(0xffffffffu, mbar_wait<true>(pv_done((j - 1) % C::NSB),
-                                                     static_cast<uint32_t>((j - 1) / C::NSB) & 1u, tmo, abort_flag)))
-          ok = false;
-        if (ok) {
-          tc_fence_after();
+        // O_t holds key tiles 0..j-1 (S_t(j) was issued after P_t(j-1)·V_{j-1} finished)
 #pragma unroll
-          for (int q = 0; q < D / 64; ++q) {
-            uint32_t o[32];
-            const uint32_t t_o = tmem_base + lane_off + C::T_O + static_cast<uint32_t>(half * (D / 2)) + 32u * q;
-            tmem_ld_32x32b_x32(t_o, o);
-            tmem_wait_ld();
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(t_o + 32u * q, o);
+          tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st_32x32b_x32(t_o, o);
-          }
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st_32x32b_x32(t_o + 32u * q, o);
         }
       }
-      if (ok) {
-        // this half's 64 probabilities (32 bf16 pairs) over columns [32h, 32h+32) of the score buffer
-        tmem_st_32x32b_x32(t_s + 32u * half, pk);
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_local(p_full(b));
-      }
+      // P row r (bf16 pairs) over the first 64 columns of the tile's score buffer
+      tmem_st_32x32b_x32(t_s, *reinterpret_cast<uint32_t(*)[32]>(pk));
+      tmem_st_32x32b_x32(t_s + 32u, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_local(p_full(t));
     }
     if (ok && !__all_sync(0xffffffffu, mbar_wait<true>(o_final, 0, tmo, abort_flag))) ok = false;
-    // combine the two halves' sums (the pair meets here whatever happened above)
-    xsum[half * C::BQ + r] = ok ? l : kFail;
-    pair_sync(quad);
-    const float l_tot = xsum[r] + xsum[C::BQ + r];
-    if (!__all_sync(0xffffffffu, ok && !isnan(l_tot))) ok = false;
-    // FINISH: O / l to bf16, staged per quarter ([32 rows][128 B] per 64 columns) in the Q tile
-    const uint32_t stg = sQ + static_cast<uint32_t>(quad * C::DC * 4096);
     if (ok) {
+      // FINISH: O / l to bf16, staged per warp ([32 rows][128 B] per 64 columns) in the tile's Q buffer
       tc_fence_after();
-      const float inv = 1.0f / l_tot;
+      const float inv = 1.0f / l;
+      const uint32_t stg = sQ + static_cast<uint32_t>(t * C::Q_TILE + quad * C::DC * 4096);
 #pragma unroll
-      for (int q = 0; q < D / 64; ++q) {
-        const int col = half * (D / 2) + 32 * q;  // first O column of this 32-column group
+      for (int q = 0; q < D / 32; ++q) {
         uint32_t o[32];
-        tmem_ld_32x32b_x32(tmem_base + lane_off + C::T_O + static_cast<uint32_t>(col), o);
+        tmem_ld_32x32b_x32(t_o + 32u * q, o);
         tmem_wait_ld();
         uint32_t ob[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           ob[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
-        const uint32_t chunk = stg + static_cast<uint32_t>(col / 64) * 4096u;
+        const uint32_t chunk = stg + static_cast<uint32_t>(q / 2) * 4096u;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const uint32_t off =
-              swizzle_offset(static_cast<uint32_t>(lane) * 128u + 16u * (4 * ((col / 32) % 2) + u), 128u);
+          const uint32_t off = swizzle_offset(static_cast<uint32_t>(lane) * 128u + 16u * (4 * (q % 2) + u), 128u);
           st_shared_v4(chunk + off, ob[4 * u], ob[4 * u + 1], ob[4 * u + 2], ob[4 * u + 3]);
         }
       }
       fence_proxy_async_smem();
-    }
-    pair_sync(quad);
-    if (ok) {
-      if (half == 0 && lane == 0) {
+      __syncwarp();
+      const int row0 = q0 + t * C::BQ + quad * 32;
+      if (lane == 0) {
 #pragma unroll
-        for (int c = 0; c < C::DC; ++c) tma_store_3d(&p.tmap_o, stg + c * 4096u, 64 * c, q0 + quad * 32, bh);
+        for (int c = 0; c < C::DC; ++c) tma_store_3d(&p.tmap_o, stg + c * 4096u, 64 * c, row0, bh);
         bulk_commit_group();
         bulk_wait_group<0>();
       }
-      if (half == 0 && p.lse != nullptr && q0 + r < p.Nq)
-        p.lse[static_cast<size_t>(bh) * p.Nq + q0 + r] = m * p.scale + logf(l_tot);
+      if (p.lse != nullptr && row0 + lane < p.Nq)
+        p.lse[static_cast<size_t>(bh) * p.Nq + row0 + lane] = m * p.scale + logf(l);
     } else if (lane == 0) {
       attn_timeout(p.status, kRoleSoftmax, abort_flag);
     }
@@ -494,7 +459,7 @@ tkg_status attn_launch(int64_t BH, int64_t Nq, int64_t Nkv, const void* Q, const
     attr_set.fetch_or(1ull << dev);
   }
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>((Nq + C::BQ - 1) / C::BQ), static_cast<unsigned>(BH), 1);
+  cfg.gridDim = dim3(static_cast<unsigned>((Nq + C::BQ * C::NT - 1) / (C::BQ * C::NT)), static_cast<unsigned>(BH), 1);
   cfg.blockDim = dim3(C::THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = stream;
