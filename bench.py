@@ -339,7 +339,6 @@ def run_tkg(args, world, rank, local):
         ref = acc.astype(np.float64) * ops.scale_a * ops.scale_b
         spot = float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
 
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * batch)]
     step_ms, kern_ms, host_ms = [], [], []
     sampler = ClockSampler(local)
     barrier(world)
@@ -348,29 +347,35 @@ def run_tkg(args, world, rank, local):
     time.sleep(0.3)  # let the sampler take its first reading
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    # The steps are enqueued back to back (no host synchronisation between them, so the GPU never
+    # waits for the host at a step boundary); per-step and per-launch events are read afterwards.
+    per_launch = graph is None and args.overlap == "off"
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+    launch_ev = ([[torch.cuda.Event(enable_timing=True) for _ in range(2 * batch)] for _ in range(args.steps)]
+                 if per_launch else None)
     t_start.record(stream)
     for s in range(args.steps):
-        s0 = torch.cuda.Event(enable_timing=True)
-        s1 = torch.cuda.Event(enable_timing=True)
-        s0.record(stream)
+        step_ev[s][0].record(stream)
         h0 = time.perf_counter()
         if graph is not None:
             with torch.cuda.stream(stream):
                 graph.replay()
         else:
             # an event between two launches would end their overlap: with it on, the step is timed whole
-            step(ev if args.overlap == "off" else None)
+            step(launch_ev[s] if per_launch else None)
         host_ms.append((time.perf_counter() - h0) * 1e3)
-        s1.record(stream)
-        s1.synchronize()
-        step_ms.append(s0.elapsed_time(s1))
-        if graph is not None or args.overlap == "on":
+        step_ev[s][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    for s in range(args.steps):
+        step_ms.append(step_ev[s][0].elapsed_time(step_ev[s][1]))
+        if per_launch:
+            kern_ms.extend(launch_ev[s][2 * i].elapsed_time(launch_ev[s][2 * i + 1]) for i in range(batch))
+        else:
             # no per-launch events (inside a graph, or between overlapped launches): the step is
             # nothing but GEMM launches, so spread its time over them
             kern_ms.extend([step_ms[-1] / batch] * batch)
-        else:
-            kern_ms.extend(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(batch))
-    t_end.record(stream)
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
     barrier(world)
@@ -419,6 +424,7 @@ def run_tkg(args, world, rank, local):
         "pct_of_burst_peak": 100.0 * value / world / peak_burst,
         "median_gemm_ms": statistics.median(kern_ms),
         "host_enqueue_ms_per_step": statistics.median(host_ms),
+        "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms)},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic_bytes(w.name),
                      "frac_of_burst_peak": achieved / peak_burst,
@@ -720,17 +726,16 @@ def run_attention(args, world, rank, local):
     time.sleep(0.3)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    step_ms = []
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
     t0.record(stream)
-    for _ in range(args.steps):
-        s0 = torch.cuda.Event(enable_timing=True)
-        s1 = torch.cuda.Event(enable_timing=True)
-        s0.record(stream)
+    for s in range(args.steps):  # enqueued back to back; read afterwards
+        step_ev[s][0].record(stream)
         step()
-        s1.record(stream)
-        s1.synchronize()
-        step_ms.append(s0.elapsed_time(s1))
+        step_ev[s][1].record(stream)
     t1.record(stream)
+    torch.cuda.synchronize(dev)
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
     barrier(world)
@@ -783,6 +788,7 @@ def run_attention(args, world, rank, local):
                    "l2": f"{n_sets} rotating input sets, {n_sets * per_set / 2**20:.0f} MiB > 129 MiB L2",
                    "launch_overlap": "programmatic dependent launch" if args.overlap == "on" else "off"},
         "median_call_ms": per_call_ms,
+        "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms)},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic_bytes(args.workload),
                      "frac_of_burst_peak": achieved / peaks["bf16_tflops"],
