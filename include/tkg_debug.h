@@ -44,10 +44,12 @@ TKG_API tkg_status tkg_debug_variant_info(int kind, int variant, int32_t info[6]
 TKG_API int tkg_debug_pick_variant(int kind, int64_t M, int64_t N, int64_t K);
 
 /* Fault injection for the device-timeout path: mode 1 makes the next GEMM's
- * producer skip the copies of its first ring stage, so the consumer's bounded
- * wait runs out and the kernel reports TKG_ERR_TIMEOUT through
- * tkg_check_status.  Mode 0 (default) disables it.  The mode applies to the
- * next GEMM launch only. */
+ * producer skip the copies of its first ring stage, mode 2 makes the next
+ * attention launch's producer skip the K copies of its first key tile; the
+ * consumer's bounded wait runs out and the kernel reports TKG_ERR_TIMEOUT
+ * through tkg_check_status.  No copy is ever in flight for the skipped stage.
+ * Mode 0 (default) disables it.  The mode applies to the next launch of that
+ * kind only. */
 TKG_API tkg_status tkg_debug_set_fault(int mode);
 
 /* Tile-visit count for the scheduler check: the next GEMM launch adds 1 to

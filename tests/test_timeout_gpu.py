@@ -47,3 +47,39 @@ def test_injected_stall_reports_timeout_then_recovers(tkg, variant):
         tkg.tkg_debug_set_fault(0)
         tkg.tkg_set_option(tkg.TKG_OPT_TIMEOUT_NS, 0)
         tkg.tkg_set_option(tkg.TKG_OPT_VARIANT, 0)
+
+
+def test_attention_injected_stall_reports_timeout_then_recovers(tkg):
+    from oracle import attention as oa
+    x = synth.attention_inputs(1, 2, 256, 384, 128, seed=17)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+    q, k, v = t(x.q), t(x.k), t(x.v)
+    o = torch.empty_like(q)
+    tkg.tkg_set_option(tkg.TKG_OPT_TIMEOUT_NS, 100_000_000)  # 0.1 s per wait
+    try:
+        tkg.tkg_debug_set_fault(2)
+        tkg.tkg_attention_fwd(1, 2, 256, 384, 128, q, k, v, o)
+        assert tkg.tkg_check_status() == tkg.TKG_ERR_TIMEOUT
+        assert tkg.tkg_check_status() == tkg.TKG_OK
+        tkg.tkg_set_option(tkg.TKG_OPT_TIMEOUT_NS, 0)
+        tkg.tkg_attention_fwd(1, 2, 256, 384, 128, q, k, v, o)
+        assert tkg.tkg_check_status() == tkg.TKG_OK
+        got = oa.bf16_decode(o.cpu().numpy().view(np.uint16))
+        ref = oa.attention_forward(x.q, x.k, x.v)
+        err = np.abs(got.reshape(ref["o"].shape) - ref["o"])
+        assert (err <= 2 * 2.0 ** -9 * (ref["pv_abs"] + np.abs(ref["o"])) + 1e-6).all()
+    finally:
+        tkg.tkg_debug_set_fault(0)
+        tkg.tkg_set_option(tkg.TKG_OPT_TIMEOUT_NS, 0)
+
+
+def test_fault_modes_are_consumed_by_their_own_kind(tkg):
+    # an armed attention fault is not taken by a GEMM launch (and the GEMM is correct)
+    ops = synth.make_operands("bf16", 256, 256, 256, "normal_sqrtk", 3, 4)
+    try:
+        tkg.tkg_debug_set_fault(2)
+        g = run_gpu(ops)
+        acc, c_ref = oracle.gemm(ops)
+        check_against_oracle("bf16", g.c_bits(), acc, c_ref)
+    finally:
+        tkg.tkg_debug_set_fault(0)

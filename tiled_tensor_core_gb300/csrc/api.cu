@@ -360,7 +360,7 @@ tkg_status gemm_launch(int kind, int64_t M, int64_t N, int64_t K, const void* A,
   p.tiles_m = static_cast<int>(tiles_m);
   p.tiles_n = static_cast<int>(tiles_n);
   p.group_m = static_cast<int>(opt_or(g_opt_group, kDefaultGroupM));
-  p.fault_mode = g_fault.exchange(0);
+  p.fault_mode = take_fault_mode(1);
   p.visits = g_visits.exchange(nullptr);
   const int64_t sched = opt_or(g_opt_schedule, TKG_SCHEDULE_STATIC);
   p.sched = sched == TKG_SCHEDULE_DYNAMIC ? kSchedDynamic : sched == TKG_SCHEDULE_SINGLE ? kSchedSingle : kSchedStatic;
@@ -543,7 +543,7 @@ tkg_status tkg_debug_set_visit_counter(unsigned int* counts) {
 }
 
 tkg_status tkg_debug_set_fault(int mode) {
-  if (mode < 0 || mode > 1) return TKG_ERR_INVALID_ARG;
+  if (mode < 0 || mode > 2) return TKG_ERR_INVALID_ARG;
   g_fault.store(mode);
   return TKG_OK;
 }
@@ -566,6 +566,11 @@ tkg_status device_sm_count(int* out) {
   const tkg_status st = current_device(&d);
   if (st == TKG_OK) *out = d->sm_count;
   return st;
+}
+
+int take_fault_mode(int mode) {
+  int expected = mode;
+  return g_fault.compare_exchange_strong(expected, 0) ? mode : 0;
 }
 
 tkg_status device_status_word(unsigned int** out) {

@@ -51,6 +51,7 @@ struct AttnParams {
   unsigned int* status;
   unsigned long long timeout_ns;
   int Nq, Nkv;
+  int fault_mode;  // 2: the producer skips the K copies of the first key tile (timeout test)
   float scale_log2;  // log2(e) / sqrt(D): scores enter exp2 pre-multiplied by it
   float scale;       // 1 / sqrt(D)
 };
@@ -182,10 +183,12 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(k_full(ks), C::KV_STAGE);
+        if (!(j == 0 && p.fault_mode == 2)) {
+          mbar_arrive_expect_tx(k_full(ks), C::KV_STAGE);
 #pragma unroll
-        for (int c = 0; c < C::DC; ++c)
-          tma_load_3d(sK + ks * C::KV_STAGE + c * C::CHUNK, &p.tmap_k, k_full(ks), 64 * c, j * C::BKV, bh);
+          for (int c = 0; c < C::DC; ++c)
+            tma_load_3d(sK + ks * C::KV_STAGE + c * C::CHUNK, &p.tmap_k, k_full(ks), 64 * c, j * C::BKV, bh);
+        }
         if (!mbar_wait(v_empty(vs), (static_cast<uint32_t>(j / C::VST) & 1u) ^ 1u, tmo, abort_flag)) {
           ok = false;
           break;
@@ -437,6 +440,7 @@ tkg_status attn_launch(int64_t BH, int64_t Nq, int64_t Nkv, const void* Q, const
   st = device_status_word(&p.status);
   if (st != TKG_OK) return st;
   p.lse = lse;
+  p.fault_mode = take_fault_mode(2);
   p.timeout_ns = timeout_ns;
   p.Nq = static_cast<int>(Nq);
   p.Nkv = static_cast<int>(Nkv);

@@ -37,6 +37,9 @@ size_t nvfp4_scratch_bytes(int blocks_a, int blocks_b, int kstages);
 
 // The current device's SM count, after the library's device check (api.cu).
 tkg_status device_sm_count(int* out);
+// Fault injection for the timeout tests: returns `mode` and disarms it if it is the
+// armed mode (tkg_debug_set_fault), else 0.
+int take_fault_mode(int mode);
 // The current device's status word (device address), after the same check.
 tkg_status device_status_word(unsigned int** out);
 // A tiled TMA tensor map of `rank` dimensions (innermost first): element
