@@ -394,6 +394,13 @@ def run_tkg(args, world, rank, local):
     if not args.no_e2e:
         e2e = run_e2e(ops, dev, w, args)
 
+    # context: cuBLAS on the same shape, operands and stream (the pages' "matches cuBLAS" claim)
+    cublas = None
+    if not args.no_cublas and w.kind in ("bf16", "fp8"):
+        cublas = run_cublas(sets, w, batch, stream, args)
+        if cublas is not None and "value" in cublas:
+            cublas["ours_over_cublas"] = value / world / cublas["value"]
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, dt, n_rows, threads = oracle_sample(ops, args.cpu_s)
@@ -432,6 +439,7 @@ def run_tkg(args, world, rank, local):
                                      f"{PEAK_RATIO[w.kind]:g} (nominal dtype ratio)")},
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "cublas": cublas,
         "gpu_launches": gemms * launches_per_gemm,
         "clocks": clocks,
         "spot_check_rel_err": spot,
@@ -562,6 +570,46 @@ def run_encoder(args, world, rank, local):
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
+
+
+def run_cublas(sets, w, batch, stream, args):
+    """cuBLAS (through torch.matmul for bf16, torch._scaled_mm for FP8 with the same per-tensor
+    scales) on the same operand sets, timed like our step: `batch` products back to back per
+    step, events around the steps.  Context only: no part of the library path."""
+    import torch
+    outs = [torch.empty_like(g.c) for g in sets]
+    if w.kind == "bf16":
+        mats = [(g.a.view(torch.bfloat16), g.b.view(torch.bfloat16)) for g in sets]
+
+        def one(i):
+            a, b = mats[i % len(sets)]
+            torch.matmul(a, b.t(), out=outs[i % len(sets)])
+    else:
+        if not hasattr(torch, "_scaled_mm"):
+            return None
+        mats = [(g.a.view(torch.float8_e4m3fn), g.b.view(torch.float8_e4m3fn), g.scale_a, g.scale_b) for g in sets]
+
+        def one(i):
+            a, b, sa, sb = mats[i % len(sets)]
+            outs[i % len(sets)] = torch._scaled_mm(a, b.t(), scale_a=sa, scale_b=sb, out_dtype=torch.bfloat16)
+    try:
+        with torch.cuda.stream(stream):
+            for i in range(batch * max(1, args.warmup)):
+                one(i)
+            torch.cuda.synchronize()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+            for s in range(args.steps):
+                ev[s][0].record(stream)
+                for i in range(batch):
+                    one(i)
+                ev[s][1].record(stream)
+            torch.cuda.synchronize()
+    except RuntimeError as e:  # a cuBLAS path torch does not offer on this build
+        return {"unavailable": str(e).splitlines()[0][:200]}
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev) / batch
+    return {"value": w.flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "how": "torch.matmul (bf16)" if w.kind == "bf16" else "torch._scaled_mm (e4m3, per-tensor scales)"}
 
 
 def run_e2e(ops, dev, w, args):
@@ -817,6 +865,7 @@ def main(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-check", action="store_true")
+    p.add_argument("--no-cublas", action="store_true", help="skip the cuBLAS comparison (bf16 / FP8 workloads)")
     p.add_argument("--graph", choices=["auto", "on", "off"], default="auto",
                    help="replay each step from a CUDA graph (auto: launch-bound workloads)")
     p.add_argument("--schedule", choices=sorted(SCHEDULE), default="static",
