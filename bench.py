@@ -277,6 +277,7 @@ def run_tkg(args, world, rank, local):
     tkg.tkg_set_option(tkg.TKG_OPT_SCHEDULE, SCHEDULE[args.schedule])
     tkg.tkg_set_option(tkg.TKG_OPT_LAUNCH_OVERLAP,
                        tkg.TKG_OVERLAP_ON if args.overlap == "on" else tkg.TKG_OVERLAP_OFF)
+    tkg.tkg_set_option(tkg.TKG_OPT_SPLIT_K, tkg.TKG_SPLIT_ON if args.split == "on" else tkg.TKG_SPLIT_OFF)
 
     w = synth.WORKLOADS[args.workload]
     ops = synth.workload_operands(args.workload)
@@ -424,7 +425,7 @@ def run_tkg(args, world, rank, local):
                    "l2": (f"{n_sets} rotating operand sets, {n_sets * footprint / 2**20:.0f} MiB > 129 MiB L2"
                           if n_sets > 1 else f"operands {footprint / 2**20:.0f} MiB > 129 MiB L2"),
                    "kernel": info, "group_m": tkg.tkg_get_option(tkg.TKG_OPT_GROUP_M),
-                   "schedule": args.schedule,
+                   "schedule": args.schedule, "split_k_tail": args.split,
                    "launch_overlap": "programmatic dependent launch" if args.overlap == "on" else "off",
                    "cuda_graph": graph is not None},
         "pct_of_peak": 100.0 * value / world / peak,
@@ -872,6 +873,8 @@ def main(argv=None):
                    help="tile schedule: persistent static grid, dynamic (cluster launch control), one cluster per tile")
     p.add_argument("--overlap", choices=["on", "off"], default="on",
                    help="launch GEMMs as programmatic dependents of the previous kernel (on) or plainly (off)")
+    p.add_argument("--split", choices=["on", "off"], default="on",
+                   help="split the tiles of a persistent grid's last, at most half-full round along K")
     args = p.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.impl == "reference":

@@ -202,8 +202,13 @@ TKG_API void tkg_shutdown(void);
  *                      TMEM scale slot per ring stage, the scale warps
  *                      signalling through the stage's own barriers (NVFP4
  *                      only), 8 = variant 7 with the scales brought into
- *                      shared memory by the ring's TMA (NVFP4 only).  A
- *                      variant the kind lacks falls back to the default.
+ *                      shared memory by the ring's TMA (NVFP4 only),
+ *                      9 = 2-SM 256x192 tiles (bf16 and FP8 only),
+ *                      10 / 11 / 12 = clusters of two CTA pairs on
+ *                      horizontally adjacent 256x256 / 256x224 / 256x192
+ *                      tiles, each A tile loaded once and multicast into
+ *                      both pairs (bf16 and FP8 only).  A variant the kind
+ *                      lacks falls back to the default.
  *  TKG_OPT_MAX_CTAS    cap the persistent grid size (0 = all SMs)
  *  TKG_OPT_LAUNCH_OVERLAP
  *                      TKG_OVERLAP_ON (default): GEMMs are launched as
@@ -225,14 +230,31 @@ TKG_API void tkg_shutdown(void);
  *                      (not available with NVFP4 variants 5-7, which return
  *                      TKG_ERR_INVALID_ARG);
  *                      TKG_SCHEDULE_SINGLE = one cluster per tile, each
- *                      computes its own tile only (non-persistent launch). */
+ *                      computes its own tile only (non-persistent launch).
+ *  TKG_OPT_SPLIT_K     TKG_SPLIT_ON (default): in the static schedule, when
+ *                      the persistent grid's last round of tiles would be
+ *                      at most half full, those tiles are cut along K into
+ *                      S = min(CTA pairs / tail tiles, 4) pieces of at
+ *                      least 4 K stages each that run first; each piece
+ *                      writes an fp32 partial to a per-stream workspace
+ *                      (one fp32 128x256 block per SM, created on the
+ *                      stream's first split launch, never while the stream
+ *                      is being captured: such launches run unsplit) and
+ *                      the last piece of a tile adds the partials in piece
+ *                      order and stores it, so results do not depend on
+ *                      timing.  Not used with A multicast (variants 10-12)
+ *                      or NVFP4 variants 5-7.  TKG_SPLIT_OFF: whole tiles
+ *                      only.  After a launch reports TKG_ERR_TIMEOUT,
+ *                      tkg_check_status frees the workspaces (they are made
+ *                      afresh on next use). */
 typedef enum tkg_option {
     TKG_OPT_TIMEOUT_NS = 1,
     TKG_OPT_GROUP_M = 2,
     TKG_OPT_VARIANT = 3,
     TKG_OPT_MAX_CTAS = 4,
     TKG_OPT_LAUNCH_OVERLAP = 5,
-    TKG_OPT_SCHEDULE = 6
+    TKG_OPT_SCHEDULE = 6,
+    TKG_OPT_SPLIT_K = 7
 } tkg_option;
 
 /* Values of TKG_OPT_LAUNCH_OVERLAP and TKG_OPT_SCHEDULE. */
@@ -241,6 +263,8 @@ typedef enum tkg_option {
 #define TKG_SCHEDULE_STATIC 1
 #define TKG_SCHEDULE_DYNAMIC 2
 #define TKG_SCHEDULE_SINGLE 3
+#define TKG_SPLIT_ON 1
+#define TKG_SPLIT_OFF 2
 TKG_API tkg_status tkg_set_option(tkg_option key, int64_t value);
 TKG_API int64_t tkg_get_option(tkg_option key);
 

@@ -43,6 +43,16 @@ TKG_API tkg_status tkg_debug_variant_info(int kind, int variant, int32_t info[6]
  * TKG_OPT_VARIANT). */
 TKG_API int tkg_debug_pick_variant(int kind, int64_t M, int64_t N, int64_t K);
 
+/* Host: the split-K head plan (TKG_OPT_SPLIT_K) for `tiles` output tiles on a
+ * persistent grid of `clusters` clusters with `num_kb` K stages per tile:
+ * *split_tiles tail tiles cut into *split_s pieces each (0 and 1: no split).
+ * Returns 0, or -1 on a null pointer or negative num_kb. */
+TKG_API int tkg_debug_split_plan(int64_t tiles, int64_t clusters, int num_kb, int* split_tiles, int* split_s);
+
+/* Host: work item w of that plan: out = {tile, first K stage, end K stage,
+ * piece index or -1 for a whole tile}.  Returns 0, or -1 on invalid input. */
+TKG_API int tkg_debug_work_item(int w, int split_tiles, int split_s, int num_kb, int out[4]);
+
 /* Fault injection for the device-timeout path: mode 1 makes the next GEMM's
  * producer skip the copies of its first ring stage, mode 2 makes the next
  * attention launch's producer skip the K copies of its first key tile; the
@@ -99,7 +109,7 @@ TKG_API tkg_status tkg_debug_mma_probe(int kind, int n, int ksteps, const void* 
  * operand forms of the attention kernel's P·V product: 10 B MN-major, 11 A
  * read from tensor memory, 12 both; 13 (n = 128): groups of 8 MMAs alternating
  * between the forms of 0 and 12, into two accumulators.  The difference of two counts divided
- * by the difference in MMAs is the per-MMA cost.  n in {128, 256} (128 for
+ * by the difference in MMAs is the per-MMA cost.  n a multiple of 32 in [64, 256] (128 for
  * kind 2 with pattern 1 or 2), count in 1..65536 (at least 2 for patterns 1
  * and 2, which issue count/2 whole pairs).  Synchronous on `stream`. */
 TKG_API tkg_status tkg_debug_mma_rate(int kind, int cta_group, int n, int count, int pattern,

@@ -127,6 +127,69 @@ def test_schedule_and_overlap_options(tkg):
     assert tkg.tkg_get_option(tkg.TKG_OPT_LAUNCH_OVERLAP) == tkg.TKG_OVERLAP_ON
 
 
+def test_split_option(tkg):
+    assert tkg.tkg_get_option(tkg.TKG_OPT_SPLIT_K) == tkg.TKG_SPLIT_ON
+    tkg.tkg_set_option(tkg.TKG_OPT_SPLIT_K, tkg.TKG_SPLIT_OFF)
+    assert tkg.tkg_get_option(tkg.TKG_OPT_SPLIT_K) == tkg.TKG_SPLIT_OFF
+    with pytest.raises(tkg.TkgError):
+        tkg.tkg_set_option(tkg.TKG_OPT_SPLIT_K, 3)
+    tkg.tkg_set_option(tkg.TKG_OPT_SPLIT_K, 0)
+    assert tkg.tkg_get_option(tkg.TKG_OPT_SPLIT_K) == tkg.TKG_SPLIT_ON
+
+
+def simulate_static(tkg, tiles, clusters, num_kb):
+    """Plan the split-K head, walk the static schedule (cluster c takes items
+    c, c + clusters, ...) and return (plan, per-tile K-block coverage, the
+    busiest cluster's work in whole-tile units)."""
+    st, ss = tkg.tkg_debug_split_plan(tiles, clusters, num_kb)
+    items = tiles + st * (ss - 1)
+    cover = np.zeros((tiles, num_kb), dtype=np.int32)
+    load = np.zeros(clusters)
+    pieces = []
+    for w in range(items):
+        tile, kb0, kb1, piece = tkg.tkg_debug_work_item(w, st, ss, num_kb)
+        assert 0 <= tile < tiles and 0 <= kb0 < kb1 <= num_kb
+        assert (piece >= 0) == (w < st * ss) and (piece < 0 or piece == w)
+        cover[tile, kb0:kb1] += 1
+        load[w % clusters] += (kb1 - kb0) / num_kb
+        if piece >= 0:
+            pieces.append((tile, piece % ss, kb0, kb1))
+    return (st, ss), cover, load.max(), pieces
+
+
+@pytest.mark.parametrize("tiles,clusters,num_kb", [
+    (256, 76, 64),     # bf16 4096^3 on 76 CTA pairs: 3 rounds + 28 tail tiles
+    (1024, 76, 64),    # FP8 8192^3
+    (1024, 76, 128),   # bf16 8192^3
+    (4096, 76, 128),   # NVFP4 16384^3: tail 68 of 76, no split
+    (16, 76, 32), (1, 76, 16), (1, 76, 3), (77, 76, 64), (152, 76, 64), (190, 76, 8), (5, 2, 40),
+    (3, 1, 64), (100, 152, 64)])
+def test_split_plan_covers_every_k_block_once_and_shortens_the_last_round(tkg, tiles, clusters, num_kb):
+    (st, ss), cover, busiest, pieces = simulate_static(tkg, tiles, clusters, num_kb)
+    assert (cover == 1).all()  # every tile's K blocks, exactly once
+    rounds = -(-tiles // clusters)
+    tail = tiles - (rounds - 1) * clusters
+    if st:
+        assert st == tail and 2 <= ss <= 4 and st * ss <= clusters and num_kb // ss >= 4
+        assert busiest == pytest.approx(rounds - 1 + 1 / ss, abs=1e-9)
+        # the pieces of one tile run side by side in the first round
+        for tile, s, kb0, kb1 in pieces:
+            assert kb0 == s * num_kb // ss and kb1 == (s + 1) * num_kb // ss
+    else:
+        assert ss == 1
+        assert 2 * tail > clusters or min(clusters // tail, 4, num_kb // 4) < 2 or clusters < 2
+        assert busiest == pytest.approx(rounds)
+
+
+def test_split_plan_bf16_4096_example(tkg):
+    # 4096^3 bf16 with 256x256 pair tiles: 256 tiles, 76 pairs, 64 K stages of 64
+    assert tkg.tkg_debug_split_plan(256, 76, 64) == (28, 2)
+    assert tkg.tkg_debug_work_item(0, 28, 2, 64) == (0, 0, 32, 0)
+    assert tkg.tkg_debug_work_item(1, 28, 2, 64) == (0, 32, 64, 1)
+    assert tkg.tkg_debug_work_item(56, 28, 2, 64) == (28, 0, 64, -1)
+    assert tkg.tkg_debug_work_item(283, 28, 2, 64) == (255, 0, 64, -1)
+
+
 def test_dynamic_schedule_rejects_static_scale_warp_variants(tkg):
     # NVFP4 variants 5-7 walk a precomputed tile sequence in their scale warps:
     # the dynamic schedule is refused for them before any CUDA call
@@ -190,7 +253,8 @@ def test_compiled_variants_fit_the_sm(tkg):
 
 def test_mma_rate_probe_arguments_checked(tkg):
     c = ctypes.c_ulonglong(0)
-    for args in [(3, 1, 256, 64, 0), (0, 3, 256, 64, 0), (0, 1, 192, 64, 0), (0, 1, 256, 0, 0),
+    for args in [(3, 1, 256, 64, 0), (0, 3, 256, 64, 0), (0, 1, 200, 64, 0), (0, 1, 288, 64, 0), (0, 1, 32, 64, 0),
+                 (0, 1, 256, 0, 0),
                  (0, 1, 256, 65537, 0), (0, 1, 256, 64, 3), (2, 1, 256, 64, 1), (0, 1, 256, 1, 1), (0, 1, 256, 64, 3), (2, 1, 256, 64, 10)]:
         assert tkg.lib.tkg_debug_mma_rate(*args, ctypes.byref(c), None) == tkg.TKG_ERR_INVALID_ARG
     assert tkg.lib.tkg_debug_mma_rate(0, 1, 256, 64, 0, None, None) == tkg.TKG_ERR_INVALID_ARG

@@ -123,6 +123,49 @@ def test_static_capped_grid_visits_each_tile_once(tkg):
     check_against_oracle("bf16", g.c_bits(), acc, c_ref)
 
 
+# ---- narrower tiles, A multicast between CTA pairs ------------------------------
+
+@pytest.fixture
+def variant(tkg, request):
+    tkg.tkg_set_option(tkg.TKG_OPT_VARIANT, request.param)
+    yield request.param
+    tkg.tkg_set_option(tkg.TKG_OPT_VARIANT, 0)
+
+
+# odd and even numbers of tile columns (the second pair's last tile of an odd
+# row lies right of C), one tile row, one column, and many rows per cluster
+MC_SHAPES = [(300, 520, 200), (256, 1024, 128), (1000, 1000, 512), (77, 100, 40), (2048, 1536, 64),
+             (512, 2100, 128)]
+
+
+@pytest.mark.parametrize("variant", [9, 10, 11, 12], indirect=True)
+@pytest.mark.parametrize("schedule", list(SCHEDULES), indirect=True)
+@pytest.mark.parametrize("kind", ["bf16", "fp8"])
+def test_tile_variants_match_oracle_and_visit_each_tile_once(tkg, variant, schedule, kind):
+    """256x192 tiles, and clusters of two CTA pairs sharing A."""
+    for i, (M, N, K) in enumerate(MC_SHAPES):
+        if kind == "fp8":
+            K = -(-K // 16) * 16
+        ops = synth.make_operands(kind, M, N, K, "normal_sqrtk" if kind == "bf16" else "normal", 70 + i, 75 + i)
+        g, counts = run_counted(tkg, ops)
+        assert (counts == 1).all(), (variant, schedule, M, N, K, np.unique(counts, return_counts=True))
+        acc, c_ref = oracle.gemm(ops)
+        check_against_oracle(kind, g.c_bits(), acc, c_ref, ops.scale_a, ops.scale_b)
+
+
+@pytest.mark.parametrize("variant", [10, 12], indirect=True)
+def test_multicast_one_cluster_walks_every_unit(tkg, variant):
+    ops = synth.small_int_operands("bf16", 1280, 1600, 256, seed=11)
+    tkg.tkg_set_option(tkg.TKG_OPT_MAX_CTAS, 4)
+    try:
+        g, counts = run_counted(tkg, ops)
+    finally:
+        tkg.tkg_set_option(tkg.TKG_OPT_MAX_CTAS, 0)
+    assert (counts == 1).all()
+    _, c_ref = oracle.gemm(ops)
+    assert np.array_equal(g.c_bits(), c_ref)
+
+
 # ---- launch overlap (programmatic dependent launch) -------------------------
 
 def _chain(tkg, overlap, schedule, reps):
@@ -165,13 +208,18 @@ def test_overlapped_launches_keep_stream_order(tkg, schedule):
     for r in range(8):
         assert np.array_equal(p2[r], o2[r]), r
         assert np.array_equal(p3[r], o3[r]), r
-    # x3[r] is a[r+1]·b1ᵀ: the identity GEMM copied a[r+1] exactly before x3 read it
+    # x3[r] is a[r+1]·b1ᵀ: the identity GEMM copied a[r+1] exactly before x3 read it (the
+    # reference runs in the same schedule, so that it splits K, or not, as the chain did)
     n = 1024
     ref = torch.empty(n, n, dtype=torch.bfloat16, device="cuda")
-    for r in range(8):
-        tkg.tkg_gemm_bf16(n, n, n, a[r + 1], b1, ref)
-        assert tkg.tkg_check_status() == tkg.TKG_OK
-        assert np.array_equal(ref.view(torch.int16).cpu().numpy(), o3[r]), r
+    tkg.tkg_set_option(tkg.TKG_OPT_SCHEDULE, schedule)
+    try:
+        for r in range(8):
+            tkg.tkg_gemm_bf16(n, n, n, a[r + 1], b1, ref)
+            assert tkg.tkg_check_status() == tkg.TKG_OK
+            assert np.array_equal(ref.view(torch.int16).cpu().numpy(), o3[r]), r
+    finally:
+        tkg.tkg_set_option(tkg.TKG_OPT_SCHEDULE, 0)
 
 
 def test_overlapped_chain_matches_oracle(tkg):

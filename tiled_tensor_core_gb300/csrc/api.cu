@@ -27,6 +27,8 @@ using namespace tkg;
 
 constexpr int64_t kDefaultTimeoutNs = 2000000000LL;
 constexpr int64_t kDefaultGroupM = 8;
+constexpr int kMaxSplit = 4;     // split-K head: at most 4 pieces per tile
+constexpr int kMinSplitKb = 4;   // of at least 4 K blocks each
 constexpr int kMaxDevices = 64;
 constexpr int kNumKinds = 3;
 
@@ -36,6 +38,7 @@ std::atomic<int64_t> g_opt_variant{0};
 std::atomic<int64_t> g_opt_max_ctas{0};
 std::atomic<int64_t> g_opt_overlap{0};
 std::atomic<int64_t> g_opt_schedule{0};
+std::atomic<int64_t> g_opt_split{0};
 std::atomic<int> g_fault{0};
 std::atomic<unsigned int*> g_visits{nullptr};
 
@@ -49,6 +52,13 @@ struct DevState {
   unsigned int* status = nullptr;
   int max_clusters[kNumKinds][kNumVariants] = {};
   cudaMemPool_t pool = nullptr;  // stream-ordered scratch for the NVFP4 scale interleave
+  // split-K head: a workspace and zeroed piece counters per stream (launches on one stream are
+  // ordered, and the kernel leaves the counters at zero), created on first use outside capture
+  struct SplitWs {
+    float* ws = nullptr;
+    unsigned int* cnt = nullptr;
+  };
+  std::unordered_map<cudaStream_t, SplitWs> split;
 };
 DevState g_dev[kMaxDevices];
 
@@ -191,16 +201,19 @@ const KernelVariant* variant_of(int kind, int id) {
   }
 }
 
-// Tile choice: the 2-SM 256 x 256 tile.  (A 256 x 224 tile would balance the
-// persistent rounds of some shapes, e.g. 4096^2 -> 304 tiles = 4 x 76, but on
-// sm_103a an N = 224 MMA takes as long as N = 256, so it gains nothing; it is
-// kept as an explicit variant.)  NVFP4 takes the scale-warp form of that tile
-// with one scale slot per ring stage and the scales riding the ring: copying
-// the block scales with tcgen05.cp costs the tensor pipe about 60 cycles per
-// copy, twelve copies per 256-deep K stage; coupling the slots to the stages
-// saves the MMA thread a second wait per stage; and reading the scales from
-// shared memory, where the ring's TMA put them stages ahead, keeps global-load
-// latency off the scale warps' critical path.
+// Tile choice: the 2-SM 256 x 256 tile.  An MMA of N columns costs about
+// max(77, N / 2) cycles on sm_103a, so narrower tiles (N = 224, 192) keep the
+// tensor pipe's rate per column, but each SM then receives more operand bytes
+// per flop (A is re-read for every tile column) and the measured throughput
+// falls with that ratio; sharing A between two CTA pairs by TMA multicast
+// (variants 10-12) saves L2 reads and power but not throughput.  Those tiles
+// are kept as explicit variants.  NVFP4 takes the scale-warp form of the
+// 256 x 256 tile with one scale slot per ring stage and the scales riding the
+// ring: copying the block scales with tcgen05.cp costs the tensor pipe about
+// 60 cycles per copy, twelve copies per 256-deep K stage; coupling the slots to
+// the stages saves the MMA thread a second wait per stage; and reading the
+// scales from shared memory, where the ring's TMA put them stages ahead, keeps
+// global-load latency off the scale warps' critical path.
 int pick_variant(int kind, int64_t M, int64_t N, int64_t K) {
   (void)K;
   (void)M;
@@ -224,12 +237,12 @@ tkg_status max_clusters(DevState& d, int kind, int id, const KernelVariant& v, i
     return TKG_ERR_CUDA;
   }
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>(v.cg * d.sm_count), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(v.cg * v.mc * d.sm_count), 1, 1);
   cfg.blockDim = dim3(static_cast<unsigned>(v.threads), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(v.smem_bytes);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(v.cg);
+  attr[0].val.clusterDim.x = static_cast<unsigned>(v.cg * v.mc);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
@@ -246,6 +259,62 @@ tkg_status max_clusters(DevState& d, int kind, int id, const KernelVariant& v, i
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Split-K head plan for `tiles` output tiles on a persistent grid of `clusters`
+// clusters walking `num_kb` K blocks per tile.  The grid takes R = ceil(tiles /
+// clusters) rounds, the last holding `tail` tiles; if that round would be at
+// most half full, the tail tiles are cut into S = min(clusters / tail, 4,
+// num_kb / 4) pieces (at least 4 K blocks each) that run first, next to whole
+// tiles, so the grid finishes after R - 1 + 1/S rounds of work instead of R.
+void split_plan(int64_t tiles, int64_t clusters, int num_kb, int* split_tiles, int* split_s) {
+  *split_tiles = 0;
+  *split_s = 1;
+  if (tiles < 1 || clusters < 2) return;
+  const int64_t rounds = (tiles + clusters - 1) / clusters;
+  const int64_t tail = tiles - (rounds - 1) * clusters;
+  if (2 * tail > clusters) return;
+  int64_t s = clusters / tail;
+  if (s > kMaxSplit) s = kMaxSplit;
+  if (s > num_kb / kMinSplitKb) s = num_kb / kMinSplitKb;
+  if (s < 2) return;
+  *split_tiles = static_cast<int>(tail);
+  *split_s = static_cast<int>(s);
+}
+
+// The stream's split workspace (created on first use; not while the stream is
+// being captured, where the caller runs without the split instead).  Capacity:
+// one 128 x 256 fp32 block per SM (pieces <= clusters, CTAs <= SMs) and eight
+// counters per SM (tail tiles x CTAs x epilogue warps).
+bool split_workspace(DevState& d, cudaStream_t stream, DevState::SplitWs* out) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = d.split.find(stream);
+    if (it != d.split.end()) {
+      *out = it->second;
+      return true;
+    }
+  }
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+    cudaGetLastError();
+    return false;
+  }
+  DevState::SplitWs w;
+  const size_t ws_bytes = static_cast<size_t>(d.sm_count) * 128 * 256 * sizeof(float);
+  const size_t cnt_bytes = static_cast<size_t>(d.sm_count) * 8 * sizeof(unsigned int);
+  if (cudaMalloc(reinterpret_cast<void**>(&w.ws), ws_bytes) != cudaSuccess ||
+      cudaMalloc(reinterpret_cast<void**>(&w.cnt), cnt_bytes) != cudaSuccess ||
+      cudaMemsetAsync(w.cnt, 0, cnt_bytes, stream) != cudaSuccess) {
+    cudaGetLastError();
+    if (w.ws) cudaFree(w.ws);
+    if (w.cnt) cudaFree(w.cnt);
+    return false;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  d.split.emplace(stream, w);
+  *out = w;
+  return true;
+}
 
 // Common host-only checks (no CUDA call), then device checks and the launch.
 tkg_status gemm_launch(int kind, int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* C,
@@ -281,6 +350,9 @@ tkg_status gemm_launch(int kind, int64_t M, int64_t N, int64_t K, const void* A,
   const int64_t tiles_m = (M + tile_m - 1) / tile_m;
   const int64_t tiles_n = (N + v->bn - 1) / v->bn;
   if (tiles_m * tiles_n > kMax) return TKG_ERR_INVALID_ARG;
+  // scheduling units: one tile, or (A multicast) `mc` horizontally adjacent tiles, one per CTA pair
+  const int64_t units = tiles_m * ((tiles_n + v->mc - 1) / v->mc);
+  const int64_t cl = static_cast<int64_t>(v->cg) * v->mc;  // CTAs per cluster
 
   DevState* d = nullptr;
   tkg_status st = current_device(&d);
@@ -291,11 +363,12 @@ tkg_status gemm_launch(int kind, int64_t M, int64_t N, int64_t K, const void* A,
   // Operand maps: rows of K elements, boxes of 128 bytes x (rows per CTA).
   const uint32_t b_rows = static_cast<uint32_t>(v->bn / v->cg);
   if (kind == 0) {
-    st = get_map(&p.tmap_a, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, K * 2, 64, 128, 128);
+    // A multicast between two CTA pairs: each CTA loads a 64-row quarter of the pair tile's A
+    st = get_map(&p.tmap_a, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, K * 2, 64, 128 / v->mc, 128);
     if (st == TKG_OK) st = get_map(&p.tmap_b, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, N, K * 2, 64, b_rows, 128);
   } else {
     const int64_t row_bytes = kind == 1 ? K : K / 2;
-    st = get_map(&p.tmap_a, A, CU_TENSOR_MAP_DATA_TYPE_UINT8, row_bytes, M, row_bytes, 128, 128, 128);
+    st = get_map(&p.tmap_a, A, CU_TENSOR_MAP_DATA_TYPE_UINT8, row_bytes, M, row_bytes, 128, 128 / v->mc, 128);
     if (st == TKG_OK)
       st = get_map(&p.tmap_b, B, CU_TENSOR_MAP_DATA_TYPE_UINT8, row_bytes, N, row_bytes, 128, b_rows, 128);
   }
@@ -373,20 +446,39 @@ tkg_status gemm_launch(int kind, int64_t M, int64_t N, int64_t K, const void* A,
   }
   int64_t grid_clusters = clusters;
   const int64_t cap = g_opt_max_ctas.load(std::memory_order_relaxed);
-  if (cap > 0 && cap / v->cg < grid_clusters) grid_clusters = cap / v->cg > 0 ? cap / v->cg : 1;
-  if (tiles_m * tiles_n < grid_clusters) grid_clusters = tiles_m * tiles_n;
-  // one cluster per tile: the hardware places them as SMs free up (and, in the
+  if (cap > 0 && cap / cl < grid_clusters) grid_clusters = cap / cl > 0 ? cap / cl : 1;
+
+  // split-K head (static schedule; not with A multicast, nor with the NVFP4 variants whose
+  // scale warps walk a precomputed sequence), planned for the clusters the grid may use
+  p.split_s = 1;
+  int64_t items = units;
+  if (p.sched == kSchedStatic && v->mc == 1 && opt_or(g_opt_split, TKG_SPLIT_ON) == TKG_SPLIT_ON &&
+      !(kind == 2 && (id == kVariant2Sm256x256Sfw || id == kVariant2Sm256x256Hybrid ||
+                      id == kVariant2Sm256x256Coupled))) {
+    int split_tiles = 0, split_s = 1;
+    split_plan(units, grid_clusters, p.num_kb, &split_tiles, &split_s);
+    DevState::SplitWs w;
+    if (split_tiles > 0 && split_workspace(*d, static_cast<cudaStream_t>(stream), &w)) {
+      p.split_tiles = split_tiles;
+      p.split_s = split_s;
+      p.split_ws = w.ws;
+      p.split_cnt = w.cnt;
+      items = units + static_cast<int64_t>(split_tiles) * (split_s - 1);
+    }
+  }
+  if (items < grid_clusters) grid_clusters = items;
+  // one cluster per unit: the hardware places them as SMs free up (and, in the
   // dynamic schedule, running clusters cancel and take over those not started)
-  if (p.sched != kSchedStatic) grid_clusters = tiles_m * tiles_n;
+  if (p.sched != kSchedStatic) grid_clusters = units;
 
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid_clusters * v->cg), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(grid_clusters * cl), 1, 1);
   cfg.blockDim = dim3(static_cast<unsigned>(v->threads), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(v->smem_bytes);
   cfg.stream = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(v->cg);
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cl);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   // programmatic dependent launch: this grid's CTAs may start (and run their
@@ -445,6 +537,15 @@ tkg_status tkg_check_status(void* stream) {
       cudaGetLastError();
       return TKG_ERR_CUDA;
     }
+    // a GEMM that gave up may have left split-K piece counts behind: drop every split
+    // workspace of the device (cudaFree waits for the device), the next use makes fresh ones
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (auto& kv : d->split) {
+      cudaFree(kv.second.ws);
+      cudaFree(kv.second.cnt);
+    }
+    d->split.clear();
+    cudaGetLastError();
   }
   return (word & kStatusTimeout) ? TKG_ERR_TIMEOUT : TKG_OK;
 }
@@ -494,6 +595,10 @@ tkg_status tkg_set_option(tkg_option key, int64_t value) {
       if (value > TKG_SCHEDULE_SINGLE) return TKG_ERR_INVALID_ARG;
       g_opt_schedule.store(value);
       return TKG_OK;
+    case TKG_OPT_SPLIT_K:
+      if (value > TKG_SPLIT_OFF) return TKG_ERR_INVALID_ARG;
+      g_opt_split.store(value);
+      return TKG_OK;
   }
   return TKG_ERR_INVALID_ARG;
 }
@@ -506,6 +611,7 @@ int64_t tkg_get_option(tkg_option key) {
     case TKG_OPT_MAX_CTAS: return g_opt_max_ctas.load();
     case TKG_OPT_LAUNCH_OVERLAP: return opt_or(g_opt_overlap, TKG_OVERLAP_ON);
     case TKG_OPT_SCHEDULE: return opt_or(g_opt_schedule, TKG_SCHEDULE_STATIC);
+    case TKG_OPT_SPLIT_K: return opt_or(g_opt_split, TKG_SPLIT_ON);
   }
   return -1;
 }
@@ -536,6 +642,22 @@ tkg_status tkg_debug_variant_info(int kind, int variant, int32_t info[6]) {
 }
 
 int tkg_debug_pick_variant(int kind, int64_t M, int64_t N, int64_t K) { return pick_variant(kind, M, N, K); }
+
+int tkg_debug_split_plan(int64_t tiles, int64_t clusters, int num_kb, int* split_tiles, int* split_s) {
+  if (!split_tiles || !split_s || num_kb < 0) return -1;
+  split_plan(tiles, clusters, num_kb, split_tiles, split_s);
+  return 0;
+}
+
+int tkg_debug_work_item(int w, int split_tiles, int split_s, int num_kb, int out[4]) {
+  if (!out || w < 0 || split_tiles < 0 || split_s < 1 || num_kb < 1) return -1;
+  const WorkItem wk = work_item(w, split_tiles, split_s, num_kb);
+  out[0] = wk.tile;
+  out[1] = wk.kb0;
+  out[2] = wk.kb1;
+  out[3] = wk.piece;
+  return 0;
+}
 
 tkg_status tkg_debug_set_visit_counter(unsigned int* counts) {
   g_visits.store(counts);

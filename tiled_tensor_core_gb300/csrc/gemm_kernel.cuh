@@ -61,6 +61,12 @@ struct GemmParams {
   const uint8_t* sf_b;  // same for B
   int sched;            // tile schedule (kSchedStatic / kSchedDynamic / kSchedSingle)
   unsigned int* visits;  // debug: if set, one increment per tile each time a CTA (pair) stores it
+  // split-K head of the static schedule (split_tiles = 0: off): the first split_tiles tiles of
+  // the tile order are cut into split_s K-ranges, run as the first work items
+  int split_tiles;
+  int split_s;
+  float* split_ws;            // fp32 partial accumulators, one block per (piece, CTA, epilogue warp)
+  unsigned int* split_cnt;    // per (split tile, CTA, epilogue warp): pieces stored so far (reset to 0)
 };
 
 // Tile schedules ("Persistent Grid Launch"; Cluster Launch Control for the
@@ -76,6 +82,30 @@ struct GemmParams {
 //   kSchedSingle:  one cluster per tile, each does its own tile only (the
 //                  non-persistent launch).
 constexpr int kSchedStatic = 0, kSchedDynamic = 1, kSchedSingle = 2;
+
+// Split-K head ("Persistent Grid Launch": the persistent grid walks T output
+// tiles in rounds of P clusters; when the last round would be at most half
+// full, its tail tiles are cut into S pieces along K instead and run first).
+// Work item w < split_tiles * S is piece s = w % S of tile w / S, covering the
+// K blocks [s * num_kb / S, (s + 1) * num_kb / S); item w >= split_tiles * S is
+// the whole tile w - split_tiles * (S - 1).  Every piece writes its fp32
+// partial accumulator to a workspace and counts itself in; the piece that
+// counts last adds the S partials in the order s = 0, 1, ... (so the result
+// does not depend on which finished last), stores the tile and resets the
+// count.  Nothing waits on another CTA.
+struct WorkItem {
+  int tile;
+  int kb0, kb1;
+  int piece;  // -1: whole tile
+};
+__host__ __device__ inline WorkItem work_item(int w, int split_tiles, int split_s, int num_kb) {
+  const int split_items = split_tiles * split_s;
+  if (w < split_items) {
+    const int s = w % split_s;
+    return WorkItem{w / split_s, s * num_kb / split_s, (s + 1) * num_kb / split_s, w};
+  }
+  return WorkItem{w - split_items + split_tiles, 0, num_kb, -1};
+}
 
 // Block-scale staging modes (NVFP4).
 //   kSfCopy: the scales ride the shared-memory ring with the operands and the
@@ -94,10 +124,15 @@ constexpr int kSchedStatic = 0, kSchedDynamic = 1, kSchedSingle = 2;
 constexpr int kSfCopy = 0, kSfWarps = 1, kSfHybrid = 2;
 
 template <Kind KIND_, int CG_, int BN_, int STAGES_, int EPI_WARPS_, int NUM_ACC_ = 2, int SF_MODE_ = kSfCopy,
-          int SF_GROUPS_ = 1, bool SF_COUPLED_ = false, bool SF_SMEM_ = false>
+          int SF_GROUPS_ = 1, bool SF_COUPLED_ = false, bool SF_SMEM_ = false, int MC_ = 1>
 struct GemmCfg {
   static constexpr Kind KIND = KIND_;
   static constexpr int CG = CG_;                // CTAs per MMA (1, or 2 for the CTA pair)
+  // CTA pairs per cluster: 2 = two pairs on horizontally adjacent tiles (same A rows)
+  // share A — each CTA loads one 64-row quarter of the pair tile's A rows and
+  // multicasts it into the same place in its counterpart of the other pair
+  static constexpr int MC = MC_;
+  static constexpr int CL = CG * MC;            // CTAs per cluster
   static constexpr int BN = BN_;                // output-tile columns (whole pair)
   static constexpr int BM = 128;                // output-tile rows per CTA = TMEM lanes
   static constexpr int STAGES = STAGES_;
@@ -185,7 +220,7 @@ struct GemmCfg {
   static constexpr int OFF_SCHED = (OFF_MISC + 16 + 15) / 16 * 16;
   // readers of every answer: each CTA's producer lane, epilogue warps and scale
   // warps, and the leader's MMA lane
-  static constexpr int SCHED_READERS = CG * (1 + EPI_WARPS + SF_WARPS) + 1;
+  static constexpr int SCHED_READERS = CL * (1 + EPI_WARPS + SF_WARPS) + MC;
   static constexpr int SMEM_BYTES = OFF_SCHED + 16 * SCHED_SLOTS + 1024;  // + slack to align the base to 1024
 
   static_assert(B_STAGE % 1024 == 0 && A_STAGE % 1024 == 0, "stages must keep 1024-byte swizzle atoms aligned");
@@ -204,6 +239,7 @@ struct GemmCfg {
   static_assert(!SF_HYBRID || SF_GROUPS == 1, "the hybrid mode's A scales need one group");
   static_assert(SF_SMEM == SF_SMEM_, "shared-memory scale staging is a form of the coupled scale-warp mode");
   static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB shared-memory limit");
+  static_assert(MC == 1 || (MC == 2 && CG == 2 && !SCALED), "A multicast: two CTA pairs, unscaled kinds");
 };
 
 __device__ __forceinline__ void record_timeout(unsigned int* status, int role, volatile int* abort_flag) {
@@ -262,17 +298,31 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = (C::CG == 2) ? cluster_ctarank() : 0u;
-  const int cluster_id = blockIdx.x / C::CG;
-  const int num_clusters = gridDim.x / C::CG;
-  const int num_tiles = p.tiles_m * p.tiles_n;
-  const TileOrder order{p.tiles_m, p.tiles_n, p.group_m};
+  const uint32_t rank = (C::CL > 1) ? cluster_ctarank() : 0u;  // rank in the cluster
+  const uint32_t prank = rank % C::CG;                         // rank in the CTA pair
+  const int pair = static_cast<int>(rank) / C::CG;             // pair in the cluster
+  const uint32_t leader = rank - prank;                        // the pair's MMA-issuing CTA
+  const int cluster_id = blockIdx.x / C::CL;
+  const int num_clusters = gridDim.x / C::CL;
+  // scheduling unit: MC horizontally adjacent output tiles, one per pair
+  const int tiles_nu = (p.tiles_n + C::MC - 1) / C::MC;
+  const int num_units = p.tiles_m * tiles_nu;
+  // work items: tiles (units), each of the split_tiles first ones replaced by split_s pieces
+  const int num_tiles = num_units + p.split_tiles * (p.split_s - 1);
+  const TileOrder order{p.tiles_m, tiles_nu, p.group_m};
+  auto work_of = [&](int w) { return work_item(w, p.split_tiles, p.split_s, p.num_kb); };
+  auto tile_coord = [&](int t, int& tm, int& tn) {
+    order.coord(t, tm, tn);
+    tn = tn * C::MC + pair;
+  };
   const uint64_t tmo = p.timeout_ns;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(full_bar(s), C::SF_COUPLED ? 1 + C::CG * 4 : 1);  // + one arrival per scale warp of the group
-      mbar_init(empty_bar(s), 1);
+      // A multicast: every CTA writes A into both pairs' stages, so a stage is free for it once
+      // both pairs' MMAs have read it
+      mbar_init(empty_bar(s), C::MC);
     }
     for (int a = 0; a < C::NUM_ACC; ++a) {
       mbar_init(tfull_bar(a), 1);
@@ -309,7 +359,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
   }
   tc_fence_before();
   __syncthreads();
-  if constexpr (C::CG == 2) {
+  if constexpr (C::CL > 1) {
     cluster_arrive();
     cluster_wait();
   }
@@ -325,7 +375,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
 
   // ---------------------------------------------------------------- tile sequence
   const int first_tile = cluster_id < num_tiles ? cluster_id : -1;
-  const uint32_t sched_empty_leader0 = (C::CG == 2) ? mapa_shared(sched_empty_bar(0), 0) : sched_empty_bar(0);
+  const uint32_t sched_empty_leader0 = (C::CL > 1) ? mapa_shared(sched_empty_bar(0), 0) : sched_empty_bar(0);
   // The tile after tile t, the k-th (k = 0, 1, ...) of this CTA's sequence, or
   // -1 when there is none.  Called by one thread of each role, in order k.
   auto next_tile = [&](int t, int k, bool& ok) -> int {
@@ -344,7 +394,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
     // decoded into a register before the slot is handed back for the next answer
     const int x = clc_first_ctaid_x(ld_shared_v4(sResp + 16u * static_cast<uint32_t>(j)));
     mbar_arrive_cluster(sched_empty_leader0 + 8u * static_cast<uint32_t>(j));
-    return x < 0 ? -1 : x / C::CG;
+    return x < 0 ? -1 : x / C::CL;
   };
   // Dynamic schedule, the leader's producer lane at the start of its k-th tile:
   // ask for the tile after it, answered into slot k % SCHED_SLOTS of every CTA
@@ -354,9 +404,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
     const uint32_t ph = static_cast<uint32_t>(k / C::SCHED_SLOTS) & 1u;
     if (!mbar_wait(sched_empty_bar(j), ph ^ 1u, tmo, abort_flag)) return false;
 #pragma unroll
-    for (int r = 0; r < C::CG; ++r)
-      mbar_arrive_expect_tx_cluster(C::CG == 2 ? mapa_shared(sched_full_bar(j), static_cast<uint32_t>(r))
-                                               : sched_full_bar(j),
+    for (int r = 0; r < C::CL; ++r)
+      mbar_arrive_expect_tx_cluster(C::CL > 1 ? mapa_shared(sched_full_bar(j), static_cast<uint32_t>(r))
+                                              : sched_full_bar(j),
                                     16u);
     clc_try_cancel_multicast(sResp + 16u * static_cast<uint32_t>(j), sched_full_bar(j));
     return true;
@@ -384,19 +434,29 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
           ok = false;
           break;
         }
+        const WorkItem wk = work_of(t);
         int tm, tn;
-        order.coord(t, tm, tn);
-        const int a_row = tm * (C::BM * C::CG) + static_cast<int>(rank) * C::BM;
-        const int b_row = tn * C::BN + static_cast<int>(rank) * C::B_ROWS;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        tile_coord(wk.tile, tm, tn);
+        const int a_row = tm * (C::BM * C::CG) + static_cast<int>(prank) * C::BM;
+        const int b_row = tn * C::BN + static_cast<int>(prank) * C::B_ROWS;
+        for (int kb = wk.kb0; kb < wk.kb1; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, tmo, abort_flag)) {
             ok = false;
             break;
           }
-          const uint32_t fb = (C::CG == 2) ? mapa_shared(full_bar(stage), 0) : full_bar(stage);
-          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), C::STAGE_TX * C::CG);
+          const uint32_t fb = (C::CG == 2) ? mapa_shared(full_bar(stage), leader) : full_bar(stage);
+          if (prank == 0) mbar_arrive_expect_tx(full_bar(stage), C::STAGE_TX * C::CG);
           if (!(first && p.fault_mode == 1)) {
-            tma_load_2d<C::CG>(sA + stage * C::A_STAGE, &p.tmap_a, fb, kb * C::K_TMAP, a_row);
+            if constexpr (C::MC == 2) {
+              // rows [64 pair, 64 pair + 64) of A half `prank`, into the same stage of this CTA
+              // and of its counterpart in the other pair (each destination's completion lands on
+              // its own pair leader's full barrier)
+              tma_load_2d_mc_pair(sA + stage * C::A_STAGE + static_cast<uint32_t>(pair) * (C::A_STAGE / 2), &p.tmap_a,
+                                  fb, kb * C::K_TMAP, a_row + pair * (C::BM / 2),
+                                  static_cast<uint16_t>((1u << prank) | (1u << (prank + 2))));
+            } else {
+              tma_load_2d<C::CG>(sA + stage * C::A_STAGE, &p.tmap_a, fb, kb * C::K_TMAP, a_row);
+            }
             tma_load_2d<C::CG>(sB + stage * C::B_STAGE, &p.tmap_b, fb, kb * C::K_TMAP, b_row);
             // staged scales: 2 KB (16 rows of 128 B) per (K stage, 128-row block), the blocks of one
             // K stage contiguous
@@ -427,7 +487,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ COMPUTE
-    if (lane == 0 && rank == 0) {
+    if (lane == 0 && prank == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int slot = 0;  // scale-warp mode: TMEM scale slot
@@ -443,7 +503,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::ACC_STRIDE);
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        const WorkItem wk = work_of(t);
+        for (int kb = wk.kb0; kb < wk.kb1; ++kb) {
           if (!mbar_wait(full_bar(stage), phase, tmo, abort_flag)) {
             ok = false;
             break;
@@ -480,7 +541,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
           for (int kk = 0; kk < C::KSTEPS; ++kk) {
             const uint64_t ad = sdesc_sw128(a0 + 32u * kk);
             const uint64_t bd = sdesc_sw128(b0 + 32u * kk);
-            const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
+            const uint32_t accum = (kb != wk.kb0 || kk != 0) ? 1u : 0u;
             if constexpr (C::KIND == Kind::BF16)
               mma_bf16<C::CG>(d_tmem, ad, bd, C::IDESC, accum);
             else if constexpr (C::KIND == Kind::FP8)
@@ -489,7 +550,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
               mma_mxf4nvf4<C::CG>(d_tmem, ad, bd, C::IDESC, sf_tmem + 4u * kk,
                                   sf_tmem + C::SF_COLS_A + (C::BN / 32) * kk, accum);
           }
-          mma_commit<C::CG>(empty_bar(stage), 0x3);
+          // the stage is free for this pair's CTAs and (A multicast) for the other pair's, which
+          // load half of this pair's A
+          mma_commit<C::CG>(empty_bar(stage), C::MC == 2 ? 0xF : 0x3);
           if constexpr (C::SF_WARPS_MODE && !C::SF_COUPLED) {
             mma_commit<C::CG>(sf_empty_bar(slot), 0x3);
             if (++slot == C::SF_SLOTS) {
@@ -503,10 +566,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
           }
         }
         if (!ok) break;
-        mma_commit<C::CG>(tfull_bar(acc), 0x3);
+        mma_commit<C::CG>(tfull_bar(acc), static_cast<uint16_t>(0x3u << (C::CG * pair)));
       }
       // No MMA may still be writing TMEM when it is released.
-      mma_commit<C::CG>(drain_bar, 0x1);
+      mma_commit<C::CG>(drain_bar, static_cast<uint16_t>(0x1u << (C::CG * pair)));
       mbar_wait(drain_bar, 0, tmo, never_abort);
       if (!ok) record_timeout(p.status, kRoleMma, abort_flag);
     }
@@ -523,13 +586,27 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
       sa = *p.a_scale;
       sb = *p.b_scale;
     }
-    const uint32_t tempty_leader0 = (C::CG == 2) ? mapa_shared(tempty_bar(0), 0) : tempty_bar(0);
+    const uint32_t tempty_leader0 = (C::CG == 2) ? mapa_shared(tempty_bar(0), leader) : tempty_bar(0);
     int it = 0;
     int chunk_ctr = 0;
     bool seq_ok = true;
+    constexpr int NCH = C::BN / C::EPI_COLS;
+    constexpr int NLD = C::EPI_COLS / 32;  // 32-column TMEM loads per chunk
+    constexpr int NPK = C::EPI_COLS / 2;   // packed bf16 pairs per row
+    constexpr int RB = C::EPI_ROW_BYTES;
+    constexpr int NQ = C::EPI_COLS / 4;    // 16-byte groups of fp32 per row per chunk
+    // split-K: this warp's block of a piece's partial accumulator: its 32 rows x its chunks,
+    // laid out [chunk][16-byte column group][lane] so that each store / load of a warp is 512
+    // contiguous bytes
+    constexpr int WS_WARP = 32 * (C::BN / SUBS);  // floats
+    auto ws_block = [&](int piece) {
+      return reinterpret_cast<float4*>(p.split_ws) +
+             ((static_cast<size_t>(piece) * C::CG + prank) * C::EPI_WARPS + ew) * (WS_WARP / 4);
+    };
     for (int t = first_tile; t >= 0; t = next_tile_warp(t, it, seq_ok), ++it) {
+      const WorkItem wk = work_of(t);
       int tm, tn;
-      order.coord(t, tm, tn);
+      tile_coord(wk.tile, tm, tn);
       const int acc = it % C::NUM_ACC;
       const uint32_t acc_phase = (it / C::NUM_ACC) & 1;
       const bool got = __all_sync(0xffffffffu, mbar_wait<true>(tfull_bar(acc), acc_phase, tmo, abort_flag));
@@ -538,17 +615,14 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
         break;
       }
       tc_fence_after();
-      if (p.visits != nullptr && ew == 0 && lane == 0 && rank == 0) atomicAdd(p.visits + t, 1u);
-      const int row0 = tm * (C::BM * C::CG) + static_cast<int>(rank) * C::BM + quad * 32;
+      const int row0 = tm * (C::BM * C::CG) + static_cast<int>(prank) * C::BM + quad * 32;
       const int col0 = tn * C::BN;
+      // A multicast with an odd number of tile columns: the second pair's last tile lies wholly
+      // right of C (its B rows were read as zeros) and is not stored
+      const bool live = tn < p.tiles_n;
       const uint32_t t_row =
           tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * C::ACC_STRIDE);
-      constexpr int NCH = C::BN / C::EPI_COLS;
-      constexpr int NLD = C::EPI_COLS / 32;  // 32-column TMEM loads per chunk
-      constexpr int NPK = C::EPI_COLS / 2;   // packed bf16 pairs per row
-      constexpr int RB = C::EPI_ROW_BYTES;
-      for (int c = sub; c < NCH; c += SUBS, ++chunk_ctr) {
-        uint32_t r[NLD][32];
+      auto load_chunk = [&](int c, uint32_t (&r)[NLD][32]) {
         __syncwarp();
 #pragma unroll
         for (int l = 0; l < NLD; ++l) tmem_ld_32x32b_x32(t_row + c * C::EPI_COLS + 32 * l, r[l]);
@@ -561,6 +635,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(tempty_leader0 + 8u * acc);
         }
+      };
+      // scale, round to bf16 and store chunk c of this warp's rows
+      auto store_chunk = [&](int c, const uint32_t (&r)[NLD][32]) {
         uint32_t pk[NPK];
 #pragma unroll
         for (int l = 0; l < NLD; ++l) {
@@ -576,7 +653,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
             pk[16 * l + j] = pack_bf16x2(x0, x1);
           }
         }
-        if (p.c_via_tma) {
+        if (!live) {
+        } else if (p.c_via_tma) {
           const uint32_t buf = stage0 + static_cast<uint32_t>(chunk_ctr & 1) * C::EPI_BUF;
           if (lane == 0) bulk_wait_group_read<1>();  // the store that last used `buf` has read it
           __syncwarp();
@@ -606,6 +684,75 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
             }
           }
         }
+        ++chunk_ctr;
+      };
+      auto count_visit = [&]() {
+        if (p.visits != nullptr && ew == 0 && lane == 0 && prank == 0 && tn < p.tiles_n)
+          atomicAdd(p.visits + tm * p.tiles_n + tn, 1u);
+      };
+      if (wk.piece < 0) {
+        count_visit();
+        for (int c = sub; c < NCH; c += SUBS) {
+          uint32_t r[NLD][32];
+          load_chunk(c, r);
+          store_chunk(c, r);
+        }
+      } else {
+        // this piece's partial accumulator -> workspace
+        float4* mine = ws_block(wk.piece);
+        for (int c = sub; c < NCH; c += SUBS) {
+          uint32_t r[NLD][32];
+          load_chunk(c, r);
+          float4* dst = mine + (c / SUBS) * (NQ * 32) + lane;
+#pragma unroll
+          for (int q = 0; q < NQ; ++q) {
+            const uint32_t* v = &r[q / 8][4 * (q % 8)];
+            __stcg(dst + q * 32, make_float4(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]),
+                                             __uint_as_float(v[3])));
+          }
+        }
+        // publish it, then count this piece in (release / acquire through the counter)
+        __threadfence();
+        __syncwarp();
+        unsigned int* cnt = p.split_cnt + (static_cast<size_t>(wk.tile) * C::CG + prank) * C::EPI_WARPS + ew;
+        unsigned int before = 0;
+        if (lane == 0) before = atomicAdd(cnt, 1u);
+        before = __shfl_sync(0xffffffffu, before, 0);
+        if (before == static_cast<unsigned int>(p.split_s - 1)) {
+          // the last piece in: add all pieces' partials, in piece order, and store the tile
+          __threadfence();
+          count_visit();
+          const float4* first = ws_block(wk.tile * p.split_s);
+          constexpr size_t PIECE_STRIDE = static_cast<size_t>(C::CG) * C::EPI_WARPS * (WS_WARP / 4);
+          for (int c = sub; c < NCH; c += SUBS) {
+            const float4* src = first + (c / SUBS) * (NQ * 32) + lane;
+            float4 sum[NQ];
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) sum[q] = __ldcg(src + q * 32);
+            for (int s = 1; s < p.split_s; ++s) {
+              float4 v[NQ];
+#pragma unroll
+              for (int q = 0; q < NQ; ++q) v[q] = __ldcg(src + s * PIECE_STRIDE + q * 32);
+#pragma unroll
+              for (int q = 0; q < NQ; ++q) {
+                sum[q].x += v[q].x;
+                sum[q].y += v[q].y;
+                sum[q].z += v[q].z;
+                sum[q].w += v[q].w;
+              }
+            }
+            uint32_t r[NLD][32];
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+              r[q / 8][4 * (q % 8) + 0] = __float_as_uint(sum[q].x);
+              r[q / 8][4 * (q % 8) + 1] = __float_as_uint(sum[q].y);
+              r[q / 8][4 * (q % 8) + 2] = __float_as_uint(sum[q].z);
+              r[q / 8][4 * (q % 8) + 3] = __float_as_uint(sum[q].w);
+            }
+            store_chunk(c, r);
+          }
+          if (lane == 0) *cnt = 0u;  // ready for the next launch (stream-ordered after this one)
+        }
       }
     }
     if (!seq_ok && lane == 0) record_timeout(p.status, kRoleEpilogue, abort_flag);
@@ -628,7 +775,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
       const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
       // where a written slot is announced: the stage's full barrier (coupled) or the slot's ready barrier
       const uint32_t ready0 = C::SF_COUPLED ? full_bar(0) : sf_ready_bar(0);
-      const uint32_t ready_leader0 = (C::CG == 2) ? mapa_shared(ready0, 0) : ready0;
+      const uint32_t ready_leader0 = (C::CG == 2) ? mapa_shared(ready0, leader) : ready0;
       const int my_tiles = cluster_id < num_tiles ? (num_tiles - 1 - cluster_id) / num_clusters + 1 : 0;
       const int steps = my_tiles * p.num_kb;
       const uint4* sfa = reinterpret_cast<const uint4*>(p.sf_a);
@@ -649,8 +796,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
         const int i = s_ / p.num_kb;
         const int kb = s_ - i * p.num_kb;
         int tm, tn;
-        order.coord(cluster_id + i * num_clusters, tm, tn);
-        const size_t ra = (static_cast<size_t>(kb) * p.sf_blocks_a + tm * C::CG + rank) * 128 + quad * 32 + lane;
+        tile_coord(cluster_id + i * num_clusters, tm, tn);
+        const size_t ra = (static_cast<size_t>(kb) * p.sf_blocks_a + tm * C::CG + prank) * 128 + quad * 32 + lane;
         const size_t rb = static_cast<size_t>(kb) * p.sf_blocks_b * 128 + static_cast<size_t>(tn) * C::BN + lane;
         v[0] = __ldg(sfa + ra);
 #pragma unroll
@@ -699,9 +846,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
         // steps with s % SF_GROUPS == sgroup.
         uint4 v0[1 + G];
         int k = 0;
+        int step = 0;  // K stages of the sequence so far: the ring position of the next one
         for (int t = first_tile; t >= 0 && ok; t = next_tile_warp(t, k, ok), ++k) {
-          for (int kb = 0; kb < p.num_kb && ok; ++kb) {
-            const int s_ = k * p.num_kb + kb;
+          const WorkItem wk = work_of(t);
+          for (int kb = wk.kb0; kb < wk.kb1 && ok; ++kb) {
+            const int s_ = step++;
             if (s_ % C::SF_GROUPS != sgroup) continue;
             ok = fetch_smem(s_, v0);
             if (!ok) break;
@@ -744,7 +893,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
     // says the atoms landed in both CTAs; it also implies the slot is free, since the producer
     // refilled the stage only after the MMAs that read the slot had completed.
     if constexpr (C::SF_HYBRID) {
-      if (lane == 0 && rank == 0) {
+      if (lane == 0 && prank == 0) {
         const int my_tiles = cluster_id < num_tiles ? (num_tiles - 1 - cluster_id) / num_clusters + 1 : 0;
         const int steps = my_tiles * p.num_kb;
         int stage = 0;
@@ -780,7 +929,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
   // ------------------------------------------------------------ teardown
   tc_fence_before();
   __syncthreads();
-  if constexpr (C::CG == 2) {
+  if constexpr (C::CL > 1) {
     cluster_arrive();
     cluster_wait();
   }
@@ -804,13 +953,15 @@ struct KernelVariant {
   int smem_bytes;
   const char* name;
   const void* func;
+  int mc;  // CTA pairs per cluster sharing A (1 or 2)
 };
 
 template <class C>
 KernelVariant make_variant(const char* name) {
   return KernelVariant{static_cast<int>(C::KIND), C::CG,         C::BN,         C::EPI_COLS,
                        C::SF_MODE,                   C::STAGES,     C::EPI_WARPS,  C::THREADS,
-                       C::SMEM_BYTES,                name,          reinterpret_cast<const void*>(&tkg_gemm_kernel<C>)};
+                       C::SMEM_BYTES,                name,          reinterpret_cast<const void*>(&tkg_gemm_kernel<C>),
+                       C::MC};
 }
 
 }  // namespace tkg

@@ -17,7 +17,12 @@ enum VariantId : int {
   kVariant2Sm256x256Hybrid = 6,  // cta_group::2, 256 x 256, A scales by scale warps, B by a copy warp (NVFP4)
   kVariant2Sm256x256Coupled = 7,  // as 5, with one TMEM scale slot per ring stage (NVFP4)
   kVariant2Sm256x256SfSmem = 8,   // as 7, the scales brought into shared memory by the ring's TMA (NVFP4)
-  kNumVariants = 9
+  kVariant2Sm256x192 = 9,          // cta_group::2, 256 x 192 tile per CTA pair (bf16 / FP8)
+  // clusters of two CTA pairs on horizontally adjacent tiles, A multicast between the pairs (bf16 / FP8)
+  kVariantMc256x256 = 10,
+  kVariantMc256x224 = 11,
+  kVariantMc256x192 = 12,
+  kNumVariants = 13
 };
 
 // Each returns the variant for `id`, or nullptr if that kind has no such variant.

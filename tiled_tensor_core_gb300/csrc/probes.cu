@@ -538,7 +538,7 @@ tkg_status tkg_debug_mma_probe(int kind, int n, int ksteps, const void* a_tile, 
 
 tkg_status tkg_debug_mma_rate(int kind, int cta_group, int n, int count, int pattern, unsigned long long* cycles,
                               void* stream) {
-  if (kind < 0 || kind > 2 || (cta_group != 1 && cta_group != 2) || (n != 128 && n != 256) || count < 1 ||
+  if (kind < 0 || kind > 2 || (cta_group != 1 && cta_group != 2) || n < 64 || n > 256 || n % 32 != 0 || count < 1 ||
       count > 65536 || pattern < 0 || pattern > 13 || !cycles)
     return TKG_ERR_INVALID_ARG;
   if (pattern >= 10 && (kind != 0 || cta_group != 1)) return TKG_ERR_INVALID_ARG;

@@ -241,6 +241,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
   }
 }
 
+// 2-D tiled load, CTA-pair form, written to the same shared-memory offset in
+// every CTA of `mask`; each destination's completion is signalled to the
+// barrier at `bar_cluster`'s offset in that destination's pair leader.
+__device__ __forceinline__ void tma_load_2d_mc_pair(uint32_t dst, const void* tmap, uint32_t bar_cluster, int32_t x,
+                                                    int32_t y, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster.cta_group::2 "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(bar_cluster), "h"(mask)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int32_t x, int32_t y) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(tmap), "r"(src),
                "r"(x), "r"(y)

@@ -70,6 +70,18 @@ def main(argv=None) -> None:
             print(f"| {name} | {cg} | {128 * cg} x 256 x {k} | " + " | ".join(cells) + " |")
 
     print()
+    print("| kind | CTA group | cycles per MMA for N = 64, 96, ..., 256 (M = 128 x CTA group) |")
+    print("|---|---|---|")
+    for kind, (name, k) in KINDS.items():
+        for cg in (1, 2):
+            cells = []
+            for n in range(64, 257, 32):
+                c0 = tkg.tkg_debug_mma_rate(kind, cg, n, 128)
+                c1 = tkg.tkg_debug_mma_rate(kind, cg, n, 1024)
+                cells.append(f"{n}: {(c1 - c0) / (1024 - 128):.1f}")
+            print(f"| {name} | {cg} | " + ", ".join(cells) + " |")
+
+    print()
     print("| bf16, one CTA, MMA (M x N x K) | A, B K-major in shared memory | B MN-major | A from tensor memory "
           "| both (attention P·V) |")
     print("|---|---|---|---|---|")

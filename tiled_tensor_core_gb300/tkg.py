@@ -33,12 +33,15 @@ TKG_OPT_VARIANT = 3
 TKG_OPT_MAX_CTAS = 4
 TKG_OPT_LAUNCH_OVERLAP = 5
 TKG_OPT_SCHEDULE = 6
+TKG_OPT_SPLIT_K = 7
 
 TKG_OVERLAP_ON = 1
 TKG_OVERLAP_OFF = 2
 TKG_SCHEDULE_STATIC = 1
 TKG_SCHEDULE_DYNAMIC = 2
 TKG_SCHEDULE_SINGLE = 3
+TKG_SPLIT_ON = 1
+TKG_SPLIT_OFF = 2
 
 KIND_BF16, KIND_FP8, KIND_NVFP4 = 0, 1, 2
 
@@ -85,6 +88,10 @@ lib.tkg_debug_variant_info.argtypes = [_i32, _i32, ctypes.POINTER(ctypes.c_int32
 lib.tkg_debug_variant_info.restype = _i32
 lib.tkg_debug_pick_variant.argtypes = [_i32, _i64, _i64, _i64]
 lib.tkg_debug_pick_variant.restype = _i32
+lib.tkg_debug_split_plan.argtypes = [_i64, _i64, _i32, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
+lib.tkg_debug_split_plan.restype = _i32
+lib.tkg_debug_work_item.argtypes = [_i32, _i32, _i32, _i32, ctypes.POINTER(ctypes.c_int32)]
+lib.tkg_debug_work_item.restype = _i32
 lib.tkg_debug_set_fault.argtypes = [_i32]
 lib.tkg_debug_set_fault.restype = _i32
 lib.tkg_debug_set_visit_counter.argtypes = [_vp]
@@ -214,6 +221,22 @@ def tkg_debug_variant_info(kind, variant):
 
 def tkg_debug_pick_variant(kind, M, N, K) -> int:
     return int(lib.tkg_debug_pick_variant(kind, M, N, K))
+
+
+def tkg_debug_split_plan(tiles, clusters, num_kb):
+    """(split_tiles, split_s) of the split-K head for this grid."""
+    t, s = ctypes.c_int32(), ctypes.c_int32()
+    if lib.tkg_debug_split_plan(tiles, clusters, num_kb, ctypes.byref(t), ctypes.byref(s)) != 0:
+        raise ValueError("tkg_debug_split_plan: invalid arguments")
+    return t.value, s.value
+
+
+def tkg_debug_work_item(w, split_tiles, split_s, num_kb):
+    """(tile, first K stage, end K stage, piece or -1) of work item w."""
+    out = (ctypes.c_int32 * 4)()
+    if lib.tkg_debug_work_item(w, split_tiles, split_s, num_kb, out) != 0:
+        raise ValueError("tkg_debug_work_item: invalid arguments")
+    return tuple(out)
 
 
 def tkg_debug_set_fault(mode: int) -> None:
