@@ -30,9 +30,12 @@
  *  - Errors detected before launch are returned and nothing is queued.  Errors
  *    detected on the device (a pipeline wait that exceeded its time limit) are
  *    recorded in a device status word and reported by tkg_check_status().
- *  - The library holds, per device, a small tensor-map cache on the host and a
- *    4-byte status word in a static device variable; tkg_shutdown() clears the
- *    host cache.  There is no CPU fallback: on a device that is not
+ *  - The library holds, per device, a small tensor-map cache on the host, a
+ *    4-byte status word in a static device variable, stream-ordered scratch
+ *    for the NVFP4 scale re-layout (tkg_gemm_nvfp4) and, per stream that ran a
+ *    split-K launch (TKG_OPT_SPLIT_K), a 128x256-fp32-per-SM workspace;
+ *    tkg_shutdown() releases the host cache and the workspaces.  There is no
+ *    CPU fallback: on a device that is not
  *    compute capability 10.3 every GEMM returns TKG_ERR_UNSUPPORTED_DEVICE.
  *  - Entry points are thread-safe.  Calls on different streams may overlap.
  */
@@ -177,9 +180,10 @@ TKG_API tkg_status tkg_check_status(void* stream);
 /* Static, never-NULL description of a status code. */
 TKG_API const char* tkg_status_string(tkg_status status);
 
-/* Releases host-side caches (tensor maps, per-device launch data).  Device
- * memory owned by the caller is untouched.  Safe to call more than once; the
- * next GEMM call re-initialises. */
+/* Releases host-side caches (tensor maps, per-device launch data) and the
+ * library's split-K workspaces (waiting for device work still using them).
+ * Device memory owned by the caller is untouched.  Safe to call more than
+ * once; the next GEMM call re-initialises. */
 TKG_API void tkg_shutdown(void);
 
 /* Tunables (process-wide).  Values persist until changed; 0 restores the
@@ -235,14 +239,19 @@ TKG_API void tkg_shutdown(void);
  *                      the persistent grid's last round of tiles would be
  *                      at most half full, those tiles are cut along K into
  *                      S = min(CTA pairs / tail tiles, 4) pieces of at
- *                      least 4 K stages each that run first; each piece
- *                      writes an fp32 partial to a per-stream workspace
- *                      (one fp32 128x256 block per SM, created on the
- *                      stream's first split launch, never while the stream
- *                      is being captured: such launches run unsplit) and
- *                      the last piece of a tile adds the partials in piece
- *                      order and stores it, so results do not depend on
- *                      timing.  Not used with A multicast (variants 10-12)
+ *                      least 16 K stages each (bf16: 1024 K elements; a
+ *                      grid of one round needs tiles of 48 K stages) that
+ *                      run first.  The pieces of a tile share its
+ *                      reduction: each writes the fp32 partials of the
+ *                      column chunks the others own to a per-stream
+ *                      workspace (one fp32 128x256 block per SM, created on
+ *                      the stream's first split launch, never while the
+ *                      stream is being captured: such launches run
+ *                      unsplit), waits (bounded) for the other pieces, and
+ *                      adds the partials of its own chunks in piece order,
+ *                      so results do not depend on timing.  The pieces are
+ *                      the first work items of distinct, co-resident CTA
+ *                      pairs.  Not used with A multicast (variants 10-12)
  *                      or NVFP4 variants 5-7.  TKG_SPLIT_OFF: whole tiles
  *                      only.  After a launch reports TKG_ERR_TIMEOUT,
  *                      tkg_check_status frees the workspaces (they are made

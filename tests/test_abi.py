@@ -162,28 +162,36 @@ def simulate_static(tkg, tiles, clusters, num_kb):
     (1024, 76, 64),    # FP8 8192^3
     (1024, 76, 128),   # bf16 8192^3
     (4096, 76, 128),   # NVFP4 16384^3: tail 68 of 76, no split
-    (16, 76, 32), (1, 76, 16), (1, 76, 3), (77, 76, 64), (152, 76, 64), (190, 76, 8), (5, 2, 40),
-    (3, 1, 64), (100, 152, 64)])
+    (16, 76, 32), (16, 76, 64), (1, 76, 16), (1, 76, 3), (1, 76, 256), (77, 76, 64), (152, 76, 64),
+    (190, 76, 8), (190, 76, 48), (5, 2, 40), (3, 1, 64), (100, 152, 64), (256, 76, 16), (256, 76, 24)])
 def test_split_plan_covers_every_k_block_once_and_shortens_the_last_round(tkg, tiles, clusters, num_kb):
     (st, ss), cover, busiest, pieces = simulate_static(tkg, tiles, clusters, num_kb)
     assert (cover == 1).all()  # every tile's K blocks, exactly once
     rounds = -(-tiles // clusters)
     tail = tiles - (rounds - 1) * clusters
     if st:
-        assert st == tail and 2 <= ss <= 4 and st * ss <= clusters and num_kb // ss >= 4
+        assert st == tail and 2 <= ss <= 4 and st * ss <= clusters and num_kb // ss >= 16
         assert busiest == pytest.approx(rounds - 1 + 1 / ss, abs=1e-9)
         # the pieces of one tile run side by side in the first round
         for tile, s, kb0, kb1 in pieces:
             assert kb0 == s * num_kb // ss and kb1 == (s + 1) * num_kb // ss
     else:
         assert ss == 1
-        assert 2 * tail > clusters or min(clusters // tail, 4, num_kb // 4) < 2 or clusters < 2
+        assert (2 * tail > clusters or min(clusters // tail, 4, num_kb // 16) < 2 or clusters < 2
+                or (rounds == 1 and num_kb < 48))
         assert busiest == pytest.approx(rounds)
 
 
 def test_split_plan_bf16_4096_example(tkg):
     # 4096^3 bf16 with 256x256 pair tiles: 256 tiles, 76 pairs, 64 K stages of 64
     assert tkg.tkg_debug_split_plan(256, 76, 64) == (28, 2)
+    # pieces keep at least 16 K stages: K = 1024 (16 stages) is not split, K = 2048 is
+    assert tkg.tkg_debug_split_plan(256, 76, 16) == (0, 1)
+    assert tkg.tkg_debug_split_plan(256, 76, 32) == (28, 2)
+    # one round of 16 tiles on 76 pairs: nothing hides the fix-up, so tiles need 48 stages
+    assert tkg.tkg_debug_split_plan(16, 76, 32) == (0, 1)
+    assert tkg.tkg_debug_split_plan(16, 76, 48) == (16, 3)
+    assert tkg.tkg_debug_split_plan(16, 76, 64) == (16, 4)
     assert tkg.tkg_debug_work_item(0, 28, 2, 64) == (0, 0, 32, 0)
     assert tkg.tkg_debug_work_item(1, 28, 2, 64) == (0, 32, 64, 1)
     assert tkg.tkg_debug_work_item(56, 28, 2, 64) == (28, 0, 64, -1)

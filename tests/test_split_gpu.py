@@ -58,15 +58,15 @@ def run_counted(tkg, ops, tiles):
 
 # (M, N, K, CTAs): 2-SM pairs, so CTAs / 2 clusters; the plan (split tiles, pieces) in comments
 CASES = {
-    "bf16": [(1280, 256, 1024, 8),    # 5 tiles on 4 pairs: (1, 4)
+    "bf16": [(1280, 256, 4096, 8),    # 5 tiles on 4 pairs: (1, 4)
              (1280, 512, 512, 12),    # 10 tiles on 6 pairs: last round 4 of 6, no split
-             (768, 256, 2048, 16),    # 3 tiles on 8 pairs: (3, 2)
-             (100, 100, 512, 8),      # one ragged tile, generic stores (N % 8 != 0): (1, 2)
-             (300, 520, 1000, 48),    # ragged edges, 6 tiles on 24 pairs: (6, 4), 16 K stages (last partial)
-             (2560, 1792, 1024, 32),  # 70 tiles on 16 pairs: (6, 2)
+             (768, 256, 4096, 16),    # 3 tiles on 8 pairs: (3, 2)
+             (100, 100, 4096, 8),     # one ragged tile, generic stores (N % 8 != 0): (1, 4)
+             (300, 520, 4000, 48),    # ragged edges, 6 tiles on 24 pairs: (6, 3), 63 K stages (last partial)
+             (2560, 1792, 2048, 32),  # 70 tiles on 16 pairs: (6, 2)
              (256, 256, 64, 8)],      # one tile of one K stage: no split
-    "fp8": [(1280, 256, 1024, 8), (100, 112, 1024, 8), (2560, 1792, 1024, 32)],    # (1, 2) each
-    "nvfp4": [(1280, 256, 2048, 8), (100, 128, 4096, 8), (2560, 1792, 2048, 32)],  # (1, 2), (1, 4), (6, 2)
+    "fp8": [(1280, 256, 4096, 8), (100, 112, 8192, 8), (2560, 1792, 4096, 32)],     # (1, 2), (1, 4), (6, 2)
+    "nvfp4": [(1280, 256, 8192, 8), (100, 128, 16384, 8), (2560, 1792, 8192, 32)],  # (1, 2), (1, 4), (6, 2)
 }
 
 
@@ -94,9 +94,9 @@ def test_split_matches_oracle_and_stores_each_tile_once(tkg, kind):
 @pytest.mark.parametrize("kind", ["bf16", "fp8", "nvfp4"])
 @pytest.mark.parametrize("ctas", [8, 16])
 def test_split_small_integers_bit_exact(tkg, kind, ctas):
-    M, N, K = (1280, 256, 1024) if ctas == 8 else (768, 256, 2048)
-    if kind == "nvfp4":
-        K *= 2
+    # 8 CTAs: 5 tiles, two rounds; 16 CTAs: 3 tiles in one round, which needs 48 K stages a tile
+    M, N = (1280, 256) if ctas == 8 else (768, 256)
+    K = {"bf16": 4096, "fp8": 4096, "nvfp4": 8192}[kind] * (1 if ctas == 8 or kind == "bf16" else 2)
     tkg.tkg_set_option(tkg.TKG_OPT_MAX_CTAS, ctas)
     (st, ss), tiles = plan_for(tkg, kind, M, N, K, ctas)
     assert st > 0
@@ -108,7 +108,7 @@ def test_split_small_integers_bit_exact(tkg, kind, ctas):
 
 
 def test_split_off_runs_whole_tiles(tkg):
-    M, N, K, ctas = 1280, 256, 1024, 8
+    M, N, K, ctas = 1280, 256, 4096, 8
     tkg.tkg_set_option(tkg.TKG_OPT_MAX_CTAS, ctas)
     ops = synth.make_operands("bf16", M, N, K, "normal_sqrtk", 5, 6)
     on = run_gpu(ops).c_bits()
@@ -125,7 +125,7 @@ def test_split_off_runs_whole_tiles(tkg):
 def test_split_on_two_streams_and_repeated_launches(tkg):
     # each stream has its own workspace; back-to-back launches on a stream reuse it (the
     # counters return to zero at the end of every launch)
-    M, N, K, ctas = 1280, 256, 1024, 8
+    M, N, K, ctas = 1280, 256, 4096, 8
     tkg.tkg_set_option(tkg.TKG_OPT_MAX_CTAS, ctas)
     from tiled_tensor_core_gb300.device import DeviceGemm
     opsets = [synth.make_operands("bf16", M, N, K, "normal_sqrtk", 40 + i, 50 + i) for i in range(2)]
@@ -141,3 +141,34 @@ def test_split_on_two_streams_and_repeated_launches(tkg):
         for g, o in zip(gs, opsets):
             acc, c_ref = oracle.gemm(o)
             check_against_oracle("bf16", g.c_bits(), acc, c_ref)
+
+
+def test_split_recovers_after_timeout_and_shutdown(tkg):
+    # a launch that gives up may leave piece counts behind: tkg_check_status drops the
+    # workspaces, and the next split launch (on fresh ones) is exact; so is one after
+    # tkg_shutdown, which frees them too
+    M, N, K, ctas = 1280, 256, 4096, 8
+    tkg.tkg_set_option(tkg.TKG_OPT_MAX_CTAS, ctas)
+    (st, ss), tiles = plan_for(tkg, "bf16", M, N, K, ctas)
+    assert st > 0
+    ops = synth.small_int_operands("bf16", M, N, K, seed=23)
+    _, c_ref = oracle.gemm(ops)
+    from tiled_tensor_core_gb300.device import DeviceGemm
+    g = DeviceGemm(ops, "cuda")
+    tkg.tkg_set_option(tkg.TKG_OPT_TIMEOUT_NS, 100_000_000)  # 0.1 s per wait
+    try:
+        tkg.tkg_debug_set_fault(1)
+        g.run()
+        assert tkg.tkg_check_status() == tkg.TKG_ERR_TIMEOUT
+    finally:
+        tkg.tkg_debug_set_fault(0)
+        tkg.tkg_set_option(tkg.TKG_OPT_TIMEOUT_NS, 0)
+    for _ in range(2):
+        g2, counts = run_counted(tkg, ops, tiles)
+        assert (counts == 1).all()
+        assert np.array_equal(g2.c_bits(), c_ref)
+    tkg.tkg_shutdown()
+    tkg.tkg_set_option(tkg.TKG_OPT_MAX_CTAS, ctas)
+    g3, counts = run_counted(tkg, ops, tiles)
+    assert (counts == 1).all()
+    assert np.array_equal(g3.c_bits(), c_ref)

@@ -28,7 +28,8 @@ using namespace tkg;
 constexpr int64_t kDefaultTimeoutNs = 2000000000LL;
 constexpr int64_t kDefaultGroupM = 8;
 constexpr int kMaxSplit = 4;     // split-K head: at most 4 pieces per tile
-constexpr int kMinSplitKb = 4;   // of at least 4 K blocks each
+constexpr int kMinSplitKb = 16;  // of at least 16 K blocks each
+constexpr int kMinSplitKbOneRound = 48;  // and, when all tiles fit in one round, 48 K blocks a tile
 constexpr int kMaxDevices = 64;
 constexpr int kNumKinds = 3;
 
@@ -264,8 +265,13 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // clusters walking `num_kb` K blocks per tile.  The grid takes R = ceil(tiles /
 // clusters) rounds, the last holding `tail` tiles; if that round would be at
 // most half full, the tail tiles are cut into S = min(clusters / tail, 4,
-// num_kb / 4) pieces (at least 4 K blocks each) that run first, next to whole
-// tiles, so the grid finishes after R - 1 + 1/S rounds of work instead of R.
+// num_kb / 16) pieces that run first, next to whole tiles, so the grid
+// finishes after R - 1 + 1/S rounds of work instead of R.  A piece's share of
+// the reduction is a chain of dependent global-memory round trips (~6 us on
+// GB300); pieces of at least 16 K blocks (bf16: 1024 K elements) keep it below
+// what the split saves when it overlaps the next tile, and a single round (no
+// next tile) needs tiles of at least 48 K blocks (measured over M = N = 1024
+// and 4096, K 512 to 16384).
 void split_plan(int64_t tiles, int64_t clusters, int num_kb, int* split_tiles, int* split_s) {
   *split_tiles = 0;
   *split_s = 1;
@@ -273,6 +279,7 @@ void split_plan(int64_t tiles, int64_t clusters, int num_kb, int* split_tiles, i
   const int64_t rounds = (tiles + clusters - 1) / clusters;
   const int64_t tail = tiles - (rounds - 1) * clusters;
   if (2 * tail > clusters) return;
+  if (rounds == 1 && num_kb < kMinSplitKbOneRound) return;
   int64_t s = clusters / tail;
   if (s > kMaxSplit) s = kMaxSplit;
   if (s > num_kb / kMinSplitKb) s = num_kb / kMinSplitKb;
@@ -284,7 +291,7 @@ void split_plan(int64_t tiles, int64_t clusters, int num_kb, int* split_tiles, i
 // The stream's split workspace (created on first use; not while the stream is
 // being captured, where the caller runs without the split instead).  Capacity:
 // one 128 x 256 fp32 block per SM (pieces <= clusters, CTAs <= SMs) and eight
-// counters per SM (tail tiles x CTAs x epilogue warps).
+// counters per SM (tail tiles <= clusters / 2, x CTAs x epilogue warps x 2).
 bool split_workspace(DevState& d, cudaStream_t stream, DevState::SplitWs* out) {
   {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -569,9 +576,16 @@ void tkg_shutdown(void) {
   for (auto& d : g_dev) {
     cudaMemPool_t pool = d.pool;
     if (pool) cudaMemPoolTrimTo(pool, 0);  // hand cached scratch back; the pool itself is reused
+    // split-K workspaces (cudaFree waits for work still using them); the status word is a
+    // static device variable and stays
+    for (auto& kv : d.split) {
+      cudaFree(kv.second.ws);
+      cudaFree(kv.second.cnt);
+    }
     d = DevState{};
     d.pool = pool;
   }
+  cudaGetLastError();  // a context already torn down at exit makes the frees fail; nothing to report
 }
 
 tkg_status tkg_set_option(tkg_option key, int64_t value) {

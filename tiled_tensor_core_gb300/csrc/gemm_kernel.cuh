@@ -66,7 +66,7 @@ struct GemmParams {
   int split_tiles;
   int split_s;
   float* split_ws;            // fp32 partial accumulators, one block per (piece, CTA, epilogue warp)
-  unsigned int* split_cnt;    // per (split tile, CTA, epilogue warp): pieces stored so far (reset to 0)
+  unsigned int* split_cnt;    // per (split tile, CTA, epilogue warp): {pieces written, pieces done}
 };
 
 // Tile schedules ("Persistent Grid Launch"; Cluster Launch Control for the
@@ -88,11 +88,16 @@ constexpr int kSchedStatic = 0, kSchedDynamic = 1, kSchedSingle = 2;
 // full, its tail tiles are cut into S pieces along K instead and run first).
 // Work item w < split_tiles * S is piece s = w % S of tile w / S, covering the
 // K blocks [s * num_kb / S, (s + 1) * num_kb / S); item w >= split_tiles * S is
-// the whole tile w - split_tiles * (S - 1).  Every piece writes its fp32
-// partial accumulator to a workspace and counts itself in; the piece that
-// counts last adds the S partials in the order s = 0, 1, ... (so the result
-// does not depend on which finished last), stores the tile and resets the
-// count.  Nothing waits on another CTA.
+// the whole tile w - split_tiles * (S - 1).  The pieces of a tile share the
+// reduction: each epilogue warp's column chunks are dealt out, chunk j to
+// piece j % S.  A piece writes the fp32 partials of the chunks it does not own
+// to a workspace, counts itself in, waits (bounded) until all S pieces have,
+// then adds, for each chunk it owns, the S partials in the order s = 0, 1, ...
+// (its own read again from tensor memory at its place), and stores the chunk:
+// the sum does not depend on timing.  The pieces of a tile are the first work
+// items of S clusters of the persistent grid, which is never larger than the
+// clusters that fit on the GPU at once, so the wait only waits for CTAs that
+// are running or about to run; the last piece past the wait resets the counts.
 struct WorkItem {
   int tile;
   int kb0, kb1;
@@ -622,14 +627,14 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
       const bool live = tn < p.tiles_n;
       const uint32_t t_row =
           tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * C::ACC_STRIDE);
-      auto load_chunk = [&](int c, uint32_t (&r)[NLD][32]) {
+      auto load_chunk = [&](int c, uint32_t (&r)[NLD][32], bool may_release) {
         __syncwarp();
 #pragma unroll
         for (int l = 0; l < NLD; ++l) tmem_ld_32x32b_x32(t_row + c * C::EPI_COLS + 32 * l, r[l]);
         tmem_wait_ld();
 #pragma unroll
         for (int l = 0; l < NLD; ++l) reg_fence(r[l]);
-        if (c + SUBS >= NCH) {
+        if (may_release && c + SUBS >= NCH) {
           // last TMEM read of this accumulator by this warp: hand it back
           tc_fence_before();
           __syncwarp();
@@ -694,16 +699,22 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
         count_visit();
         for (int c = sub; c < NCH; c += SUBS) {
           uint32_t r[NLD][32];
-          load_chunk(c, r);
+          load_chunk(c, r, true);
           store_chunk(c, r);
         }
       } else {
-        // this piece's partial accumulator -> workspace
+        const int S = p.split_s;
+        const int my_s = wk.piece % S;
+        constexpr int NLOC = (NCH + SUBS - 1) / SUBS;  // this warp's chunks: c = sub + SUBS * j
+        constexpr size_t PIECE_STRIDE = static_cast<size_t>(C::CG) * C::EPI_WARPS * (WS_WARP / 4);
+        // 1. partials of the chunks other pieces own -> this piece's workspace block
         float4* mine = ws_block(wk.piece);
-        for (int c = sub; c < NCH; c += SUBS) {
+        for (int j = 0; j < NLOC; ++j) {
+          const int c = sub + SUBS * j;
+          if (c >= NCH || j % S == my_s) continue;
           uint32_t r[NLD][32];
-          load_chunk(c, r);
-          float4* dst = mine + (c / SUBS) * (NQ * 32) + lane;
+          load_chunk(c, r, false);
+          float4* dst = mine + j * (NQ * 32) + lane;
 #pragma unroll
           for (int q = 0; q < NQ; ++q) {
             const uint32_t* v = &r[q / 8][4 * (q % 8)];
@@ -711,34 +722,58 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
                                              __uint_as_float(v[3])));
           }
         }
-        // publish it, then count this piece in (release / acquire through the counter)
+        // 2. count in (fence + atomic), wait until all S pieces have (acquire), bounded
+        unsigned int* cnt = p.split_cnt + 2 * ((static_cast<size_t>(wk.tile) * C::CG + prank) * C::EPI_WARPS + ew);
         __threadfence();
         __syncwarp();
-        unsigned int* cnt = p.split_cnt + (static_cast<size_t>(wk.tile) * C::CG + prank) * C::EPI_WARPS + ew;
-        unsigned int before = 0;
-        if (lane == 0) before = atomicAdd(cnt, 1u);
-        before = __shfl_sync(0xffffffffu, before, 0);
-        if (before == static_cast<unsigned int>(p.split_s - 1)) {
-          // the last piece in: add all pieces' partials, in piece order, and store the tile
-          __threadfence();
-          count_visit();
-          const float4* first = ws_block(wk.tile * p.split_s);
-          constexpr size_t PIECE_STRIDE = static_cast<size_t>(C::CG) * C::EPI_WARPS * (WS_WARP / 4);
-          for (int c = sub; c < NCH; c += SUBS) {
-            const float4* src = first + (c / SUBS) * (NQ * 32) + lane;
+        int arrived = 1;
+        if (lane == 0) {
+          atomicAdd(cnt, 1u);
+          const uint64_t t0 = globaltimer_ns();
+          while (ld_acquire_gpu(cnt) < static_cast<unsigned int>(S)) {
+            if (*abort_flag || globaltimer_ns() - t0 > tmo) {
+              arrived = 0;
+              break;
+            }
+            __nanosleep(64);
+          }
+        }
+        arrived = __shfl_sync(0xffffffffu, arrived, 0);
+        __threadfence();
+        if (arrived) {
+          // 3. the chunks this piece owns: the S partials added in piece order, stored as bf16
+          const float4* first = ws_block(wk.tile * S) + lane;
+          for (int j = my_s; j < NLOC; j += S) {
+            const int c = sub + SUBS * j;
+            if (c >= NCH) break;
+            if (j == 0) count_visit();
             float4 sum[NQ];
+            for (int s2 = 0; s2 < S; ++s2) {
+              float4 part[NQ];
+              if (s2 == my_s) {
+                uint32_t r[NLD][32];
+                load_chunk(c, r, false);
 #pragma unroll
-            for (int q = 0; q < NQ; ++q) sum[q] = __ldcg(src + q * 32);
-            for (int s = 1; s < p.split_s; ++s) {
-              float4 v[NQ];
+                for (int q = 0; q < NQ; ++q) {
+                  const uint32_t* v = &r[q / 8][4 * (q % 8)];
+                  part[q] = make_float4(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]),
+                                        __uint_as_float(v[3]));
+                }
+              } else {
+                const float4* src = first + s2 * PIECE_STRIDE + j * (NQ * 32);
 #pragma unroll
-              for (int q = 0; q < NQ; ++q) v[q] = __ldcg(src + s * PIECE_STRIDE + q * 32);
+                for (int q = 0; q < NQ; ++q) part[q] = __ldcg(src + q * 32);
+              }
 #pragma unroll
               for (int q = 0; q < NQ; ++q) {
-                sum[q].x += v[q].x;
-                sum[q].y += v[q].y;
-                sum[q].z += v[q].z;
-                sum[q].w += v[q].w;
+                if (s2 == 0) {
+                  sum[q] = part[q];
+                } else {
+                  sum[q].x += part[q].x;
+                  sum[q].y += part[q].y;
+                  sum[q].z += part[q].z;
+                  sum[q].w += part[q].w;
+                }
               }
             }
             uint32_t r[NLD][32];
@@ -751,7 +786,17 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
             }
             store_chunk(c, r);
           }
-          if (lane == 0) *cnt = 0u;  // ready for the next launch (stream-ordered after this one)
+        } else if (lane == 0) {
+          record_timeout(p.status, kRoleEpilogue, abort_flag);
+        }
+        // the accumulator has been read for the last time: hand it back
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(tempty_leader0 + 8u * acc);
+        // 4. the last piece past the wait resets both counts for the next launch
+        if (arrived && lane == 0 && atomicAdd(cnt + 1, 1u) == static_cast<unsigned int>(S - 1)) {
+          cnt[0] = 0u;
+          cnt[1] = 0u;
         }
       }
     }
