@@ -94,6 +94,33 @@ struct AttnCfg {
 
 constexpr int kRoleLoad = 0, kRoleMma = 1, kRoleSoftmax = 2;
 
+// Paired fp32 arithmetic (two lanes of a 64-bit register, each rounded as the
+// scalar instruction would be) and the three-input maximum: the same results
+// as the scalar forms in fewer issued instructions.
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f32x2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f32x2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 __device__ __forceinline__ void attn_timeout(unsigned int* status, int role, volatile int* abort_flag) {
   atomicOr(status, 1u | (1u << (8 + role)));
   *abort_flag = 1;
@@ -313,12 +340,16 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
           for (int i = 0; i < 32; ++i)
             if (32 * q + i >= valid) s[q][i] = __float_as_uint(-INFINITY);
       }
-      // tile row maximum: eight independent chains, then a tree
+      // tile row maximum: eight independent chains of three-input maxima, then a tree
       float mx[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) mx[e] = __uint_as_float(s[0][e]);
 #pragma unroll
-      for (int e = 8; e < 128; ++e) mx[e % 8] = fmaxf(mx[e % 8], __uint_as_float(s[e / 32][e % 32]));
+      for (int e = 8; e < 128; e += 16)
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          mx[c] = fmax3(mx[c], __uint_as_float(s[(e + c) / 32][(e + c) % 32]),
+                        __uint_as_float(s[(e + 8 + c) / 32][(e + 8 + c) % 32]));
 #pragma unroll
       for (int w = 4; w >= 1; w /= 2)
 #pragma unroll
@@ -335,18 +366,27 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
         m = mt;
       }
       const float neg = -m * c2;
-      float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      // scores scaled in pairs (s * c2 - m * c2), exponentiated, summed in pairs: sum k
+      // (k = 0..3) collects the pairs i = k, k + 4, ...; lane 0 the even, lane 1 the odd keys
+      const uint64_t c2x2 = f32x2_pack(c2, c2), negx2 = f32x2_pack(neg, neg);
+      uint64_t lsx2[4] = {0ull, 0ull, 0ull, 0ull};
       uint32_t pk[64];
 #pragma unroll
       for (int q = 0; q < 4; ++q)
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float x0 = ex2_approx(fmaf(__uint_as_float(s[q][2 * i]), c2, neg));
-          const float x1 = ex2_approx(fmaf(__uint_as_float(s[q][2 * i + 1]), c2, neg));
-          ls[(2 * i) % 8] += x0;
-          ls[(2 * i + 1) % 8] += x1;
+          const uint64_t y = f32x2_fma(f32x2_pack(__uint_as_float(s[q][2 * i]), __uint_as_float(s[q][2 * i + 1])),
+                                       c2x2, negx2);
+          float y0, y1;
+          f32x2_unpack(y, y0, y1);
+          const float x0 = ex2_approx(y0);
+          const float x1 = ex2_approx(y1);
+          lsx2[i % 4] = f32x2_add(lsx2[i % 4], f32x2_pack(x0, x1));
           pk[16 * q + i] = pack_bf16x2(x0, x1);
         }
+      float ls[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) f32x2_unpack(lsx2[k], ls[2 * k], ls[2 * k + 1]);
 #pragma unroll
       for (int w = 4; w >= 1; w /= 2)
 #pragma unroll
