@@ -15,20 +15,20 @@
 // per CTA sharing the K and V tiles:
 //   warp 0, one lane   LOAD     TMA (3-D maps over [B·H][N][D]) of both Q tiles
 //                               once and of K_j, V_j into two rings
-//   warp 1, one lane   COMPUTE  per query tile t: S_t(j) = Q_t·K_jᵀ into the TMEM
-//                               score buffer the two tiles use in turn,
-//                               O_t += P_t(j)·V_j into the tile's TMEM accumulator
-//                               (P read from tensor memory, V as an MN-major
-//                               shared operand)
+//   warp 1, one lane   COMPUTE  per query tile t: S_t(j) = Q_t·K_jᵀ into the
+//                               tile's TMEM score buffer, O_t += P_t(j)·V_j
+//                               into its TMEM accumulator (P read from tensor
+//                               memory, V as an MN-major shared operand)
 //   warps 2-5 (A),     SOFTMAX  one thread per query row (its TMEM lane): scores
 //   warps 6-9 (B)      / FINISH from TMEM, running max and sum, P_t(j) (bf16)
-//                               into the tile's own TMEM columns, rescale of
-//                               the row's O when its maximum grew; at the end
-//                               O / l to bf16, a TMA store, the log-sum-exp
-// The two tiles' softmax phases alternate: the tensor core computes one tile's
-// P·V and next scores while the other tile's softmax runs.  P never touches
-// shared memory.  Every wait is bounded (TKG_OPT_TIMEOUT_NS) and reported
-// through the status word.
+//                               written over the first half of the tile's
+//                               score buffer, rescale of the row's O when its
+//                               maximum grew; at the end O / l to bf16, a TMA
+//                               store, the log-sum-exp
+// The tensor core runs P_A(j)·V_j, S_A(j+1), P_B(j)·V_j, S_B(j+1), ...: while
+// one tile's softmax runs, the tensor core has the other tile's P·V and next
+// scores to compute.  P never touches shared memory.  Every wait is bounded
+// (TKG_OPT_TIMEOUT_NS) and reported through the status word.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -72,13 +72,13 @@ struct AttnCfg {
   static constexpr int OFF_V = OFF_K + KST * KV_STAGE;
   static constexpr int OFF_Q = OFF_V + VST * KV_STAGE;  // tile t at OFF_Q + t * Q_TILE; the output staging at the end
   static constexpr int OFF_BAR = OFF_Q + NT * Q_TILE;
-  static constexpr int NUM_BARS = 1 + 2 * KST + 2 * VST + 3 * NT + 3;
+  static constexpr int NUM_BARS = 1 + 2 * KST + 2 * VST + 3 * NT + 2;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NUM_BARS;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr int THREADS = 64 + 32 * 4 * NT;  // producer, MMA, one softmax warpgroup per query tile
-  // TMEM columns: one score buffer [0, 128) used by the two tiles in turn,
-  // tile t's P (bf16 pairs) at 128 + 64 t, its output accumulator at 256 + D t
-  static constexpr uint32_t T_S = 0, T_P = 128, T_O = 128 + 64 * NT;
+  // TMEM columns: tile t's score buffer at 128 t (its P, bf16 pairs, over the
+  // first 64 of them once the scores are read), its output accumulator at 256 + D t
+  static constexpr uint32_t T_S = 0, T_O = 128 * NT;
   static constexpr uint32_t TMEM_COLS = 512;
   // S = Q·Kᵀ: M = 128, N = BKV, both K-major;  O += P·V: M = 128, N = D, P from
   // tensor memory, V an MN-major shared operand (bit 16)
@@ -140,16 +140,13 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
   auto v_full = [&](int s) { return bar0 + 8u * (1 + 2 * C::KST + s); };
   auto v_empty = [&](int s) { return bar0 + 8u * (1 + 2 * C::KST + C::VST + s); };
   constexpr int B1 = 1 + 2 * C::KST + 2 * C::VST;
-  // query tile t: S_t(j) is in the score buffer / P_t(j) was written (and O_t rescaled) /
-  // P_t(j)·V_j has finished (P_t's columns are free, O_t holds key tiles 0..j)
+  // query tile t: S_t(j) is in its score buffer / P_t(j) was written (and O_t rescaled) /
+  // P_t(j)·V_j has finished (the score buffer is free, O_t holds key tiles 0..j)
   auto s_full = [&](int t) { return bar0 + 8u * (B1 + t); };
   auto p_full = [&](int t) { return bar0 + 8u * (B1 + C::NT + t); };
   auto pv_done = [&](int t) { return bar0 + 8u * (B1 + 2 * C::NT + t); };
-  // the score buffer's current scores have been loaded by their softmax warpgroup
-  // (uses alternate A(0), B(0), A(1), B(1), ...; use u completes the barrier's u-th phase)
-  const uint32_t s_free = bar0 + 8u * (B1 + 3 * C::NT);
-  const uint32_t o_final = bar0 + 8u * (B1 + 3 * C::NT + 1);  // the last P·V finished
-  const uint32_t drain = bar0 + 8u * (B1 + 3 * C::NT + 2);
+  const uint32_t o_final = bar0 + 8u * (B1 + 3 * C::NT);  // the last P·V finished
+  const uint32_t drain = bar0 + 8u * (B1 + 3 * C::NT + 1);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* never_abort = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
@@ -176,7 +173,6 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
       mbar_init(p_full(t), 4);  // one arrival per warp of the tile's softmax warpgroup
       mbar_init(pv_done(t), 1);
     }
-    mbar_init(s_free, 4);
     mbar_init(o_final, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -240,20 +236,17 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ COMPUTE
-    // The score buffer is used by S_A(0), S_B(0), S_A(1), S_B(1), ...; each use
-    // waits only until the previous one's scores are in its softmax warps'
-    // registers.  Per key tile j and tile t: S_t(j+1) first (so the next scores
-    // are ready when the softmax warps finish tile j), then P_t(j)·V_j once the
-    // softmax has written P_t(j).  The softmax writes P_t(j) into the tile's own
-    // columns only after P_t(j-1)·V_{j-1} has finished, which also makes its O
-    // rescale safe.  Each barrier's phases are waited on in order.
+    // Per key tile j: P_A(j)·V_j, S_A(j+1), P_B(j)·V_j, S_B(j+1).  S_t(j+1)
+    // overwrites the score buffer P_t(j) was read from, and MMAs on different
+    // accumulators are not ordered by the hardware, so it waits until
+    // P_t(j)·V_j has finished.  The softmax of tile t runs between S_t(j+1)
+    // and P_t(j+1)·V_{j+1}, while the tensor core computes the other tile's
+    // products.  Each barrier's phases are waited on in order.
     if (lane == 0) {
       bool ok = mbar_wait(q_full, 0, tmo, abort_flag);
       tc_fence_after();
-      // S_t(j): use u = 2j + t of the score buffer, after use u-1 was loaded
       auto issue_s = [&](int t, int j) -> bool {
-        const int u = C::NT * j + t;
-        if (u > 0 && !mbar_wait(s_free, static_cast<uint32_t>(u - 1) & 1u, tmo, abort_flag)) return false;
+        if (j > 0 && !mbar_wait(pv_done(t), static_cast<uint32_t>(j - 1) & 1u, tmo, abort_flag)) return false;
         if (t == 0 && !mbar_wait(k_full(j % C::KST), static_cast<uint32_t>(j / C::KST) & 1u, tmo, abort_flag))
           return false;
         tc_fence_after();
@@ -263,7 +256,7 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t ad = sdesc_sw128(q_t + (kk / 4) * C::CHUNK + 32u * (kk % 4));
           const uint64_t bd = sdesc_sw128(k0 + (kk / 4) * C::CHUNK + 32u * (kk % 4));
-          mma_bf16<1>(tmem_base + C::T_S, ad, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
+          mma_bf16<1>(tmem_base + C::T_S + 128u * t, ad, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
         }
         mma_commit_local(s_full(t));
         if (t == C::NT - 1) mma_commit_local(k_empty(j % C::KST));  // the last reader of K_j
@@ -275,7 +268,7 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
           return false;
         tc_fence_after();
         const uint32_t v0 = sV + (j % C::VST) * C::KV_STAGE;
-        const uint32_t a0 = tmem_base + C::T_P + 64u * t;
+        const uint32_t a0 = tmem_base + C::T_S + 128u * t;  // P_t(j): bf16 pairs over the scores
 #pragma unroll
         for (int kk = 0; kk < C::BKV / 16; ++kk) {
           // A: 16 keys of P_t = 8 of its columns; B: 16 rows of V (keys), D columns
@@ -290,8 +283,8 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
       for (int t = 0; t < C::NT && ok; ++t) ok = issue_s(t, 0);
       for (int j = 0; j < nkv && ok; ++j) {
         for (int t = 0; t < C::NT && ok; ++t) {
-          if (j + 1 < nkv) ok = issue_s(t, j + 1);
-          if (ok) ok = issue_pv(t, j);
+          ok = issue_pv(t, j);
+          if (ok && j + 1 < nkv) ok = issue_s(t, j + 1);
         }
       }
       if (ok) mma_commit_local(o_final);
@@ -308,8 +301,8 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
     const int t = (warp - 2) / 4;
     const int quad = warp & 3;  // TMEM lane quarter this warp may access (rows 32 quad ..)
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t t_s = tmem_base + lane_off + C::T_S;
-    const uint32_t t_p = tmem_base + lane_off + C::T_P + 64u * static_cast<uint32_t>(t);
+    const uint32_t t_s = tmem_base + lane_off + C::T_S + 128u * static_cast<uint32_t>(t);
+    const uint32_t t_p = t_s;  // P over the first 64 score columns, once the scores are read
     const uint32_t t_o = tmem_base + lane_off + C::T_O + static_cast<uint32_t>(D * t);
     const float c2 = p.scale_log2;
     float m = -INFINITY;  // reference maximum of the raw scores of this row (lazily raised)
@@ -327,10 +320,6 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
       tmem_wait_ld();
 #pragma unroll
       for (int q = 0; q < 4; ++q) reg_fence(s[q]);
-      // the scores are in registers: the buffer may take the other tile's scores
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_local(s_free);
       // keys of this tile past the end of the sequence score -inf (only the last tile has any)
       const int valid = p.Nkv - j * C::BKV;
       if (valid < C::BKV) {
@@ -392,14 +381,8 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
 #pragma unroll
         for (int e = 0; e < w; ++e) ls[e] += ls[e + w];
       l = l * alpha + ls[0];
-      // P_t's columns and O_t are free once P_t(j-1)·V_{j-1} has finished (the barrier is at
-      // most one completion behind: the wait for tile j-1 saw P_t(j-2)·V_{j-2} finish)
-      if (j >= 1 && !__all_sync(0xffffffffu, mbar_wait<true>(pv_done(t), static_cast<uint32_t>(j - 1) & 1u, tmo,
-                                                              abort_flag))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
+      // P_t(j-1)·V_{j-1} finished before S_t(j) was issued: O_t holds key tiles 0..j-1 and
+      // nothing reads the score buffer, so P_t(j) may go over the scores and O_t be rescaled
       if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.0f)) {
         // O_t holds key tiles 0..j-1
 #pragma unroll
@@ -412,7 +395,7 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
           tmem_st_32x32b_x32(t_o + 32u * q, o);
         }
       }
-      // P row (bf16 pairs) into the tile's 64 P columns
+      // P row (bf16 pairs) over the first 64 score columns
       tmem_st_32x32b_x32(t_p, *reinterpret_cast<uint32_t(*)[32]>(pk));
       tmem_st_32x32b_x32(t_p + 32u, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
       tmem_wait_st();
