@@ -16,18 +16,21 @@
 //   warp 0, one lane   LOAD     TMA (3-D maps over [B·H][N][D]) of both Q tiles
 //                               once and of K_j, V_j into two rings
 //   warp 1, one lane   COMPUTE  per query tile t: S_t(j) = Q_t·K_jᵀ into the
-//                               tile's TMEM score buffer, O_t += P_t(j)·V_j
-//                               into its TMEM accumulator (P read from tensor
-//                               memory, V as an MN-major shared operand)
-//   warps 2-5 (A),     SOFTMAX  one thread per query row (its TMEM lane): scores
-//   warps 6-9 (B)      / FINISH from TMEM, running max and sum, P_t(j) (bf16)
+//                               tile's TMEM score buffer
+//   warp 2, one lane   COMPUTE  O_t += P_t(j)·V_j into the tile's TMEM
+//                               accumulator (P read from tensor memory, V as an
+//                               MN-major shared operand)
+//   warps 3-6 (A),     SOFTMAX  one thread per query row (its TMEM lane): scores
+//   warps 7-10 (B)     / FINISH from TMEM, running max and sum, P_t(j) (bf16)
 //                               written over the first half of the tile's
 //                               score buffer, rescale of the row's O when its
 //                               maximum grew; at the end O / l to bf16, a TMA
 //                               store, the log-sum-exp
 // The tensor core runs P_A(j)·V_j, S_A(j+1), P_B(j)·V_j, S_B(j+1), ...: while
 // one tile's softmax runs, the tensor core has the other tile's P·V and next
-// scores to compute.  P never touches shared memory.  Every wait is bounded
+// scores to compute, and with two issuing threads one of them waits on its
+// barriers while the other's MMAs keep the tensor core fed (the tensor core
+// queues only one or two MMAs ahead).  P never touches shared memory.  Every wait is bounded
 // (TKG_OPT_TIMEOUT_NS) and reported through the status word.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -72,10 +75,10 @@ struct AttnCfg {
   static constexpr int OFF_V = OFF_K + KST * KV_STAGE;
   static constexpr int OFF_Q = OFF_V + VST * KV_STAGE;  // tile t at OFF_Q + t * Q_TILE; the output staging at the end
   static constexpr int OFF_BAR = OFF_Q + NT * Q_TILE;
-  static constexpr int NUM_BARS = 1 + 2 * KST + 2 * VST + 3 * NT + 2;
+  static constexpr int NUM_BARS = 1 + 2 * KST + 2 * VST + 4 * NT + 2;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NUM_BARS;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
-  static constexpr int THREADS = 64 + 32 * 4 * NT;  // producer, MMA, one softmax warpgroup per query tile
+  static constexpr int THREADS = 96 + 32 * 4 * NT;  // producer, two MMA issuers, a softmax warpgroup per query tile
   // TMEM columns: tile t's score buffer at 128 t (its P, bf16 pairs, over the
   // first 64 of them once the scores are read), its output accumulator at 256 + D t
   static constexpr uint32_t T_S = 0, T_O = 128 * NT;
@@ -145,8 +148,10 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
   auto s_full = [&](int t) { return bar0 + 8u * (B1 + t); };
   auto p_full = [&](int t) { return bar0 + 8u * (B1 + C::NT + t); };
   auto pv_done = [&](int t) { return bar0 + 8u * (B1 + 2 * C::NT + t); };
-  const uint32_t o_final = bar0 + 8u * (B1 + 3 * C::NT);  // the last P·V finished
-  const uint32_t drain = bar0 + 8u * (B1 + 3 * C::NT + 1);
+  // S_t(j) has been issued (the P·V thread keeps the tensor core's order P_A·V, S_A, P_B·V, S_B)
+  auto s_issued = [&](int t) { return bar0 + 8u * (B1 + 3 * C::NT + t); };
+  const uint32_t o_final = bar0 + 8u * (B1 + 4 * C::NT);  // the last P·V finished
+  const uint32_t drain = bar0 + 8u * (B1 + 4 * C::NT + 1);  // both issuers' MMAs finished
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* never_abort = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
@@ -172,9 +177,10 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
       mbar_init(s_full(t), 1);
       mbar_init(p_full(t), 4);  // one arrival per warp of the tile's softmax warpgroup
       mbar_init(pv_done(t), 1);
+      mbar_init(s_issued(t), 1);
     }
     mbar_init(o_final, 1);
-    mbar_init(drain, 1);
+    mbar_init(drain, 2);
     *abort_flag = 0;
     *never_abort = 0;
     fence_mbar_init();
@@ -234,61 +240,82 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 2) {
     // ------------------------------------------------------------ COMPUTE
-    // Per key tile j: P_A(j)·V_j, S_A(j+1), P_B(j)·V_j, S_B(j+1).  S_t(j+1)
-    // overwrites the score buffer P_t(j) was read from, and MMAs on different
-    // accumulators are not ordered by the hardware, so it waits until
-    // P_t(j)·V_j has finished.  The softmax of tile t runs between S_t(j+1)
-    // and P_t(j+1)·V_{j+1}, while the tensor core computes the other tile's
-    // products.  Each barrier's phases are waited on in order.
+    // Two issuing threads: warp 1 issues the score products S_t(j), warp 2
+    // the products P_t(j)·V_j, so that one waits on its barriers while the
+    // other's MMAs keep the tensor core busy.  The tensor core is kept to the
+    // order P_A(j)·V_j, S_A(j+1), P_B(j)·V_j, S_B(j+1): each tile's softmax
+    // runs between its S_t(j+1) and its P_t(j+1)·V_{j+1}, while the other
+    // tile's products are computed.  S_t(j+1) overwrites the score buffer
+    // P_t(j) was read from, and MMAs on different accumulators are not ordered
+    // by the hardware, so it waits until P_t(j)·V_j has finished; a P·V waits
+    // until the score product before it in that order has been issued.  Each
+    // thread's commits track its own MMAs.  Each barrier's phases are waited
+    // on in order.
     if (lane == 0) {
       bool ok = mbar_wait(q_full, 0, tmo, abort_flag);
       tc_fence_after();
-      auto issue_s = [&](int t, int j) -> bool {
-        if (j > 0 && !mbar_wait(pv_done(t), static_cast<uint32_t>(j - 1) & 1u, tmo, abort_flag)) return false;
-        if (t == 0 && !mbar_wait(k_full(j % C::KST), static_cast<uint32_t>(j / C::KST) & 1u, tmo, abort_flag))
-          return false;
-        tc_fence_after();
-        const uint32_t k0 = sK + (j % C::KST) * C::KV_STAGE;
-        const uint32_t q_t = sQ + t * C::Q_TILE;
+      if (warp == 1) {
+        for (int j = 0; j < nkv && ok; ++j) {
+          for (int t = 0; t < C::NT && ok; ++t) {
+            if (j > 0 && !mbar_wait(pv_done(t), static_cast<uint32_t>(j - 1) & 1u, tmo, abort_flag)) {
+              ok = false;
+              break;
+            }
+            if (t == 0 && !mbar_wait(k_full(j % C::KST), static_cast<uint32_t>(j / C::KST) & 1u, tmo, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t k0 = sK + (j % C::KST) * C::KV_STAGE;
+            const uint32_t q_t = sQ + t * C::Q_TILE;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(q_t + (kk / 4) * C::CHUNK + 32u * (kk % 4));
-          const uint64_t bd = sdesc_sw128(k0 + (kk / 4) * C::CHUNK + 32u * (kk % 4));
-          mma_bf16<1>(tmem_base + C::T_S + 128u * t, ad, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint64_t ad = sdesc_sw128(q_t + (kk / 4) * C::CHUNK + 32u * (kk % 4));
+              const uint64_t bd = sdesc_sw128(k0 + (kk / 4) * C::CHUNK + 32u * (kk % 4));
+              mma_bf16<1>(tmem_base + C::T_S + 128u * t, ad, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
+            }
+            mbar_arrive_local(s_issued(t));
+            mma_commit_local(s_full(t));
+            if (t == C::NT - 1) mma_commit_local(k_empty(j % C::KST));  // the last reader of K_j
+          }
         }
-        mma_commit_local(s_full(t));
-        if (t == C::NT - 1) mma_commit_local(k_empty(j % C::KST));  // the last reader of K_j
-        return true;
-      };
-      auto issue_pv = [&](int t, int j) -> bool {
-        if (!mbar_wait(p_full(t), static_cast<uint32_t>(j) & 1u, tmo, abort_flag)) return false;
-        if (t == 0 && !mbar_wait(v_full(j % C::VST), static_cast<uint32_t>(j / C::VST) & 1u, tmo, abort_flag))
-          return false;
-        tc_fence_after();
-        const uint32_t v0 = sV + (j % C::VST) * C::KV_STAGE;
-        const uint32_t a0 = tmem_base + C::T_S + 128u * t;  // P_t(j): bf16 pairs over the scores
+      } else {
+        for (int j = 0; j < nkv && ok; ++j) {
+          for (int t = 0; t < C::NT && ok; ++t) {
+            // the score product issued before this P·V: S_B(j) for tile A, S_A(j+1) for tile B
+            const int tp = (t + C::NT - 1) % C::NT;
+            const int jp = t == 0 ? j : j + 1;
+            if (jp < nkv && !mbar_wait(s_issued(tp), static_cast<uint32_t>(jp) & 1u, tmo, abort_flag)) {
+              ok = false;
+              break;
+            }
+            if (!mbar_wait(p_full(t), static_cast<uint32_t>(j) & 1u, tmo, abort_flag)) {
+              ok = false;
+              break;
+            }
+            if (t == 0 && !mbar_wait(v_full(j % C::VST), static_cast<uint32_t>(j / C::VST) & 1u, tmo, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t v0 = sV + (j % C::VST) * C::KV_STAGE;
+            const uint32_t a0 = tmem_base + C::T_S + 128u * t;  // P_t(j): bf16 pairs over the scores
 #pragma unroll
-        for (int kk = 0; kk < C::BKV / 16; ++kk) {
-          // A: 16 keys of P_t = 8 of its columns; B: 16 rows of V (keys), D columns
-          const uint64_t bd = sdesc_sw128_mn(v0 + 2048u * kk, C::CHUNK);
-          mma_bf16_ts(tmem_base + C::T_O + static_cast<uint32_t>(D * t), a0 + 8u * kk, bd, C::IDESC_PV,
-                      (j > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < C::BKV / 16; ++kk) {
+              // A: 16 keys of P_t = 8 of its columns; B: 16 rows of V (keys), D columns
+              const uint64_t bd = sdesc_sw128_mn(v0 + 2048u * kk, C::CHUNK);
+              mma_bf16_ts(tmem_base + C::T_O + static_cast<uint32_t>(D * t), a0 + 8u * kk, bd, C::IDESC_PV,
+                          (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit_local(pv_done(t));
+            if (t == C::NT - 1) mma_commit_local(v_empty(j % C::VST));  // the last reader of V_j
+          }
         }
-        mma_commit_local(pv_done(t));
-        if (t == C::NT - 1) mma_commit_local(v_empty(j % C::VST));  // the last reader of V_j
-        return true;
-      };
-      for (int t = 0; t < C::NT && ok; ++t) ok = issue_s(t, 0);
-      for (int j = 0; j < nkv && ok; ++j) {
-        for (int t = 0; t < C::NT && ok; ++t) {
-          ok = issue_pv(t, j);
-          if (ok && j + 1 < nkv) ok = issue_s(t, j + 1);
-        }
+        if (ok) mma_commit_local(o_final);
       }
-      if (ok) mma_commit_local(o_final);
-      // no MMA may still be writing TMEM when it is released
+      // no MMA of either thread may still be writing TMEM when it is released
       mma_commit_local(drain);
       mbar_wait(drain, 0, tmo, never_abort);
       if (!ok) attn_timeout(p.status, kRoleMma, abort_flag);
@@ -296,9 +323,9 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
     __syncwarp();
   } else {
     // ------------------------------------------------------------ SOFTMAX / FINISH
-    // Warpgroup t (warps 2+4t .. 5+4t) owns query tile t, one thread per row
+    // Warpgroup t (warps 3+4t .. 6+4t) owns query tile t, one thread per row
     // (its TMEM lane).
-    const int t = (warp - 2) / 4;
+    const int t = (warp - 3) / 4;
     const int quad = warp & 3;  // TMEM lane quarter this warp may access (rows 32 quad ..)
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t t_s = tmem_base + lane_off + C::T_S + 128u * static_cast<uint32_t>(t);
