@@ -259,11 +259,13 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
       if (warp == 1) {
         for (int j = 0; j < nkv && ok; ++j) {
           for (int t = 0; t < C::NT && ok; ++t) {
-            if (j > 0 && !mbar_wait(pv_done(t), static_cast<uint32_t>(j - 1) & 1u, tmo, abort_flag)) {
+            // the wait that usually has completed first, the ordering one last: once it is seen,
+            // the MMAs go out at once
+            if (t == 0 && !mbar_wait(k_full(j % C::KST), static_cast<uint32_t>(j / C::KST) & 1u, tmo, abort_flag)) {
               ok = false;
               break;
             }
-            if (t == 0 && !mbar_wait(k_full(j % C::KST), static_cast<uint32_t>(j / C::KST) & 1u, tmo, abort_flag)) {
+            if (j > 0 && !mbar_wait(pv_done(t), static_cast<uint32_t>(j - 1) & 1u, tmo, abort_flag)) {
               ok = false;
               break;
             }
@@ -284,18 +286,19 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
       } else {
         for (int j = 0; j < nkv && ok; ++j) {
           for (int t = 0; t < C::NT && ok; ++t) {
-            // the score product issued before this P·V: S_B(j) for tile A, S_A(j+1) for tile B
-            const int tp = (t + C::NT - 1) % C::NT;
-            const int jp = t == 0 ? j : j + 1;
-            if (jp < nkv && !mbar_wait(s_issued(tp), static_cast<uint32_t>(jp) & 1u, tmo, abort_flag)) {
-              ok = false;
-              break;
-            }
+            // P and V (usually ready) first; last the score product that goes before this P·V
+            // in the tensor core's order: S_B(j) for tile A, S_A(j+1) for tile B
             if (!mbar_wait(p_full(t), static_cast<uint32_t>(j) & 1u, tmo, abort_flag)) {
               ok = false;
               break;
             }
             if (t == 0 && !mbar_wait(v_full(j % C::VST), static_cast<uint32_t>(j / C::VST) & 1u, tmo, abort_flag)) {
+              ok = false;
+              break;
+            }
+            const int tp = (t + C::NT - 1) % C::NT;
+            const int jp = t == 0 ? j : j + 1;
+            if (jp < nkv && !mbar_wait(s_issued(tp), static_cast<uint32_t>(jp) & 1u, tmo, abort_flag)) {
               ok = false;
               break;
             }
