@@ -43,12 +43,6 @@ TKG_API tkg_status tkg_debug_variant_info(int kind, int variant, int32_t info[6]
  * TKG_OPT_VARIANT). */
 TKG_API int tkg_debug_pick_variant(int kind, int64_t M, int64_t N, int64_t K);
 
-/* Host: the number of kernels one tkg_gemm_<kind> call of this shape launches
- * (NVFP4: 2 when its block scales are first re-laid out by a kernel of their
- * own, 1 when the GEMM reads them straight from the caller's arrays; else 1),
- * or -1 for an unknown kind. */
-TKG_API int tkg_debug_gemm_launches(int kind, int64_t M, int64_t N, int64_t K);
-
 /* Host: the split-K head plan (TKG_OPT_SPLIT_K) for `tiles` output tiles on a
  * persistent grid of `clusters` clusters with `num_kb` K stages per tile:
  * *split_tiles tail tiles cut into *split_s pieces each (0 and 1: no split).

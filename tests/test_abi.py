@@ -127,21 +127,6 @@ def test_schedule_and_overlap_options(tkg):
     assert tkg.tkg_get_option(tkg.TKG_OPT_LAUNCH_OVERLAP) == tkg.TKG_OVERLAP_ON
 
 
-def test_gemm_launch_count(tkg):
-    # NVFP4 with K % 256 == 0 reads its block scales in place: one kernel; otherwise the scales are
-    # re-laid out first: two.  bf16 / FP8: one.
-    assert tkg.tkg_debug_gemm_launches(2, 16384, 16384, 16384) == 1
-    assert tkg.tkg_debug_gemm_launches(2, 300, 520, 416) == 2
-    assert tkg.tkg_debug_gemm_launches(0, 4096, 4096, 4096) == 1
-    assert tkg.tkg_debug_gemm_launches(1, 8192, 8192, 8192) == 1
-    assert tkg.tkg_debug_gemm_launches(7, 1, 1, 1) == -1
-    tkg.tkg_set_option(tkg.TKG_OPT_VARIANT, 7)  # staged scales from global memory
-    try:
-        assert tkg.tkg_debug_gemm_launches(2, 16384, 16384, 16384) == 2
-    finally:
-        tkg.tkg_set_option(tkg.TKG_OPT_VARIANT, 0)
-
-
 def test_split_option(tkg):
     assert tkg.tkg_get_option(tkg.TKG_OPT_SPLIT_K) == tkg.TKG_SPLIT_ON
     tkg.tkg_set_option(tkg.TKG_OPT_SPLIT_K, tkg.TKG_SPLIT_OFF)

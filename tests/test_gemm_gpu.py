@@ -45,7 +45,7 @@ SMALL_SHAPES = {
              (1000, 1000, 512)],
     "fp8": [(128, 256, 128), (256, 256, 256), (300, 520, 208), (77, 100, 48), (1, 16, 16), (1000, 1000, 512)],
     "nvfp4": [(128, 256, 256), (256, 256, 512), (300, 520, 416), (77, 100, 96), (1, 16, 32), (1000, 1000, 1024),
-              (520, 300, 288), (300, 520, 768), (77, 100, 256)],
+              (520, 300, 288)],
 }
 
 
@@ -153,23 +153,3 @@ def test_nvfp4_repeated_calls_reuse_scratch(tkg):
         g = run_gpu(ops)
         acc, c_ref = oracle.gemm(ops)
         check_against_oracle("nvfp4", g.c_bits(), acc, c_ref, ops.scale_a, ops.scale_b)
-
-
-@pytest.mark.parametrize("shape", [(256, 256, 512), (300, 520, 768), (1000, 1000, 1024), (77, 100, 256)])
-def test_nvfp4_scales_read_in_place_match_staged_scales(tkg, shape):
-    """K % 256 == 0: the default variant's TMA reads the caller's row-major scales in place
-    (one launch); variant 7 takes the same scales through the staged copy.  Same MMAs, same
-    scales: the outputs are identical."""
-    M, N, K = shape
-    assert tkg.tkg_debug_gemm_launches(2, M, N, K) == 1
-    ops = synth.make_operands("nvfp4", M, N, K, "normal", 61, 62)
-    direct = run_gpu(ops).c_bits()
-    tkg.tkg_set_option(tkg.TKG_OPT_VARIANT, 7)
-    try:
-        assert tkg.tkg_debug_gemm_launches(2, M, N, K) == 2
-        staged = run_gpu(ops).c_bits()
-    finally:
-        tkg.tkg_set_option(tkg.TKG_OPT_VARIANT, 0)
-    assert np.array_equal(direct, staged)
-    acc, c_ref = oracle.gemm(ops)
-    check_against_oracle("nvfp4", direct, acc, c_ref, ops.scale_a, ops.scale_b)

@@ -261,10 +261,6 @@ tkg_status max_clusters(DevState& d, int kind, int id, const KernelVariant& v, i
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// NVFP4 variants whose scales ride the operand ring read them straight from the caller's
-// row-major arrays when a row of scales is a whole number of 16-byte TMA units.
-bool nvfp4_direct_scales(const KernelVariant& v, int64_t K) { return v.sf_smem != 0 && K % 256 == 0; }
-
 // Split-K head plan for `tiles` output tiles on a persistent grid of `clusters`
 // clusters walking `num_kb` K blocks per tile.  The grid takes R = ceil(tiles /
 // clusters) rounds, the last holding `tail` tiles; if that round would be at
@@ -387,17 +383,7 @@ tkg_status gemm_launch(int kind, int64_t M, int64_t N, int64_t K, const void* A,
   const int64_t k_bytes = kind == 0 ? K * 2 : kind == 1 ? K : K / 2;
   p.num_kb = static_cast<int>((k_bytes + 127) / 128);
   uint8_t* scratch = nullptr;
-  if (kind == 2 && nvfp4_direct_scales(*v, K)) {
-    // The scales ride the operand ring and each stage takes a [rows][16 scales] box: TMA can
-    // read those boxes straight from the caller's row-major [rows][K/16] arrays when a row is
-    // a whole number of 16-byte units (K % 256 == 0), so no staged copy is made.
-    p.sf_direct = 1;
-    st = get_map(&p.tmap_sfa, scales->a_block_scale, CU_TENSOR_MAP_DATA_TYPE_UINT8, K / 16, M, K / 16, 16, 128, 0);
-    if (st == TKG_OK)
-      st = get_map(&p.tmap_sfb, scales->b_block_scale, CU_TENSOR_MAP_DATA_TYPE_UINT8, K / 16, N, K / 16, 16,
-                   static_cast<uint32_t>(v->bn), 0);
-    if (st != TKG_OK) return st;
-  } else if (kind == 2) {
+  if (kind == 2) {
     // Interleaved block scales (stream-ordered scratch, freed after the GEMM in stream order).
     p.sf_blocks_a = static_cast<int>(tiles_m * v->cg);
     p.sf_blocks_b = static_cast<int>(tiles_n * (v->bn / 128));
@@ -670,12 +656,6 @@ tkg_status tkg_debug_variant_info(int kind, int variant, int32_t info[6]) {
 }
 
 int tkg_debug_pick_variant(int kind, int64_t M, int64_t N, int64_t K) { return pick_variant(kind, M, N, K); }
-
-int tkg_debug_gemm_launches(int kind, int64_t M, int64_t N, int64_t K) {
-  const KernelVariant* v = variant_of(kind, pick_variant(kind, M, N, K));
-  if (!v) return -1;
-  return (kind == 2 && !nvfp4_direct_scales(*v, K)) ? 2 : 1;
-}
 
 int tkg_debug_split_plan(int64_t tiles, int64_t clusters, int num_kb, int* split_tiles, int* split_s) {
   if (!split_tiles || !split_s || num_kb < 0) return -1;

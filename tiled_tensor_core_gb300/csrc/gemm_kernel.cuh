@@ -59,8 +59,6 @@ struct GemmParams {
   int sf_blocks_b;  // same for B
   const uint8_t* sf_a;  // NVFP4 scale-warp mode: staged A scales in global memory
   const uint8_t* sf_b;  // same for B
-  int sf_direct;        // NVFP4, scales riding the ring: tmap_sfa / tmap_sfb cover the caller's row-major
-                        // [rows][K/16] scales (x = 16 bytes per 256-deep K stage) instead of staged runs
   int sched;            // tile schedule (kSchedStatic / kSchedDynamic / kSchedSingle)
   unsigned int* visits;  // debug: if set, one increment per tile each time a CTA (pair) stores it
   // split-K head of the static schedule (split_tiles = 0: off): the first split_tiles tiles of
@@ -472,15 +470,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
             if constexpr (C::SF_SMEM) {
               const uint32_t sfb_bar = sf_full_bar(stage);
               mbar_arrive_expect_tx(sfb_bar, C::SF_TX);
-              if (p.sf_direct) {
-                // [128 or BN rows][16 scales] boxes of the caller's matrices: the same bytes, in the
-                // same order, as a staged run (rows and K past the matrix read as zero)
-                tma_load_2d<1>(sSFA + stage * C::SFA_STAGE, &p.tmap_sfa, sfb_bar, 16 * kb, a_row);
-                tma_load_2d<1>(sSFB + stage * C::SFB_STAGE, &p.tmap_sfb, sfb_bar, 16 * kb, tn * C::BN);
-              } else {
-                tma_load_2d<1>(sSFA + stage * C::SFA_STAGE, &p.tmap_sfa, sfb_bar, 0, ya);
-                tma_load_2d<1>(sSFB + stage * C::SFB_STAGE, &p.tmap_sfb, sfb_bar, 0, yb);
-              }
+              tma_load_2d<1>(sSFA + stage * C::SFA_STAGE, &p.tmap_sfa, sfb_bar, 0, ya);
+              tma_load_2d<1>(sSFB + stage * C::SFB_STAGE, &p.tmap_sfb, sfb_bar, 0, yb);
             } else {
               if constexpr (C::SFA_IN_SMEM) tma_load_2d<C::CG>(sSFA + stage * C::SFA_STAGE, &p.tmap_sfa, fb, 0, ya);
               if constexpr (C::SFB_IN_SMEM) tma_load_2d<C::CG>(sSFB + stage * C::SFB_STAGE, &p.tmap_sfb, fb, 0, yb);
@@ -1008,7 +999,6 @@ struct KernelVariant {
   const char* name;
   const void* func;
   int mc;  // CTA pairs per cluster sharing A (1 or 2)
-  int sf_smem;  // NVFP4: the block scales ride the operand ring into shared memory
 };
 
 template <class C>
@@ -1016,7 +1006,7 @@ KernelVariant make_variant(const char* name) {
   return KernelVariant{static_cast<int>(C::KIND), C::CG,         C::BN,         C::EPI_COLS,
                        C::SF_MODE,                   C::STAGES,     C::EPI_WARPS,  C::THREADS,
                        C::SMEM_BYTES,                name,          reinterpret_cast<const void*>(&tkg_gemm_kernel<C>),
-                       C::MC,                        C::SF_SMEM ? 1 : 0};
+                       C::MC};
 }
 
 }  // namespace tkg

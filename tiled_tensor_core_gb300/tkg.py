@@ -88,8 +88,6 @@ lib.tkg_debug_variant_info.argtypes = [_i32, _i32, ctypes.POINTER(ctypes.c_int32
 lib.tkg_debug_variant_info.restype = _i32
 lib.tkg_debug_pick_variant.argtypes = [_i32, _i64, _i64, _i64]
 lib.tkg_debug_pick_variant.restype = _i32
-lib.tkg_debug_gemm_launches.argtypes = [_i32, _i64, _i64, _i64]
-lib.tkg_debug_gemm_launches.restype = _i32
 lib.tkg_debug_split_plan.argtypes = [_i64, _i64, _i32, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
 lib.tkg_debug_split_plan.restype = _i32
 lib.tkg_debug_work_item.argtypes = [_i32, _i32, _i32, _i32, ctypes.POINTER(ctypes.c_int32)]
@@ -223,10 +221,6 @@ def tkg_debug_variant_info(kind, variant):
 
 def tkg_debug_pick_variant(kind, M, N, K) -> int:
     return int(lib.tkg_debug_pick_variant(kind, M, N, K))
-
-
-def tkg_debug_gemm_launches(kind, M, N, K) -> int:
-    return int(lib.tkg_debug_gemm_launches(kind, M, N, K))
 
 
 def tkg_debug_split_plan(tiles, clusters, num_kb):
