@@ -317,9 +317,16 @@ bool split_workspace(DevState& d, cudaStream_t stream, DevState::SplitWs* out) {
     if (w.cnt) cudaFree(w.cnt);
     return false;
   }
-  std::lock_guard<std::mutex> lk(g_mu);
-  d.split.emplace(stream, w);
-  *out = w;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto ins = d.split.emplace(stream, w);
+    *out = ins.first->second;
+    if (ins.second) return true;
+  }
+  // another thread made this stream's workspace meanwhile: use that one
+  cudaFree(w.ws);
+  cudaFree(w.cnt);
+  cudaGetLastError();
   return true;
 }
 
