@@ -30,7 +30,9 @@
 // one tile's softmax runs, the tensor core has the other tile's P·V and next
 // scores to compute, and with two issuing threads one of them waits on its
 // barriers while the other's MMAs keep the tensor core fed (the tensor core
-// queues only one or two MMAs ahead).  P never touches shared memory.  Every wait is bounded
+// queues only one or two MMAs ahead).  At D = 64 tensor memory has room for P
+// columns of each tile's own, so the next scores wait only until the softmax
+// has read the previous ones.  P never touches shared memory.  Every wait is bounded
 // (TKG_OPT_TIMEOUT_NS) and reported through the status word.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -75,13 +77,18 @@ struct AttnCfg {
   static constexpr int OFF_V = OFF_K + KST * KV_STAGE;
   static constexpr int OFF_Q = OFF_V + VST * KV_STAGE;  // tile t at OFF_Q + t * Q_TILE; the output staging at the end
   static constexpr int OFF_BAR = OFF_Q + NT * Q_TILE;
-  static constexpr int NUM_BARS = 1 + 2 * KST + 2 * VST + 4 * NT + 2;
+  static constexpr int NUM_BARS = 1 + 2 * KST + 2 * VST + 5 * NT + 2;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NUM_BARS;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr int THREADS = 96 + 32 * 4 * NT;  // producer, two MMA issuers, a softmax warpgroup per query tile
   // TMEM columns: tile t's score buffer at 128 t (its P, bf16 pairs, over the
   // first 64 of them once the scores are read), its output accumulator at 256 + D t
-  static constexpr uint32_t T_S = 0, T_O = 128 * NT;
+  // D = 64: room for P columns of its own per tile (S 128, P 64, O 64 per tile), so the
+  // next scores wait only until the softmax has read the previous ones
+  static constexpr bool SEP_P = (D == 64);
+  static constexpr uint32_t T_S = 0, T_O = (SEP_P ? 192 : 128) * NT;
+  static constexpr uint32_t S_STRIDE = SEP_P ? 192 : 128;  // tile t's scores at T_S + S_STRIDE t
+  static constexpr uint32_t P_OFF = SEP_P ? 128 : 0;       // its P at T_S + S_STRIDE t + P_OFF
   static constexpr uint32_t TMEM_COLS = 512;
   // S = Q·Kᵀ: M = 128, N = BKV, both K-major;  O += P·V: M = 128, N = D, P from
   // tensor memory, V an MN-major shared operand (bit 16)
@@ -150,8 +157,10 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
   auto pv_done = [&](int t) { return bar0 + 8u * (B1 + 2 * C::NT + t); };
   // S_t(j) has been issued (the P·V thread keeps the tensor core's order P_A·V, S_A, P_B·V, S_B)
   auto s_issued = [&](int t) { return bar0 + 8u * (B1 + 3 * C::NT + t); };
-  const uint32_t o_final = bar0 + 8u * (B1 + 4 * C::NT);  // the last P·V finished
-  const uint32_t drain = bar0 + 8u * (B1 + 4 * C::NT + 1);  // both issuers' MMAs finished
+  // separate P columns (D = 64): S_t(j) has been read into the softmax warps' registers
+  auto s_loaded = [&](int t) { return bar0 + 8u * (B1 + 4 * C::NT + t); };
+  const uint32_t o_final = bar0 + 8u * (B1 + 5 * C::NT);  // the last P·V finished
+  const uint32_t drain = bar0 + 8u * (B1 + 5 * C::NT + 1);  // both issuers' MMAs finished
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* never_abort = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
@@ -178,6 +187,7 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
       mbar_init(p_full(t), 4);  // one arrival per warp of the tile's softmax warpgroup
       mbar_init(pv_done(t), 1);
       mbar_init(s_issued(t), 1);
+      mbar_init(s_loaded(t), 4);  // one arrival per warp of the tile's softmax warpgroup
     }
     mbar_init(o_final, 1);
     mbar_init(drain, 2);
@@ -265,7 +275,10 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
               ok = false;
               break;
             }
-            if (j > 0 && !mbar_wait(pv_done(t), static_cast<uint32_t>(j - 1) & 1u, tmo, abort_flag)) {
+            // the score buffer is free once S_t(j-1) has been read (P elsewhere) or, with P over
+            // the scores, once P_t(j-1)·V_{j-1} has finished
+            if (j > 0 && !mbar_wait(C::SEP_P ? s_loaded(t) : pv_done(t), static_cast<uint32_t>(j - 1) & 1u, tmo,
+                                    abort_flag)) {
               ok = false;
               break;
             }
@@ -276,9 +289,9 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint64_t ad = sdesc_sw128(q_t + (kk / 4) * C::CHUNK + 32u * (kk % 4));
               const uint64_t bd = sdesc_sw128(k0 + (kk / 4) * C::CHUNK + 32u * (kk % 4));
-              mma_bf16<1>(tmem_base + C::T_S + 128u * t, ad, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
+              mma_bf16<1>(tmem_base + C::T_S + C::S_STRIDE * t, ad, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
             }
-            mbar_arrive_local(s_issued(t));
+            if constexpr (!C::SEP_P) mbar_arrive_local(s_issued(t));
             mma_commit_local(s_full(t));
             if (t == C::NT - 1) mma_commit_local(k_empty(j % C::KST));  // the last reader of K_j
           }
@@ -296,15 +309,18 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
               ok = false;
               break;
             }
+            // (not with P in columns of its own: the score thread then runs up to two products
+            // ahead, past what a parity wait on this barrier can tell apart, and the order is free)
             const int tp = (t + C::NT - 1) % C::NT;
             const int jp = t == 0 ? j : j + 1;
-            if (jp < nkv && !mbar_wait(s_issued(tp), static_cast<uint32_t>(jp) & 1u, tmo, abort_flag)) {
+            if (!C::SEP_P && jp < nkv &&
+                !mbar_wait(s_issued(tp), static_cast<uint32_t>(jp) & 1u, tmo, abort_flag)) {
               ok = false;
               break;
             }
             tc_fence_after();
             const uint32_t v0 = sV + (j % C::VST) * C::KV_STAGE;
-            const uint32_t a0 = tmem_base + C::T_S + 128u * t;  // P_t(j): bf16 pairs over the scores
+            const uint32_t a0 = tmem_base + C::T_S + C::S_STRIDE * t + C::P_OFF;  // P_t(j), bf16 pairs
 #pragma unroll
             for (int kk = 0; kk < C::BKV / 16; ++kk) {
               // A: 16 keys of P_t = 8 of its columns; B: 16 rows of V (keys), D columns
@@ -331,8 +347,8 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
     const int t = (warp - 3) / 4;
     const int quad = warp & 3;  // TMEM lane quarter this warp may access (rows 32 quad ..)
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t t_s = tmem_base + lane_off + C::T_S + 128u * static_cast<uint32_t>(t);
-    const uint32_t t_p = t_s;  // P over the first 64 score columns, once the scores are read
+    const uint32_t t_s = tmem_base + lane_off + C::T_S + C::S_STRIDE * static_cast<uint32_t>(t);
+    const uint32_t t_p = t_s + C::P_OFF;  // P: its own columns, or over the scores once they are read
     const uint32_t t_o = tmem_base + lane_off + C::T_O + static_cast<uint32_t>(D * t);
     const float c2 = p.scale_log2;
     float m = -INFINITY;  // reference maximum of the raw scores of this row (lazily raised)
@@ -350,6 +366,12 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
       tmem_wait_ld();
 #pragma unroll
       for (int q = 0; q < 4; ++q) reg_fence(s[q]);
+      if constexpr (C::SEP_P) {
+        // the scores are in registers: the buffer may take the next ones
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_local(s_loaded(t));
+      }
       // keys of this tile past the end of the sequence score -inf (only the last tile has any)
       const int valid = p.Nkv - j * C::BKV;
       if (valid < C::BKV) {
@@ -411,8 +433,16 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
 #pragma unroll
         for (int e = 0; e < w; ++e) ls[e] += ls[e + w];
       l = l * alpha + ls[0];
-      // P_t(j-1)·V_{j-1} finished before S_t(j) was issued: O_t holds key tiles 0..j-1 and
-      // nothing reads the score buffer, so P_t(j) may go over the scores and O_t be rescaled
+      // P_t(j) may be written and O_t rescaled once P_t(j-1)·V_{j-1} has finished: with P over
+      // the scores that was so before S_t(j) was issued; with P in its own columns, wait for it
+      if constexpr (C::SEP_P) {
+        if (j >= 1 && !__all_sync(0xffffffffu, mbar_wait<true>(pv_done(t), static_cast<uint32_t>(j - 1) & 1u, tmo,
+                                                                abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
       if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.0f)) {
         // O_t holds key tiles 0..j-1
 #pragma unroll
@@ -425,7 +455,7 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
           tmem_st_32x32b_x32(t_o + 32u * q, o);
         }
       }
-      // P row (bf16 pairs) over the first 64 score columns
+      // P row (bf16 pairs)
       tmem_st_32x32b_x32(t_p, *reinterpret_cast<uint32_t(*)[32]>(pk));
       tmem_st_32x32b_x32(t_p + 32u, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
       tmem_wait_st();
