@@ -193,7 +193,9 @@ TKG_API void tkg_shutdown(void);
  *                      tile order (default 8; the paper's {8, N, M/8} order,
  *                      "Block Launch Order and L2 Cache Reuse", Table 3)
  *  TKG_OPT_VARIANT     force a kernel variant: 0 = the default (8 for
- *                      NVFP4, else 2), 1 = 1-SM 128x256 tiles, 2 = 2-SM
+ *                      NVFP4; for bf16 and FP8 13 when K >= 4096 and the
+ *                      256x512 tiles number at least 304, else 2), 1 = 1-SM
+ *                      128x256 tiles, 2 = 2-SM
  *                      (CTA pair) 256x256 tiles, 3 = 2-SM 256x128 tiles,
  *                      4 = 2-SM 256x224 tiles (bf16 and FP8 only),
  *                      5 = 2-SM 256x256 tiles whose block scales are
@@ -211,8 +213,11 @@ TKG_API void tkg_shutdown(void);
  *                      10 / 11 / 12 = clusters of two CTA pairs on
  *                      horizontally adjacent 256x256 / 256x224 / 256x192
  *                      tiles, each A tile loaded once and multicast into
- *                      both pairs (bf16 and FP8 only).  A variant the kind
- *                      lacks falls back to the default.
+ *                      both pairs (bf16 and FP8 only), 13 = 2-SM 256x512
+ *                      tiles, two N = 256 MMAs per K step into all 512
+ *                      tensor-memory columns (bf16 and FP8 only; no split-K
+ *                      head).  A variant the kind lacks falls back to the
+ *                      default.
  *  TKG_OPT_MAX_CTAS    cap the persistent grid size (0 = all SMs)
  *  TKG_OPT_LAUNCH_OVERLAP
  *                      TKG_OVERLAP_ON (default): GEMMs are launched as

@@ -32,12 +32,12 @@ def variant(tkg, request):
     tkg.tkg_set_option(tkg.TKG_OPT_VARIANT, 0)
 
 
-VARIANTS = [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12]
+VARIANTS = [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13]
 
 
 def skip_absent(kind, variant):
-    """Variants 4 and 9-12 are bf16 / FP8 only and 5-8 NVFP4 only; others would rerun the default."""
-    if (variant in (4, 9, 10, 11, 12) and kind == "nvfp4") or (variant in (5, 6, 7, 8) and kind != "nvfp4"):
+    """Variants 4 and 9-13 are bf16 / FP8 only and 5-8 NVFP4 only; others would rerun the default."""
+    if (variant in (4, 9, 10, 11, 12, 13) and kind == "nvfp4") or (variant in (5, 6, 7, 8) and kind != "nvfp4"):
         pytest.skip("variant not compiled for this kind")
 
 SMALL_SHAPES = {

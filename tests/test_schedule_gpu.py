@@ -138,11 +138,11 @@ MC_SHAPES = [(300, 520, 200), (256, 1024, 128), (1000, 1000, 512), (77, 100, 40)
              (512, 2100, 128)]
 
 
-@pytest.mark.parametrize("variant", [9, 10, 11, 12], indirect=True)
+@pytest.mark.parametrize("variant", [9, 10, 11, 12, 13], indirect=True)
 @pytest.mark.parametrize("schedule", list(SCHEDULES), indirect=True)
 @pytest.mark.parametrize("kind", ["bf16", "fp8"])
 def test_tile_variants_match_oracle_and_visit_each_tile_once(tkg, variant, schedule, kind):
-    """256x192 tiles, and clusters of two CTA pairs sharing A."""
+    """256x192 and 256x512 tiles, and clusters of two CTA pairs sharing A."""
     for i, (M, N, K) in enumerate(MC_SHAPES):
         if kind == "fp8":
             K = -(-K // 16) * 16

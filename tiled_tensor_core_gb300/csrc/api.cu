@@ -215,13 +215,23 @@ const KernelVariant* variant_of(int kind, int id) {
 // the stages saves the MMA thread a second wait per stage; and reading the
 // scales from shared memory, where the ring's TMA put them stages ahead, keeps
 // global-load latency off the scale warps' critical path.
+//
+// bf16 / FP8 with long K and many tiles take the 256 x 512 pair tile instead: it
+// moves a third fewer operand bytes per flop, which draws less power, and under
+// the power cap that buys clock (8192^3 bf16: 1779 against 1710 TFLOP/s, at
+// 1601 against 1507 MHz); it keeps a single accumulator (a tile's store does not
+// overlap the next tile) and coarser rounds of tiles, so it loses with short K
+// (16384 x 8192 x 2048: 1674 against 1706) or few tiles (4096^3: 1609 against
+// 1639, where the split-K head of the 256 x 256 tile helps more).
+constexpr int64_t kWideMinK = 4096;
+constexpr int64_t kWideMinTiles = 4 * 76;  // four rounds of 256 x 512 tiles on GB300's 76 CTA pairs
 int pick_variant(int kind, int64_t M, int64_t N, int64_t K) {
-  (void)K;
-  (void)M;
-  (void)N;
   const int forced = static_cast<int>(g_opt_variant.load(std::memory_order_relaxed));
   if (forced > 0 && variant_of(kind, forced)) return forced;
-  return kind == 2 ? kVariant2Sm256x256SfSmem : kVariant2Sm256x256;
+  if (kind == 2) return kVariant2Sm256x256SfSmem;
+  const int64_t wide_tiles = ((M + 255) / 256) * ((N + 511) / 512);
+  if (K >= kWideMinK && wide_tiles >= kWideMinTiles) return kVariant2Sm256x512;
+  return kVariant2Sm256x256;
 }
 
 // Occupancy-limited number of co-resident clusters for a variant (cached).
@@ -375,7 +385,8 @@ tkg_status gemm_launch(int kind, int64_t M, int64_t N, int64_t K, const void* A,
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
   // Operand maps: rows of K elements, boxes of 128 bytes x (rows per CTA).
-  const uint32_t b_rows = static_cast<uint32_t>(v->bn / v->cg);
+  // rows of one B box: a CTA's share of one MMA's N (512-wide tiles load two boxes per stage)
+  const uint32_t b_rows = static_cast<uint32_t>((v->bn > 256 ? 256 : v->bn) / v->cg);
   if (kind == 0) {
     // A multicast between two CTA pairs: each CTA loads a 64-row quarter of the pair tile's A
     st = get_map(&p.tmap_a, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, K * 2, 64, 128 / v->mc, 128);
@@ -466,7 +477,7 @@ tkg_status gemm_launch(int kind, int64_t M, int64_t N, int64_t K, const void* A,
   // scale warps walk a precomputed sequence), planned for the clusters the grid may use
   p.split_s = 1;
   int64_t items = units;
-  if (p.sched == kSchedStatic && v->mc == 1 && opt_or(g_opt_split, TKG_SPLIT_ON) == TKG_SPLIT_ON &&
+  if (p.sched == kSchedStatic && v->mc == 1 && v->bn <= 256 && opt_or(g_opt_split, TKG_SPLIT_ON) == TKG_SPLIT_ON &&
       !(kind == 2 && (id == kVariant2Sm256x256Sfw || id == kVariant2Sm256x256Hybrid ||
                       id == kVariant2Sm256x256Coupled))) {
     int split_tiles = 0, split_s = 1;

@@ -162,6 +162,11 @@ struct GemmCfg {
   static constexpr int K_TMAP = (KIND == Kind::BF16) ? 64 : 128;
   static constexpr int KSTEPS = 4;              // MMAs per stage: 32 bytes of K each
   static constexpr int B_ROWS = BN / CG;        // B rows staged by each CTA
+  // tiles wider than one MMA (BN = 512): NSUB MMAs of N = 256 per K step, into adjacent
+  // accumulator column ranges; each CTA stages B_ROWS / NSUB rows of B for each of them
+  static constexpr int NSUB = BN > 256 ? BN / 256 : 1;
+  static constexpr int MMA_N = BN / NSUB;
+  static constexpr int B_SUB_ROWS = B_ROWS / NSUB;
   static constexpr int A_STAGE = BM * ROW_BYTES;
   static constexpr int B_BOX = B_ROWS * ROW_BYTES;             // bytes of one B tile load
   static constexpr int B_STAGE = (B_BOX + 1023) / 1024 * 1024;  // keeps every stage 1024-byte aligned
@@ -182,7 +187,7 @@ struct GemmCfg {
   // land on the CTA's own sf_full barrier instead
   static constexpr int STAGE_TX = A_STAGE + B_BOX + (SF_SMEM_ ? 0 : SFA_STAGE + SFB_STAGE);
   static constexpr int SF_TX = SFA_STAGE + SFB_STAGE;
-  static constexpr int ACC_STRIDE = BN <= 128 ? 128 : 256;  // accumulators start on aligned columns
+  static constexpr int ACC_STRIDE = BN <= 128 ? 128 : BN <= 256 ? 256 : BN;  // accumulators start on aligned columns
   static constexpr int ACC_COLS = NUM_ACC * ACC_STRIDE;
   // TMEM columns of one stage's scales: A: 4 per MMA (row m at column m/32);
   // B: BN/32 per MMA (row n at column n/32).
@@ -203,9 +208,9 @@ struct GemmCfg {
   static constexpr uint32_t EPI_SWZ = select_swizzle(EPI_ROW_BYTES);
   static constexpr int EPI_BUF = 32 * EPI_ROW_BYTES;  // one warp's 32-row staging tile
   static constexpr int THREADS = 64 + 32 * (EPI_WARPS + SF_WARPS + CP_WARPS);
-  static constexpr uint32_t IDESC = (KIND == Kind::BF16)   ? idesc_dense(kFmtBF16, BM * CG, BN)
-                                    : (KIND == Kind::FP8) ? idesc_dense(kFmtE4M3, BM * CG, BN)
-                                                          : idesc_mxf4nvf4(BM * CG, BN);
+  static constexpr uint32_t IDESC = (KIND == Kind::BF16)   ? idesc_dense(kFmtBF16, BM * CG, MMA_N)
+                                    : (KIND == Kind::FP8) ? idesc_dense(kFmtE4M3, BM * CG, MMA_N)
+                                                          : idesc_mxf4nvf4(BM * CG, MMA_N);
 
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
@@ -230,7 +235,8 @@ struct GemmCfg {
 
   static_assert(B_STAGE % 1024 == 0 && A_STAGE % 1024 == 0, "stages must keep 1024-byte swizzle atoms aligned");
   static_assert((OFF_SFA % 1024) == 0 && (OFF_EPI % 1024) == 0, "region alignment");
-  static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN must be a multiple of 32 in [64,256]");
+  static_assert(BN % 32 == 0 && BN >= 64 && (BN <= 256 || BN == 512), "BN: a multiple of 32 in [64,256], or 512");
+  static_assert(NSUB == 1 || (!SCALED && MC == 1 && NUM_ACC == 1 && CG == 2), "512-wide tiles: bf16 / FP8 pairs");
   static_assert(B_ROWS % 8 == 0, "B rows per CTA must fill whole 8-row swizzle atoms");
   static_assert(EPI_BUF % (8 * EPI_SWZ) == 0, "staging tiles must keep swizzle atoms aligned");
   static_assert(!SCALED || BN % 128 == 0, "block-scaled tiles cover whole 128-row scale blocks of B");
@@ -443,7 +449,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
         int tm, tn;
         tile_coord(wk.tile, tm, tn);
         const int a_row = tm * (C::BM * C::CG) + static_cast<int>(prank) * C::BM;
-        const int b_row = tn * C::BN + static_cast<int>(prank) * C::B_ROWS;
+        // this CTA's rows of B for each MMA of the K step (one MMA unless the tile is 512 wide)
+        const int b_row = tn * C::BN + static_cast<int>(prank) * C::B_SUB_ROWS;
         for (int kb = wk.kb0; kb < wk.kb1; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, tmo, abort_flag)) {
             ok = false;
@@ -462,7 +469,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
             } else {
               tma_load_2d<C::CG>(sA + stage * C::A_STAGE, &p.tmap_a, fb, kb * C::K_TMAP, a_row);
             }
-            tma_load_2d<C::CG>(sB + stage * C::B_STAGE, &p.tmap_b, fb, kb * C::K_TMAP, b_row);
+#pragma unroll
+            for (int sub = 0; sub < C::NSUB; ++sub)
+              tma_load_2d<C::CG>(sB + stage * C::B_STAGE + sub * C::B_SUB_ROWS * C::ROW_BYTES, &p.tmap_b, fb,
+                                 kb * C::K_TMAP, b_row + sub * C::MMA_N);
             // staged scales: 2 KB (16 rows of 128 B) per (K stage, 128-row block), the blocks of one
             // K stage contiguous
             const int ya = (kb * p.sf_blocks_a + a_row / 128) * 16;
@@ -547,7 +557,17 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
             const uint64_t ad = sdesc_sw128(a0 + 32u * kk);
             const uint64_t bd = sdesc_sw128(b0 + 32u * kk);
             const uint32_t accum = (kb != wk.kb0 || kk != 0) ? 1u : 0u;
-            if constexpr (C::KIND == Kind::BF16)
+            if constexpr (C::NSUB > 1) {
+#pragma unroll
+              for (int sub = 0; sub < C::NSUB; ++sub) {
+                const uint64_t bds = sdesc_sw128(b0 + static_cast<uint32_t>(sub * C::B_SUB_ROWS * C::ROW_BYTES) + 32u * kk);
+                const uint32_t d = d_tmem + static_cast<uint32_t>(sub * C::MMA_N);
+                if constexpr (C::KIND == Kind::BF16)
+                  mma_bf16<C::CG>(d, ad, bds, C::IDESC, accum);
+                else
+                  mma_f8f6f4<C::CG>(d, ad, bds, C::IDESC, accum);
+              }
+            } else if constexpr (C::KIND == Kind::BF16)
               mma_bf16<C::CG>(d_tmem, ad, bd, C::IDESC, accum);
             else if constexpr (C::KIND == Kind::FP8)
               mma_f8f6f4<C::CG>(d_tmem, ad, bd, C::IDESC, accum);

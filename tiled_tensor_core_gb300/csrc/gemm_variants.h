@@ -22,7 +22,8 @@ enum VariantId : int {
   kVariantMc256x256 = 10,
   kVariantMc256x224 = 11,
   kVariantMc256x192 = 12,
-  kNumVariants = 13
+  kVariant2Sm256x512 = 13,  // cta_group::2, 256 x 512 tile per CTA pair: two N = 256 MMAs per K step (bf16 / FP8)
+  kNumVariants = 14
 };
 
 // Each returns the variant for `id`, or nullptr if that kind has no such variant.
