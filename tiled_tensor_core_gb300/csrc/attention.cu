@@ -77,7 +77,7 @@ struct AttnCfg {
   static constexpr int OFF_V = OFF_K + KST * KV_STAGE;
   static constexpr int OFF_Q = OFF_V + VST * KV_STAGE;  // tile t at OFF_Q + t * Q_TILE; the output staging at the end
   static constexpr int OFF_BAR = OFF_Q + NT * Q_TILE;
-  static constexpr int NUM_BARS = 1 + 2 * KST + 2 * VST + 5 * NT + 2;
+  static constexpr int NUM_BARS = 1 + 2 * KST + 2 * VST + 6 * NT + 1;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NUM_BARS;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr int THREADS = 96 + 32 * 4 * NT;  // producer, two MMA issuers, a softmax warpgroup per query tile
@@ -159,8 +159,9 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
   auto s_issued = [&](int t) { return bar0 + 8u * (B1 + 3 * C::NT + t); };
   // separate P columns (D = 64): S_t(j) has been read into the softmax warps' registers
   auto s_loaded = [&](int t) { return bar0 + 8u * (B1 + 4 * C::NT + t); };
-  const uint32_t o_final = bar0 + 8u * (B1 + 5 * C::NT);  // the last P·V finished
-  const uint32_t drain = bar0 + 8u * (B1 + 5 * C::NT + 1);  // both issuers' MMAs finished
+  // tile t's last P·V has finished (its finish need not wait for the other tile's)
+  auto o_final = [&](int t) { return bar0 + 8u * (B1 + 5 * C::NT + t); };
+  const uint32_t drain = bar0 + 8u * (B1 + 6 * C::NT);  // both issuers' MMAs finished
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* never_abort = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
@@ -189,7 +190,7 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
       mbar_init(s_issued(t), 1);
       mbar_init(s_loaded(t), 4);  // one arrival per warp of the tile's softmax warpgroup
     }
-    mbar_init(o_final, 1);
+    for (int t = 0; t < C::NT; ++t) mbar_init(o_final(t), 1);
     mbar_init(drain, 2);
     *abort_flag = 0;
     *never_abort = 0;
@@ -330,9 +331,9 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
             }
             mma_commit_local(pv_done(t));
             if (t == C::NT - 1) mma_commit_local(v_empty(j % C::VST));  // the last reader of V_j
+            if (j == nkv - 1) mma_commit_local(o_final(t));
           }
         }
-        if (ok) mma_commit_local(o_final);
       }
       // no MMA of either thread may still be writing TMEM when it is released
       mma_commit_local(drain);
@@ -463,7 +464,7 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_fwd_kernel(const 
       __syncwarp();
       if (lane == 0) mbar_arrive_local(p_full(t));
     }
-    if (ok && !__all_sync(0xffffffffu, mbar_wait<true>(o_final, 0, tmo, abort_flag))) ok = false;
+    if (ok && !__all_sync(0xffffffffu, mbar_wait<true>(o_final(t), 0, tmo, abort_flag))) ok = false;
     if (ok) {
       // FINISH: O / l to bf16, staged per warp ([32 rows][128 B] per 64 columns) in the tile's Q buffer
       tc_fence_after();
