@@ -47,8 +47,8 @@ DTYPE = {"bf16": "bf16", "fp8": "e4m3", "nvfp4": "e2m1+e4m3"}
 # DRAM bytes (read + write) per launch of the dominant kernel, from one ncu capture
 # (profiles/), valid only while the kernel sources hash to the value recorded with it.
 TRAFFIC = {
-    "bf16_4096": {"bytes": 110_346_240, "src": "0d3b537a8238a280"},       # profiles/gemm_bf16_4096_ncu_full.md
-    "nvfp4_16384": {"bytes": 1_945_815_808, "src": "0d3b537a8238a280"},   # profiles/gemm_nvfp4_16384_ncu_full.md
+    "bf16_4096": {"bytes": 111_793_920, "src": "65fcc9042c647780"},       # profiles/gemm_bf16_4096_ncu_full.md
+    "nvfp4_16384": {"bytes": 1_974_272_256, "src": "65fcc9042c647780"},   # profiles/gemm_nvfp4_16384_ncu_full.md
     "attn_n4096_d128": {"bytes": 1_062_650_368, "src": "ebade320dad335df"},  # profiles/attention_fwd_4096_d128_ncu_full.md
 }
 GEMM_SOURCES = ("tkg_device.cuh", "gemm_kernel.cuh", "gemm_bf16.cu", "gemm_fp8.cu", "gemm_nvfp4.cu")

@@ -276,6 +276,22 @@ __device__ __forceinline__ void mma_commit(uint32_t bar, uint16_t mask) {
   }
 }
 
+// 32 lanes x 16 consecutive fp32 columns of tensor memory (the split-K reduction's own partial,
+// a quarter chunk at a time), and the matching register tie after tcgen05.wait::ld.
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
+  asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]));
+  asm volatile("" : "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+               "+r"(r[15]));
+}
+
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -620,6 +636,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
     constexpr int NPK = C::EPI_COLS / 2;   // packed bf16 pairs per row
     constexpr int RB = C::EPI_ROW_BYTES;
     constexpr int NQ = C::EPI_COLS / 4;    // 16-byte groups of fp32 per row per chunk
+    static_assert(NQ % 4 == 0, "the split-K reduction takes 16 columns at a time");
     // split-K: this warp's block of a piece's partial accumulator: its 32 rows x its chunks,
     // laid out [chunk][16-byte column group][lane] so that each store / load of a warp is 512
     // contiguous bytes
@@ -661,23 +678,18 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
           if (lane == 0) mbar_arrive_cluster(tempty_leader0 + 8u * acc);
         }
       };
-      // scale, round to bf16 and store chunk c of this warp's rows
-      auto store_chunk = [&](int c, const uint32_t (&r)[NLD][32]) {
-        uint32_t pk[NPK];
-#pragma unroll
-        for (int l = 0; l < NLD; ++l) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            float x0 = __uint_as_float(r[l][2 * j]), x1 = __uint_as_float(r[l][2 * j + 1]);
-            if constexpr (C::KIND != Kind::BF16) {
-              x0 = x0 * sa;
-              x0 = x0 * sb;
-              x1 = x1 * sa;
-              x1 = x1 * sb;
-            }
-            pk[16 * l + j] = pack_bf16x2(x0, x1);
-          }
+      // two fp32 values, scaled (FP8 / NVFP4: by scale_a, then scale_b) and rounded to a bf16 pair
+      auto scale_pack = [&](float x0, float x1) -> uint32_t {
+        if constexpr (C::KIND != Kind::BF16) {
+          x0 = x0 * sa;
+          x0 = x0 * sb;
+          x1 = x1 * sa;
+          x1 = x1 * sb;
         }
+        return pack_bf16x2(x0, x1);
+      };
+      // store chunk c of this warp's rows, given as packed bf16 pairs
+      auto store_chunk = [&](int c, const uint32_t (&pk)[NPK]) {
         if (!live) {
         } else if (p.c_via_tma) {
           const uint32_t buf = stage0 + static_cast<uint32_t>(chunk_ctr & 1) * C::EPI_BUF;
@@ -720,7 +732,13 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
         for (int c = sub; c < NCH; c += SUBS) {
           uint32_t r[NLD][32];
           load_chunk(c, r, true);
-          store_chunk(c, r);
+          uint32_t pk[NPK];
+#pragma unroll
+          for (int l = 0; l < NLD; ++l)
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              pk[16 * l + j] = scale_pack(__uint_as_float(r[l][2 * j]), __uint_as_float(r[l][2 * j + 1]));
+          store_chunk(c, pk);
         }
       } else {
         const int S = p.split_s;
@@ -732,14 +750,18 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
         for (int j = 0; j < NLOC; ++j) {
           const int c = sub + SUBS * j;
           if (c >= NCH || j % S == my_s) continue;
-          uint32_t r[NLD][32];
-          load_chunk(c, r, false);
           float4* dst = mine + j * (NQ * 32) + lane;
+          __syncwarp();
 #pragma unroll
-          for (int q = 0; q < NQ; ++q) {
-            const uint32_t* v = &r[q / 8][4 * (q % 8)];
-            __stcg(dst + q * 32, make_float4(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]),
-                                             __uint_as_float(v[3])));
+          for (int q0 = 0; q0 < NQ; q0 += 4) {
+            uint32_t o[16];
+            tmem_ld_32x32b_x16(t_row + static_cast<uint32_t>(c * C::EPI_COLS + 4 * q0), o);
+            tmem_wait_ld();
+            reg_fence16(o);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              __stcg(dst + (q0 + q) * 32, make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
+                                                      __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3])));
           }
         }
         // 2. count in (fence + atomic), wait until all S pieces have (acquire), bounded
@@ -767,44 +789,48 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
             const int c = sub + SUBS * j;
             if (c >= NCH) break;
             if (j == 0) count_visit();
-            float4 sum[NQ];
-            for (int s2 = 0; s2 < S; ++s2) {
-              float4 part[NQ];
-              if (s2 == my_s) {
-                uint32_t r[NLD][32];
-                load_chunk(c, r, false);
+            // a quarter chunk (16 columns) at a time: the S partials added in piece order, this
+            // piece's own read from tensor memory at its place, then scaled and packed, so that
+            // no fp32 chunk stays in registers (the 128-register kernels hold no more)
+            uint32_t pk[NPK];
 #pragma unroll
-                for (int q = 0; q < NQ; ++q) {
-                  const uint32_t* v = &r[q / 8][4 * (q % 8)];
-                  part[q] = make_float4(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]),
-                                        __uint_as_float(v[3]));
-                }
-              } else {
-                const float4* src = first + s2 * PIECE_STRIDE + j * (NQ * 32);
+            for (int q0 = 0; q0 < NQ; q0 += 4) {
+              float4 sum[4];
+              for (int s2 = 0; s2 < S; ++s2) {
+                float4 part[4];
+                if (s2 == my_s) {
+                  uint32_t o[16];
+                  tmem_ld_32x32b_x16(t_row + static_cast<uint32_t>(c * C::EPI_COLS + 4 * q0), o);
+                  tmem_wait_ld();
+                  reg_fence16(o);
 #pragma unroll
-                for (int q = 0; q < NQ; ++q) part[q] = __ldcg(src + q * 32);
-              }
-#pragma unroll
-              for (int q = 0; q < NQ; ++q) {
-                if (s2 == 0) {
-                  sum[q] = part[q];
+                  for (int q = 0; q < 4; ++q)
+                    part[q] = make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
+                                          __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3]));
                 } else {
-                  sum[q].x += part[q].x;
-                  sum[q].y += part[q].y;
-                  sum[q].z += part[q].z;
-                  sum[q].w += part[q].w;
+                  const float4* src = first + s2 * PIECE_STRIDE + j * (NQ * 32) + q0 * 32;
+#pragma unroll
+                  for (int q = 0; q < 4; ++q) part[q] = __ldcg(src + q * 32);
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  if (s2 == 0) {
+                    sum[q] = part[q];
+                  } else {
+                    sum[q].x += part[q].x;
+                    sum[q].y += part[q].y;
+                    sum[q].z += part[q].z;
+                    sum[q].w += part[q].w;
+                  }
                 }
               }
-            }
-            uint32_t r[NLD][32];
 #pragma unroll
-            for (int q = 0; q < NQ; ++q) {
-              r[q / 8][4 * (q % 8) + 0] = __float_as_uint(sum[q].x);
-              r[q / 8][4 * (q % 8) + 1] = __float_as_uint(sum[q].y);
-              r[q / 8][4 * (q % 8) + 2] = __float_as_uint(sum[q].z);
-              r[q / 8][4 * (q % 8) + 3] = __float_as_uint(sum[q].w);
+              for (int q = 0; q < 4; ++q) {
+                pk[2 * (q0 + q)] = scale_pack(sum[q].x, sum[q].y);
+                pk[2 * (q0 + q) + 1] = scale_pack(sum[q].z, sum[q].w);
+              }
             }
-            store_chunk(c, r);
+            store_chunk(c, pk);
           }
         } else if (lane == 0) {
           record_timeout(p.status, kRoleEpilogue, abort_flag);
