@@ -56,6 +56,33 @@ def _compile(src: str, extra: list[str]) -> str:
     return obj
 
 
+def resource_usage(src: str) -> list[dict]:
+    """Compile one csrc/*.cu with ptxas reporting (to a scratch object) and return,
+    per kernel entry, its mangled name, registers per thread and spill bytes."""
+    import re
+    import tempfile
+    with tempfile.TemporaryDirectory() as tmp:
+        cmd = [_nvcc(), *NVCC_FLAGS, "-Xptxas", "-v", "-c", src, "-o", os.path.join(tmp, "x.o")]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
+    out, cur = [], None
+    for line in r.stderr.splitlines():
+        m = re.search(r"Compiling entry function '(\S+)'", line)
+        if m:
+            cur = {"name": m.group(1)}
+            continue
+        m = re.search(r"(\d+) bytes spill stores, (\d+) bytes spill loads", line)
+        if m and cur is not None:
+            cur["spill_stores"], cur["spill_loads"] = int(m.group(1)), int(m.group(2))
+        m = re.search(r"Used (\d+) registers", line)
+        if m and cur is not None:
+            cur["registers"] = int(m.group(1))
+            out.append(cur)
+            cur = None
+    return out
+
+
 def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     """Compile every csrc/*.cu and link _tkg.so.  Returns the library path."""
     srcs = sources()
