@@ -1,23 +1,40 @@
 """Shared-memory swizzle and bank-conflict model — TEST INFRASTRUCTURE ONLY.
 
 Restates, in plain Python, the three XOR swizzles of the ThunderKittens shared
-tiles and the bank-conflict model used to justify them:
+tiles and a bank-conflict count written from the shared-memory bank
+definition, to check the swizzles against the conflict degrees the pages print:
 
 * Swizzle of a byte address for an S-byte swizzle (S in {32, 64, 128}):
   the 16-byte chunk index (address bits 4 and up) is XOR-ed with the row index
   taken from address bits 7 and up, modulo S/16 chunks — i.e.
-  addr ^ (((addr mod 8S) >> 7) << 4).  (Paper summary, "Shared Memory Tiles:
-  Automated Swizzling", the 32/64/128-byte list; the 128-byte case is the same
-  as addr ^ (((addr >> 7) & 7) << 4) in the blog's model, "Warp level".)
+  addr ^ (((addr mod 8S) >> 7) << 4).  (Paper summary "ThunderKittens: Simple,
+  Fast, and Adorable AI Kernels", section "Shared Memory Tiles: Automated
+  Swizzling", the 32/64/128-byte list; for S = 128 this is the XOR of bits 4-6
+  with bits 7-9 in the blog "ThunderKittens: 16x16 Tiles, ...", section
+  "Warp level".)
 * Selection: the widest of 128/64/32 bytes that the tile's row width in bytes
   is a multiple of (same section; blog "Warp level").
-* Bank model: 32 banks of 4 bytes; a warp of 32 threads each supplies one
-  16-byte row address, served in 4 phases of 8 threads; the conflict degree
-  of a phase is the largest number of accesses landing in one bank (blog,
-  "Warp level", the modelled load).
+* Bank conflicts, from the definition of the banks: shared memory is 32 banks
+  of 4-byte words, word w living in bank w mod 32, so 128 consecutive bytes
+  touch every bank once.  A 16-byte (128-bit) access that starts on a 16-byte
+  boundary covers exactly one group of 4 adjacent banks, group
+  (address / 16) mod 8.  The 32 lanes' 16-byte accesses are served 128 bytes
+  at a time, i.e. in wavefronts of 8 lanes; inside a wavefront, lanes that
+  name the same 16 bytes are served together, and distinct 16-byte words that
+  fall in the same bank group are served one after another.  The conflict
+  degree of the access is the largest such count in any wavefront (1 =
+  conflict-free).  The access modelled is the one the blog uses: lane t reads
+  the first 16 bytes of row t of a tile whose rows are `row_stride` bytes
+  apart.
 """
 
-BANKS = 32
+NUM_BANKS = 32
+BANK_WIDTH = 4                                   # bytes per bank word
+ACCESS_BYTES = 16                                # one 128-bit access per lane
+BANKS_PER_ACCESS = ACCESS_BYTES // BANK_WIDTH    # 4
+BANK_GROUPS = NUM_BANKS // BANKS_PER_ACCESS      # 8 groups of 4 banks
+LANES_PER_WAVEFRONT = BANK_GROUPS                # 8 lanes x 16 B = one pass over the banks
+WARP_LANES = 32
 
 
 def swizzle(addr: int, s_bytes: int) -> int:
@@ -34,18 +51,31 @@ def select_swizzle(row_bytes: int) -> int:
     return 0
 
 
-def bank(addr: int) -> int:
-    return (addr // 4) % BANKS
+def bank_of(byte_addr: int) -> int:
+    """Bank holding the 4-byte word that contains `byte_addr`."""
+    return (byte_addr // BANK_WIDTH) % NUM_BANKS
 
 
-def max_conflict(row_stride: int, s_bytes: int = 0) -> int:
-    worst = 0
-    for phase in range(4):
-        counts = {}
-        for t in range(phase * 8, phase * 8 + 8):
-            a = swizzle(t * row_stride, s_bytes)
-            for w in range(4):
-                b = bank(a + 4 * w)
-                counts[b] = counts.get(b, 0) + 1
-        worst = max(worst, max(counts.values()))
+def bank_group(byte_addr: int) -> int:
+    """The group of 4 adjacent banks a 16-byte-aligned 16-byte access covers."""
+    assert byte_addr % ACCESS_BYTES == 0, "16-byte accesses start on 16-byte boundaries"
+    return bank_of(byte_addr) // BANKS_PER_ACCESS
+
+
+def conflict_degree(lane_addrs) -> int:
+    """Worst number of serialised passes over one bank group, over the
+    wavefronts of a warp whose lanes make the given 16-byte accesses."""
+    lane_addrs = list(lane_addrs)
+    worst = 1
+    for w0 in range(0, len(lane_addrs), LANES_PER_WAVEFRONT):
+        words_per_group = [set() for _ in range(BANK_GROUPS)]
+        for a in lane_addrs[w0:w0 + LANES_PER_WAVEFRONT]:
+            words_per_group[bank_group(a)].add(a)
+        worst = max(worst, max(len(words) for words in words_per_group))
     return worst
+
+
+def row_load_conflict(row_stride: int, s_bytes: int = 0) -> int:
+    """Conflict degree of lane t reading the first 16 bytes of row t (t < 32)
+    of a tile with `row_stride`-byte rows, stored with the S-byte swizzle."""
+    return conflict_degree(swizzle(lane * row_stride, s_bytes) for lane in range(WARP_LANES))
