@@ -106,22 +106,33 @@ TKG_API tkg_status tkg_gemm_nvfp4(int64_t M, int64_t N, int64_t K, const void* A
 
 /* NVFP4 GEMM that allocates no memory.  The pages have no counterpart: this
  * entry point exists for callers that cannot allocate device memory during a
- * call (for example a caller whose allocator is owned by another framework, or
- * one running under a fixed device-memory budget), because tkg_gemm_nvfp4
- * takes the scratch for its on-device re-layout of the block scales from a
- * stream-ordered memory pool.  Same operation, arguments, layouts and result
- * as tkg_gemm_nvfp4.
+ * call (for example a caller whose device memory belongs to another
+ * framework's allocator, one held to a fixed device-memory budget, or one that
+ * must not let a call allocate and synchronise in the middle of its own work),
+ * because tkg_gemm_nvfp4 takes the scratch for its on-device re-layout of the
+ * block scales from a stream-ordered memory pool and may make a per-stream
+ * split-K workspace.  Same operation, arguments and layouts as
+ * tkg_gemm_nvfp4, planned and launched by the same code, with two
+ * differences: the scratch is a fixed array, and the split-K head is never
+ * used.  The result is within the NVFP4 tolerance of tkg_gemm_nvfp4's (for
+ * shapes where that one runs a split-K head the fp32 summation order differs,
+ * so the two need not be bit-identical).  TKG_OPT_SCHEDULE,
+ * TKG_OPT_LAUNCH_OVERLAP, TKG_OPT_GROUP_M and TKG_OPT_MAX_CTAS apply as usual.
  *  - Scratch: a fixed device array of TKG_NVFP4_NOALLOC_SCRATCH_BYTES inside
  *    the library, held by every device that loads the library until the
- *    process exits.  A call needs (Ba + Bb) * ceil(K/256) * 2048 bytes, with
- *    Ba = ceil(M/256)*2 and Bb = ceil(N/256)*2 for the default kernel; larger
- *    problems are rejected with TKG_ERR_INVALID_ARG before any GPU work.
+ *    process exits.  A call needs (Ta * 2 + Tn * 2) * ceil(K/256) * 2048
+ *    bytes, Ta = ceil(M/256) and Tn = ceil(N/256) being the 256-row and
+ *    256-column tile counts of the NVFP4 kernel (its only variant); the limit
+ *    fits M = N = K = 16384 exactly.  Larger problems are rejected with
+ *    TKG_ERR_INVALID_ARG before any GPU work.
  *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress); make that first call before any stream capture.
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
  *  - All calls share the one array and each call overwrites the part it uses,
  *    so calls whose GPU work overlaps (e.g. on two streams) race and give
  *    wrong results; order them on one stream or with events.
- *  - It never calls cudaMalloc, cudaFree or any other allocating routine. */
+ *  - It never calls cudaMalloc, cudaFree or any other allocating routine, and
+ *    encodes its tensor maps on the stack (no host-side cache entry). */
 #define TKG_NVFP4_NOALLOC_SCRATCH_BYTES (32u << 20)
 TKG_API tkg_status tkg_gemm_nvfp4_noalloc(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* C,
                                           const tkg_scales* scales, void* stream);
@@ -194,30 +205,16 @@ TKG_API void tkg_shutdown(void);
  *                      "Block Launch Order and L2 Cache Reuse", Table 3)
  *  TKG_OPT_VARIANT     force a kernel variant: 0 = the default (8 for
  *                      NVFP4; for bf16 and FP8 13 when K >= 4096 and the
- *                      256x512 tiles number at least 304, else 2), 1 = 1-SM
- *                      128x256 tiles, 2 = 2-SM
- *                      (CTA pair) 256x256 tiles, 3 = 2-SM 256x128 tiles,
- *                      4 = 2-SM 256x224 tiles (bf16 and FP8 only),
- *                      5 = 2-SM 256x256 tiles whose block scales are
- *                      written to tensor memory by eight scale warps with
- *                      tcgen05.st instead of tensor-pipe copies (NVFP4
- *                      only; NVFP4 variants 1-3 copy them with
- *                      tcgen05.cp), 6 = 2-SM 256x256 tiles whose A scales
- *                      are written by four scale warps and B scales copied
- *                      by a copy warp (NVFP4 only), 7 = variant 5 with one
- *                      TMEM scale slot per ring stage, the scale warps
- *                      signalling through the stage's own barriers (NVFP4
- *                      only), 8 = variant 7 with the scales brought into
- *                      shared memory by the ring's TMA (NVFP4 only),
- *                      9 = 2-SM 256x192 tiles (bf16 and FP8 only),
- *                      10 / 11 / 12 = clusters of two CTA pairs on
- *                      horizontally adjacent 256x256 / 256x224 / 256x192
- *                      tiles, each A tile loaded once and multicast into
- *                      both pairs (bf16 and FP8 only), 13 = 2-SM 256x512
- *                      tiles, two N = 256 MMAs per K step into all 512
- *                      tensor-memory columns (bf16 and FP8 only; no split-K
- *                      head).  A variant the kind lacks falls back to the
- *                      default.
+ *                      256x512 tiles fill at least four rounds of the
+ *                      device's CTA pairs, else 2); 2 = 2-SM (CTA pair)
+ *                      256x256 tiles, two tensor-memory accumulators (bf16
+ *                      and FP8); 8 = 2-SM 256x256 tiles, one accumulator,
+ *                      the block scales brought into shared memory by the
+ *                      ring's TMA and written to tensor memory by eight
+ *                      scale warps (NVFP4); 13 = 2-SM 256x512 tiles, two
+ *                      N = 256 MMAs per K step into all 512 tensor-memory
+ *                      columns (bf16 and FP8; no split-K head).  A variant
+ *                      the kind lacks falls back to the default.
  *  TKG_OPT_MAX_CTAS    cap the persistent grid size (0 = all SMs)
  *  TKG_OPT_LAUNCH_OVERLAP
  *                      TKG_OVERLAP_ON (default): GEMMs are launched as
@@ -235,9 +232,7 @@ TKG_API void tkg_shutdown(void);
  *                      ... in the grouped order;
  *                      TKG_SCHEDULE_DYNAMIC = one cluster per tile is
  *                      launched and running clusters cancel the launch of
- *                      clusters that have not started and take their tiles
- *                      (not available with NVFP4 variants 5-7, which return
- *                      TKG_ERR_INVALID_ARG);
+ *                      clusters that have not started and take their tiles;
  *                      TKG_SCHEDULE_SINGLE = one cluster per tile, each
  *                      computes its own tile only (non-persistent launch).
  *  TKG_OPT_SPLIT_K     TKG_SPLIT_ON (default): in the static schedule, when
@@ -256,9 +251,8 @@ TKG_API void tkg_shutdown(void);
  *                      adds the partials of its own chunks in piece order,
  *                      so results do not depend on timing.  The pieces are
  *                      the first work items of distinct, co-resident CTA
- *                      pairs.  Not used with A multicast (variants 10-12)
- *                      or NVFP4 variants 5-7.  TKG_SPLIT_OFF: whole tiles
- *                      only.  After a launch reports TKG_ERR_TIMEOUT,
+ *                      pairs.  Not used with the 256x512 tile (variant
+ *                      13).  TKG_SPLIT_OFF: whole tiles only.  After a launch reports TKG_ERR_TIMEOUT,
  *                      tkg_check_status frees the workspaces (they are made
  *                      afresh on next use). */
 typedef enum tkg_option {

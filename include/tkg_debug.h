@@ -40,8 +40,9 @@ TKG_API uint32_t tkg_debug_select_swizzle(uint32_t row_bytes);
 TKG_API tkg_status tkg_debug_variant_info(int kind, int variant, int32_t info[6]);
 
 /* Host: the variant id tkg_gemm_<kind> would launch for this shape (after
- * TKG_OPT_VARIANT). */
-TKG_API int tkg_debug_pick_variant(int kind, int64_t M, int64_t N, int64_t K);
+ * TKG_OPT_VARIANT) on a device of `sm_count` SMs; sm_count <= 0 asks the
+ * current device (returns -1 if there is none). */
+TKG_API int tkg_debug_pick_variant(int kind, int64_t M, int64_t N, int64_t K, int sm_count);
 
 /* Host: the split-K head plan (TKG_OPT_SPLIT_K) for `tiles` output tiles on a
  * persistent grid of `clusters` clusters with `num_kb` K stages per tile:
@@ -89,31 +90,6 @@ TKG_API tkg_status tkg_debug_tma_swizzle_probe(int s_bytes, const void* src, voi
 TKG_API tkg_status tkg_debug_mma_probe(int kind, int n, int ksteps, const void* a_tile, const void* b_tile,
                                const uint32_t* sfa_words, const uint32_t* sfb_words, const int32_t* sf_cols,
                                float* d_out, void* stream);
-
-/* Device: tensor-core issue rate.  One thread issues `count` MMAs of one
- * kind (0 bf16 K=16, 1 e4m3 K=32, 2 nvfp4 block-scaled K=64: 32 bytes of K
- * per row each) and shape (128*cta_group) x n back to back, cta_group 1 (one
- * CTA) or 2 (a CTA pair, cta_group::2), operands rotating over shared-memory
- * stages; *cycles (host) receives the SM cycles from the first issue until
- * their commit lands.  pattern 0: one accumulator; 1: consecutive pairs of
- * MMAs share A and accumulate into two accumulators (a 2x1 tile); 2: as 1,
- * the pair's first MMA filling the A collector buffer and the second reusing
- * it (collector::a::fill / ::lastuse); 3 (kind 2 only): one accumulator with
- * the scale-factor addresses moving per MMA and per 4-MMA stage as in the
- * GEMM; 4: one accumulator, and after every 4 MMAs the GEMM's per-stage
- * synchronisation work (two completed mbarrier waits with
- * tcgen05.fence::after_thread_sync, two tcgen05.commit); 5, 6, 7: only the
- * commits, only the waits, only the fences; 8: only the waits, with acquire
- * at CTA instead of cluster scope; 9: as 0 with varied operand bits instead
- * of one repeated byte; 10-12 (kind 0, cta_group 1 only): as 0 with the
- * operand forms of the attention kernel's P·V product: 10 B MN-major, 11 A
- * read from tensor memory, 12 both; 13 (n = 128): groups of 8 MMAs alternating
- * between the forms of 0 and 12, into two accumulators.  The difference of two counts divided
- * by the difference in MMAs is the per-MMA cost.  n a multiple of 32 in [64, 256] (128 for
- * kind 2 with pattern 1 or 2), count in 1..65536 (at least 2 for patterns 1
- * and 2, which issue count/2 whole pairs).  Synchronous on `stream`. */
-TKG_API tkg_status tkg_debug_mma_rate(int kind, int cta_group, int n, int count, int pattern,
-                                      unsigned long long* cycles, void* stream);
 
 #ifdef __cplusplus
 }

@@ -198,21 +198,6 @@ def test_split_plan_bf16_4096_example(tkg):
     assert tkg.tkg_debug_work_item(283, 28, 2, 64) == (255, 0, 64, -1)
 
 
-def test_dynamic_schedule_rejects_static_scale_warp_variants(tkg):
-    # NVFP4 variants 5-7 walk a precomputed tile sequence in their scale warps:
-    # the dynamic schedule is refused for them before any CUDA call
-    A, B, C = 1 << 12, 1 << 13, 1 << 14
-    s4 = tkg.tkg_scales(1 << 12, 1 << 12, 1 << 14, 1 << 14)
-    tkg.tkg_set_option(tkg.TKG_OPT_SCHEDULE, tkg.TKG_SCHEDULE_DYNAMIC)
-    try:
-        for v in (5, 6, 7):
-            tkg.tkg_set_option(tkg.TKG_OPT_VARIANT, v)
-            assert tkg.lib.tkg_gemm_nvfp4(256, 256, 256, A, B, C, s4, None) == tkg.TKG_ERR_INVALID_ARG
-    finally:
-        tkg.tkg_set_option(tkg.TKG_OPT_VARIANT, 0)
-        tkg.tkg_set_option(tkg.TKG_OPT_SCHEDULE, 0)
-
-
 @pytest.mark.parametrize("tiles_m,tiles_n,group_m", [(1, 1, 8), (16, 16, 8), (32, 32, 8), (64, 32, 12),
                                                      (13, 7, 8), (7, 13, 8), (5, 3, 1), (3, 5, 100), (33, 1, 8)])
 def test_tile_order_visits_every_tile_once(tkg, tiles_m, tiles_n, group_m):
@@ -247,25 +232,31 @@ def test_swizzle_selection_matches_definition(tkg):
 
 
 def test_compiled_variants_fit_the_sm(tkg):
+    compiled = {0: (2, 13), 1: (2, 13), 2: (8,)}
     for kind in (0, 1, 2):
-        for v in (1, 2, 3, 4, 5, 6, 7, 8):
-            if (kind == 2 and v == 4) or (kind != 2 and v in (5, 6, 7, 8)):
+        for v in range(1, 16):
+            if v not in compiled[kind]:
                 with pytest.raises(tkg.TkgError):
                     tkg.tkg_debug_variant_info(kind, v)
                 continue
             info = tkg.tkg_debug_variant_info(kind, v)
             assert info["smem_bytes"] <= 232448
-            assert info["threads"] in (192, 352, 448)
-            assert info["cta_group"] in (1, 2)
+            assert info["threads"] in (192, 448)
+            assert info["cta_group"] == 2
 
 
-def test_mma_rate_probe_arguments_checked(tkg):
-    c = ctypes.c_ulonglong(0)
-    for args in [(3, 1, 256, 64, 0), (0, 3, 256, 64, 0), (0, 1, 200, 64, 0), (0, 1, 288, 64, 0), (0, 1, 32, 64, 0),
-                 (0, 1, 256, 0, 0),
-                 (0, 1, 256, 65537, 0), (0, 1, 256, 64, 3), (2, 1, 256, 64, 1), (0, 1, 256, 1, 1), (0, 1, 256, 64, 3), (2, 1, 256, 64, 10)]:
-        assert tkg.lib.tkg_debug_mma_rate(*args, ctypes.byref(c), None) == tkg.TKG_ERR_INVALID_ARG
-    assert tkg.lib.tkg_debug_mma_rate(0, 1, 256, 64, 0, None, None) == tkg.TKG_ERR_INVALID_ARG
+@pytest.mark.parametrize("sms", [152, 148, 132, 76])
+def test_default_tile_follows_the_device_sm_count(tkg, sms):
+    # bf16 / FP8 take the 256x512 tile for K >= 4096 once its tiles fill four rounds of the
+    # device's CTA pairs (SMs / 2), else the 256x256 tile; NVFP4 always its one variant
+    need = 4 * (sms // 2)
+    for kind in (0, 1):
+        for M, N in [(8192, 8192), (4096, 4096), (16384, 8192)]:
+            wide = -(-M // 256) * -(-N // 512)
+            want = 13 if wide >= need else 2
+            assert tkg.tkg_debug_pick_variant(kind, M, N, 8192, sms) == want, (kind, M, N, sms)
+            assert tkg.tkg_debug_pick_variant(kind, M, N, 2048, sms) == 2
+    assert tkg.tkg_debug_pick_variant(2, 16384, 16384, 16384, sms) == 8
 
 
 def test_quantize_arguments_checked_before_any_gpu_work(tkg):

@@ -32,13 +32,10 @@ def variant(tkg, request):
     tkg.tkg_set_option(tkg.TKG_OPT_VARIANT, 0)
 
 
-VARIANTS = [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13]
-
-
-def skip_absent(kind, variant):
-    """Variants 4 and 9-13 are bf16 / FP8 only and 5-8 NVFP4 only; others would rerun the default."""
-    if (variant in (4, 9, 10, 11, 12, 13) and kind == "nvfp4") or (variant in (5, 6, 7, 8) and kind != "nvfp4"):
-        pytest.skip("variant not compiled for this kind")
+# the compiled variants of each kind: 256x256 and 256x512 pair tiles (bf16 / FP8), the
+# block-scaled 256x256 pair tile (NVFP4)
+KIND_VARIANTS = {"bf16": [2, 13], "fp8": [2, 13], "nvfp4": [8]}
+KIND_VARIANT_PAIRS = [(k, v) for k, vs in KIND_VARIANTS.items() for v in vs]
 
 SMALL_SHAPES = {
     "bf16": [(128, 256, 64), (256, 256, 256), (300, 520, 200), (77, 100, 40), (1, 8, 8), (513, 136, 1032),
@@ -49,10 +46,8 @@ SMALL_SHAPES = {
 }
 
 
-@pytest.mark.parametrize("variant", VARIANTS, indirect=True)
-@pytest.mark.parametrize("kind", ["bf16", "fp8", "nvfp4"])
+@pytest.mark.parametrize("kind,variant", KIND_VARIANT_PAIRS, indirect=["variant"])
 def test_small_shapes_match_oracle(tkg, variant, kind):
-    skip_absent(kind, variant)
     for i, (M, N, K) in enumerate(SMALL_SHAPES[kind]):
         ops = synth.make_operands(kind, M, N, K, "normal_sqrtk" if kind == "bf16" else "normal", 31 + i, 47 + i)
         g = run_gpu(ops)
@@ -60,11 +55,9 @@ def test_small_shapes_match_oracle(tkg, variant, kind):
         check_against_oracle(kind, g.c_bits(), acc, c_ref, ops.scale_a, ops.scale_b)
 
 
-@pytest.mark.parametrize("variant", VARIANTS, indirect=True)
-@pytest.mark.parametrize("kind", ["bf16", "fp8", "nvfp4"])
+@pytest.mark.parametrize("kind,variant", KIND_VARIANT_PAIRS, indirect=["variant"])
 @pytest.mark.parametrize("shape", [(256, 256, 256), (300, 392, 128), (129, 64, 256), (200, 264, 544)])
 def test_small_integers_bit_exact(tkg, variant, kind, shape):
-    skip_absent(kind, variant)
     M, N, K = shape
     ops = synth.small_int_operands(kind, M, N, K, seed=sum(shape))
     g = run_gpu(ops)
@@ -72,11 +65,9 @@ def test_small_integers_bit_exact(tkg, variant, kind, shape):
     assert np.array_equal(g.c_bits(), c_ref)
 
 
-@pytest.mark.parametrize("variant", VARIANTS, indirect=True)
-@pytest.mark.parametrize("kind", ["bf16", "fp8", "nvfp4"])
+@pytest.mark.parametrize("kind,variant", KIND_VARIANT_PAIRS, indirect=["variant"])
 @pytest.mark.parametrize("identity", [True, False])
 def test_permutation_exact(tkg, variant, kind, identity):
-    skip_absent(kind, variant)
     ops, perm = synth.permutation_operands(kind, 384, 256, seed=3, identity=identity)
     g = run_gpu(ops)
     _, c_ref = oracle.gemm(ops)

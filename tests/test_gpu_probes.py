@@ -97,18 +97,3 @@ def test_single_tile_nvfp4_mma_scale_layout(tkg, oracle_mod, n):
     assert tkg.tkg_debug_mma_probe(2, n, 1, d_a, d_b, d_sfa, d_sfb, [0, 0], d_out) == tkg.TKG_OK
     acc, _ = oracle_mod.gemm_nvfp4(ops.a, ops.b, ops.sfa, ops.sfb, 1.0, 1.0)
     assert np.array_equal(d_out.cpu().numpy(), acc)
-
-
-@pytest.mark.gpu
-@pytest.mark.parametrize("cta_group", [1, 2])
-@pytest.mark.parametrize("kind", [0, 1, 2])
-def test_mma_rate_probe_times_back_to_back_mmas(tkg, kind, cta_group):
-    """The issue-rate timer runs every kind and CTA-group form to completion,
-    and more MMAs take longer: a per-MMA cost between 32 and 4096 cycles."""
-    for pattern in (0, 1, 2, 3, 4, 5, 6, 7, 8, 9) if kind == 2 else (0, 1, 2, 4, 5, 6, 7, 8, 9):
-        n = 128 if (kind == 2 and pattern) else 256
-        short = tkg.tkg_debug_mma_rate(kind, cta_group, n, 128, pattern)
-        long = tkg.tkg_debug_mma_rate(kind, cta_group, n, 1024, pattern)
-        per = (long - short) / (1024 - 128)
-        assert 0 < short < long
-        assert 32 <= per <= 4096

@@ -2,7 +2,11 @@
 bounded.  Fault injection makes the producer skip the copies of its first ring
 stage (no copy is in flight for it), so the compute role's wait on that stage
 runs out; the kernel records the timeout in the status word, every role stops,
-tensor memory is released, and the context stays usable for the next call."""
+tensor memory is released, and the context stays usable for the next call.
+Every compiled GEMM variant is stalled this way: the 256x256 pair tile with its
+two accumulators, the 256x512 pair tile with its single accumulator and four
+48 KB stages, and the NVFP4 kernel, whose eight scale warps also wait (for the
+stage's scales in shared memory) and must give up in turn."""
 import numpy as np
 import pytest
 
@@ -26,10 +30,12 @@ def tkg():
     mod.tkg_set_option(mod.TKG_OPT_VARIANT, 0)
 
 
-@pytest.mark.parametrize("variant", [1, 2])
-def test_injected_stall_reports_timeout_then_recovers(tkg, variant):
+@pytest.mark.parametrize("kind,variant,shape", [("bf16", 2, (512, 512, 512)), ("bf16", 13, (512, 1024, 4096)),
+                                                ("fp8", 13, (512, 1024, 4096)), ("nvfp4", 8, (512, 512, 2048))])
+def test_injected_stall_reports_timeout_then_recovers(tkg, kind, variant, shape):
     from tiled_tensor_core_gb300.device import DeviceGemm
-    ops = synth.make_operands("bf16", 512, 512, 512, "normal_sqrtk", 1, 2)
+    M, N, K = shape
+    ops = synth.make_operands(kind, M, N, K, "normal_sqrtk" if kind == "bf16" else "normal", 1, 2)
     tkg.tkg_set_option(tkg.TKG_OPT_VARIANT, variant)
     tkg.tkg_set_option(tkg.TKG_OPT_TIMEOUT_NS, 100_000_000)  # 0.1 s per wait
     try:
@@ -42,7 +48,7 @@ def test_injected_stall_reports_timeout_then_recovers(tkg, variant):
         tkg.tkg_set_option(tkg.TKG_OPT_TIMEOUT_NS, 0)
         g2 = run_gpu(ops)
         acc, c_ref = oracle.gemm(ops)
-        check_against_oracle("bf16", g2.c_bits(), acc, c_ref)
+        check_against_oracle(kind, g2.c_bits(), acc, c_ref, ops.scale_a, ops.scale_b)
     finally:
         tkg.tkg_debug_set_fault(0)
         tkg.tkg_set_option(tkg.TKG_OPT_TIMEOUT_NS, 0)

@@ -48,6 +48,7 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 struct DevState {
   bool ready = false;
+  int dev = -1;
   int sm_count = 0;
   int cc_major = 0, cc_minor = 0;
   unsigned int* status = nullptr;
@@ -127,24 +128,33 @@ tkg_status device_state_locked(int dev, DevState** out) {
       return TKG_ERR_CUDA;
     }
     d.status = static_cast<unsigned int*>(sp);
+    d.dev = dev;
     for (auto& row : d.max_clusters)
       for (int& v : row) v = 0;
-    if (!d.pool) {
-      cudaMemPoolProps props{};
-      props.allocType = cudaMemAllocationTypePinned;
-      props.location.type = cudaMemLocationTypeDevice;
-      props.location.id = dev;
-      if (cudaMemPoolCreate(&d.pool, &props) != cudaSuccess) {
-        cudaGetLastError();
-        d.pool = nullptr;
-        return TKG_ERR_CUDA;
-      }
-      uint64_t keep = UINT64_MAX;  // keep freed blocks for reuse by the next call
-      cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
-    }
     d.ready = true;
   }
   *out = &d;
+  return TKG_OK;
+}
+
+// The device's stream-ordered memory pool for the NVFP4 scale scratch, made on
+// the first regular NVFP4 call (the allocation-free entry point never makes it).
+tkg_status device_pool(DevState& d, cudaMemPool_t* out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!d.pool) {
+    cudaMemPoolProps props{};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = d.dev;
+    if (cudaMemPoolCreate(&d.pool, &props) != cudaSuccess) {
+      cudaGetLastError();
+      d.pool = nullptr;
+      return TKG_ERR_CUDA;
+    }
+    uint64_t keep = UINT64_MAX;  // keep freed blocks for reuse by the next call
+    cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+  }
+  *out = d.pool;
   return TKG_OK;
 }
 
@@ -162,15 +172,9 @@ tkg_status current_device(DevState** out) {
 
 // 2-D row-major tensor map: d0 = elements per row (innermost), d1 = rows,
 // pitch in bytes, box b0 x b1 elements, swizzle in bytes (0/32/64/128).
-tkg_status get_map(CUtensorMap* out, const void* ptr, CUtensorMapDataType dtype, uint64_t d0, uint64_t d1,
-                   uint64_t pitch, uint32_t b0, uint32_t b1, int swz) {
-  const MapKey key{ptr, static_cast<int>(dtype), d0, d1, pitch, b0, b1, swz};
-  std::lock_guard<std::mutex> lk(g_mu);
-  auto it = g_maps.find(key);
-  if (it != g_maps.end()) {
-    *out = it->second;
-    return TKG_OK;
-  }
+// Encoded on the caller's stack, no cache.  Caller holds g_mu.
+tkg_status encode_map_2d_locked(CUtensorMap* out, const void* ptr, CUtensorMapDataType dtype, uint64_t d0,
+                                uint64_t d1, uint64_t pitch, uint32_t b0, uint32_t b1, int swz) {
   tkg_status st = ensure_encode_locked();
   if (st != TKG_OK) return st;
   CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_NONE;
@@ -181,12 +185,28 @@ tkg_status get_map(CUtensorMap* out, const void* ptr, CUtensorMapDataType dtype,
   const cuuint64_t strides[1] = {pitch};
   const cuuint32_t box[2] = {b0, b1};
   const cuuint32_t estr[2] = {1, 1};
-  CUtensorMap m;
-  std::memset(&m, 0, sizeof(m));
-  CUresult r = g_encode(&m, dtype, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+  std::memset(out, 0, sizeof(*out));
+  CUresult r = g_encode(out, dtype, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return TKG_ERR_INVALID_ARG;
+  return r == CUDA_SUCCESS ? TKG_OK : TKG_ERR_INVALID_ARG;
+}
+
+// The same map, through the host-side cache (a miss adds an entry) unless
+// `cached` is false.
+tkg_status get_map(CUtensorMap* out, const void* ptr, CUtensorMapDataType dtype, uint64_t d0, uint64_t d1,
+                   uint64_t pitch, uint32_t b0, uint32_t b1, int swz, bool cached = true) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!cached) return encode_map_2d_locked(out, ptr, dtype, d0, d1, pitch, b0, b1, swz);
+  const MapKey key{ptr, static_cast<int>(dtype), d0, d1, pitch, b0, b1, swz};
+  auto it = g_maps.find(key);
+  if (it != g_maps.end()) {
+    *out = it->second;
+    return TKG_OK;
+  }
+  CUtensorMap m;
+  const tkg_status st = encode_map_2d_locked(&m, ptr, dtype, d0, d1, pitch, b0, b1, swz);
+  if (st != TKG_OK) return st;
   if (g_maps.size() >= kMaxMaps) g_maps.clear();
   g_maps.emplace(key, m);
   *out = m;
@@ -206,15 +226,13 @@ const KernelVariant* variant_of(int kind, int id) {
 // max(77, N / 2) cycles on sm_103a, so narrower tiles (N = 224, 192) keep the
 // tensor pipe's rate per column, but each SM then receives more operand bytes
 // per flop (A is re-read for every tile column) and the measured throughput
-// falls with that ratio; sharing A between two CTA pairs by TMA multicast
-// (variants 10-12) saves L2 reads and power but not throughput.  Those tiles
-// are kept as explicit variants.  NVFP4 takes the scale-warp form of the
-// 256 x 256 tile with one scale slot per ring stage and the scales riding the
-// ring: copying the block scales with tcgen05.cp costs the tensor pipe about
-// 60 cycles per copy, twelve copies per 256-deep K stage; coupling the slots to
-// the stages saves the MMA thread a second wait per stage; and reading the
-// scales from shared memory, where the ring's TMA put them stages ahead, keeps
-// global-load latency off the scale warps' critical path.
+// falls with that ratio; sharing A between two CTA pairs by TMA multicast saved
+// L2 reads and power but not throughput.  NVFP4 takes the scale-warp form of
+// the 256 x 256 tile with the scales riding the ring: copying the block scales
+// with tcgen05.cp costs the tensor pipe about 60 cycles per copy, twelve copies
+// per 256-deep K stage, and reading the scales from shared memory, where the
+// ring's TMA put them stages ahead, keeps global-load latency off the scale
+// warps' critical path.
 //
 // bf16 / FP8 with long K and many tiles take the 256 x 512 pair tile instead: it
 // moves a third fewer operand bytes per flop, which draws less power, and under
@@ -222,15 +240,16 @@ const KernelVariant* variant_of(int kind, int id) {
 // 1601 against 1507 MHz); it keeps a single accumulator (a tile's store does not
 // overlap the next tile) and coarser rounds of tiles, so it loses with short K
 // (16384 x 8192 x 2048: 1674 against 1706) or few tiles (4096^3: 1609 against
-// 1639, where the split-K head of the 256 x 256 tile helps more).
+// 1639, where the split-K head of the 256 x 256 tile helps more).  "Many" is
+// four rounds of 256 x 512 tiles over the device's CTA pairs (SMs / 2).
 constexpr int64_t kWideMinK = 4096;
-constexpr int64_t kWideMinTiles = 4 * 76;  // four rounds of 256 x 512 tiles on GB300's 76 CTA pairs
-int pick_variant(int kind, int64_t M, int64_t N, int64_t K) {
+constexpr int64_t kWideMinRounds = 4;
+int pick_variant(int kind, int64_t M, int64_t N, int64_t K, int sm_count) {
   const int forced = static_cast<int>(g_opt_variant.load(std::memory_order_relaxed));
   if (forced > 0 && variant_of(kind, forced)) return forced;
   if (kind == 2) return kVariant2Sm256x256SfSmem;
   const int64_t wide_tiles = ((M + 255) / 256) * ((N + 511) / 512);
-  if (K >= kWideMinK && wide_tiles >= kWideMinTiles) return kVariant2Sm256x512;
+  if (K >= kWideMinK && wide_tiles >= kWideMinRounds * (sm_count / 2)) return kVariant2Sm256x512;
   return kVariant2Sm256x256;
 }
 
@@ -248,12 +267,12 @@ tkg_status max_clusters(DevState& d, int kind, int id, const KernelVariant& v, i
     return TKG_ERR_CUDA;
   }
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>(v.cg * v.mc * d.sm_count), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(v.cg * d.sm_count), 1, 1);
   cfg.blockDim = dim3(static_cast<unsigned>(v.threads), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(v.smem_bytes);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(v.cg * v.mc);
+  attr[0].val.clusterDim.x = static_cast<unsigned>(v.cg);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
@@ -340,9 +359,12 @@ bool split_workspace(DevState& d, cudaStream_t stream, DevState::SplitWs* out) {
   return true;
 }
 
-// Common host-only checks (no CUDA call), then device checks and the launch.
-tkg_status gemm_launch(int kind, int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* C,
-                       const tkg_scales* scales, void* stream) {
+}  // namespace
+
+namespace tkg {
+
+tkg_status check_gemm_args(int kind, int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C,
+                           const tkg_scales* scales) {
   const int64_t kMax = 0x7FFFFFFF;
   if (M < 1 || N < 1 || K < 1 || M > kMax || N > kMax || K > kMax) return TKG_ERR_INVALID_ARG;
   const int64_t k_align = kind == 0 ? 8 : kind == 1 ? 16 : 32;
@@ -361,90 +383,69 @@ tkg_status gemm_launch(int kind, int64_t M, int64_t N, int64_t K, const void* A,
     return TKG_ERR_MISALIGNED;
   if (kind == 2 && (!aligned16(scales->a_block_scale) || !aligned16(scales->b_block_scale)))
     return TKG_ERR_MISALIGNED;
+  return TKG_OK;
+}
 
-  const int id = pick_variant(kind, M, N, K);
-  const KernelVariant* v = variant_of(kind, id);
-  if (!v) return TKG_ERR_INTERNAL;
-  // the dynamic schedule reaches every role through the answer ring; the
-  // scale warps of these NVFP4 variants walk a precomputed static sequence
-  if (opt_or(g_opt_schedule, TKG_SCHEDULE_STATIC) == TKG_SCHEDULE_DYNAMIC &&
-      (id == kVariant2Sm256x256Sfw || id == kVariant2Sm256x256Hybrid || id == kVariant2Sm256x256Coupled))
-    return TKG_ERR_INVALID_ARG;
-  const int64_t tile_m = 128LL * v->cg;
-  const int64_t tiles_m = (M + tile_m - 1) / tile_m;
-  const int64_t tiles_n = (N + v->bn - 1) / v->bn;
-  if (tiles_m * tiles_n > kMax) return TKG_ERR_INVALID_ARG;
-  // scheduling units: one tile, or (A multicast) `mc` horizontally adjacent tiles, one per CTA pair
-  const int64_t units = tiles_m * ((tiles_n + v->mc - 1) / v->mc);
-  const int64_t cl = static_cast<int64_t>(v->cg) * v->mc;  // CTAs per cluster
+tkg_status plan_gemm(int kind, int64_t M, int64_t N, int64_t K, int sm_count, GemmPlan* out) {
+  GemmPlan g;
+  g.id = pick_variant(kind, M, N, K, sm_count);
+  g.v = variant_of(kind, g.id);
+  if (!g.v) return TKG_ERR_INTERNAL;
+  const int64_t tile_m = 128LL * g.v->cg;
+  g.tiles_m = (M + tile_m - 1) / tile_m;
+  g.tiles_n = (N + g.v->bn - 1) / g.v->bn;
+  if (g.tiles_m * g.tiles_n > 0x7FFFFFFF) return TKG_ERR_INVALID_ARG;
+  const int64_t k_bytes = kind == 0 ? K * 2 : kind == 1 ? K : K / 2;
+  g.num_kb = static_cast<int>((k_bytes + 127) / 128);
+  if (kind == 2) {
+    g.sf_blocks_a = static_cast<int>(g.tiles_m * g.v->cg);
+    g.sf_blocks_b = static_cast<int>(g.tiles_n * (g.v->bn / 128));
+    g.sf_bytes = nvfp4_scratch_bytes(g.sf_blocks_a, g.sf_blocks_b, g.num_kb);
+    g.sf_b_off = static_cast<size_t>(g.sf_blocks_a) * g.num_kb * 2048;
+  }
+  *out = g;
+  return TKG_OK;
+}
 
+tkg_status gemm_params(GemmParams* out, const GemmPlan& g, int kind, int64_t M, int64_t N, int64_t K, const void* A,
+                       const void* B, void* C, const tkg_scales* scales, const uint8_t* sf_scratch, bool cached_maps) {
   DevState* d = nullptr;
   tkg_status st = current_device(&d);
   if (st != TKG_OK) return st;
-
-  GemmParams p;
+  GemmParams& p = *out;
   std::memset(&p, 0, sizeof(p));
-  // Operand maps: rows of K elements, boxes of 128 bytes x (rows per CTA).
-  // rows of one B box: a CTA's share of one MMA's N (512-wide tiles load two boxes per stage)
-  const uint32_t b_rows = static_cast<uint32_t>((v->bn > 256 ? 256 : v->bn) / v->cg);
+  const KernelVariant& v = *g.v;
+  // Operand maps: rows of K elements, boxes of 128 bytes x (rows per CTA); rows of one B box: a
+  // CTA's share of one MMA's N (512-wide tiles load two boxes per stage)
+  const uint32_t b_rows = static_cast<uint32_t>((v.bn > 256 ? 256 : v.bn) / v.cg);
   if (kind == 0) {
-    // A multicast between two CTA pairs: each CTA loads a 64-row quarter of the pair tile's A
-    st = get_map(&p.tmap_a, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, K * 2, 64, 128 / v->mc, 128);
-    if (st == TKG_OK) st = get_map(&p.tmap_b, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, N, K * 2, 64, b_rows, 128);
+    st = get_map(&p.tmap_a, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, K * 2, 64, 128, 128, cached_maps);
+    if (st == TKG_OK)
+      st = get_map(&p.tmap_b, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, N, K * 2, 64, b_rows, 128, cached_maps);
   } else {
     const int64_t row_bytes = kind == 1 ? K : K / 2;
-    st = get_map(&p.tmap_a, A, CU_TENSOR_MAP_DATA_TYPE_UINT8, row_bytes, M, row_bytes, 128, 128 / v->mc, 128);
+    st = get_map(&p.tmap_a, A, CU_TENSOR_MAP_DATA_TYPE_UINT8, row_bytes, M, row_bytes, 128, 128, 128, cached_maps);
     if (st == TKG_OK)
-      st = get_map(&p.tmap_b, B, CU_TENSOR_MAP_DATA_TYPE_UINT8, row_bytes, N, row_bytes, 128, b_rows, 128);
+      st = get_map(&p.tmap_b, B, CU_TENSOR_MAP_DATA_TYPE_UINT8, row_bytes, N, row_bytes, 128, b_rows, 128,
+                   cached_maps);
   }
-  if (st != TKG_OK) return st;
-  const int64_t k_bytes = kind == 0 ? K * 2 : kind == 1 ? K : K / 2;
-  p.num_kb = static_cast<int>((k_bytes + 127) / 128);
-  uint8_t* scratch = nullptr;
-  if (kind == 2) {
-    // Interleaved block scales (stream-ordered scratch, freed after the GEMM in stream order).
-    p.sf_blocks_a = static_cast<int>(tiles_m * v->cg);
-    p.sf_blocks_b = static_cast<int>(tiles_n * (v->bn / 128));
-    const size_t bytes = nvfp4_scratch_bytes(p.sf_blocks_a, p.sf_blocks_b, p.num_kb);
-    const size_t b_off = static_cast<size_t>(p.sf_blocks_a) * p.num_kb * 2048;
-    cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&scratch), bytes, d->pool, cs) != cudaSuccess) {
-      cudaGetLastError();
-      return TKG_ERR_CUDA;
-    }
-    if (nvfp4_interleave_scales(scales->a_block_scale, scales->b_block_scale, static_cast<int>(M),
-                                static_cast<int>(N), static_cast<int>(K), p.sf_blocks_a, p.sf_blocks_b, p.num_kb,
-                                v->sf_mode, scratch, b_off, cs,
-                                opt_or(g_opt_overlap, TKG_OVERLAP_ON) == TKG_OVERLAP_ON) != cudaSuccess) {
-      cudaGetLastError();
-      cudaFreeAsync(scratch, cs);
-      return TKG_ERR_CUDA;
-    }
-    p.sf_a = scratch;
-    p.sf_b = scratch + b_off;
-    st = get_map(&p.tmap_sfa, scratch, CU_TENSOR_MAP_DATA_TYPE_UINT8, 128,
-                 static_cast<uint64_t>(p.sf_blocks_a) * p.num_kb * 16, 128, 128, 16, 0);
+  if (st == TKG_OK && kind == 2) {
+    // the staged scales: runs of 16 rows x 128 bytes, one box per (K stage, 128-row block) of A and
+    // BN/128 boxes' worth for B
+    p.sf_blocks_a = g.sf_blocks_a;
+    p.sf_blocks_b = g.sf_blocks_b;
+    st = get_map(&p.tmap_sfa, sf_scratch, CU_TENSOR_MAP_DATA_TYPE_UINT8, 128,
+                 static_cast<uint64_t>(g.sf_blocks_a) * g.num_kb * 16, 128, 128, 16, 0, cached_maps);
     if (st == TKG_OK)
-      st = get_map(&p.tmap_sfb, scratch + b_off, CU_TENSOR_MAP_DATA_TYPE_UINT8, 128,
-                   static_cast<uint64_t>(p.sf_blocks_b) * p.num_kb * 16, 128, 128,
-                   static_cast<uint32_t>(16 * (v->bn / 128)), 0);
-    if (st != TKG_OK) {
-      cudaFreeAsync(scratch, cs);
-      return st;
-    }
+      st = get_map(&p.tmap_sfb, sf_scratch + g.sf_b_off, CU_TENSOR_MAP_DATA_TYPE_UINT8, 128,
+                   static_cast<uint64_t>(g.sf_blocks_b) * g.num_kb * 16, 128, 128,
+                   static_cast<uint32_t>(16 * (v.bn / 128)), 0, cached_maps);
   }
   p.c_via_tma = (N % 8 == 0) ? 1 : 0;
-  auto release = [&]() {
-    if (scratch) cudaFreeAsync(scratch, static_cast<cudaStream_t>(stream));
-  };
-  if (p.c_via_tma) {
-    st = get_map(&p.tmap_c, C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, N * 2, static_cast<uint32_t>(v->epi_cols), 32,
-                 static_cast<int>(select_swizzle(static_cast<uint32_t>(v->epi_cols) * 2)));
-    if (st != TKG_OK) {
-      release();
-      return st;
-    }
-  }
+  if (st == TKG_OK && p.c_via_tma)
+    st = get_map(&p.tmap_c, C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, N * 2, static_cast<uint32_t>(v.epi_cols), 32,
+                 static_cast<int>(select_swizzle(static_cast<uint32_t>(v.epi_cols) * 2)), cached_maps);
+  if (st != TKG_OK) return st;
   p.c_ptr = C;
   if (kind != 0) {
     p.a_scale = scales->a_scale;
@@ -455,31 +456,35 @@ tkg_status gemm_launch(int kind, int64_t M, int64_t N, int64_t K, const void* A,
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
-  p.tiles_m = static_cast<int>(tiles_m);
-  p.tiles_n = static_cast<int>(tiles_n);
+  p.tiles_m = static_cast<int>(g.tiles_m);
+  p.tiles_n = static_cast<int>(g.tiles_n);
+  p.num_kb = g.num_kb;
   p.group_m = static_cast<int>(opt_or(g_opt_group, kDefaultGroupM));
+  p.split_s = 1;
   p.fault_mode = take_fault_mode(1);
   p.visits = g_visits.exchange(nullptr);
   const int64_t sched = opt_or(g_opt_schedule, TKG_SCHEDULE_STATIC);
   p.sched = sched == TKG_SCHEDULE_DYNAMIC ? kSchedDynamic : sched == TKG_SCHEDULE_SINGLE ? kSchedSingle : kSchedStatic;
+  return TKG_OK;
+}
 
+tkg_status gemm_enqueue(int kind, const GemmPlan& g, GemmParams& p, void* stream, bool allow_split) {
+  DevState* d = nullptr;
+  tkg_status st = current_device(&d);
+  if (st != TKG_OK) return st;
+  const KernelVariant& v = *g.v;
+  const int64_t cl = v.cg;  // CTAs per cluster
+  const int64_t units = g.tiles_m * g.tiles_n;
   int clusters = 0;
-  st = max_clusters(*d, kind, id, *v, &clusters);
-  if (st != TKG_OK) {
-    release();
-    return st;
-  }
+  st = max_clusters(*d, kind, g.id, v, &clusters);
+  if (st != TKG_OK) return st;
   int64_t grid_clusters = clusters;
   const int64_t cap = g_opt_max_ctas.load(std::memory_order_relaxed);
   if (cap > 0 && cap / cl < grid_clusters) grid_clusters = cap / cl > 0 ? cap / cl : 1;
 
-  // split-K head (static schedule; not with A multicast, nor with the NVFP4 variants whose
-  // scale warps walk a precomputed sequence), planned for the clusters the grid may use
-  p.split_s = 1;
+  // split-K head (static schedule, tiles of one MMA width), planned for the clusters the grid may use
   int64_t items = units;
-  if (p.sched == kSchedStatic && v->mc == 1 && v->bn <= 256 && opt_or(g_opt_split, TKG_SPLIT_ON) == TKG_SPLIT_ON &&
-      !(kind == 2 && (id == kVariant2Sm256x256Sfw || id == kVariant2Sm256x256Hybrid ||
-                      id == kVariant2Sm256x256Coupled))) {
+  if (allow_split && p.sched == kSchedStatic && v.bn <= 256 && opt_or(g_opt_split, TKG_SPLIT_ON) == TKG_SPLIT_ON) {
     int split_tiles = 0, split_s = 1;
     split_plan(units, grid_clusters, p.num_kb, &split_tiles, &split_s);
     DevState::SplitWs w;
@@ -492,14 +497,14 @@ tkg_status gemm_launch(int kind, int64_t M, int64_t N, int64_t K, const void* A,
     }
   }
   if (items < grid_clusters) grid_clusters = items;
-  // one cluster per unit: the hardware places them as SMs free up (and, in the
+  // one cluster per tile: the hardware places them as SMs free up (and, in the
   // dynamic schedule, running clusters cancel and take over those not started)
   if (p.sched != kSchedStatic) grid_clusters = units;
 
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(grid_clusters * cl), 1, 1);
-  cfg.blockDim = dim3(static_cast<unsigned>(v->threads), 1, 1);
-  cfg.dynamicSmemBytes = static_cast<size_t>(v->smem_bytes);
+  cfg.blockDim = dim3(static_cast<unsigned>(v.threads), 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(v.smem_bytes);
   cfg.stream = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -512,15 +517,59 @@ tkg_status gemm_launch(int kind, int64_t M, int64_t N, int64_t K, const void* A,
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = opt_or(g_opt_overlap, TKG_OVERLAP_ON) == TKG_OVERLAP_ON ? 2 : 1;
+  cfg.numAttrs = launch_overlap() ? 2 : 1;
   void* args[] = {&p};
-  if (cudaLaunchKernelExC(&cfg, v->func, args) != cudaSuccess) {
+  if (cudaLaunchKernelExC(&cfg, v.func, args) != cudaSuccess) {
     cudaGetLastError();
-    release();
     return TKG_ERR_CUDA;
   }
-  release();
   return TKG_OK;
+}
+
+bool launch_overlap() { return opt_or(g_opt_overlap, TKG_OVERLAP_ON) == TKG_OVERLAP_ON; }
+
+}  // namespace tkg
+
+namespace {
+
+// Checks, the plan, the NVFP4 scale scratch (stream-ordered pool, freed after
+// the GEMM in stream order) and its re-layout, the parameters, the launch.
+tkg_status gemm_launch(int kind, int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* C,
+                       const tkg_scales* scales, void* stream) {
+  tkg_status st = check_gemm_args(kind, M, N, K, A, B, C, scales);
+  if (st != TKG_OK) return st;
+  DevState* d = nullptr;
+  st = current_device(&d);
+  if (st != TKG_OK) return st;
+  GemmPlan g;
+  st = plan_gemm(kind, M, N, K, d->sm_count, &g);
+  if (st != TKG_OK) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  uint8_t* scratch = nullptr;
+  auto release = [&]() {
+    if (scratch) cudaFreeAsync(scratch, cs);
+  };
+  if (kind == 2) {
+    cudaMemPool_t pool = nullptr;
+    st = device_pool(*d, &pool);
+    if (st != TKG_OK) return st;
+    if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&scratch), g.sf_bytes, pool, cs) != cudaSuccess) {
+      cudaGetLastError();
+      return TKG_ERR_CUDA;
+    }
+    if (nvfp4_interleave_scales(scales->a_block_scale, scales->b_block_scale, static_cast<int>(M),
+                                static_cast<int>(N), static_cast<int>(K), g.sf_blocks_a, g.sf_blocks_b, g.num_kb,
+                                scratch, g.sf_b_off, cs, launch_overlap()) != cudaSuccess) {
+      cudaGetLastError();
+      release();
+      return TKG_ERR_CUDA;
+    }
+  }
+  GemmParams p;
+  st = gemm_params(&p, g, kind, M, N, K, A, B, C, scales, scratch, true);
+  if (st == TKG_OK) st = gemm_enqueue(kind, g, p, stream, true);
+  release();
+  return st;
 }
 
 }  // namespace
@@ -673,7 +722,17 @@ tkg_status tkg_debug_variant_info(int kind, int variant, int32_t info[6]) {
   return TKG_OK;
 }
 
-int tkg_debug_pick_variant(int kind, int64_t M, int64_t N, int64_t K) { return pick_variant(kind, M, N, K); }
+int tkg_debug_pick_variant(int kind, int64_t M, int64_t N, int64_t K, int sm_count) {
+  if (sm_count <= 0) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return -1;
+    }
+  }
+  return pick_variant(kind, M, N, K, sm_count);
+}
 
 int tkg_debug_split_plan(int64_t tiles, int64_t clusters, int num_kb, int* split_tiles, int* split_s) {
   if (!split_tiles || !split_s || num_kb < 0) return -1;
@@ -758,19 +817,5 @@ tkg_status encode_tiled_map(CUtensorMap* out, CUtensorMapDataType dtype, int ran
                               CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? TKG_OK : TKG_ERR_INVALID_ARG;
-}
-}  // namespace tkg
-
-// Address of the current device's status word, without any other per-device
-// set-up (used by the entry point that must not allocate).
-namespace tkg {
-tkg_status status_word_address(unsigned int** out) {
-  void* sp = nullptr;
-  if (cudaGetSymbolAddress(&sp, g_tkg_status) != cudaSuccess) {
-    cudaGetLastError();
-    return TKG_ERR_CUDA;
-  }
-  *out = static_cast<unsigned int*>(sp);
-  return TKG_OK;
 }
 }  // namespace tkg

@@ -57,8 +57,6 @@ struct GemmParams {
   int fault_mode;  // 0 = none; 1 = the producer skips the loads of its first stage (timeout test)
   int sf_blocks_a;  // NVFP4: 128-row scale blocks per K stage in the staged A scales
   int sf_blocks_b;  // same for B
-  const uint8_t* sf_a;  // NVFP4 scale-warp mode: staged A scales in global memory
-  const uint8_t* sf_b;  // same for B
   int sched;            // tile schedule (kSchedStatic / kSchedDynamic / kSchedSingle)
   unsigned int* visits;  // debug: if set, one increment per tile each time a CTA (pair) stores it
   // split-K head of the static schedule (split_tiles = 0: off): the first split_tiles tiles of
@@ -112,49 +110,28 @@ __host__ __device__ inline WorkItem work_item(int w, int split_tiles, int split_
   return WorkItem{w - split_items + split_tiles, 0, num_kb, -1};
 }
 
-// Block-scale staging modes (NVFP4).
-//   kSfCopy: the scales ride the shared-memory ring with the operands and the
-//            MMA thread copies them shared -> TMEM with tcgen05.cp.32x128b.warpx4
-//            (12 copies per 256-K stage of a 256x256 tile).
-//   kSfWarps: scale warps (SF_GROUPS groups of four, one warp per TMEM lane
-//            quarter; group g takes every SF_GROUPS-th stage) read them from
-//            global memory ahead of use and write them with tcgen05.st into a
-//            ring of TMEM slots of their own; the tensor pipe only runs MMAs and
-//            the shared-memory ring only carries operands.
-//   kSfHybrid: B's scales ride the operand ring and a copy warp (not the MMA
-//            thread) copies them with tcgen05.cp.32x128b.warpx4, whose
-//            four-quarter broadcast is the replication B's layout needs; four
-//            scale warps write A's scales (one 16-byte row each) with
-//            tcgen05.st.  TMEM scale slots follow the ring stages.
-constexpr int kSfCopy = 0, kSfWarps = 1, kSfHybrid = 2;
-
-template <Kind KIND_, int CG_, int BN_, int STAGES_, int EPI_WARPS_, int NUM_ACC_ = 2, int SF_MODE_ = kSfCopy,
-          int SF_GROUPS_ = 1, bool SF_COUPLED_ = false, bool SF_SMEM_ = false, int MC_ = 1>
+// NVFP4 block scales.  The caller's row-major [rows][K/16] e4m3 scales are
+// first rewritten on the device into 2 KB runs, one per (256-deep K stage,
+// 128-row block), [row][16 scales] inside a run.  The producer's TMA brings
+// each stage's runs (A: this CTA's 128 rows; B: all BN rows of the tile, since
+// every CTA of a pair multiplies by all of B) into shared memory beside the
+// operands, on the CTA's own sf_full barrier.  SF_GROUPS groups of four scale
+// warps (one warp per TMEM lane quarter; group g takes every SF_GROUPS-th
+// stage) read them there and write them with tcgen05.st into the stage's TMEM
+// scale slot, then arrive on the stage's full barrier, so the MMA thread waits
+// once per stage and the tensor pipe only runs MMAs (copying the scales with
+// tcgen05.cp instead costs the tensor pipe about 60 cycles per copy, twelve
+// copies per stage of a 256 x 256 tile).
+template <Kind KIND_, int CG_, int BN_, int STAGES_, int EPI_WARPS_, int NUM_ACC_ = 2, int SF_GROUPS_ = 2>
 struct GemmCfg {
   static constexpr Kind KIND = KIND_;
-  static constexpr int CG = CG_;                // CTAs per MMA (1, or 2 for the CTA pair)
-  // CTA pairs per cluster: 2 = two pairs on horizontally adjacent tiles (same A rows)
-  // share A — each CTA loads one 64-row quarter of the pair tile's A rows and
-  // multicasts it into the same place in its counterpart of the other pair
-  static constexpr int MC = MC_;
-  static constexpr int CL = CG * MC;            // CTAs per cluster
+  static constexpr int CG = CG_;                // CTAs per MMA (1, or 2 for the CTA pair) = CTAs per cluster
   static constexpr int BN = BN_;                // output-tile columns (whole pair)
   static constexpr int BM = 128;                // output-tile rows per CTA = TMEM lanes
   static constexpr int STAGES = STAGES_;
   static constexpr int EPI_WARPS = EPI_WARPS_;  // 4 or 8
   static constexpr int NUM_ACC = NUM_ACC_;      // fp32 accumulators in TMEM (2 = epilogue overlaps next tile)
   static constexpr bool SCALED = (KIND == Kind::NVFP4);
-  static constexpr int SF_MODE = SF_MODE_;
-  static constexpr bool SF_WARPS_MODE = SCALED && SF_MODE == kSfWarps;
-  static constexpr bool SF_HYBRID = SCALED && SF_MODE == kSfHybrid;
-  static constexpr bool SF_ST = SF_WARPS_MODE || SF_HYBRID;  // scale warps write scales with tcgen05.st
-  // scale-warp mode with one TMEM scale slot per ring stage: the scale warps wait on the stage's
-  // empty barrier and arrive on its full barrier, so the MMA thread waits once per stage
-  static constexpr bool SF_COUPLED = SF_WARPS_MODE && SF_COUPLED_;
-  // coupled scale-warp mode whose scales ride the operand ring: the producer's TMA brings each
-  // stage's scales (row layout) into shared memory, landing on the CTA's own sf_full barrier, and
-  // the scale warps read them from there instead of from global memory
-  static constexpr bool SF_SMEM = SF_COUPLED && SF_SMEM_;
   static constexpr int ROW_BYTES = 128;         // K bytes per operand row per stage
   static constexpr uint32_t SWZ = select_swizzle(ROW_BYTES);
   static_assert(SWZ == 128, "operand rows must take the 128-byte swizzle");
@@ -170,22 +147,16 @@ struct GemmCfg {
   static constexpr int A_STAGE = BM * ROW_BYTES;
   static constexpr int B_BOX = B_ROWS * ROW_BYTES;             // bytes of one B tile load
   static constexpr int B_STAGE = (B_BOX + 1023) / 1024 * 1024;  // keeps every stage 1024-byte aligned
-  // NVFP4 block scales, copy mode, per stage: 4 interleaved 512-byte atoms
-  // (one per MMA) for each 128 rows.  Each CTA stages its own 128 rows of A's
-  // scales and the scales of all BN rows of B (every CTA of a pair multiplies
-  // by all of B).  Scale-warp mode keeps no scales in shared memory.
-  static constexpr bool SFA_IN_SMEM = SCALED && (SF_MODE == kSfCopy || SF_SMEM_);
-  static constexpr bool SFB_IN_SMEM = SCALED && (SF_MODE != kSfWarps || SF_SMEM_);
-  static constexpr int SF_ATOM = 512;
-  static constexpr int SFA_STAGE = SFA_IN_SMEM ? KSTEPS * SF_ATOM : 0;
-  static constexpr int SFB_BLOCKS = BN / 128;   // 128-row blocks of B scales per tile
-  static constexpr int SFB_STAGE = SFB_IN_SMEM ? SFB_BLOCKS * KSTEPS * SF_ATOM : 0;
-  static constexpr int SF_GROUPS = SF_ST ? SF_GROUPS_ : 0;
+  // NVFP4 block scales per stage in shared memory: 16 bytes (the 16 scales of 256 K elements) per row,
+  // this CTA's 128 rows of A and all BN rows of B
+  static constexpr int SF_ROW_BYTES = 16;
+  static constexpr int SFA_STAGE = SCALED ? BM * SF_ROW_BYTES : 0;
+  static constexpr int SFB_STAGE = SCALED ? BN * SF_ROW_BYTES : 0;
+  static constexpr int SF_GROUPS = SCALED ? SF_GROUPS_ : 0;
   static constexpr int SF_WARPS = 4 * SF_GROUPS;
-  static constexpr int CP_WARPS = SF_HYBRID ? 1 : 0;
-  // bytes landing per CTA per stage on the (leader's) full barrier; in SF_SMEM mode the scales
-  // land on the CTA's own sf_full barrier instead
-  static constexpr int STAGE_TX = A_STAGE + B_BOX + (SF_SMEM_ ? 0 : SFA_STAGE + SFB_STAGE);
+  // operand bytes landing per CTA per stage on the (leader's) full barrier; the scales land on the
+  // CTA's own sf_full barrier
+  static constexpr int STAGE_TX = A_STAGE + B_BOX;
   static constexpr int SF_TX = SFA_STAGE + SFB_STAGE;
   static constexpr int ACC_STRIDE = BN <= 128 ? 128 : BN <= 256 ? 256 : BN;  // accumulators start on aligned columns
   static constexpr int ACC_COLS = NUM_ACC * ACC_STRIDE;
@@ -194,12 +165,8 @@ struct GemmCfg {
   static constexpr int SF_COLS_A = 4 * KSTEPS;
   static constexpr int SF_COLS_B = (BN / 32) * KSTEPS;
   static constexpr int SF_COLS_STAGE = SCALED ? SF_COLS_A + SF_COLS_B : 0;
-  // TMEM scale slots: one per ring stage in copy mode; in scale-warp mode a ring
-  // of their own, as many as fit beside the accumulators (at most STAGES)
-  static constexpr int SF_SLOTS = (!SF_WARPS_MODE || SF_COUPLED) ? STAGES
-                                : ((512 - ACC_COLS) / SF_COLS_STAGE < STAGES ? (512 - ACC_COLS) / SF_COLS_STAGE
-                                                                             : STAGES);
-  static constexpr int TMEM_USED = ACC_COLS + (SCALED ? SF_SLOTS * SF_COLS_STAGE : 0);
+  // one TMEM scale slot per ring stage
+  static constexpr int TMEM_USED = ACC_COLS + STAGES * SF_COLS_STAGE;
   static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128
                                  : TMEM_USED <= 256 ? 256 : 512;
   // output columns per epilogue chunk: 64 (rows of 128 B of bf16) when BN allows, else 32 (64 B)
@@ -207,7 +174,7 @@ struct GemmCfg {
   static constexpr int EPI_ROW_BYTES = EPI_COLS * 2;
   static constexpr uint32_t EPI_SWZ = select_swizzle(EPI_ROW_BYTES);
   static constexpr int EPI_BUF = 32 * EPI_ROW_BYTES;  // one warp's 32-row staging tile
-  static constexpr int THREADS = 64 + 32 * (EPI_WARPS + SF_WARPS + CP_WARPS);
+  static constexpr int THREADS = 64 + 32 * (EPI_WARPS + SF_WARPS);
   static constexpr uint32_t IDESC = (KIND == Kind::BF16)   ? idesc_dense(kFmtBF16, BM * CG, MMA_N)
                                     : (KIND == Kind::FP8) ? idesc_dense(kFmtE4M3, BM * CG, MMA_N)
                                                           : idesc_mxf4nvf4(BM * CG, MMA_N);
@@ -218,9 +185,9 @@ struct GemmCfg {
   static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
   static constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_STAGE;
   static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * 2 * EPI_BUF;
-  static constexpr int NUM_BARS =
-      2 * STAGES + 2 * NUM_ACC + 1 + ((SF_WARPS_MODE && !SF_COUPLED) ? 2 * SF_SLOTS : SF_HYBRID ? SF_SLOTS : 0) +
-      (SF_SMEM ? STAGES : 0);
+  // full / empty per stage, tensor-memory full / empty per accumulator, drain, and (NVFP4) the
+  // per-stage sf_full barriers
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1 + (SCALED ? STAGES : 0);
   // dynamic schedule: ring of cancellation answers (16 bytes each) with a full
   // barrier per slot in every CTA and an empty barrier per slot in the leader,
   // after the barriers above
@@ -230,27 +197,23 @@ struct GemmCfg {
   static constexpr int OFF_SCHED = (OFF_MISC + 16 + 15) / 16 * 16;
   // readers of every answer: each CTA's producer lane, epilogue warps and scale
   // warps, and the leader's MMA lane
-  static constexpr int SCHED_READERS = CL * (1 + EPI_WARPS + SF_WARPS) + MC;
+  static constexpr int SCHED_READERS = CG * (1 + EPI_WARPS + SF_WARPS) + 1;
   static constexpr int SMEM_BYTES = OFF_SCHED + 16 * SCHED_SLOTS + 1024;  // + slack to align the base to 1024
 
   static_assert(B_STAGE % 1024 == 0 && A_STAGE % 1024 == 0, "stages must keep 1024-byte swizzle atoms aligned");
   static_assert((OFF_SFA % 1024) == 0 && (OFF_EPI % 1024) == 0, "region alignment");
   static_assert(BN % 32 == 0 && BN >= 64 && (BN <= 256 || BN == 512), "BN: a multiple of 32 in [64,256], or 512");
-  static_assert(NSUB == 1 || (!SCALED && MC == 1 && NUM_ACC == 1 && CG == 2), "512-wide tiles: bf16 / FP8 pairs");
+  static_assert(NSUB == 1 || (!SCALED && NUM_ACC == 1 && CG == 2), "512-wide tiles: bf16 / FP8 pairs");
   static_assert(B_ROWS % 8 == 0, "B rows per CTA must fill whole 8-row swizzle atoms");
   static_assert(EPI_BUF % (8 * EPI_SWZ) == 0, "staging tiles must keep swizzle atoms aligned");
   static_assert(!SCALED || BN % 128 == 0, "block-scaled tiles cover whole 128-row scale blocks of B");
   static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "epilogue is one or two warpgroups");
   static_assert(NUM_ACC == 1 || NUM_ACC == 2, "one or two accumulators");
   static_assert(TMEM_USED <= 512, "tensor memory has 512 columns");
-  static_assert(!SF_ST || (ACC_COLS % 16 == 0 && SF_COLS_STAGE % 16 == 0 && SF_COLS_A == 16),
+  static_assert(!SCALED || (ACC_COLS % 16 == 0 && SF_COLS_STAGE % 16 == 0 && SF_COLS_A == 16),
                 "scale columns are written 16 at a time at 16-column-aligned addresses");
-  static_assert(!SF_ST || SF_SLOTS >= 2, "the scale warps run at least one slot ahead");
-  static_assert(!SF_ST || SF_GROUPS == 1 || SF_GROUPS == 2, "one or two groups of scale warps");
-  static_assert(!SF_HYBRID || SF_GROUPS == 1, "the hybrid mode's A scales need one group");
-  static_assert(SF_SMEM == SF_SMEM_, "shared-memory scale staging is a form of the coupled scale-warp mode");
+  static_assert(!SCALED || SF_GROUPS == 1 || SF_GROUPS == 2, "one or two groups of scale warps");
   static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB shared-memory limit");
-  static_assert(MC == 1 || (MC == 2 && CG == 2 && !SCALED), "A multicast: two CTA pairs, unscaled kinds");
 };
 
 __device__ __forceinline__ void record_timeout(unsigned int* status, int role, volatile int* abort_flag) {
@@ -308,13 +271,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + C::NUM_ACC + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * C::STAGES + 2 * C::NUM_ACC);
-  // scale-warp and hybrid modes: TMEM scale slot j was written (leader's; one arrival per warp of
-  // the scale group that wrote it in each CTA of the pair, plus, hybrid, the copy warp's commit) /
-  // scale-warp mode: was read by its MMAs (every CTA's, one commit; the hybrid mode's slots follow
-  // the ring stages, so the stage's empty barrier says it)
-  auto sf_ready_bar = [&](int j) { return bar0 + 8u * (2 * C::STAGES + 2 * C::NUM_ACC + 1 + j); };
-  auto sf_empty_bar = [&](int j) { return bar0 + 8u * (2 * C::STAGES + 2 * C::NUM_ACC + 1 + C::SF_SLOTS + j); };
-  // SF_SMEM: stage s's scales landed in this CTA's shared memory (the coupled mode has no slot barriers)
+  // NVFP4: stage s's block scales landed in this CTA's shared memory
   auto sf_full_bar = [&](int st) { return bar0 + 8u * (2 * C::STAGES + 2 * C::NUM_ACC + 1 + st); };
   auto sched_full_bar = [&](int j) { return bar0 + 8u * (C::SCHED_BAR0 + j); };
   auto sched_empty_bar = [&](int j) { return bar0 + 8u * (C::SCHED_BAR0 + C::SCHED_SLOTS + j); };
@@ -325,46 +282,30 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = (C::CL > 1) ? cluster_ctarank() : 0u;  // rank in the cluster
-  const uint32_t prank = rank % C::CG;                         // rank in the CTA pair
-  const int pair = static_cast<int>(rank) / C::CG;             // pair in the cluster
-  const uint32_t leader = rank - prank;                        // the pair's MMA-issuing CTA
-  const int cluster_id = blockIdx.x / C::CL;
-  const int num_clusters = gridDim.x / C::CL;
-  // scheduling unit: MC horizontally adjacent output tiles, one per pair
-  const int tiles_nu = (p.tiles_n + C::MC - 1) / C::MC;
-  const int num_units = p.tiles_m * tiles_nu;
-  // work items: tiles (units), each of the split_tiles first ones replaced by split_s pieces
+  // a cluster is one CTA, or the CTA pair of the 2-SM MMA whose rank-0 CTA (the leader) issues it
+  const uint32_t prank = (C::CG > 1) ? cluster_ctarank() : 0u;  // rank in the CTA pair
+  constexpr uint32_t leader = 0;
+  const int cluster_id = blockIdx.x / C::CG;
+  const int num_clusters = gridDim.x / C::CG;
+  const int num_units = p.tiles_m * p.tiles_n;
+  // work items: tiles, each of the split_tiles first ones replaced by split_s pieces
   const int num_tiles = num_units + p.split_tiles * (p.split_s - 1);
-  const TileOrder order{p.tiles_m, tiles_nu, p.group_m};
+  const TileOrder order{p.tiles_m, p.tiles_n, p.group_m};
   auto work_of = [&](int w) { return work_item(w, p.split_tiles, p.split_s, p.num_kb); };
-  auto tile_coord = [&](int t, int& tm, int& tn) {
-    order.coord(t, tm, tn);
-    tn = tn * C::MC + pair;
-  };
+  auto tile_coord = [&](int t, int& tm, int& tn) { order.coord(t, tm, tn); };
   const uint64_t tmo = p.timeout_ns;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(full_bar(s), C::SF_COUPLED ? 1 + C::CG * 4 : 1);  // + one arrival per scale warp of the group
-      // A multicast: every CTA writes A into both pairs' stages, so a stage is free for it once
-      // both pairs' MMAs have read it
-      mbar_init(empty_bar(s), C::MC);
+      mbar_init(full_bar(s), C::SCALED ? 1 + C::CG * 4 : 1);  // + one arrival per scale warp of the group
+      mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < C::NUM_ACC; ++a) {
       mbar_init(tfull_bar(a), 1);
       mbar_init(tempty_bar(a), C::CG * C::EPI_WARPS);
     }
     mbar_init(drain_bar, 1);
-    if constexpr (C::SF_WARPS_MODE && !C::SF_COUPLED) {
-      for (int j = 0; j < C::SF_SLOTS; ++j) {
-        mbar_init(sf_ready_bar(j), C::CG * 4);  // one group of four scale warps per CTA writes a slot
-        mbar_init(sf_empty_bar(j), 1);
-      }
-    } else if constexpr (C::SF_HYBRID) {
-      for (int j = 0; j < C::SF_SLOTS; ++j) mbar_init(sf_ready_bar(j), C::CG * 4 + 1);
-    }
-    if constexpr (C::SF_SMEM) {
+    if constexpr (C::SCALED) {
       for (int st = 0; st < C::STAGES; ++st) mbar_init(sf_full_bar(st), 1);
     }
     for (int j = 0; j < C::SCHED_SLOTS; ++j) {
@@ -376,8 +317,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
     fence_mbar_init();
     tma_prefetch_desc(&p.tmap_a);
     tma_prefetch_desc(&p.tmap_b);
-    if constexpr (C::SFA_IN_SMEM) tma_prefetch_desc(&p.tmap_sfa);
-    if constexpr (C::SFB_IN_SMEM) tma_prefetch_desc(&p.tmap_sfb);
+    if constexpr (C::SCALED) {
+      tma_prefetch_desc(&p.tmap_sfa);
+      tma_prefetch_desc(&p.tmap_sfb);
+    }
     if (p.c_via_tma) tma_prefetch_desc(&p.tmap_c);
   }
   if (warp == 1) {
@@ -386,7 +329,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
   }
   tc_fence_before();
   __syncthreads();
-  if constexpr (C::CL > 1) {
+  if constexpr (C::CG > 1) {
     cluster_arrive();
     cluster_wait();
   }
@@ -402,7 +345,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
 
   // ---------------------------------------------------------------- tile sequence
   const int first_tile = cluster_id < num_tiles ? cluster_id : -1;
-  const uint32_t sched_empty_leader0 = (C::CL > 1) ? mapa_shared(sched_empty_bar(0), 0) : sched_empty_bar(0);
+  const uint32_t sched_empty_leader0 = (C::CG > 1) ? mapa_shared(sched_empty_bar(0), 0) : sched_empty_bar(0);
   // The tile after tile t, the k-th (k = 0, 1, ...) of this CTA's sequence, or
   // -1 when there is none.  Called by one thread of each role, in order k.
   auto next_tile = [&](int t, int k, bool& ok) -> int {
@@ -421,7 +364,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
     // decoded into a register before the slot is handed back for the next answer
     const int x = clc_first_ctaid_x(ld_shared_v4(sResp + 16u * static_cast<uint32_t>(j)));
     mbar_arrive_cluster(sched_empty_leader0 + 8u * static_cast<uint32_t>(j));
-    return x < 0 ? -1 : x / C::CL;
+    return x < 0 ? -1 : x / C::CG;
   };
   // Dynamic schedule, the leader's producer lane at the start of its k-th tile:
   // ask for the tile after it, answered into slot k % SCHED_SLOTS of every CTA
@@ -431,8 +374,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
     const uint32_t ph = static_cast<uint32_t>(k / C::SCHED_SLOTS) & 1u;
     if (!mbar_wait(sched_empty_bar(j), ph ^ 1u, tmo, abort_flag)) return false;
 #pragma unroll
-    for (int r = 0; r < C::CL; ++r)
-      mbar_arrive_expect_tx_cluster(C::CL > 1 ? mapa_shared(sched_full_bar(j), static_cast<uint32_t>(r))
+    for (int r = 0; r < C::CG; ++r)
+      mbar_arrive_expect_tx_cluster(C::CG > 1 ? mapa_shared(sched_full_bar(j), static_cast<uint32_t>(r))
                                               : sched_full_bar(j),
                                     16u);
     clc_try_cancel_multicast(sResp + 16u * static_cast<uint32_t>(j), sched_full_bar(j));
@@ -457,7 +400,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
       bool first = true;
       int k = 0;
       for (int t = first_tile; t >= 0 && ok; t = next_tile(t, k, ok), ++k) {
-        if (p.sched == kSchedDynamic && rank == 0 && !request_tile(k)) {
+        if (p.sched == kSchedDynamic && prank == 0 && !request_tile(k)) {
           ok = false;
           break;
         }
@@ -475,32 +418,20 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
           const uint32_t fb = (C::CG == 2) ? mapa_shared(full_bar(stage), leader) : full_bar(stage);
           if (prank == 0) mbar_arrive_expect_tx(full_bar(stage), C::STAGE_TX * C::CG);
           if (!(first && p.fault_mode == 1)) {
-            if constexpr (C::MC == 2) {
-              // rows [64 pair, 64 pair + 64) of A half `prank`, into the same stage of this CTA
-              // and of its counterpart in the other pair (each destination's completion lands on
-              // its own pair leader's full barrier)
-              tma_load_2d_mc_pair(sA + stage * C::A_STAGE + static_cast<uint32_t>(pair) * (C::A_STAGE / 2), &p.tmap_a,
-                                  fb, kb * C::K_TMAP, a_row + pair * (C::BM / 2),
-                                  static_cast<uint16_t>((1u << prank) | (1u << (prank + 2))));
-            } else {
-              tma_load_2d<C::CG>(sA + stage * C::A_STAGE, &p.tmap_a, fb, kb * C::K_TMAP, a_row);
-            }
+            tma_load_2d<C::CG>(sA + stage * C::A_STAGE, &p.tmap_a, fb, kb * C::K_TMAP, a_row);
 #pragma unroll
             for (int sub = 0; sub < C::NSUB; ++sub)
               tma_load_2d<C::CG>(sB + stage * C::B_STAGE + sub * C::B_SUB_ROWS * C::ROW_BYTES, &p.tmap_b, fb,
                                  kb * C::K_TMAP, b_row + sub * C::MMA_N);
-            // staged scales: 2 KB (16 rows of 128 B) per (K stage, 128-row block), the blocks of one
-            // K stage contiguous
-            const int ya = (kb * p.sf_blocks_a + a_row / 128) * 16;
-            const int yb = (kb * p.sf_blocks_b + (tn * C::BN) / 128) * 16;
-            if constexpr (C::SF_SMEM) {
+            if constexpr (C::SCALED) {
+              // staged scales: 2 KB (16 rows of 128 B) per (K stage, 128-row block), the blocks of
+              // one K stage contiguous; they land on this CTA's own sf_full barrier
+              const int ya = (kb * p.sf_blocks_a + a_row / 128) * 16;
+              const int yb = (kb * p.sf_blocks_b + (tn * C::BN) / 128) * 16;
               const uint32_t sfb_bar = sf_full_bar(stage);
               mbar_arrive_expect_tx(sfb_bar, C::SF_TX);
               tma_load_2d<1>(sSFA + stage * C::SFA_STAGE, &p.tmap_sfa, sfb_bar, 0, ya);
               tma_load_2d<1>(sSFB + stage * C::SFB_STAGE, &p.tmap_sfb, sfb_bar, 0, yb);
-            } else {
-              if constexpr (C::SFA_IN_SMEM) tma_load_2d<C::CG>(sSFA + stage * C::SFA_STAGE, &p.tmap_sfa, fb, 0, ya);
-              if constexpr (C::SFB_IN_SMEM) tma_load_2d<C::CG>(sSFB + stage * C::SFB_STAGE, &p.tmap_sfb, fb, 0, yb);
             }
           }
           first = false;
@@ -521,8 +452,6 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
     if (lane == 0 && prank == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      int slot = 0;  // scale-warp mode: TMEM scale slot
-      uint32_t slot_phase = 0;
       bool ok = true;
       int it = 0;
       for (int t = first_tile; t >= 0 && ok; t = next_tile(t, it, ok), ++it) {
@@ -543,31 +472,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
           tc_fence_after();
           const uint32_t a0 = sA + stage * C::A_STAGE;
           const uint32_t b0 = sB + stage * C::B_STAGE;
-          // this stage's scale columns: copy mode reuses them only after the ring stage itself is
-          // released; scale-warp mode has a slot ring of its own
-          const uint32_t sf_tmem = tmem_base + static_cast<uint32_t>(
-                                                   C::ACC_COLS + ((C::SF_WARPS_MODE && !C::SF_COUPLED) ? slot : stage) *
-                                                                     C::SF_COLS_STAGE);
-          if constexpr (C::SF_ST && !C::SF_COUPLED) {
-            const bool ready = C::SF_WARPS_MODE ? mbar_wait(sf_ready_bar(slot), slot_phase, tmo, abort_flag)
-                                                : mbar_wait(sf_ready_bar(stage), phase, tmo, abort_flag);
-            if (!ready) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-          } else if constexpr (C::SCALED && !C::SF_ST) {
-            const uint32_t sfa0 = sSFA + stage * C::SFA_STAGE;
-            const uint32_t sfb0 = sSFB + stage * C::SFB_STAGE;
-#pragma unroll
-            for (int kk = 0; kk < C::KSTEPS; ++kk) {
-              tmem_cp_32x128b_warpx4<C::CG>(sf_tmem + 4u * kk, sdesc_plain_rows16(sfa0 + kk * C::SF_ATOM));
-#pragma unroll
-              for (int j = 0; j < C::SFB_BLOCKS; ++j)
-                tmem_cp_32x128b_warpx4<C::CG>(sf_tmem + C::SF_COLS_A + (C::BN / 32) * kk + 4u * j,
-                                              sdesc_plain_rows16(sfb0 + (j * C::KSTEPS + kk) * C::SF_ATOM));
-            }
-          }
+          // this stage's TMEM scale slot (NVFP4): the stage's full barrier also counts the scale
+          // warps that wrote it
+          const uint32_t sf_tmem = tmem_base + static_cast<uint32_t>(C::ACC_COLS + stage * C::SF_COLS_STAGE);
 #pragma unroll
           for (int kk = 0; kk < C::KSTEPS; ++kk) {
             const uint64_t ad = sdesc_sw128(a0 + 32u * kk);
@@ -591,26 +498,18 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
               mma_mxf4nvf4<C::CG>(d_tmem, ad, bd, C::IDESC, sf_tmem + 4u * kk,
                                   sf_tmem + C::SF_COLS_A + (C::BN / 32) * kk, accum);
           }
-          // the stage is free for this pair's CTAs and (A multicast) for the other pair's, which
-          // load half of this pair's A
-          mma_commit<C::CG>(empty_bar(stage), C::MC == 2 ? 0xF : 0x3);
-          if constexpr (C::SF_WARPS_MODE && !C::SF_COUPLED) {
-            mma_commit<C::CG>(sf_empty_bar(slot), 0x3);
-            if (++slot == C::SF_SLOTS) {
-              slot = 0;
-              slot_phase ^= 1u;
-            }
-          }
+          // the stage (operands and, NVFP4, scale slot) is free for both CTAs of the pair
+          mma_commit<C::CG>(empty_bar(stage), (1u << C::CG) - 1u);
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        mma_commit<C::CG>(tfull_bar(acc), static_cast<uint16_t>(0x3u << (C::CG * pair)));
+        mma_commit<C::CG>(tfull_bar(acc), static_cast<uint16_t>((1u << C::CG) - 1u));
       }
       // No MMA may still be writing TMEM when it is released.
-      mma_commit<C::CG>(drain_bar, static_cast<uint16_t>(0x1u << (C::CG * pair)));
+      mma_commit<C::CG>(drain_bar, 0x1u);
       mbar_wait(drain_bar, 0, tmo, never_abort);
       if (!ok) record_timeout(p.status, kRoleMma, abort_flag);
     }
@@ -659,9 +558,6 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
       tc_fence_after();
       const int row0 = tm * (C::BM * C::CG) + static_cast<int>(prank) * C::BM + quad * 32;
       const int col0 = tn * C::BN;
-      // A multicast with an odd number of tile columns: the second pair's last tile lies wholly
-      // right of C (its B rows were read as zeros) and is not stored
-      const bool live = tn < p.tiles_n;
       const uint32_t t_row =
           tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * C::ACC_STRIDE);
       auto load_chunk = [&](int c, uint32_t (&r)[NLD][32], bool may_release) {
@@ -690,8 +586,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
       };
       // store chunk c of this warp's rows, given as packed bf16 pairs
       auto store_chunk = [&](int c, const uint32_t (&pk)[NPK]) {
-        if (!live) {
-        } else if (p.c_via_tma) {
+        if (p.c_via_tma) {
           const uint32_t buf = stage0 + static_cast<uint32_t>(chunk_ctr & 1) * C::EPI_BUF;
           if (lane == 0) bulk_wait_group_read<1>();  // the store that last used `buf` has read it
           __syncwarp();
@@ -724,7 +619,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
         ++chunk_ctr;
       };
       auto count_visit = [&]() {
-        if (p.visits != nullptr && ew == 0 && lane == 0 && prank == 0 && tn < p.tiles_n)
+        if (p.visits != nullptr && ew == 0 && lane == 0 && prank == 0)
           atomicAdd(p.visits + tm * p.tiles_n + tn, 1u);
       };
       if (wk.piece < 0) {
@@ -850,30 +745,28 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
     if (lane == 0) bulk_wait_group<0>();
     __syncwarp();
   } else if (warp < 2 + C::EPI_WARPS + C::SF_WARPS) {
-    // ------------------------------------------------------------ SCALES (scale-warp and hybrid modes)
-    // One warp per TMEM lane quarter q.  For each (tile, K stage) of the CTA it
-    // reads the staged scales ([K stage][128-row block][row][16 scales] in
-    // global memory, ahead of use) and writes them into the step's TMEM scale
-    // slot with tcgen05.st: A's row 32q+lane to lane 32q+lane, column 4t+q of
-    // the slot's A columns (one word = the 4 scales of MMA t); in scale-warp
-    // mode also B's rows 32g+lane (g < BN/32) to lane 32q+lane, column
-    // (BN/32)t+g of the slot's B columns, in every quarter (each quarter's rows
-    // read all of B's scales).
-    if constexpr (C::SF_ST) {
-      constexpr int G = C::SF_WARPS_MODE ? C::BN / 32 : 0;  // B rows per lane this warp loads and stores
+    // ------------------------------------------------------------ SCALES (NVFP4)
+    // One warp per TMEM lane quarter q.  For each K stage of the CTA's tile
+    // sequence (this group's share of them) it reads the stage's block scales
+    // from shared memory once the producer's TMA has put them there, and
+    // writes them into the stage's TMEM scale slot with tcgen05.st: A's row
+    // 32q+lane to lane 32q+lane, column 4t+q of the slot's A columns (one word
+    // = the 4 scales of MMA t); B's rows 32g+lane (g < BN/32) to lane
+    // 32q+lane, column (BN/32)t+g of the slot's B columns, in every quarter
+    // (each quarter's rows read all of B's scales).  Then it arrives on the
+    // stage's full barrier in the leader CTA.  The slot is free when the
+    // scales land: the producer refilled the stage only after the MMAs that
+    // last read the slot had completed.
+    if constexpr (C::SCALED) {
+      constexpr int G = C::BN / 32;  // B rows per lane this warp loads and stores
       const int quad = warp & 3;
       const int sgroup = (warp - 2 - C::EPI_WARPS) / 4;  // this warp takes steps sgroup, sgroup + SF_GROUPS, ...
       const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
-      // where a written slot is announced: the stage's full barrier (coupled) or the slot's ready barrier
-      const uint32_t ready0 = C::SF_COUPLED ? full_bar(0) : sf_ready_bar(0);
-      const uint32_t ready_leader0 = (C::CG == 2) ? mapa_shared(ready0, leader) : ready0;
-      const int my_tiles = cluster_id < num_tiles ? (num_tiles - 1 - cluster_id) / num_clusters + 1 : 0;
-      const int steps = my_tiles * p.num_kb;
-      const uint4* sfa = reinterpret_cast<const uint4*>(p.sf_a);
-      const uint4* sfb = reinterpret_cast<const uint4*>(p.sf_b);
-      // scales of step s: [0] = this lane's A row, [1 + g] = B row 32g + lane (scale-warp mode)
-      // SF_SMEM: read them from the stage's shared-memory copy once it has landed
-      auto fetch_smem = [&](int s_, uint4 (&v)[1 + G]) -> bool {
+      const uint32_t ready_leader0 = (C::CG == 2) ? mapa_shared(full_bar(0), leader) : full_bar(0);
+      bool ok = true;
+      // scales of step s: [0] = this lane's A row, [1 + g] = B row 32g + lane, from the stage's
+      // shared-memory copy once it has landed
+      auto fetch = [&](int s_, uint4 (&v)[1 + G]) -> bool {
         const int j = s_ % C::STAGES;
         const uint32_t ph = static_cast<uint32_t>(s_ / C::STAGES) & 1u;
         if (!__all_sync(0xffffffffu, mbar_wait(sf_full_bar(j), ph, tmo, abort_flag))) return false;
@@ -883,28 +776,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
           v[1 + g] = ld_shared_v4(sSFB + j * C::SFB_STAGE + static_cast<uint32_t>(g * 32 + lane) * 16u);
         return true;
       };
-      auto fetch = [&](int s_, uint4 (&v)[1 + G]) {
-        const int i = s_ / p.num_kb;
-        const int kb = s_ - i * p.num_kb;
-        int tm, tn;
-        tile_coord(cluster_id + i * num_clusters, tm, tn);
-        const size_t ra = (static_cast<size_t>(kb) * p.sf_blocks_a + tm * C::CG + prank) * 128 + quad * 32 + lane;
-        const size_t rb = static_cast<size_t>(kb) * p.sf_blocks_b * 128 + static_cast<size_t>(tn) * C::BN + lane;
-        v[0] = __ldg(sfa + ra);
-#pragma unroll
-        for (int g = 0; g < G; ++g) v[1 + g] = __ldg(sfb + rb + 32 * g);
-        (void)rb;
-        (void)sfb;
-      };
-      bool ok = true;
-      // step s into slot s % SF_SLOTS once the MMAs of step s - SF_SLOTS have read it
-      auto put = [&](int s_, const uint4 (&v)[1 + G]) -> bool {
-        const int j = s_ % C::SF_SLOTS;
-        const uint32_t ph = static_cast<uint32_t>(s_ / C::SF_SLOTS) & 1u;
-        if constexpr (!C::SF_SMEM) {  // SF_SMEM: the slot is free once the stage's scales have landed
-          const uint32_t freed = (C::SF_WARPS_MODE && !C::SF_COUPLED) ? sf_empty_bar(j) : empty_bar(j);
-          if (!__all_sync(0xffffffffu, mbar_wait(freed, ph ^ 1u, tmo, abort_flag))) return false;
-        }
+      // step s into the TMEM slot of its ring stage
+      auto put = [&](int s_, const uint4 (&v)[1 + G]) {
+        const int j = s_ % C::STAGES;
         tc_fence_after();
         const uint32_t cols = lane_base + static_cast<uint32_t>(C::ACC_COLS + j * C::SF_COLS_STAGE);
         // A: only column 4t + q of MMA t is read by this quarter's rows
@@ -912,107 +786,37 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
         tmem_st_32x32b_x1(cols + 4u + static_cast<uint32_t>(quad), v[0].y);
         tmem_st_32x32b_x1(cols + 8u + static_cast<uint32_t>(quad), v[0].z);
         tmem_st_32x32b_x1(cols + 12u + static_cast<uint32_t>(quad), v[0].w);
-        if constexpr (G > 0) {
-          uint32_t rbw[G * C::KSTEPS];
+        uint32_t rbw[G * C::KSTEPS];
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            rbw[0 * G + g] = v[1 + g].x;
-            rbw[1 * G + g] = v[1 + g].y;
-            rbw[2 * G + g] = v[1 + g].z;
-            rbw[3 * G + g] = v[1 + g].w;
-          }
-#pragma unroll
-          for (int h = 0; h < (G * C::KSTEPS) / 16; ++h)
-            tmem_st_32x32b_x16(cols + C::SF_COLS_A + 16u * h, *reinterpret_cast<uint32_t(*)[16]>(rbw + 16 * h));
+        for (int g = 0; g < G; ++g) {
+          rbw[0 * G + g] = v[1 + g].x;
+          rbw[1 * G + g] = v[1 + g].y;
+          rbw[2 * G + g] = v[1 + g].z;
+          rbw[3 * G + g] = v[1 + g].w;
         }
+#pragma unroll
+        for (int h = 0; h < (G * C::KSTEPS) / 16; ++h)
+          tmem_st_32x32b_x16(cols + C::SF_COLS_A + 16u * h, *reinterpret_cast<uint32_t(*)[16]>(rbw + 16 * h));
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(ready_leader0 + 8u * j);
-        return true;
       };
-      if constexpr (C::SF_SMEM) {
-        // the scales are already on chip: read each step's just before writing it.  Step s is
-        // K stage kb of the k-th tile of the sequence, s = k * num_kb + kb; this group takes the
-        // steps with s % SF_GROUPS == sgroup.
-        uint4 v0[1 + G];
-        int k = 0;
-        int step = 0;  // K stages of the sequence so far: the ring position of the next one
-        for (int t = first_tile; t >= 0 && ok; t = next_tile_warp(t, k, ok), ++k) {
-          const WorkItem wk = work_of(t);
-          for (int kb = wk.kb0; kb < wk.kb1 && ok; ++kb) {
-            const int s_ = step++;
-            if (s_ % C::SF_GROUPS != sgroup) continue;
-            ok = fetch_smem(s_, v0);
-            if (!ok) break;
-            ok = put(s_, v0);
-          }
-        }
-        (void)steps;
-      } else if constexpr (C::SF_GROUPS == 1) {
-        // two register sets, so that the loads of step s + 2 fly while step s waits for its slot
-        uint4 v0[1 + G], v1[1 + G];
-        if (steps > 0) fetch(0, v0);
-        if (steps > 1) fetch(1, v1);
-        for (int s_ = 0; s_ < steps && ok; s_ += 2) {
-          ok = put(s_, v0);
-          if (!ok) break;
-          if (s_ + 2 < steps) fetch(s_ + 2, v0);
-          if (s_ + 1 < steps) {
-            ok = put(s_ + 1, v1);
-            if (!ok) break;
-            if (s_ + 3 < steps) fetch(s_ + 3, v1);
-          }
-        }
-      } else {
-        // one register set: the loads of this group's next step fly while the other group works
-        uint4 v0[1 + G];
-        if (sgroup < steps) fetch(sgroup, v0);
-        for (int s_ = sgroup; s_ < steps && ok; s_ += C::SF_GROUPS) {
-          ok = put(s_, v0);
-          if (!ok) break;
-          if (s_ + C::SF_GROUPS < steps) fetch(s_ + C::SF_GROUPS, v0);
+      // Step s is K stage kb of the k-th work item of the sequence; this group takes the steps
+      // with s % SF_GROUPS == sgroup.
+      uint4 v0[1 + G];
+      int k = 0;
+      int step = 0;  // K stages of the sequence so far: the ring position of the next one
+      for (int t = first_tile; t >= 0 && ok; t = next_tile_warp(t, k, ok), ++k) {
+        const WorkItem wk = work_of(t);
+        for (int kb = wk.kb0; kb < wk.kb1 && ok; ++kb) {
+          const int s_ = step++;
+          if (s_ % C::SF_GROUPS != sgroup) continue;
+          ok = fetch(s_, v0);
+          if (ok) put(s_, v0);
         }
       }
       if (!ok && lane == 0) record_timeout(p.status, kRoleProducer, abort_flag);
-      __syncwarp();
-    }
-  } else {
-    // ------------------------------------------------------------ B SCALE COPIES (hybrid mode)
-    // One lane of the leader CTA copies each stage's B scale atoms shared -> TMEM (in both CTAs
-    // of a pair) and commits the copies to the stage's sf_ready barrier.  The stage's full barrier
-    // says the atoms landed in both CTAs; it also implies the slot is free, since the producer
-    // refilled the stage only after the MMAs that read the slot had completed.
-    if constexpr (C::SF_HYBRID) {
-      if (lane == 0 && prank == 0) {
-        const int my_tiles = cluster_id < num_tiles ? (num_tiles - 1 - cluster_id) / num_clusters + 1 : 0;
-        const int steps = my_tiles * p.num_kb;
-        int stage = 0;
-        uint32_t phase = 0;
-        bool ok = true;
-        for (int s_ = 0; s_ < steps; ++s_) {
-          if (!mbar_wait(full_bar(stage), phase, tmo, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sf_tmem = tmem_base + static_cast<uint32_t>(C::ACC_COLS + stage * C::SF_COLS_STAGE);
-          const uint32_t sfb0 = sSFB + stage * C::SFB_STAGE;
-#pragma unroll
-          for (int kk = 0; kk < C::KSTEPS; ++kk) {
-#pragma unroll
-            for (int j = 0; j < C::SFB_BLOCKS; ++j)
-              tmem_cp_32x128b_warpx4<C::CG>(sf_tmem + C::SF_COLS_A + (C::BN / 32) * kk + 4u * j,
-                                            sdesc_plain_rows16(sfb0 + (j * C::KSTEPS + kk) * C::SF_ATOM));
-          }
-          mma_commit<C::CG>(sf_ready_bar(stage), 0x1);
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (!ok) record_timeout(p.status, kRoleMma, abort_flag);
-      }
       __syncwarp();
     }
   }
@@ -1020,7 +824,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
   // ------------------------------------------------------------ teardown
   tc_fence_before();
   __syncthreads();
-  if constexpr (C::CL > 1) {
+  if constexpr (C::CG > 1) {
     cluster_arrive();
     cluster_wait();
   }
@@ -1037,22 +841,19 @@ struct KernelVariant {
   int cg;
   int bn;
   int epi_cols;  // columns of one epilogue TMA store box (64: 128-byte swizzle, 32: 64-byte swizzle)
-  int sf_mode;   // NVFP4 block-scale staging mode (kSfCopy / kSfWarps)
   int stages;
   int epi_warps;
   int threads;
   int smem_bytes;
   const char* name;
   const void* func;
-  int mc;  // CTA pairs per cluster sharing A (1 or 2)
 };
 
 template <class C>
 KernelVariant make_variant(const char* name) {
-  return KernelVariant{static_cast<int>(C::KIND), C::CG,         C::BN,         C::EPI_COLS,
-                       C::SF_MODE,                   C::STAGES,     C::EPI_WARPS,  C::THREADS,
-                       C::SMEM_BYTES,                name,          reinterpret_cast<const void*>(&tkg_gemm_kernel<C>),
-                       C::MC};
+  return KernelVariant{static_cast<int>(C::KIND), C::CG,        C::BN,         C::EPI_COLS,
+                       C::STAGES,                 C::EPI_WARPS, C::THREADS,    C::SMEM_BYTES,
+                       name,                      reinterpret_cast<const void*>(&tkg_gemm_kernel<C>)};
 }
 
 }  // namespace tkg

@@ -6,47 +6,24 @@
 //
 // The tensor core reads the scales of one MMA (64 K elements = 4 scales per
 // row) from tensor memory: row m of a 128-row block at lane m, column
-// (base + m/32), byte = 16-element slice.  tcgen05.cp.32x128b.warpx4 produces
-// that from a 512-byte shared "atom" laid out [r = 0..31][q = 0..3][slice 0..3]
-// holding the scales of rows 32q + r.  The caller's row-major [rows][K/16]
-// scales are rewritten into such atoms by interleave_scales_kernel, ordered
-// [stage-k][128-row block][MMA of the stage][atom], so that every ring stage
-// loads one contiguous 2 KB run per 128 rows with a plain 2-D TMA box.
-//
-// The scale-warp variants take the same 2 KB runs in plain row order,
-// [stage-k][128-row block][row][16 scales]: their scale warps read one row's
-// 16 bytes straight from global memory and write them to the row's own TMEM
-// lane with tcgen05.st, so the shared-memory ring only holds operands (six
-// 32 KB stages instead of five of 38 KB).
+// (base + m/32), byte = 16-element slice.  The caller's row-major [rows][K/16]
+// scales are first rewritten by interleave_scales_kernel into 2 KB runs, one
+// per (256-deep K stage, 128-row block), [row][16 scales] inside a run, the
+// runs of one K stage contiguous, so that every ring stage loads one
+// contiguous run per 128 rows with a plain 2-D TMA box.  Scale warps read a
+// row's 16 bytes from the stage's shared-memory copy and write them to the
+// row's own TMEM lane with tcgen05.st (gemm_kernel.cuh).
 #include <cuda_bf16.h>
 
 #include "gemm_variants.h"
 
 namespace tkg {
 
-using Nvfp4_1Sm_256 = GemmCfg<Kind::NVFP4, 1, 256, 3, 4, 1>;
-using Nvfp4_2Sm_256 = GemmCfg<Kind::NVFP4, 2, 256, 5, 4, 1>;
-using Nvfp4_2Sm_128 = GemmCfg<Kind::NVFP4, 2, 128, 6, 4, 2>;
-using Nvfp4_2Sm_256_Sfw = GemmCfg<Kind::NVFP4, 2, 256, 6, 4, 1, kSfWarps, 2>;
-using Nvfp4_2Sm_256_Hyb = GemmCfg<Kind::NVFP4, 2, 256, 5, 4, 1, kSfHybrid, 1>;
-using Nvfp4_2Sm_256_Sfc = GemmCfg<Kind::NVFP4, 2, 256, 5, 4, 1, kSfWarps, 2, true>;
-using Nvfp4_2Sm_256_Sfs = GemmCfg<Kind::NVFP4, 2, 256, 5, 4, 1, kSfWarps, 2, true, true>;
+using Nvfp4_2Sm_256 = GemmCfg<Kind::NVFP4, 2, 256, 5, 4, 1, 2>;
 
 const KernelVariant* nvfp4_variant(int id) {
-  static const KernelVariant v1 = make_variant<Nvfp4_1Sm_256>("nvfp4_1sm_128x256_s3");
-  static const KernelVariant v2 = make_variant<Nvfp4_2Sm_256>("nvfp4_2sm_256x256_s5");
-  static const KernelVariant v3 = make_variant<Nvfp4_2Sm_128>("nvfp4_2sm_256x128_s6");
-  static const KernelVariant v5 = make_variant<Nvfp4_2Sm_256_Sfw>("nvfp4_2sm_256x256_s6_sfw8");
-  static const KernelVariant v6 = make_variant<Nvfp4_2Sm_256_Hyb>("nvfp4_2sm_256x256_s5_hybrid");
-  static const KernelVariant v7 = make_variant<Nvfp4_2Sm_256_Sfc>("nvfp4_2sm_256x256_s5_sfw8_coupled");
-  static const KernelVariant v8 = make_variant<Nvfp4_2Sm_256_Sfs>("nvfp4_2sm_256x256_s5_sfw8_smem");
+  static const KernelVariant v8 = make_variant<Nvfp4_2Sm_256>("nvfp4_2sm_256x256_s5_sfw8_smem");
   switch (id) {
-    case kVariant1Sm128x256: return &v1;
-    case kVariant2Sm256x256: return &v2;
-    case kVariant2Sm256x128: return &v3;
-    case kVariant2Sm256x256Sfw: return &v5;
-    case kVariant2Sm256x256Hybrid: return &v6;
-    case kVariant2Sm256x256Coupled: return &v7;
     case kVariant2Sm256x256SfSmem: return &v8;
     default: return nullptr;
   }
@@ -56,18 +33,16 @@ namespace {
 
 struct InterleaveArgs {
   const uint8_t* src;  // row-major [rows][k16] e4m3 scales
-  uint8_t* dst;        // atoms [kstages][blocks][4][512]
+  uint8_t* dst;        // runs [kstages][blocks][128 rows][16 scales]
   int rows;            // valid rows
   int k16;             // scales per row (K / 16)
   int blocks;          // 128-row blocks in dst (rows padded with zero scales)
   int kstages;         // 256-element K stages in dst (padded with zero scales)
-  int row_layout;      // 0: per-MMA atoms; 1: [row][16 scales] runs
 };
 
 // One CTA rewrites one 128-row block for two consecutive K stages (32 source
 // bytes per row, i.e. whole 32-byte sectors).  Scales of rows or K positions
-// past the matrix are written as 0.  Either layout keeps each (K stage, block)
-// in its own 2 KB run.
+// past the matrix are written as 0.
 __global__ void __launch_bounds__(256) interleave_scales_kernel(InterleaveArgs a, InterleaveArgs b, int blocks_a) {
   // launched as a programmatic dependent: the previous GEMM may still read the
   // scratch this kernel rewrites, or a previous kernel still write the scales
@@ -96,23 +71,20 @@ __global__ void __launch_bounds__(256) interleave_scales_kernel(InterleaveArgs a
         if (col + j < s.k16) v |= static_cast<uint32_t>(__ldg(p + col + j)) << (8 * j);
     }
     const size_t run = static_cast<size_t>(kb) * s.blocks + rb;
-    const size_t off = s.row_layout ? run * 2048 + r_in * 16 + t * 4
-                                    : (run * 4 + t) * 512 + (r_in & 31) * 16 + (r_in >> 5) * 4;
+    const size_t off = run * 2048 + r_in * 16 + t * 4;
     *reinterpret_cast<uint32_t*>(s.dst + off) = v;
   }
 }
 
 }  // namespace
 
-// Rewrites both operands' scales into `scratch` (see the layout above).
-// Returns the byte offset of B's atoms inside `scratch`.
+// Rewrites both operands' scales into `scratch` (see the layout above), B's
+// runs at byte offset `b_offset`.
 cudaError_t nvfp4_interleave_scales(const uint8_t* sfa, const uint8_t* sfb, int M, int N, int K, int blocks_a,
-                                    int blocks_b, int kstages, int sf_mode, uint8_t* scratch, size_t b_offset,
+                                    int blocks_b, int kstages, uint8_t* scratch, size_t b_offset,
                                     cudaStream_t stream, bool overlap) {
-  const int rows_a = sf_mode == kSfWarps || sf_mode == kSfHybrid ? 1 : 0;
-  const int rows_b = sf_mode == kSfWarps ? 1 : 0;
-  InterleaveArgs a{sfa, scratch, M, K / 16, blocks_a, kstages, rows_a};
-  InterleaveArgs b{sfb, scratch + b_offset, N, K / 16, blocks_b, kstages, rows_b};
+  InterleaveArgs a{sfa, scratch, M, K / 16, blocks_a, kstages};
+  InterleaveArgs b{sfb, scratch + b_offset, N, K / 16, blocks_b, kstages};
   const int kpairs = (kstages + 1) / 2;
   const int grid_a = blocks_a * kpairs;
   const int grid_b = blocks_b * kpairs;

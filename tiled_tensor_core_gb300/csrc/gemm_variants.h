@@ -6,23 +6,16 @@
 
 namespace tkg {
 
-// Variant ids (also the values of TKG_OPT_VARIANT).
+// Variant ids (also the values of TKG_OPT_VARIANT).  The ids are those of the
+// kernel forms measured while the tile shape was chosen; the forms that lost
+// (1-SM 128 x 256, 256 x 128 / 192 / 224 pair tiles, NVFP4 scale staging by
+// tensor-pipe copies or from global memory) are no longer compiled.
 enum VariantId : int {
   kVariantAuto = 0,
-  kVariant1Sm128x256 = 1,  // cta_group::1, 128 x 256 tile per CTA
-  kVariant2Sm256x256 = 2,  // cta_group::2, 256 x 256 tile per CTA pair
-  kVariant2Sm256x128 = 3,  // cta_group::2, 256 x 128 tile per CTA pair
-  kVariant2Sm256x224 = 4,  // cta_group::2, 256 x 224 tile per CTA pair (bf16 / FP8)
-  kVariant2Sm256x256Sfw = 5,  // cta_group::2, 256 x 256, block scales written by scale warps (NVFP4)
-  kVariant2Sm256x256Hybrid = 6,  // cta_group::2, 256 x 256, A scales by scale warps, B by a copy warp (NVFP4)
-  kVariant2Sm256x256Coupled = 7,  // as 5, with one TMEM scale slot per ring stage (NVFP4)
-  kVariant2Sm256x256SfSmem = 8,   // as 7, the scales brought into shared memory by the ring's TMA (NVFP4)
-  kVariant2Sm256x192 = 9,          // cta_group::2, 256 x 192 tile per CTA pair (bf16 / FP8)
-  // clusters of two CTA pairs on horizontally adjacent tiles, A multicast between the pairs (bf16 / FP8)
-  kVariantMc256x256 = 10,
-  kVariantMc256x224 = 11,
-  kVariantMc256x192 = 12,
-  kVariant2Sm256x512 = 13,  // cta_group::2, 256 x 512 tile per CTA pair: two N = 256 MMAs per K step (bf16 / FP8)
+  kVariant2Sm256x256 = 2,         // cta_group::2, 256 x 256 tile per CTA pair (bf16 / FP8)
+  kVariant2Sm256x256SfSmem = 8,   // cta_group::2, 256 x 256, block scales through shared memory and
+                                  // scale warps into tensor memory (NVFP4)
+  kVariant2Sm256x512 = 13,        // cta_group::2, 256 x 512 tile per CTA pair: two N = 256 MMAs per K step (bf16 / FP8)
   kNumVariants = 14
 };
 
@@ -32,14 +25,46 @@ const KernelVariant* fp8_variant(int id);
 const KernelVariant* nvfp4_variant(int id);
 
 // NVFP4: rewrite row-major [rows][K/16] block scales of A and B into the
-// 2 KB per (K stage, 128-row block) runs the GEMM stages (A's at scratch, B's
-// at scratch + b_offset), laid out for the variant's `sf_mode`.  One kernel
+// 2 KB per (K stage, 128-row block) runs, [row][16 scales] inside a run, that
+// the GEMM stages (A's at scratch, B's at scratch + b_offset).  One kernel
 // launch on `stream`, as a programmatic dependent of the previous kernel if
 // `overlap` (it waits for that kernel before touching memory either way).
 cudaError_t nvfp4_interleave_scales(const uint8_t* sfa, const uint8_t* sfb, int M, int N, int K, int blocks_a,
-                                    int blocks_b, int kstages, int sf_mode, uint8_t* scratch, size_t b_offset,
+                                    int blocks_b, int kstages, uint8_t* scratch, size_t b_offset,
                                     cudaStream_t stream, bool overlap);
 size_t nvfp4_scratch_bytes(int blocks_a, int blocks_b, int kstages);
+
+// ---------------------------------------------------------------- launch (api.cu)
+
+// What a GEMM launch runs: the variant (TKG_OPT_VARIANT, else the default for
+// the shape), its tile counts and K stages and, NVFP4, the staged block-scale
+// geometry (2 KB runs per (K stage, 128-row block); B's after A's).
+struct GemmPlan {
+  int id = 0;
+  const KernelVariant* v = nullptr;
+  int64_t tiles_m = 0, tiles_n = 0;
+  int num_kb = 0;
+  int sf_blocks_a = 0, sf_blocks_b = 0;
+  size_t sf_bytes = 0, sf_b_off = 0;
+};
+// Host-only argument checks of the GEMM entry points (no CUDA call).
+tkg_status check_gemm_args(int kind, int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C,
+                           const tkg_scales* scales);
+// Host only (no CUDA call); `sm_count` decides between the bf16 / FP8 tiles.
+tkg_status plan_gemm(int kind, int64_t M, int64_t N, int64_t K, int sm_count, GemmPlan* out);
+// The kernel parameters of a planned GEMM on the current device: tensor maps
+// (through the host-side map cache if `cached_maps`, else encoded on the
+// stack), sizes, options, and (NVFP4) the staged scales at `sf_scratch`.
+tkg_status gemm_params(GemmParams* out, const GemmPlan& g, int kind, int64_t M, int64_t N, int64_t K, const void* A,
+                       const void* B, void* C, const tkg_scales* scales, const uint8_t* sf_scratch, bool cached_maps);
+// Launches the planned GEMM on `stream`: the persistent grid (or one cluster
+// per tile) sized by the variant's co-resident clusters (cached per device),
+// the split-K head if `allow_split` and the options ask for it (it needs a
+// per-stream workspace the library allocates), programmatic dependent launch
+// per TKG_OPT_LAUNCH_OVERLAP.
+tkg_status gemm_enqueue(int kind, const GemmPlan& g, GemmParams& p, void* stream, bool allow_split);
+// TKG_OPT_LAUNCH_OVERLAP is on.
+bool launch_overlap();
 
 // The current device's SM count, after the library's device check (api.cu).
 tkg_status device_sm_count(int* out);

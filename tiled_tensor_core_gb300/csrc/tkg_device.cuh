@@ -248,18 +248,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
   }
 }
 
-// 2-D tiled load, CTA-pair form, written to the same shared-memory offset in
-// every CTA of `mask`; each destination's completion is signalled to the
-// barrier at `bar_cluster`'s offset in that destination's pair leader.
-__device__ __forceinline__ void tma_load_2d_mc_pair(uint32_t dst, const void* tmap, uint32_t bar_cluster, int32_t x,
-                                                    int32_t y, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster.cta_group::2 "
-      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(tmap), "r"(x), "r"(y), "r"(bar_cluster), "h"(mask)
-      : "memory");
-}
-
 __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int32_t x, int32_t y) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(tmap), "r"(src),
                "r"(x), "r"(y)
@@ -355,18 +343,6 @@ __device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr, uint32_t mn_s
   return d;
 }
 
-// Shared-memory descriptor of an unswizzled source of rows of 16 bytes stored
-// back to back (core matrices of 8 rows x 16 B, 128 B apart): the layout of a
-// 32-row x 128-bit tcgen05.cp source.
-__device__ __forceinline__ uint64_t sdesc_plain_rows16(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>(128u >> 4) << 16;
-  d |= static_cast<uint64_t>(128u >> 4) << 32;
-  d |= static_cast<uint64_t>(1u) << 46;
-  return d;
-}
-
 // Instruction descriptor, dense kinds (kind::f16, kind::f8f6f4): D fp32
 // (bits 4-5 = 1), A/B format in bits 7-9 / 10-12, both K-major, N>>3 in bits
 // 17-22, M>>4 in bits 24-28.
@@ -459,16 +435,6 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask) {
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
       "h"(mask)
       : "memory");
-}
-
-// Shared -> TMEM copy of 32 rows x 128 bits, replicated into all four 32-lane
-// sub-partitions (used to stage block-scale factors).
-template <int CG>
-__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
-  if constexpr (CG == 1)
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-  else
-    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // 32 lanes x 32 consecutive fp32 columns: thread i of the warp receives lane

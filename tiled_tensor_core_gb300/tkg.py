@@ -86,7 +86,7 @@ lib.tkg_debug_select_swizzle.argtypes = [ctypes.c_uint32]
 lib.tkg_debug_select_swizzle.restype = ctypes.c_uint32
 lib.tkg_debug_variant_info.argtypes = [_i32, _i32, ctypes.POINTER(ctypes.c_int32)]
 lib.tkg_debug_variant_info.restype = _i32
-lib.tkg_debug_pick_variant.argtypes = [_i32, _i64, _i64, _i64]
+lib.tkg_debug_pick_variant.argtypes = [_i32, _i64, _i64, _i64, _i32]
 lib.tkg_debug_pick_variant.restype = _i32
 lib.tkg_debug_split_plan.argtypes = [_i64, _i64, _i32, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
 lib.tkg_debug_split_plan.restype = _i32
@@ -104,8 +104,6 @@ lib.tkg_quantize_fp8.argtypes = [_i64, _i64, _vp, _vp, _vp, _vp]
 lib.tkg_quantize_fp8.restype = _i32
 lib.tkg_quantize_nvfp4.argtypes = [_i64, _i64, _vp, _vp, _vp, _vp, _vp]
 lib.tkg_quantize_nvfp4.restype = _i32
-lib.tkg_debug_mma_rate.argtypes = [_i32, _i32, _i32, _i32, _i32, ctypes.POINTER(ctypes.c_ulonglong), _vp]
-lib.tkg_debug_mma_rate.restype = _i32
 
 
 def _addr(x) -> int | None:
@@ -219,8 +217,9 @@ def tkg_debug_variant_info(kind, variant):
     return dict(zip(("cta_group", "tile_n", "stages", "epilogue_warps", "threads", "smem_bytes"), list(info)))
 
 
-def tkg_debug_pick_variant(kind, M, N, K) -> int:
-    return int(lib.tkg_debug_pick_variant(kind, M, N, K))
+def tkg_debug_pick_variant(kind, M, N, K, sm_count=0) -> int:
+    """Variant the GEMM of this shape launches on a device of sm_count SMs (0: the current device)."""
+    return int(lib.tkg_debug_pick_variant(kind, M, N, K, sm_count))
 
 
 def tkg_debug_split_plan(tiles, clusters, num_kb):
@@ -272,10 +271,3 @@ def tkg_quantize_nvfp4(rows, cols, x, q_packed, block_scales, global_scale, stre
                                 _stream(stream))
     return _check(st, "tkg_quantize_nvfp4") if check else st
 
-
-def tkg_debug_mma_rate(kind, cta_group, n, count, pattern=0, stream=None) -> int:
-    """SM cycles for `count` back-to-back MMAs (see tkg_debug.h)."""
-    c = ctypes.c_ulonglong(0)
-    _check(lib.tkg_debug_mma_rate(kind, cta_group, n, count, pattern, ctypes.byref(c), _stream(stream)),
-           "tkg_debug_mma_rate")
-    return int(c.value)
