@@ -2,12 +2,22 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl tkg|reference]
 
-A step is one batch of independent GEMMs of the chosen workload (default: the
-bf16 M=N=K=4096 problem), run back to back through the C ABI with operands
-resident in HBM.  Operands rotate over several copies whose total size exceeds
-the 129 MB L2, so every GEMM reads its inputs from HBM.  Rank 0 prints one
-JSON line.  Under torchrun each rank runs its own replica (weak scaling, no
-collective on the data path); the time is the maximum over ranks.
+Default: the GEMM suite.  Every GEMM workload of the study (bf16 256^3, 4096^3,
+8192^3 and 16384x8192x2048, FP8 e4m3 8192^3, NVFP4 16384^3) is measured in
+turn; the JSON line's headline fields are those of the largest, NVFP4
+M=N=K=16384, and `configs` carries one entry per workload with its own value,
+roofline, cpu_baseline, e2e, clocks and parity check.  For each workload a step
+is one batch of independent GEMMs run back to back through the C ABI with
+operands resident in HBM; operands rotate over copies whose total exceeds the
+129 MB L2, so every GEMM reads its inputs from HBM.  After the timed steps the
+output is compared with the CPU oracle on sampled rows at the contract's
+tolerance; a mismatch makes the run exit non-zero.
+
+--workload NAME measures one workload (a GEMM, an input encoder or attention)
+and prints its own line.  Rank 0 prints one JSON line.  Under torchrun each
+rank runs its own replica (weak scaling, no collective on the data path); the
+time is the maximum over ranks.  --gpus N without torchrun relaunches the
+script under torchrun with N processes.
 
 --impl reference times the CPU oracle (the plain C reference) on the host
 cores on a bounded sample of the same workload, with the same metric.
@@ -39,6 +49,9 @@ BATCH = {"bf16_256": 2000, "bf16_4096": 400, "bf16_8192": 60, "bf16_skinny": 100
          "nvfp4_16384": 30, "bf16_4096_k64": 4000, "bf16_4096_k128": 3000, "bf16_4096_k256": 2000,
          "bf16_4096_k512": 1500, "bf16_4096_k1024": 1000}
 SCHEDULE = {"static": 1, "dynamic": 2, "single": 3}
+# the default run: every GEMM workload of the study, headline on the largest
+SUITE = ["bf16_256", "bf16_4096", "bf16_8192", "bf16_skinny", "fp8_8192", "nvfp4_16384"]
+HEADLINE = "nvfp4_16384"
 # dense tensor-core peak relative to bf16 (nominal GB300 ratios: bf16 2.25, fp8 4.5, fp4 13.5 PFLOP/s)
 PEAK_RATIO = {"bf16": 1.0, "fp8": 2.0, "nvfp4": 6.0}
 DTYPE = {"bf16": "bf16", "fp8": "e4m3", "nvfp4": "e2m1+e4m3"}
@@ -78,6 +91,18 @@ def traffic_bytes(workload: str):
     if rec and rec["src"] == kernel_source_hash(files):
         return rec["bytes"]
     return None
+
+
+def algorithmic_bytes(w) -> int:
+    """Minimal HBM bytes of one GEMM: A and B read once (plus, NVFP4, the per-16
+    block scales and the two fp32 tensor scales), C written once."""
+    if w.kind == "bf16":
+        ab = 2 * (w.M + w.N) * w.K
+    elif w.kind == "fp8":
+        ab = (w.M + w.N) * w.K + 8
+    else:
+        ab = (w.M + w.N) * w.K // 2 + (w.M + w.N) * w.K // 16 + 8
+    return ab + 2 * w.M * w.N
 
 
 def load_peaks():
@@ -197,45 +222,60 @@ def oracle_sample(ops, target_s: float):
     return 2.0 * n_rows * N * K / dt / 1e12, dt, n_rows, threads
 
 
-# ---------------------------------------------------------------- reference arm
+# ---------------------------------------------------------------- parity gate
 
-def run_reference_encoder(args):
-    """The oracle's encoder, as it stands, on a row sample of the same tensor per step."""
+# Tolerances of the GEMM contract: bf16 output against the oracle's bf16 output
+# (relative Frobenius <= 1e-3, |delta| <= 1e-2 (|ref| + 1) elementwise); FP8 /
+# NVFP4 against the oracle's fp32 accumulation of the same decoded values times
+# the per-tensor scales (relative Frobenius <= 2e-3).
+BF16_REL_FRO, BF16_ELEM, SCALED_REL_FRO = 1e-3, 1e-2, 2e-3
+PARITY_ROWS = 32
+
+
+def parity_rows(M: int, seed: int) -> np.ndarray:
+    """At least PARITY_ROWS rows: the edges of 128-row CTA tiles and 256-row pair
+    tiles, every 32-row TMEM lane quarter of the first tile, the last rows, and
+    seeded random rows."""
+    fixed = [0, 1, 31, 32, 63, 64, 95, 96, 127, 128, 159, 160, 191, 192, 223, 224, 255, 256, 383, 511,
+             M // 2, M // 2 + 127, M - 129, M - 128, M - 2, M - 1]
+    rows = sorted({r for r in fixed if 0 <= r < M})
+    rng = np.random.default_rng(seed)
+    while len(rows) < min(M, PARITY_ROWS + 8):
+        rows = sorted(set(rows) | {int(r) for r in rng.integers(0, M, size=8)})
+    return np.array(rows, dtype=np.int64)
+
+
+def parity_check(ops, c_rows_bits: np.ndarray, rows: np.ndarray) -> dict:
+    """Compare sampled output rows (bf16 bits) with the oracle at the contract tolerance."""
     import oracle
+    acc, c_ref = oracle.gemm(ops, rows=rows)
+    to64 = lambda b: (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)  # noqa: E731
+    got = to64(c_rows_bits)
+    out = {"rows": int(len(rows)), "finite": bool(np.isfinite(got).all())}
+    if ops.kind == "bf16":
+        ref = to64(c_ref)
+        out["rel_fro"] = float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300))
+        out["max_elem"] = float((np.abs(got - ref) / (np.abs(ref) + 1.0)).max())
+        out["tol"] = {"rel_fro": BF16_REL_FRO, "elem": BF16_ELEM, "against": "oracle bf16 output"}
+        out["pass"] = out["finite"] and out["rel_fro"] <= BF16_REL_FRO and out["max_elem"] <= BF16_ELEM
+    else:
+        ref = acc.astype(np.float64) * ops.scale_a * ops.scale_b
+        out["rel_fro"] = float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300))
+        out["tol"] = {"rel_fro": SCALED_REL_FRO, "against": "oracle fp32 accumulation x scales"}
+        out["pass"] = out["finite"] and out["rel_fro"] <= SCALED_REL_FRO
+    return out
 
-    kind, rows, cols, seed = ENCODERS[args.workload]
-    r = max(16, min(rows, int(rows * min(1.0, args.ref_step_s / 10.0))))
-    xs = synth.draw_fp32(seed, r, cols, "normal")
-    fn = oracle.quantize_fp8 if kind == "fp8" else oracle.quantize_nvfp4
-    nb = 2 * 4 * r * cols + (r * cols if kind == "fp8" else r * cols // 2 + r * cols // 16)
-    for _ in range(args.warmup):
-        fn(xs[:16])
-    times = []
-    for _ in range(args.steps):
-        t = time.perf_counter()
-        fn(xs)
-        times.append(time.perf_counter() - t)
-    value = nb * args.steps / sum(times) / 1e9
-    line = {"metric": "encoder GB/s (algorithmic bytes: 2 reads of fp32 x + encoded output, / time)",
-            "value": value, "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1e3 * sum(times) / args.steps, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32", "data": "synthetic", "impl": "reference",
-            "config": {"workload": f"{kind} encoder of an fp32 [{rows}][{cols}] N(0,1) tensor", "rows": rows,
-                       "cols": cols},
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{r} of {rows} rows per step"},
-            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    print(json.dumps(line), flush=True)
-    return 0
 
+# ---------------------------------------------------------------- reference arm
 
 def run_reference(args, world, rank):
     if rank != 0:
         return 0
     if args.workload in ENCODERS:
         return run_reference_encoder(args)
-    w = synth.WORKLOADS[args.workload]
-    ops = synth.workload_operands(args.workload)
+    name = args.workload or HEADLINE
+    w = synth.WORKLOADS[name]
+    ops = synth.workload_operands(name)
     for _ in range(args.warmup):
         oracle_sample(ops, 0.1)
     times = []
@@ -263,24 +303,26 @@ def run_reference(args, world, rank):
 
 # ---------------------------------------------------------------- GPU arm
 
-def run_tkg(args, world, rank, local):
-    import torch
-    from tiled_tensor_core_gb300 import tkg
-    from tiled_tensor_core_gb300.device import DeviceGemm
-
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if args.variant:
-        tkg.tkg_set_option(tkg.TKG_OPT_VARIANT, args.variant)
-    if args.group_m:
-        tkg.tkg_set_option(tkg.TKG_OPT_GROUP_M, args.group_m)
+def set_options(tkg, args):
+    tkg.tkg_set_option(tkg.TKG_OPT_VARIANT, args.variant)
+    tkg.tkg_set_option(tkg.TKG_OPT_GROUP_M, args.group_m)
     tkg.tkg_set_option(tkg.TKG_OPT_SCHEDULE, SCHEDULE[args.schedule])
     tkg.tkg_set_option(tkg.TKG_OPT_LAUNCH_OVERLAP,
                        tkg.TKG_OVERLAP_ON if args.overlap == "on" else tkg.TKG_OVERLAP_OFF)
     tkg.tkg_set_option(tkg.TKG_OPT_SPLIT_K, tkg.TKG_SPLIT_ON if args.split == "on" else tkg.TKG_SPLIT_OFF)
 
-    w = synth.WORKLOADS[args.workload]
-    ops = synth.workload_operands(args.workload)
+
+def measure_gemm(name, args, world, rank, local, cpu_s):
+    """Warm-up, timed steps, parity gate, e2e, cuBLAS context and oracle timing of one
+    GEMM workload.  Returns its entry (a dict); entry["parity"]["pass"] is False on a
+    mismatch with the oracle."""
+    import torch
+    from tiled_tensor_core_gb300 import tkg
+    from tiled_tensor_core_gb300.device import DeviceGemm
+
+    dev = torch.device("cuda", local)
+    w = synth.WORKLOADS[name]
+    ops = synth.workload_operands(name)
     base = DeviceGemm(ops, dev)
     footprint = base.input_bytes() + base.output_bytes()
     n_sets = 1 if footprint >= 2 * L2_BYTES else min(16, math.ceil(4 * L2_BYTES / footprint))
@@ -295,7 +337,7 @@ def run_tkg(args, world, rank, local):
             g.scale_a, g.scale_b = base.scale_a.clone(), base.scale_b.clone()
         g.c = torch.empty_like(base.c)
         sets.append(g)
-    batch = args.batch or BATCH[args.workload]
+    batch = args.batch or BATCH[name]
     stream = torch.cuda.Stream(device=dev)
     sptr = int(stream.cuda_stream)
     launches_per_gemm = 2 if w.kind == "nvfp4" else 1
@@ -309,12 +351,14 @@ def run_tkg(args, world, rank, local):
             if events is not None:
                 events[2 * i + 1].record(stream)
 
+    for g in sets:
+        g.c.fill_(float("nan"))
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             step()
     st = tkg.tkg_check_status(sptr)
     if st != tkg.TKG_OK:
-        raise RuntimeError(f"warm-up failed: {tkg.status_string(st)}")
+        raise RuntimeError(f"{name}: warm-up failed: {tkg.status_string(st)}")
 
     # Launch-bound workloads replay the step from a CUDA graph (captured after the
     # warm-up, so every lazy set-up is done); the GEMM launches are unchanged.
@@ -329,20 +373,12 @@ def run_tkg(args, world, rank, local):
                 graph.replay()
         torch.cuda.synchronize(dev)
 
-    # correctness spot check of the last warm-up output against the oracle (cheap: a few rows)
-    spot = None
-    if rank == 0 and not args.no_check:
-        import oracle
-        rows = np.array([0, ops.M // 2, ops.M - 1], dtype=np.int64)
-        acc, c_ref = oracle.gemm(ops, rows=rows)
-        got = sets[(batch - 1) % n_sets].c[torch.from_numpy(rows).to(dev)].view(torch.int16).cpu().numpy()
-        got = (got.view(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-        ref = acc.astype(np.float64) * ops.scale_a * ops.scale_b
-        spot = float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
-
     step_ms, kern_ms, host_ms = [], [], []
     sampler = ClockSampler(local)
     barrier(world)
+    torch.cuda.synchronize(dev)
+    for g in sets:  # the parity check below reads outputs written inside the timed region
+        g.c.fill_(float("nan"))
     torch.cuda.synchronize(dev)
     sampler.start()
     time.sleep(0.3)  # let the sampler take its first reading
@@ -356,33 +392,34 @@ def run_tkg(args, world, rank, local):
     launch_ev = ([[torch.cuda.Event(enable_timing=True) for _ in range(2 * batch)] for _ in range(args.steps)]
                  if per_launch else None)
     t_start.record(stream)
-    for s in range(args.steps):
-        step_ev[s][0].record(stream)
+    for s_ in range(args.steps):
+        step_ev[s_][0].record(stream)
         h0 = time.perf_counter()
         if graph is not None:
             with torch.cuda.stream(stream):
                 graph.replay()
         else:
             # an event between two launches would end their overlap: with it on, the step is timed whole
-            step(launch_ev[s] if per_launch else None)
+            step(launch_ev[s_] if per_launch else None)
         host_ms.append((time.perf_counter() - h0) * 1e3)
-        step_ev[s][1].record(stream)
+        step_ev[s_][1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
-    for s in range(args.steps):
-        step_ms.append(step_ev[s][0].elapsed_time(step_ev[s][1]))
+    for s_ in range(args.steps):
+        step_ms.append(step_ev[s_][0].elapsed_time(step_ev[s_][1]))
         if per_launch:
-            kern_ms.extend(launch_ev[s][2 * i].elapsed_time(launch_ev[s][2 * i + 1]) for i in range(batch))
+            kern_ms.extend(launch_ev[s_][2 * i].elapsed_time(launch_ev[s_][2 * i + 1]) for i in range(batch))
         else:
             # no per-launch events (inside a graph, or between overlapped launches): the step is
-            # nothing but GEMM launches, so spread its time over them
+            # nothing but GEMM launches (and, NVFP4, the scale re-layout before each), so spread its
+            # time over the GEMMs
             kern_ms.extend([step_ms[-1] / batch] * batch)
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
     barrier(world)
     st = tkg.tkg_check_status(sptr)
     if st != tkg.TKG_OK:
-        raise RuntimeError(f"timed run failed: {tkg.status_string(st)}")
+        raise RuntimeError(f"{name}: timed run failed: {tkg.status_string(st)}")
     total_ms = t_start.elapsed_time(t_end)
     total_ms = max_over_ranks(total_ms, world, dev)
     gemms = args.steps * batch
@@ -390,7 +427,12 @@ def run_tkg(args, world, rank, local):
     kern_avg_ms = sum(kern_ms) / len(kern_ms)
     achieved = w.flops / (kern_avg_ms * 1e-3) / 1e12
 
-    # end to end through the public API: pinned host inputs -> device, GEMM, result -> host
+    # parity gate on every rank: sampled rows of an output written by the timed steps
+    rows = parity_rows(w.M, seed=w.M + w.N + w.K)
+    last = sets[(gemms - 1) % n_sets] if graph is None else sets[(batch - 1) % n_sets]
+    c_rows = last.c[torch.from_numpy(rows).to(dev)].view(torch.int16).cpu().numpy().view(np.uint16)
+    parity = parity_check(ops, c_rows, rows) if not args.no_check else {"skipped": True, "pass": True}
+
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(ops, dev, w, args)
@@ -403,51 +445,90 @@ def run_tkg(args, world, rank, local):
             cublas["ours_over_cublas"] = value / world / cublas["value"]
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, dt, n_rows, threads = oracle_sample(ops, args.cpu_s)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and cpu_s > 0:
+        v, dt, n_rows, threads = oracle_sample(ops, cpu_s)
         cpu = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": f"{n_rows} of {w.M} output rows of the same workload ({dt:.1f} s)"}
 
     peaks = load_peaks()
-    # The timed region is a long back-to-back run (power-capped regime): the sustained
-    # measured bf16 figure is the matching denominator; the burst one is reported too.
-    peak = peaks["bf16_tflops_sustained"] * PEAK_RATIO[w.kind]
+    # Denominators: the measured bf16 peak x the nominal dtype ratio.  The timed region is about a
+    # second of back-to-back launches: `frac` uses the burst figure (the lower fraction), and the
+    # fraction of the sustained (power-capped, seconds-long) figure is given beside it.
     peak_burst = peaks["bf16_tflops"] * PEAK_RATIO[w.kind]
-    info = tkg.tkg_debug_variant_info({"bf16": 0, "fp8": 1, "nvfp4": 2}[w.kind],
-                                      tkg.tkg_debug_pick_variant({"bf16": 0, "fp8": 1, "nvfp4": 2}[w.kind],
-                                                                 w.M, w.N, w.K))
-    line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": DTYPE[w.kind], "data": "synthetic",
-        "config": {"workload": w.description, "M": w.M, "N": w.N, "K": w.K, "gemms_per_step": batch,
-                   "global_batch": batch * world, "parallelism": f"replicas{world}",
-                   "l2": (f"{n_sets} rotating operand sets, {n_sets * footprint / 2**20:.0f} MiB > 129 MiB L2"
-                          if n_sets > 1 else f"operands {footprint / 2**20:.0f} MiB > 129 MiB L2"),
-                   "kernel": info, "group_m": tkg.tkg_get_option(tkg.TKG_OPT_GROUP_M),
-                   "schedule": args.schedule, "split_k_tail": args.split,
-                   "launch_overlap": "programmatic dependent launch" if args.overlap == "on" else "off",
-                   "cuda_graph": graph is not None},
-        "pct_of_peak": 100.0 * value / world / peak,
-        "pct_of_burst_peak": 100.0 * value / world / peak_burst,
+    peak_sust = peaks["bf16_tflops_sustained"] * PEAK_RATIO[w.kind]
+    kid = {"bf16": 0, "fp8": 1, "nvfp4": 2}[w.kind]
+    info = tkg.tkg_debug_variant_info(kid, tkg.tkg_debug_pick_variant(kid, w.M, w.N, w.K))
+    alg_bytes = algorithmic_bytes(w)
+    entry = {
+        "workload": name, "description": w.description, "M": w.M, "N": w.N, "K": w.K, "dtype": DTYPE[w.kind],
+        "value": value, "unit": "TFLOP/s", "ms_per_step": total_ms / args.steps, "gemms_per_step": batch,
         "median_gemm_ms": statistics.median(kern_ms),
-        "host_enqueue_ms_per_step": statistics.median(host_ms),
         "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms)},
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": traffic_bytes(w.name),
-                     "frac_of_burst_peak": achieved / peak_burst,
-                     "peak_source": (f"{peaks['source']} bf16 sustained (back-to-back cuBLAS) x "
-                                     f"{PEAK_RATIO[w.kind]:g} (nominal dtype ratio)")},
-        "cpu_baseline": cpu,
-        "e2e": e2e,
-        "cublas": cublas,
+        "host_enqueue_ms_per_step": statistics.median(host_ms),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_burst, "unit": "TFLOP/s",
+                     "frac": achieved / peak_burst, "traffic": traffic_bytes(name),
+                     "algorithmic_bytes": alg_bytes,
+                     "peak_sustained": peak_sust, "frac_of_sustained_peak": achieved / peak_sust,
+                     "peak_source": (f"{peaks['source']} bf16 burst (cuBLAS) x {PEAK_RATIO[w.kind]:g} "
+                                     "(nominal dtype ratio); sustained beside it")},
+        "achieved_hbm_gbs_algorithmic": alg_bytes / (kern_avg_ms * 1e-3) / 1e9,
+        "cpu_baseline": cpu, "e2e": e2e, "cublas": cublas, "clocks": clocks, "parity": parity,
         "gpu_launches": gemms * launches_per_gemm,
-        "clocks": clocks,
-        "spot_check_rel_err": spot,
+        "kernel": info,
+        "l2": (f"{n_sets} rotating operand sets, {n_sets * footprint / 2**20:.0f} MiB > 129 MiB L2"
+               if n_sets > 1 else f"operands {footprint / 2**20:.0f} MiB > 129 MiB L2"),
+        "cuda_graph": graph is not None,
     }
+    del sets, base
+    torch.cuda.empty_cache()
+    return entry
+
+
+def line_from_entry(e, args, world, extra_config=None):
+    """The contract's JSON line for one measured GEMM entry."""
+    w = synth.WORKLOADS[e["workload"]]
+    config = {"workload": w.description, "M": w.M, "N": w.N, "K": w.K, "gemms_per_step": e["gemms_per_step"],
+              "global_batch": e["gemms_per_step"] * world, "parallelism": f"replicas{world}", "l2": e["l2"],
+              "kernel": e["kernel"], "group_m": args.group_m or 8, "schedule": args.schedule,
+              "split_k_tail": args.split,
+              "launch_overlap": "programmatic dependent launch" if args.overlap == "on" else "off",
+              "cuda_graph": e["cuda_graph"]}
+    if extra_config:
+        config.update(extra_config)
+    return {
+        "metric": METRIC, "value": e["value"], "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": e["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": e["dtype"], "data": "synthetic", "config": config,
+        "roofline": e["roofline"], "cpu_baseline": e["cpu_baseline"], "e2e": e["e2e"],
+        "gpu_launches": e["gpu_launches"], "clocks": e["clocks"], "parity": e["parity"],
+        "median_gemm_ms": e["median_gemm_ms"], "step_ms": e["step_ms"],
+        "host_enqueue_ms_per_step": e["host_enqueue_ms_per_step"], "cublas": e["cublas"],
+    }
+
+
+def run_tkg(args, world, rank, local):
+    import torch
+    from tiled_tensor_core_gb300 import tkg
+
+    torch.cuda.set_device(local)
+    set_options(tkg, args)
+    if args.workload:
+        e = measure_gemm(args.workload, args, world, rank, local, args.cpu_s)
+        if rank == 0:
+            print(json.dumps(line_from_entry(e, args, world)), flush=True)
+        return 0 if e["parity"]["pass"] else 3
+    entries = []
+    for name in SUITE:
+        cpu_s = args.cpu_s if name == HEADLINE else args.cpu_s_other
+        entries.append(measure_gemm(name, args, world, rank, local, cpu_s))
+    head = next(e for e in entries if e["workload"] == HEADLINE)
+    line = line_from_entry(head, args, world, {"suite": SUITE, "headline": HEADLINE})
+    line["configs"] = entries
+    line["gpu_launches_all_configs"] = sum(e["gpu_launches"] for e in entries)
+    line["parity_all_pass"] = all(e["parity"]["pass"] for e in entries)
     if rank == 0:
         print(json.dumps(line), flush=True)
-    return 0
+    return 0 if line["parity_all_pass"] else 3
 
 
 # ---------------------------------------------------------------- input encoders
@@ -849,23 +930,39 @@ def run_attention(args, world, rank, local):
     return 0
 
 
+def relaunch_under_torchrun(n: int, argv) -> int:
+    """--gpus N without torchrun: run this script under torchrun with N processes
+    (one replica per GPU; rank 0 prints the line)."""
+    import socket
+    with socket.socket() as sock:
+        sock.bind(("127.0.0.1", 0))
+        port = sock.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd)
+
+
 def main(argv=None):
+    argv = list(sys.argv[1:] if argv is None else argv)
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["tkg", "reference"], default="tkg")
     p.add_argument("--workload", choices=sorted(synth.WORKLOADS) + sorted(ENCODERS) + sorted(synth.ATTN_WORKLOADS),
-                   default="bf16_4096")
+                   default=None, help="one workload (default: the GEMM suite, headline NVFP4 16384^3)")
     p.add_argument("--batch", type=int, default=0, help="GEMMs per step (default: per workload)")
     p.add_argument("--variant", type=int, default=0)
     p.add_argument("--group-m", type=int, default=0)
     p.add_argument("--e2e-steps", type=int, default=10)
-    p.add_argument("--cpu-s", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
+    p.add_argument("--cpu-s", type=float, default=20.0,
+                   help="seconds of oracle work for the headline's (or --workload's) cpu_baseline")
+    p.add_argument("--cpu-s-other", type=float, default=2.0,
+                   help="seconds of oracle work for each other suite workload's cpu_baseline")
     p.add_argument("--ref-step-s", type=float, default=3.0, help="seconds of oracle work per reference step")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--no-check", action="store_true")
+    p.add_argument("--no-check", action="store_true", help="skip the parity gate (never for a reported number)")
     p.add_argument("--no-cublas", action="store_true", help="skip the cuBLAS comparison (bf16 / FP8 workloads)")
     p.add_argument("--graph", choices=["auto", "on", "off"], default="auto",
                    help="replay each step from a CUDA graph (auto: launch-bound workloads)")
@@ -877,12 +974,17 @@ def main(argv=None):
                    help="split the tiles of a persistent grid's last, at most half-full round along K")
     args = p.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    world_env = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        return relaunch_under_torchrun(args.gpus, argv)
+    if args.gpus != world_env:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world_env}; launch one process per GPU", file=sys.stderr)
+        return 2
     if args.impl == "reference":
-        world = int(os.environ.get("WORLD_SIZE", "1"))
         rank = int(os.environ.get("RANK", "0"))
         if args.workload in synth.ATTN_WORKLOADS:
             return run_reference_attention(args) if rank == 0 else 0
-        return run_reference(args, world, rank)
+        return run_reference(args, world_env, rank)
     world, rank, local = dist_setup(args)
     if args.workload in ENCODERS:
         return run_encoder(args, world, rank, local)

@@ -65,3 +65,22 @@ def test_reference_arm_prints_on_rank_zero_only():
     assert line["impl"] == "reference" and line["value"] > 0
     for key in ("metric", "unit", "n_gpus", "steps", "warmup", "cpu_baseline", "e2e", "config"):
         assert key in line
+
+
+def test_gpus_flag_relaunches_one_process_per_replica():
+    # --gpus 2 outside torchrun: the script relaunches itself under torchrun with two ranks
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+                        "--workload", "bf16_256", "--steps", "1", "--warmup", "3", "--ref-step-s", "0.05"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [json.loads(ln) for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1 and lines[0]["n_gpus"] == 2
+
+
+def test_gpus_flag_disagreeing_with_the_launcher_is_refused():
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+                        "--workload", "bf16_256", "--steps", "1"], cwd=ROOT, env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 2 and "WORLD_SIZE" in r.stderr
