@@ -310,6 +310,8 @@ def set_options(tkg, args):
     tkg.tkg_set_option(tkg.TKG_OPT_LAUNCH_OVERLAP,
                        tkg.TKG_OVERLAP_ON if args.overlap == "on" else tkg.TKG_OVERLAP_OFF)
     tkg.tkg_set_option(tkg.TKG_OPT_SPLIT_K, tkg.TKG_SPLIT_ON if args.split == "on" else tkg.TKG_SPLIT_OFF)
+    tkg.tkg_set_option(tkg.TKG_OPT_K_ORDER,
+                       tkg.TKG_K_ORDER_SERPENTINE if args.k_order == "serpentine" else tkg.TKG_K_ORDER_FORWARD)
 
 
 def measure_gemm(name, args, world, rank, local, cpu_s):
@@ -484,13 +486,18 @@ def measure_gemm(name, args, world, rank, local, cpu_s):
     return entry
 
 
+def tkg_group_m() -> int:
+    from tiled_tensor_core_gb300 import tkg
+    return int(tkg.tkg_get_option(tkg.TKG_OPT_GROUP_M))
+
+
 def line_from_entry(e, args, world, extra_config=None):
     """The contract's JSON line for one measured GEMM entry."""
     w = synth.WORKLOADS[e["workload"]]
     config = {"workload": w.description, "M": w.M, "N": w.N, "K": w.K, "gemms_per_step": e["gemms_per_step"],
               "global_batch": e["gemms_per_step"] * world, "parallelism": f"replicas{world}", "l2": e["l2"],
-              "kernel": e["kernel"], "group_m": args.group_m or 8, "schedule": args.schedule,
-              "split_k_tail": args.split,
+              "kernel": e["kernel"], "group_m": tkg_group_m(), "schedule": args.schedule,
+              "split_k_tail": args.split, "k_order": args.k_order,
               "launch_overlap": "programmatic dependent launch" if args.overlap == "on" else "off",
               "cuda_graph": e["cuda_graph"]}
     if extra_config:
@@ -972,6 +979,8 @@ def main(argv=None):
                    help="launch GEMMs as programmatic dependents of the previous kernel (on) or plainly (off)")
     p.add_argument("--split", choices=["on", "off"], default="on",
                    help="split the tiles of a persistent grid's last, at most half-full round along K")
+    p.add_argument("--k-order", choices=["serpentine", "forward"], default="serpentine",
+                   help="K walk of a CTA's odd-numbered tiles: from the last K block down (serpentine) or up")
     args = p.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     world_env = int(os.environ.get("WORLD_SIZE", "1"))

@@ -201,8 +201,10 @@ TKG_API void tkg_shutdown(void);
  * default.  Returns TKG_ERR_INVALID_ARG for an unknown key or bad value.
  *  TKG_OPT_TIMEOUT_NS  limit for any single pipeline wait on the device (default 2 s)
  *  TKG_OPT_GROUP_M     super-group height in output tiles for the L2-aware
- *                      tile order (default 8; the paper's {8, N, M/8} order,
- *                      "Block Launch Order and L2 Cache Reuse", Table 3)
+ *                      tile order (default 16: the {G, N, M/G} order of
+ *                      "Block Launch Order and L2 Cache Reuse", Table 3,
+ *                      where the paper takes G = 8; 16 reads the least
+ *                      from HBM on GB300 with 256-row pair tiles)
  *  TKG_OPT_VARIANT     force a kernel variant: 0 = the default (8 for
  *                      NVFP4; for bf16 and FP8 13 when K >= 4096 and the
  *                      256x512 tiles fill at least four rounds of the
@@ -213,7 +215,9 @@ TKG_API void tkg_shutdown(void);
  *                      ring's TMA and written to tensor memory by eight
  *                      scale warps (NVFP4); 13 = 2-SM 256x512 tiles, two
  *                      N = 256 MMAs per K step into all 512 tensor-memory
- *                      columns (bf16 and FP8; no split-K head).  A variant
+ *                      columns, the second reusing A from the tensor
+ *                      core's collector buffer (bf16 and FP8; no split-K
+ *                      head).  A variant
  *                      the kind lacks falls back to the default.
  *  TKG_OPT_MAX_CTAS    cap the persistent grid size (0 = all SMs)
  *  TKG_OPT_LAUNCH_OVERLAP
@@ -254,7 +258,14 @@ TKG_API void tkg_shutdown(void);
  *                      pairs.  Not used with the 256x512 tile (variant
  *                      13).  TKG_SPLIT_OFF: whole tiles only.  After a launch reports TKG_ERR_TIMEOUT,
  *                      tkg_check_status frees the workspaces (they are made
- *                      afresh on next use). */
+ *                      afresh on next use).
+ *  TKG_OPT_K_ORDER     TKG_K_ORDER_SERPENTINE (default): each CTA (pair)
+ *                      walks the K blocks of its odd-numbered work items
+ *                      from the last one down, so that a round of tiles
+ *                      starts on the ends of the operand panels the
+ *                      previous round read last, which are still in L2;
+ *                      TKG_K_ORDER_FORWARD: every item from K block 0 up.
+ *                      Only the fp32 summation order changes. */
 typedef enum tkg_option {
     TKG_OPT_TIMEOUT_NS = 1,
     TKG_OPT_GROUP_M = 2,
@@ -262,7 +273,8 @@ typedef enum tkg_option {
     TKG_OPT_MAX_CTAS = 4,
     TKG_OPT_LAUNCH_OVERLAP = 5,
     TKG_OPT_SCHEDULE = 6,
-    TKG_OPT_SPLIT_K = 7
+    TKG_OPT_SPLIT_K = 7,
+    TKG_OPT_K_ORDER = 8
 } tkg_option;
 
 /* Values of TKG_OPT_LAUNCH_OVERLAP and TKG_OPT_SCHEDULE. */
@@ -273,6 +285,8 @@ typedef enum tkg_option {
 #define TKG_SCHEDULE_SINGLE 3
 #define TKG_SPLIT_ON 1
 #define TKG_SPLIT_OFF 2
+#define TKG_K_ORDER_SERPENTINE 1
+#define TKG_K_ORDER_FORWARD 2
 TKG_API tkg_status tkg_set_option(tkg_option key, int64_t value);
 TKG_API int64_t tkg_get_option(tkg_option key);
 

@@ -98,16 +98,26 @@ def test_misaligned_pointers_rejected(tkg):
 
 
 def test_options_roundtrip(tkg):
-    assert tkg.tkg_get_option(tkg.TKG_OPT_GROUP_M) == 8
+    assert tkg.tkg_get_option(tkg.TKG_OPT_GROUP_M) == 16
     tkg.tkg_set_option(tkg.TKG_OPT_GROUP_M, 12)
     assert tkg.tkg_get_option(tkg.TKG_OPT_GROUP_M) == 12
     tkg.tkg_set_option(tkg.TKG_OPT_GROUP_M, 0)
-    assert tkg.tkg_get_option(tkg.TKG_OPT_GROUP_M) == 8
+    assert tkg.tkg_get_option(tkg.TKG_OPT_GROUP_M) == 16
     assert tkg.tkg_get_option(tkg.TKG_OPT_TIMEOUT_NS) == 2_000_000_000
     with pytest.raises(tkg.TkgError):
         tkg.tkg_set_option(tkg.TKG_OPT_VARIANT, 99)
     with pytest.raises(tkg.TkgError):
         tkg.tkg_set_option(77, 1)
+
+
+def test_k_order_option(tkg):
+    assert tkg.tkg_get_option(tkg.TKG_OPT_K_ORDER) == tkg.TKG_K_ORDER_SERPENTINE
+    tkg.tkg_set_option(tkg.TKG_OPT_K_ORDER, tkg.TKG_K_ORDER_FORWARD)
+    assert tkg.tkg_get_option(tkg.TKG_OPT_K_ORDER) == tkg.TKG_K_ORDER_FORWARD
+    tkg.tkg_set_option(tkg.TKG_OPT_K_ORDER, 0)
+    assert tkg.tkg_get_option(tkg.TKG_OPT_K_ORDER) == tkg.TKG_K_ORDER_SERPENTINE
+    with pytest.raises(tkg.TkgError):
+        tkg.tkg_set_option(tkg.TKG_OPT_K_ORDER, 3)
 
 
 def test_schedule_and_overlap_options(tkg):

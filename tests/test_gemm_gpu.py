@@ -32,8 +32,9 @@ def variant(tkg, request):
     tkg.tkg_set_option(tkg.TKG_OPT_VARIANT, 0)
 
 
-# the compiled variants of each kind: 256x256 and 256x512 pair tiles (bf16 / FP8), the
-# block-scaled 256x256 pair tile (NVFP4)
+# the compiled variants of each kind: 256x256 and 256x512 pair tiles (bf16 / FP8; the latter with
+# its K step's two MMAs sharing A through the collector buffer), the block-scaled 256x256 pair
+# tile (NVFP4)
 KIND_VARIANTS = {"bf16": [2, 13], "fp8": [2, 13], "nvfp4": [8]}
 KIND_VARIANT_PAIRS = [(k, v) for k, vs in KIND_VARIANTS.items() for v in vs]
 
@@ -144,3 +145,30 @@ def test_nvfp4_repeated_calls_reuse_scratch(tkg):
         g = run_gpu(ops)
         acc, c_ref = oracle.gemm(ops)
         check_against_oracle("nvfp4", g.c_bits(), acc, c_ref, ops.scale_a, ops.scale_b)
+
+
+# ---- K order of a CTA's work items -------------------------------------------
+
+@pytest.mark.parametrize("order", ["serpentine", "forward"])
+@pytest.mark.parametrize("kind,variant", [("bf16", 2), ("bf16", 13), ("fp8", 13), ("nvfp4", 8)])
+def test_k_order_keeps_results(tkg, kind, variant, order):
+    """Two CTA pairs walk many tiles each, so half of every pair's tiles run their K blocks
+    backwards in the serpentine order: exact on small integers, and within tolerance."""
+    tkg.tkg_set_option(tkg.TKG_OPT_VARIANT, variant)
+    tkg.tkg_set_option(tkg.TKG_OPT_K_ORDER,
+                       tkg.TKG_K_ORDER_SERPENTINE if order == "serpentine" else tkg.TKG_K_ORDER_FORWARD)
+    tkg.tkg_set_option(tkg.TKG_OPT_MAX_CTAS, 4)
+    try:
+        M, N, K = 1280, 1536, {"bf16": 640, "fp8": 768, "nvfp4": 1536}[kind]
+        ops = synth.small_int_operands(kind, M, N, K, seed=K)
+        g = run_gpu(ops)
+        _, c_ref = oracle.gemm(ops)
+        assert np.array_equal(g.c_bits(), c_ref)
+        ops = synth.make_operands(kind, M, N, K, "normal_sqrtk" if kind == "bf16" else "normal", 12, 13)
+        g = run_gpu(ops)
+        acc, c_ref = oracle.gemm(ops)
+        check_against_oracle(kind, g.c_bits(), acc, c_ref, ops.scale_a, ops.scale_b)
+    finally:
+        tkg.tkg_set_option(tkg.TKG_OPT_MAX_CTAS, 0)
+        tkg.tkg_set_option(tkg.TKG_OPT_K_ORDER, 0)
+        tkg.tkg_set_option(tkg.TKG_OPT_VARIANT, 0)

@@ -8,11 +8,11 @@
 namespace tkg {
 
 using Fp8_2Sm_256 = GemmCfg<Kind::FP8, 2, 256, 6, 4>;
-using Fp8_2Sm_512 = GemmCfg<Kind::FP8, 2, 512, 4, 4, 1>;
+using Fp8_2Sm_512 = GemmCfg<Kind::FP8, 2, 512, 4, 4, 1, 2, true>;
 
 const KernelVariant* fp8_variant(int id) {
   static const KernelVariant v2 = make_variant<Fp8_2Sm_256>("fp8_2sm_256x256_s6");
-  static const KernelVariant v13 = make_variant<Fp8_2Sm_512>("fp8_2sm_256x512_s4");
+  static const KernelVariant v13 = make_variant<Fp8_2Sm_512>("fp8_2sm_256x512_s4_colla");
   switch (id) {
     case kVariant2Sm256x256: return &v2;
     case kVariant2Sm256x512: return &v13;

@@ -65,6 +65,7 @@ struct GemmParams {
   int split_s;
   float* split_ws;            // fp32 partial accumulators, one block per (piece, CTA, epilogue warp)
   unsigned int* split_cnt;    // per (split tile, CTA, epilogue warp): {pieces written, pieces done}
+  int k_serpentine;           // 1: a CTA's odd-numbered work items walk their K blocks from the last one down
 };
 
 // Tile schedules ("Persistent Grid Launch"; Cluster Launch Control for the
@@ -122,7 +123,8 @@ __host__ __device__ inline WorkItem work_item(int w, int split_tiles, int split_
 // once per stage and the tensor pipe only runs MMAs (copying the scales with
 // tcgen05.cp instead costs the tensor pipe about 60 cycles per copy, twelve
 // copies per stage of a 256 x 256 tile).
-template <Kind KIND_, int CG_, int BN_, int STAGES_, int EPI_WARPS_, int NUM_ACC_ = 2, int SF_GROUPS_ = 2>
+template <Kind KIND_, int CG_, int BN_, int STAGES_, int EPI_WARPS_, int NUM_ACC_ = 2, int SF_GROUPS_ = 2,
+          bool COLL_A_ = false>
 struct GemmCfg {
   static constexpr Kind KIND = KIND_;
   static constexpr int CG = CG_;                // CTAs per MMA (1, or 2 for the CTA pair) = CTAs per cluster
@@ -144,6 +146,9 @@ struct GemmCfg {
   static constexpr int NSUB = BN > 256 ? BN / 256 : 1;
   static constexpr int MMA_N = BN / NSUB;
   static constexpr int B_SUB_ROWS = B_ROWS / NSUB;
+  // 512-wide tiles: the K step's two MMAs share A; with COLL_A the first keeps A in the tensor
+  // core's collector buffer and the second takes it from there instead of shared memory
+  static constexpr bool COLL_A = COLL_A_;
   static constexpr int A_STAGE = BM * ROW_BYTES;
   static constexpr int B_BOX = B_ROWS * ROW_BYTES;             // bytes of one B tile load
   static constexpr int B_STAGE = (B_BOX + 1023) / 1024 * 1024;  // keeps every stage 1024-byte aligned
@@ -203,7 +208,8 @@ struct GemmCfg {
   static_assert(B_STAGE % 1024 == 0 && A_STAGE % 1024 == 0, "stages must keep 1024-byte swizzle atoms aligned");
   static_assert((OFF_SFA % 1024) == 0 && (OFF_EPI % 1024) == 0, "region alignment");
   static_assert(BN % 32 == 0 && BN >= 64 && (BN <= 256 || BN == 512), "BN: a multiple of 32 in [64,256], or 512");
-  static_assert(NSUB == 1 || (!SCALED && NUM_ACC == 1 && CG == 2), "512-wide tiles: bf16 / FP8 pairs");
+  static_assert(NSUB == 1 || (NSUB == 2 && !SCALED && NUM_ACC == 1 && CG == 2), "512-wide tiles: bf16 / FP8 pairs");
+  static_assert(!COLL_A || NSUB == 2, "the A collector is shared by the two MMAs of a 512-wide K step");
   static_assert(B_ROWS % 8 == 0, "B rows per CTA must fill whole 8-row swizzle atoms");
   static_assert(EPI_BUF % (8 * EPI_SWZ) == 0, "staging tiles must keep swizzle atoms aligned");
   static_assert(!SCALED || BN % 128 == 0, "block-scaled tiles cover whole 128-row scale blocks of B");
@@ -410,7 +416,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
         const int a_row = tm * (C::BM * C::CG) + static_cast<int>(prank) * C::BM;
         // this CTA's rows of B for each MMA of the K step (one MMA unless the tile is 512 wide)
         const int b_row = tn * C::BN + static_cast<int>(prank) * C::B_SUB_ROWS;
-        for (int kb = wk.kb0; kb < wk.kb1; ++kb) {
+        // serpentine K: odd items start where the previous item's K walk ended, on the
+        // operand panels' tails that are still in L2
+        const bool rev = p.k_serpentine && (k & 1);
+        for (int i = 0; i < wk.kb1 - wk.kb0; ++i) {
+          const int kb = rev ? wk.kb1 - 1 - i : wk.kb0 + i;
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, tmo, abort_flag)) {
             ok = false;
             break;
@@ -464,7 +474,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::ACC_STRIDE);
         const WorkItem wk = work_of(t);
-        for (int kb = wk.kb0; kb < wk.kb1; ++kb) {
+        // K blocks in the producer's order (see the LOAD role); only the first MMA of the item
+        // overwrites the accumulator
+        for (int i = 0; i < wk.kb1 - wk.kb0; ++i) {
           if (!mbar_wait(full_bar(stage), phase, tmo, abort_flag)) {
             ok = false;
             break;
@@ -479,16 +491,19 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
           for (int kk = 0; kk < C::KSTEPS; ++kk) {
             const uint64_t ad = sdesc_sw128(a0 + 32u * kk);
             const uint64_t bd = sdesc_sw128(b0 + 32u * kk);
-            const uint32_t accum = (kb != wk.kb0 || kk != 0) ? 1u : 0u;
+            const uint32_t accum = (i != 0 || kk != 0) ? 1u : 0u;
             if constexpr (C::NSUB > 1) {
-#pragma unroll
-              for (int sub = 0; sub < C::NSUB; ++sub) {
-                const uint64_t bds = sdesc_sw128(b0 + static_cast<uint32_t>(sub * C::B_SUB_ROWS * C::ROW_BYTES) + 32u * kk);
-                const uint32_t d = d_tmem + static_cast<uint32_t>(sub * C::MMA_N);
-                if constexpr (C::KIND == Kind::BF16)
-                  mma_bf16<C::CG>(d, ad, bds, C::IDESC, accum);
-                else
-                  mma_f8f6f4<C::CG>(d, ad, bds, C::IDESC, accum);
+              // the two N = 256 halves of the tile, into adjacent accumulator column ranges
+              constexpr int C0 = C::COLL_A ? kCollFill : kCollNone;
+              constexpr int C1 = C::COLL_A ? kCollLastUse : kCollNone;
+              const uint64_t bd1 = sdesc_sw128(b0 + static_cast<uint32_t>(C::B_SUB_ROWS * C::ROW_BYTES) + 32u * kk);
+              const uint32_t d1 = d_tmem + static_cast<uint32_t>(C::MMA_N);
+              if constexpr (C::KIND == Kind::BF16) {
+                mma_bf16<C::CG, C0>(d_tmem, ad, bd, C::IDESC, accum);
+                mma_bf16<C::CG, C1>(d1, ad, bd1, C::IDESC, accum);
+              } else {
+                mma_f8f6f4<C::CG, C0>(d_tmem, ad, bd, C::IDESC, accum);
+                mma_f8f6f4<C::CG, C1>(d1, ad, bd1, C::IDESC, accum);
               }
             } else if constexpr (C::KIND == Kind::BF16)
               mma_bf16<C::CG>(d_tmem, ad, bd, C::IDESC, accum);

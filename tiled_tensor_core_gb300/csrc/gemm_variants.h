@@ -15,7 +15,8 @@ enum VariantId : int {
   kVariant2Sm256x256 = 2,         // cta_group::2, 256 x 256 tile per CTA pair (bf16 / FP8)
   kVariant2Sm256x256SfSmem = 8,   // cta_group::2, 256 x 256, block scales through shared memory and
                                   // scale warps into tensor memory (NVFP4)
-  kVariant2Sm256x512 = 13,        // cta_group::2, 256 x 512 tile per CTA pair: two N = 256 MMAs per K step (bf16 / FP8)
+  kVariant2Sm256x512 = 13,        // cta_group::2, 256 x 512 tile per CTA pair: two N = 256 MMAs per K step, the
+                                  // second taking A from the tensor core's collector buffer (bf16 / FP8)
   kNumVariants = 14
 };
 

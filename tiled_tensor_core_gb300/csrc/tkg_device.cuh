@@ -360,39 +360,48 @@ __host__ __device__ constexpr uint32_t idesc_mxf4nvf4(int M, int N) {
 constexpr uint32_t kFmtBF16 = 1;  // kind::f16 operand format
 constexpr uint32_t kFmtE4M3 = 0;  // kind::f8f6f4 operand format
 
-template <int CG>
+// Use of the tensor core's A collector buffer by a dense MMA
+// (tcgen05.mma ... .collector::a::*): kCollFill reads A from shared memory and
+// keeps it in the buffer, kCollLastUse takes A from the buffer (no shared-memory
+// read) and then releases it.  Two consecutive MMAs with the same A descriptor
+// issued fill / lastuse read A once.
+constexpr int kCollNone = 0, kCollFill = 1, kCollLastUse = 2;
+
+#define TKG_MMA_DENSE_ASM(HEAD)                                                                        \
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t" HEAD " [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem), \
+               "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)                                    \
+               : "memory")
+
+// D[tmem] (+)= A · Bᵀ, bf16 operands (kind::f16), fp32 accumulator; `accumulate` = 0 overwrites D.
+template <int CG, int COLL = kCollNone>
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                          uint32_t accumulate) {
+  static_assert(CG == 2 || COLL == kCollNone, "collector use is built for the CTA-pair form");
   if constexpr (CG == 1)
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
+    TKG_MMA_DENSE_ASM("tcgen05.mma.cta_group::1.kind::f16");
+  else if constexpr (COLL == kCollFill)
+    TKG_MMA_DENSE_ASM("tcgen05.mma.cta_group::2.kind::f16.collector::a::fill");
+  else if constexpr (COLL == kCollLastUse)
+    TKG_MMA_DENSE_ASM("tcgen05.mma.cta_group::2.kind::f16.collector::a::lastuse");
   else
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
+    TKG_MMA_DENSE_ASM("tcgen05.mma.cta_group::2.kind::f16");
 }
 
-template <int CG>
+// The same with e4m3 operands (kind::f8f6f4; the formats are in the instruction descriptor).
+template <int CG, int COLL = kCollNone>
 __device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                            uint32_t accumulate) {
+  static_assert(CG == 2 || COLL == kCollNone, "collector use is built for the CTA-pair form");
   if constexpr (CG == 1)
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
+    TKG_MMA_DENSE_ASM("tcgen05.mma.cta_group::1.kind::f8f6f4");
+  else if constexpr (COLL == kCollFill)
+    TKG_MMA_DENSE_ASM("tcgen05.mma.cta_group::2.kind::f8f6f4.collector::a::fill");
+  else if constexpr (COLL == kCollLastUse)
+    TKG_MMA_DENSE_ASM("tcgen05.mma.cta_group::2.kind::f8f6f4.collector::a::lastuse");
   else
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
+    TKG_MMA_DENSE_ASM("tcgen05.mma.cta_group::2.kind::f8f6f4");
 }
+#undef TKG_MMA_DENSE_ASM
 
 template <int CG>
 __device__ __forceinline__ void mma_mxf4nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,

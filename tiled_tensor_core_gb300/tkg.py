@@ -34,6 +34,7 @@ TKG_OPT_MAX_CTAS = 4
 TKG_OPT_LAUNCH_OVERLAP = 5
 TKG_OPT_SCHEDULE = 6
 TKG_OPT_SPLIT_K = 7
+TKG_OPT_K_ORDER = 8
 
 TKG_OVERLAP_ON = 1
 TKG_OVERLAP_OFF = 2
@@ -42,6 +43,8 @@ TKG_SCHEDULE_DYNAMIC = 2
 TKG_SCHEDULE_SINGLE = 3
 TKG_SPLIT_ON = 1
 TKG_SPLIT_OFF = 2
+TKG_K_ORDER_SERPENTINE = 1
+TKG_K_ORDER_FORWARD = 2
 
 KIND_BF16, KIND_FP8, KIND_NVFP4 = 0, 1, 2
 
