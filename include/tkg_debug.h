@@ -36,8 +36,9 @@ TKG_API uint32_t tkg_debug_select_swizzle(uint32_t row_bytes);
 
 /* Host: describe a compiled variant.  kind: 0 bf16, 1 fp8, 2 nvfp4; variant as
  * TKG_OPT_VARIANT (>= 1).  info receives {cta_group, tile_n, stages,
- * epilogue_warps, threads, smem_bytes}.  TKG_ERR_INVALID_ARG if absent. */
-TKG_API tkg_status tkg_debug_variant_info(int kind, int variant, int32_t info[6]);
+ * epilogue_warps, threads, smem_bytes, tile_m} (tile_m: output-tile rows of a
+ * CTA pair).  TKG_ERR_INVALID_ARG if absent. */
+TKG_API tkg_status tkg_debug_variant_info(int kind, int variant, int32_t info[7]);
 
 /* Host: the variant id tkg_gemm_<kind> would launch for this shape (after
  * TKG_OPT_VARIANT) on a device of `sm_count` SMs; sm_count <= 0 asks the

@@ -41,7 +41,7 @@ def schedule(tkg, request):
 def tiles_of(tkg, kind, M, N, K):
     info = tkg.tkg_debug_variant_info({"bf16": 0, "fp8": 1, "nvfp4": 2}[kind],
                                       tkg.tkg_debug_pick_variant({"bf16": 0, "fp8": 1, "nvfp4": 2}[kind], M, N, K))
-    tm = -(-M // (128 * info["cta_group"]))
+    tm = -(-M // info["tile_m"])
     tn = -(-N // info["tile_n"])
     return tm * tn
 
@@ -132,8 +132,8 @@ def variant(tkg, request):
     tkg.tkg_set_option(tkg.TKG_OPT_VARIANT, 0)
 
 
-# odd and even numbers of 512-wide tile columns, one tile row, one column, a ragged last column,
-# and many rows per cluster
+# odd and even numbers of 512-wide tile columns, one tile row, one column, ragged last rows and
+# columns, and many tiles per cluster
 WIDE_SHAPES = [(300, 520, 200), (256, 1024, 128), (1000, 1000, 512), (77, 100, 40), (2048, 1536, 64),
                (512, 2100, 128)]
 

@@ -37,7 +37,7 @@ def plan_for(tkg, kind, M, N, K, ctas):
     kid = KIND_ID[kind]
     info = tkg.tkg_debug_variant_info(kid, tkg.tkg_debug_pick_variant(kid, M, N, K))
     cg = info["cta_group"]
-    tiles = -(-M // (128 * cg)) * -(-N // info["tile_n"])
+    tiles = -(-M // info["tile_m"]) * -(-N // info["tile_n"])
     k_bytes = {"bf16": 2 * K, "fp8": K, "nvfp4": K // 2}[kind]
     num_kb = -(-k_bytes // 128)
     return tkg.tkg_debug_split_plan(tiles, ctas // cg, num_kb), tiles

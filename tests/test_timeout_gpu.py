@@ -4,9 +4,10 @@ stage (no copy is in flight for it), so the compute role's wait on that stage
 runs out; the kernel records the timeout in the status word, every role stops,
 tensor memory is released, and the context stays usable for the next call.
 Every compiled GEMM variant is stalled this way: the 256x256 pair tile with its
-two accumulators, the 256x512 pair tile with its single accumulator and four
-48 KB stages, and the NVFP4 kernel, whose eight scale warps also wait (for the
-stage's scales in shared memory) and must give up in turn."""
+two accumulators, the 256x512 pair tile with a single accumulator and four
+48 KB stages, and the NVFP4 kernel, whose four scale warps also wait
+(for the stage's scales in shared memory) and must give up in turn, as must its
+eight epilogue warps."""
 import numpy as np
 import pytest
 

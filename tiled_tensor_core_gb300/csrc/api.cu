@@ -395,7 +395,7 @@ tkg_status plan_gemm(int kind, int64_t M, int64_t N, int64_t K, int sm_count, Ge
   g.id = pick_variant(kind, M, N, K, sm_count);
   g.v = variant_of(kind, g.id);
   if (!g.v) return TKG_ERR_INTERNAL;
-  const int64_t tile_m = 128LL * g.v->cg;
+  const int64_t tile_m = g.v->tile_m;
   g.tiles_m = (M + tile_m - 1) / tile_m;
   g.tiles_n = (N + g.v->bn - 1) / g.v->bn;
   if (g.tiles_m * g.tiles_n > 0x7FFFFFFF) return TKG_ERR_INVALID_ARG;
@@ -487,9 +487,11 @@ tkg_status gemm_enqueue(int kind, const GemmPlan& g, GemmParams& p, void* stream
   const int64_t cap = g_opt_max_ctas.load(std::memory_order_relaxed);
   if (cap > 0 && cap / cl < grid_clusters) grid_clusters = cap / cl > 0 ? cap / cl : 1;
 
-  // split-K head (static schedule, tiles of one MMA width), planned for the clusters the grid may use
+  // split-K head (static schedule, tiles of one MMA per K step), planned for the clusters the grid
+  // may use
   int64_t items = units;
-  if (allow_split && p.sched == kSchedStatic && v.bn <= 256 && opt_or(g_opt_split, TKG_SPLIT_ON) == TKG_SPLIT_ON) {
+  if (allow_split && p.sched == kSchedStatic && v.bn <= 256 && v.tile_m == 128 * v.cg &&
+      opt_or(g_opt_split, TKG_SPLIT_ON) == TKG_SPLIT_ON) {
     int split_tiles = 0, split_s = 1;
     split_plan(units, grid_clusters, p.num_kb, &split_tiles, &split_s);
     DevState::SplitWs w;
@@ -720,7 +722,7 @@ uint32_t tkg_debug_swizzle_offset(uint32_t off, uint32_t s_bytes) { return swizz
 
 uint32_t tkg_debug_select_swizzle(uint32_t row_bytes) { return select_swizzle(row_bytes); }
 
-tkg_status tkg_debug_variant_info(int kind, int variant, int32_t info[6]) {
+tkg_status tkg_debug_variant_info(int kind, int variant, int32_t info[7]) {
   const KernelVariant* v = variant_of(kind, variant);
   if (!v || !info) return TKG_ERR_INVALID_ARG;
   info[0] = v->cg;
@@ -729,6 +731,7 @@ tkg_status tkg_debug_variant_info(int kind, int variant, int32_t info[6]) {
   info[3] = v->epi_warps;
   info[4] = v->threads;
   info[5] = v->smem_bytes;
+  info[6] = v->tile_m;
   return TKG_OK;
 }
 

@@ -124,12 +124,13 @@ __host__ __device__ inline WorkItem work_item(int w, int split_tiles, int split_
 // tcgen05.cp instead costs the tensor pipe about 60 cycles per copy, twelve
 // copies per stage of a 256 x 256 tile).
 template <Kind KIND_, int CG_, int BN_, int STAGES_, int EPI_WARPS_, int NUM_ACC_ = 2, int SF_GROUPS_ = 2,
-          bool COLL_A_ = false>
+          bool COLL_A_ = false, int EPI_BUFS_ = 2>
 struct GemmCfg {
   static constexpr Kind KIND = KIND_;
   static constexpr int CG = CG_;                // CTAs per MMA (1, or 2 for the CTA pair) = CTAs per cluster
   static constexpr int BN = BN_;                // output-tile columns (whole pair)
   static constexpr int BM = 128;                // output-tile rows per CTA = TMEM lanes
+  static constexpr int TILE_M = BM * CG;        // output-tile rows (whole pair)
   static constexpr int STAGES = STAGES_;
   static constexpr int EPI_WARPS = EPI_WARPS_;  // 4 or 8
   static constexpr int NUM_ACC = NUM_ACC_;      // fp32 accumulators in TMEM (2 = epilogue overlaps next tile)
@@ -179,6 +180,9 @@ struct GemmCfg {
   static constexpr int EPI_ROW_BYTES = EPI_COLS * 2;
   static constexpr uint32_t EPI_SWZ = select_swizzle(EPI_ROW_BYTES);
   static constexpr int EPI_BUF = 32 * EPI_ROW_BYTES;  // one warp's 32-row staging tile
+  // staging tiles per epilogue warp: 2 lets a chunk's shared-memory writes overlap the previous
+  // chunk's TMA store; 1 halves the staging memory (eight epilogue warps then fit beside the ring)
+  static constexpr int EPI_BUFS = EPI_BUFS_;
   static constexpr int THREADS = 64 + 32 * (EPI_WARPS + SF_WARPS);
   static constexpr uint32_t IDESC = (KIND == Kind::BF16)   ? idesc_dense(kFmtBF16, BM * CG, MMA_N)
                                     : (KIND == Kind::FP8) ? idesc_dense(kFmtE4M3, BM * CG, MMA_N)
@@ -189,7 +193,7 @@ struct GemmCfg {
   static constexpr int OFF_SFA = OFF_B + STAGES * B_STAGE;
   static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
   static constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_STAGE;
-  static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * 2 * EPI_BUF;
+  static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_BUFS * EPI_BUF;
   // full / empty per stage, tensor-memory full / empty per accumulator, drain, and (NVFP4) the
   // per-stage sf_full barriers
   static constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1 + (SCALED ? STAGES : 0);
@@ -212,6 +216,7 @@ struct GemmCfg {
   static_assert(!COLL_A || NSUB == 2, "the A collector is shared by the two MMAs of a 512-wide K step");
   static_assert(B_ROWS % 8 == 0, "B rows per CTA must fill whole 8-row swizzle atoms");
   static_assert(EPI_BUF % (8 * EPI_SWZ) == 0, "staging tiles must keep swizzle atoms aligned");
+  static_assert(EPI_BUFS == 1 || EPI_BUFS == 2, "one or two staging tiles per epilogue warp");
   static_assert(!SCALED || BN % 128 == 0, "block-scaled tiles cover whole 128-row scale blocks of B");
   static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "epilogue is one or two warpgroups");
   static_assert(NUM_ACC == 1 || NUM_ACC == 2, "one or two accumulators");
@@ -413,7 +418,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
         const WorkItem wk = work_of(t);
         int tm, tn;
         tile_coord(wk.tile, tm, tn);
-        const int a_row = tm * (C::BM * C::CG) + static_cast<int>(prank) * C::BM;
+        const int a_row = tm * C::TILE_M + static_cast<int>(prank) * C::BM;
         // this CTA's rows of B for each MMA of the K step (one MMA unless the tile is 512 wide)
         const int b_row = tn * C::BN + static_cast<int>(prank) * C::B_SUB_ROWS;
         // serpentine K: odd items start where the previous item's K walk ended, on the
@@ -535,7 +540,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
     const int ew = warp - 2;
     const int quad = warp & 3;  // the TMEM lane quarter this warp may read
     const int sub = ew / 4;
-    const uint32_t stage0 = sEpi + static_cast<uint32_t>(ew) * 2u * C::EPI_BUF;
+    const uint32_t stage0 = sEpi + static_cast<uint32_t>(ew * C::EPI_BUFS * C::EPI_BUF);
     float sa = 1.0f, sb = 1.0f;
     if constexpr (C::KIND != Kind::BF16) {
       sa = *p.a_scale;
@@ -545,7 +550,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
     int it = 0;
     int chunk_ctr = 0;
     bool seq_ok = true;
-    constexpr int NCH = C::BN / C::EPI_COLS;
+    constexpr int NCH = C::BN / C::EPI_COLS;  // chunks of the accumulator
     constexpr int NLD = C::EPI_COLS / 32;  // 32-column TMEM loads per chunk
     constexpr int NPK = C::EPI_COLS / 2;   // packed bf16 pairs per row
     constexpr int RB = C::EPI_ROW_BYTES;
@@ -555,6 +560,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
     // laid out [chunk][16-byte column group][lane] so that each store / load of a warp is 512
     // contiguous bytes
     constexpr int WS_WARP = 32 * (C::BN / SUBS);  // floats
+    // tiles of one MMA per K step may be split along K; the 256x512 tile never is
+    constexpr bool CAN_SPLIT = C::NSUB == 1;
     auto ws_block = [&](int piece) {
       return reinterpret_cast<float4*>(p.split_ws) +
              ((static_cast<size_t>(piece) * C::CG + prank) * C::EPI_WARPS + ew) * (WS_WARP / 4);
@@ -571,8 +578,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
         break;
       }
       tc_fence_after();
-      const int row0 = tm * (C::BM * C::CG) + static_cast<int>(prank) * C::BM + quad * 32;
+      const int row0 = tm * C::TILE_M + static_cast<int>(prank) * C::BM + quad * 32;
       const int col0 = tn * C::BN;
+
       const uint32_t t_row =
           tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * C::ACC_STRIDE);
       auto load_chunk = [&](int c, uint32_t (&r)[NLD][32], bool may_release) {
@@ -602,8 +610,12 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
       // store chunk c of this warp's rows, given as packed bf16 pairs
       auto store_chunk = [&](int c, const uint32_t (&pk)[NPK]) {
         if (p.c_via_tma) {
-          const uint32_t buf = stage0 + static_cast<uint32_t>(chunk_ctr & 1) * C::EPI_BUF;
-          if (lane == 0) bulk_wait_group_read<1>();  // the store that last used `buf` has read it
+          uint32_t buf = stage0 + static_cast<uint32_t>(chunk_ctr % C::EPI_BUFS) * C::EPI_BUF;
+          // one staging tile: its row addresses are loop-invariant, and the 128-register kernels
+          // cannot keep them live across the tile loop; make the base opaque so they are
+          // recomputed per chunk
+          if constexpr (C::EPI_BUFS == 1) asm volatile("mov.b32 %0, %0;" : "+r"(buf));
+          if (lane == 0) bulk_wait_group_read<C::EPI_BUFS - 1>();  // the store that last used `buf` has read it
           __syncwarp();
           const uint32_t row_off = static_cast<uint32_t>(lane) * RB;
 #pragma unroll
@@ -637,7 +649,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
         if (p.visits != nullptr && ew == 0 && lane == 0 && prank == 0)
           atomicAdd(p.visits + tm * p.tiles_n + tn, 1u);
       };
-      if (wk.piece < 0) {
+      if (!CAN_SPLIT || wk.piece < 0) {
         count_visit();
         for (int c = sub; c < NCH; c += SUBS) {
           uint32_t r[NLD][32];
@@ -855,6 +867,7 @@ struct KernelVariant {
   int kind;
   int cg;
   int bn;
+  int tile_m;    // output-tile rows (whole CTA pair)
   int epi_cols;  // columns of one epilogue TMA store box (64: 128-byte swizzle, 32: 64-byte swizzle)
   int stages;
   int epi_warps;
@@ -866,9 +879,9 @@ struct KernelVariant {
 
 template <class C>
 KernelVariant make_variant(const char* name) {
-  return KernelVariant{static_cast<int>(C::KIND), C::CG,        C::BN,         C::EPI_COLS,
-                       C::STAGES,                 C::EPI_WARPS, C::THREADS,    C::SMEM_BYTES,
-                       name,                      reinterpret_cast<const void*>(&tkg_gemm_kernel<C>)};
+  return KernelVariant{static_cast<int>(C::KIND), C::CG,        C::BN,      C::TILE_M,    C::EPI_COLS,
+                       C::STAGES,                 C::EPI_WARPS, C::THREADS, C::SMEM_BYTES, name,
+                       reinterpret_cast<const void*>(&tkg_gemm_kernel<C>)};
 }
 
 }  // namespace tkg

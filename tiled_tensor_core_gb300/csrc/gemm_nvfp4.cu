@@ -19,10 +19,12 @@
 
 namespace tkg {
 
-using Nvfp4_2Sm_256 = GemmCfg<Kind::NVFP4, 2, 256, 5, 4, 1, 2>;
+// five 38 KB ring stages, one accumulator, eight epilogue warps (two per TMEM lane quarter, each
+// draining half of the columns, one staging tile each) and one group of four scale warps
+using Nvfp4_2Sm_256 = GemmCfg<Kind::NVFP4, 2, 256, 5, 8, 1, 1, false, 1>;
 
 const KernelVariant* nvfp4_variant(int id) {
-  static const KernelVariant v8 = make_variant<Nvfp4_2Sm_256>("nvfp4_2sm_256x256_s5_sfw8_smem");
+  static const KernelVariant v8 = make_variant<Nvfp4_2Sm_256>("nvfp4_2sm_256x256_s5_epi8_sfw4_smem");
   switch (id) {
     case kVariant2Sm256x256SfSmem: return &v8;
     default: return nullptr;

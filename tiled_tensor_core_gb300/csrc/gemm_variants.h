@@ -8,13 +8,14 @@ namespace tkg {
 
 // Variant ids (also the values of TKG_OPT_VARIANT).  The ids are those of the
 // kernel forms measured while the tile shape was chosen; the forms that lost
-// (1-SM 128 x 256, 256 x 128 / 192 / 224 pair tiles, NVFP4 scale staging by
+// (1-SM 128 x 256, 256 x 128 / 192 / 224 pair tiles, A multicast between two
+// pairs, a 512 x 256 pair tile whose two MMAs share B, NVFP4 scale staging by
 // tensor-pipe copies or from global memory) are no longer compiled.
 enum VariantId : int {
   kVariantAuto = 0,
   kVariant2Sm256x256 = 2,         // cta_group::2, 256 x 256 tile per CTA pair (bf16 / FP8)
   kVariant2Sm256x256SfSmem = 8,   // cta_group::2, 256 x 256, block scales through shared memory and
-                                  // scale warps into tensor memory (NVFP4)
+                                  // four scale warps into tensor memory, eight epilogue warps (NVFP4)
   kVariant2Sm256x512 = 13,        // cta_group::2, 256 x 512 tile per CTA pair: two N = 256 MMAs per K step, the
                                   // second taking A from the tensor core's collector buffer (bf16 / FP8)
   kNumVariants = 14

@@ -215,9 +215,10 @@ def tkg_debug_select_swizzle(row_bytes) -> int:
 
 
 def tkg_debug_variant_info(kind, variant):
-    info = (ctypes.c_int32 * 6)()
+    info = (ctypes.c_int32 * 7)()
     _check(lib.tkg_debug_variant_info(kind, variant, info), "tkg_debug_variant_info")
-    return dict(zip(("cta_group", "tile_n", "stages", "epilogue_warps", "threads", "smem_bytes"), list(info)))
+    return dict(zip(("cta_group", "tile_n", "stages", "epilogue_warps", "threads", "smem_bytes", "tile_m"),
+                    list(info)))
 
 
 def tkg_debug_pick_variant(kind, M, N, K, sm_count=0) -> int:
