@@ -57,12 +57,16 @@ PEAK_RATIO = {"bf16": 1.0, "fp8": 2.0, "nvfp4": 6.0}
 DTYPE = {"bf16": "bf16", "fp8": "e4m3", "nvfp4": "e2m1+e4m3"}
 
 
-# DRAM bytes (read + write) per launch of the dominant kernel, from one ncu capture
-# (profiles/), valid only while the kernel sources hash to the value recorded with it.
+# DRAM bytes (read + write) per launch of the dominant kernel, from one full-size ncu capture
+# (profiles/gemm_*_ncu.md, profiles/attention_fwd_4096_d128_ncu.md), valid only while the kernel
+# sources hash to the value recorded with it.
 TRAFFIC = {
-    "bf16_4096": {"bytes": 111_793_920, "src": "65fcc9042c647780"},       # profiles/gemm_bf16_4096_ncu_full.md
-    "nvfp4_16384": {"bytes": 1_974_272_256, "src": "65fcc9042c647780"},   # profiles/gemm_nvfp4_16384_ncu_full.md
-    "attn_n4096_d128": {"bytes": 1_062_650_368, "src": "ebade320dad335df"},  # profiles/attention_fwd_4096_d128_ncu_full.md
+    "bf16_4096": {"bytes": 93_894_656, "src": "fce8d2b1bb141552"},
+    "bf16_8192": {"bytes": 831_954_176, "src": "fce8d2b1bb141552"},
+    "bf16_skinny": {"bytes": 431_350_272, "src": "fce8d2b1bb141552"},
+    "fp8_8192": {"bytes": 395_776_768, "src": "fce8d2b1bb141552"},
+    "nvfp4_16384": {"bytes": 1_621_055_232, "src": "fce8d2b1bb141552"},
+    "attn_n4096_d128": {"bytes": 1_062_417_152, "src": "55fd825c5402713b"},
 }
 GEMM_SOURCES = ("tkg_device.cuh", "gemm_kernel.cuh", "gemm_bf16.cu", "gemm_fp8.cu", "gemm_nvfp4.cu")
 ATTN_SOURCES = ("tkg_device.cuh", "attention.cu")
