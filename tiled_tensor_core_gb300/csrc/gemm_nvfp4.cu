@@ -42,9 +42,12 @@ struct InterleaveArgs {
   int kstages;         // 256-element K stages in dst (padded with zero scales)
 };
 
-// One CTA rewrites one 128-row block for two consecutive K stages (32 source
-// bytes per row, i.e. whole 32-byte sectors).  Scales of rows or K positions
-// past the matrix are written as 0.
+// One CTA rewrites one 128-row block for two consecutive K stages: thread t moves the 16 scales of
+// row t % 128 for stage kb0 + t / 128 (one 16-byte load from the row-major source, one 16-byte store
+// into the stage's run), so a warp writes 512 contiguous bytes and the two halves of the CTA read
+// each source row's 32 bytes (one sector) together.  Scales of rows or K positions past the matrix
+// are written as 0; a stage that runs past the last K position, or a row pitch that is not a
+// multiple of 16 bytes, takes byte loads.
 __global__ void __launch_bounds__(256) interleave_scales_kernel(InterleaveArgs a, InterleaveArgs b, int blocks_a) {
   // launched as a programmatic dependent: the previous GEMM may still read the
   // scratch this kernel rewrites, or a previous kernel still write the scales
@@ -54,28 +57,26 @@ __global__ void __launch_bounds__(256) interleave_scales_kernel(InterleaveArgs a
   const InterleaveArgs& s = is_a ? a : b;
   const int local = is_a ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x) - blocks_a;
   const int rb = local % s.blocks;
-  const int kb0 = 2 * (local / s.blocks);
+  const int r_in = static_cast<int>(threadIdx.x) & 127;
+  const int kb = 2 * (local / s.blocks) + (static_cast<int>(threadIdx.x) >> 7);
+  if (kb >= s.kstages) return;
+  const int row = rb * 128 + r_in;
+  const int col = kb * 16;
+  uint4 v = make_uint4(0u, 0u, 0u, 0u);
+  if (row < s.rows && col < s.k16) {
+    const uint8_t* src = s.src + static_cast<size_t>(row) * s.k16 + col;
+    if ((s.k16 & 15) == 0 && col + 16 <= s.k16) {
+      v = __ldg(reinterpret_cast<const uint4*>(src));
+    } else {
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    const int lin = static_cast<int>(threadIdx.x) + 256 * w;  // 0..1023
-    const int r_in = lin >> 3;                                // row within the block
-    const int word = lin & 7;
-    const int kb = kb0 + (word >> 2);
-    const int t = word & 3;                                   // MMA within the stage
-    if (kb >= s.kstages) continue;
-    const int row = rb * 128 + r_in;
-    const int col = kb * 16 + 4 * t;
-    uint32_t v = 0;
-    if (row < s.rows) {
-      const uint8_t* p = s.src + static_cast<size_t>(row) * s.k16;
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (col + j < s.k16) v |= static_cast<uint32_t>(__ldg(p + col + j)) << (8 * j);
+      for (int j = 0; j < 16; ++j)
+        if (col + j < s.k16) w[j >> 2] |= static_cast<uint32_t>(__ldg(src + j)) << (8 * (j & 3));
+      v = make_uint4(w[0], w[1], w[2], w[3]);
     }
-    const size_t run = static_cast<size_t>(kb) * s.blocks + rb;
-    const size_t off = run * 2048 + r_in * 16 + t * 4;
-    *reinterpret_cast<uint32_t*>(s.dst + off) = v;
   }
+  const size_t run = static_cast<size_t>(kb) * s.blocks + rb;
+  *reinterpret_cast<uint4*>(s.dst + run * 2048 + static_cast<size_t>(r_in) * 16) = v;
 }
 
 }  // namespace
