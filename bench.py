@@ -58,21 +58,25 @@ DTYPE = {"bf16": "bf16", "fp8": "e4m3", "nvfp4": "e2m1+e4m3"}
 
 
 # DRAM bytes (read + write) per launch of the dominant kernel, from one full-size ncu capture
-# (profiles/gemm_*_ncu.md, profiles/attention_fwd_4096_d128_ncu.md), valid only while the kernel
-# sources hash to the value recorded with it.
+# (profiles/gemm_*_ncu.md, profiles/attention_fwd_4096_d128_ncu.md), valid only while the sources of
+# that kernel hash to the value recorded with it.
 TRAFFIC = {
-    "bf16_4096": {"bytes": 93_894_656, "src": "fce8d2b1bb141552"},
-    "bf16_8192": {"bytes": 831_954_176, "src": "fce8d2b1bb141552"},
-    "bf16_skinny": {"bytes": 431_350_272, "src": "fce8d2b1bb141552"},
-    "fp8_8192": {"bytes": 395_776_768, "src": "fce8d2b1bb141552"},
-    "nvfp4_16384": {"bytes": 1_621_055_232, "src": "fce8d2b1bb141552"},
+    "bf16_4096": {"bytes": 93_894_656, "src": "08c2b4e0fac8c8d3"},
+    "bf16_8192": {"bytes": 831_954_176, "src": "08c2b4e0fac8c8d3"},
+    "bf16_skinny": {"bytes": 431_350_272, "src": "08c2b4e0fac8c8d3"},
+    "fp8_8192": {"bytes": 395_776_768, "src": "debcfee094d747c7"},
+    "nvfp4_16384": {"bytes": 1_621_055_232, "src": "5a47adf3141762d3"},
     "attn_n4096_d128": {"bytes": 1_062_417_152, "src": "55fd825c5402713b"},
 }
-GEMM_SOURCES = ("tkg_device.cuh", "gemm_kernel.cuh", "gemm_bf16.cu", "gemm_fp8.cu", "gemm_nvfp4.cu")
-ATTN_SOURCES = ("tkg_device.cuh", "attention.cu")
+KERNEL_SOURCES = {
+    "bf16": ("tkg_device.cuh", "gemm_kernel.cuh", "gemm_bf16.cu"),
+    "fp8": ("tkg_device.cuh", "gemm_kernel.cuh", "gemm_fp8.cu"),
+    "nvfp4": ("tkg_device.cuh", "gemm_kernel.cuh", "gemm_nvfp4.cu"),
+    "attn": ("tkg_device.cuh", "attention.cu"),
+}
 
 
-def kernel_source_hash(files=GEMM_SOURCES) -> str:
+def kernel_source_hash(files) -> str:
     """Hash of kernel sources with comments and blank lines removed, so that a
     comment edit does not invalidate a recorded capture but any code change does."""
     import hashlib
@@ -91,8 +95,10 @@ def kernel_source_hash(files=GEMM_SOURCES) -> str:
 
 def traffic_bytes(workload: str):
     rec = TRAFFIC.get(workload)
-    files = ATTN_SOURCES if workload.startswith("attn_") else GEMM_SOURCES
-    if rec and rec["src"] == kernel_source_hash(files):
+    if rec is None:
+        return None
+    kind = "attn" if workload.startswith("attn_") else workload.split("_")[0]
+    if rec["src"] == kernel_source_hash(KERNEL_SOURCES[kind]):
         return rec["bytes"]
     return None
 
