@@ -84,7 +84,7 @@ TKG_API tkg_status tkg_debug_tma_swizzle_probe(int s_bytes, const void* src, voi
  * sfa_words / sfb_words are the 32-bit contents of 8 tensor-memory columns
  * for each of the 128 lanes ([128][8], lane-major) of the A and B scale
  * regions, and sf_cols[2*i], sf_cols[2*i+1] (each 0..7) select the column of
- * each region used by MMA i.  n in {64, 128, 256}, ksteps in 1..4.
+ * each region used by MMA i.  n in {64, 128, 192, 256}, ksteps in 1..4.
  * a_tile, b_tile, sfa_words, sfb_words and d_out are device pointers (the
  * scale arrays may be NULL for kinds 0 and 1); sf_cols is a host array of
  * 2*ksteps entries (may be NULL for kinds 0 and 1).  Synchronous on `stream`. */

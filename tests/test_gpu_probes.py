@@ -78,7 +78,7 @@ def _sf_words(sf_rows, quarter_lanes):
     return words
 
 
-@pytest.mark.parametrize("n", [128, 256])
+@pytest.mark.parametrize("n", [128, 192, 256])
 def test_single_tile_nvfp4_mma_scale_layout(tkg, oracle_mod, n):
     # one block-scaled MMA (K = 64): 4 scales per row, slice j in byte j;
     # A's row m read at lane m, column m // 32; B's row n at lane n % 32, column n // 32
@@ -95,5 +95,27 @@ def test_single_tile_nvfp4_mma_scale_layout(tkg, oracle_mod, n):
     d_sfb = torch.from_numpy(sfb.view(np.int32)).cuda()
     d_out = torch.full((128, n), float("nan"), dtype=torch.float32, device="cuda")
     assert tkg.tkg_debug_mma_probe(2, n, 1, d_a, d_b, d_sfa, d_sfb, [0, 0], d_out) == tkg.TKG_OK
+    acc, _ = oracle_mod.gemm_nvfp4(ops.a, ops.b, ops.sfa, ops.sfb, 1.0, 1.0)
+    assert np.array_equal(d_out.cpu().numpy(), acc)
+
+
+def test_single_tile_nvfp4_n192_b_scales_at_an_offset(tkg, oracle_mod):
+    # N = 192 reads B's scales from six columns starting at the address the MMA is given: placed
+    # two columns in, the result shows the scale address, not column 0, decides where they are read
+    n = 192
+    ops = synth.small_int_operands("nvfp4", 128, n, 64, seed=1920)
+    a_tile = np.zeros((128, 128), np.uint8)
+    b_tile = np.zeros((n, 128), np.uint8)
+    a_tile[:, :32] = ops.a
+    b_tile[:, :32] = ops.b
+    sfa = _sf_words(ops.sfa, [0, 1, 2, 3])
+    sfb = np.zeros((128, 8), dtype=np.uint32)
+    sfb[:, 2:] = _sf_words(ops.sfb, [0, 1, 2, 3])[:, :6]
+    d_a = torch.from_numpy(a_tile).cuda()
+    d_b = torch.from_numpy(b_tile).cuda()
+    d_sfa = torch.from_numpy(sfa.view(np.int32)).cuda()
+    d_sfb = torch.from_numpy(sfb.view(np.int32)).cuda()
+    d_out = torch.full((128, n), float("nan"), dtype=torch.float32, device="cuda")
+    assert tkg.tkg_debug_mma_probe(2, n, 1, d_a, d_b, d_sfa, d_sfb, [0, 2], d_out) == tkg.TKG_OK
     acc, _ = oracle_mod.gemm_nvfp4(ops.a, ops.b, ops.sfa, ops.sfb, 1.0, 1.0)
     assert np.array_equal(d_out.cpu().numpy(), acc)

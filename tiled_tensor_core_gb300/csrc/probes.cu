@@ -215,7 +215,7 @@ tkg_status tkg_debug_tma_swizzle_probe(int s_bytes, const void* src, void* dst, 
 tkg_status tkg_debug_mma_probe(int kind, int n, int ksteps, const void* a_tile, const void* b_tile,
                                const uint32_t* sfa_words, const uint32_t* sfb_words, const int32_t* sf_cols,
                                float* d_out, void* stream) {
-  if (kind < 0 || kind > 2 || !(n == 64 || n == 128 || n == 256) || ksteps < 1 || ksteps > 4 || !a_tile ||
+  if (kind < 0 || kind > 2 || !(n == 64 || n == 128 || n == 192 || n == 256) || ksteps < 1 || ksteps > 4 || !a_tile ||
       !b_tile || !d_out)
     return TKG_ERR_INVALID_ARG;
   if (kind == 2 && (!sfa_words || !sfb_words || !sf_cols)) return TKG_ERR_INVALID_ARG;
