@@ -451,7 +451,7 @@ def measure_gemm(name, args, world, rank, local, cpu_s):
 
     # context: cuBLAS on the same shape, operands and stream (the pages' "matches cuBLAS" claim)
     cublas = None
-    if not args.no_cublas and w.kind in ("bf16", "fp8"):
+    if not args.no_cublas:
         cublas = run_cublas(sets, w, batch, stream, args)
         if cublas is not None and "value" in cublas:
             cublas["ours_over_cublas"] = value / world / cublas["value"]
@@ -683,10 +683,24 @@ def run_cublas(sets, w, batch, stream, args):
         def one(i):
             a, b = mats[i % len(sets)]
             torch.matmul(a, b.t(), out=outs[i % len(sets)])
-    else:
+    elif w.kind == "fp8":
         if not hasattr(torch, "_scaled_mm"):
             return None
         mats = [(g.a.view(torch.float8_e4m3fn), g.b.view(torch.float8_e4m3fn), g.scale_a, g.scale_b) for g in sets]
+
+        def one(i):
+            a, b, sa, sb = mats[i % len(sets)]
+            outs[i % len(sets)] = torch._scaled_mm(a, b.t(), scale_a=sa, scale_b=sb, out_dtype=torch.bfloat16)
+    else:
+        # NVFP4: the same packed e2m1 operands and e4m3 block scales, the scales re-laid out (once,
+        # untimed) into the 128 x 4 blocked order cuBLAS documents for 16-element block scaling;
+        # cuBLAS applies the block scales only (the two per-tensor scales are one multiply in the
+        # epilogue)
+        if not hasattr(torch, "_scaled_mm") or not hasattr(torch, "float4_e2m1fn_x2"):
+            return {"unavailable": "this torch build has no float4_e2m1fn_x2 / _scaled_mm"}
+        mats = [(g.a.view(torch.float4_e2m1fn_x2), g.b.view(torch.float4_e2m1fn_x2),
+                 cublas_blocked_scales(g.sfa).view(torch.float8_e4m3fn),
+                 cublas_blocked_scales(g.sfb).view(torch.float8_e4m3fn)) for g in sets]
 
         def one(i):
             a, b, sa, sb = mats[i % len(sets)]
@@ -707,8 +721,23 @@ def run_cublas(sets, w, batch, stream, args):
     except RuntimeError as e:  # a cuBLAS path torch does not offer on this build
         return {"unavailable": str(e).splitlines()[0][:200]}
     ms = statistics.median(a.elapsed_time(b) for a, b in ev) / batch
-    return {"value": w.flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-            "how": "torch.matmul (bf16)" if w.kind == "bf16" else "torch._scaled_mm (e4m3, per-tensor scales)"}
+    how = {"bf16": "torch.matmul (bf16)", "fp8": "torch._scaled_mm (e4m3, per-tensor scales)",
+           "nvfp4": "torch._scaled_mm (e2m1, e4m3 scales per 16 elements)"}[w.kind]
+    return {"value": w.flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "how": how}
+
+
+def cublas_blocked_scales(sf):
+    """Row-major [rows][K/16] e4m3 block scales -> cuBLAS's blocked layout: the matrix padded to
+    128-row x 4-column blocks, blocks in row-major order, and inside a block the scale of row r,
+    column c at byte 16 * (r % 32) + 4 * (r // 32) + c."""
+    import torch
+    rows, cols = sf.shape
+    pr, pc = -(-rows // 128) * 128, -(-cols // 4) * 4
+    padded = torch.zeros((pr, pc), dtype=torch.uint8, device=sf.device)
+    padded[:rows, :cols] = sf.view(torch.uint8)
+    blocks = padded.view(pr // 128, 128, pc // 4, 4).permute(0, 2, 1, 3)  # [row block][col block][128][4]
+    inner = blocks.reshape(pr // 128, pc // 4, 4, 32, 4).transpose(2, 3)  # [..][r % 32][r // 32][c]
+    return inner.reshape(pr, pc).contiguous()
 
 
 def run_e2e(ops, dev, w, args):
@@ -980,7 +1009,7 @@ def main(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-check", action="store_true", help="skip the parity gate (never for a reported number)")
-    p.add_argument("--no-cublas", action="store_true", help="skip the cuBLAS comparison (bf16 / FP8 workloads)")
+    p.add_argument("--no-cublas", action="store_true", help="skip the cuBLAS comparison")
     p.add_argument("--graph", choices=["auto", "on", "off"], default="auto",
                    help="replay each step from a CUDA graph (auto: launch-bound workloads)")
     p.add_argument("--schedule", choices=sorted(SCHEDULE), default="static",

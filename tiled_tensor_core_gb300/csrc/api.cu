@@ -251,7 +251,7 @@ constexpr int64_t kWideMinRounds = 4;
 int pick_variant(int kind, int64_t M, int64_t N, int64_t K, int sm_count) {
   const int forced = static_cast<int>(g_opt_variant.load(std::memory_order_relaxed));
   if (forced > 0 && variant_of(kind, forced)) return forced;
-  if (kind == 2) return kVariant2Sm256x256SfSmem;
+  if (kind == 2) return kVariant2Sm256x256SfCopy;
   const int64_t wide_tiles = ((M + 255) / 256) * ((N + 511) / 512);
   if (K >= kWideMinK && wide_tiles >= kWideMinRounds * (sm_count / 2)) return kVariant2Sm256x512;
   return kVariant2Sm256x256;
@@ -566,7 +566,7 @@ tkg_status gemm_launch(int kind, int64_t M, int64_t N, int64_t K, const void* A,
     }
     if (nvfp4_interleave_scales(scales->a_block_scale, scales->b_block_scale, static_cast<int>(M),
                                 static_cast<int>(N), static_cast<int>(K), g.sf_blocks_a, g.sf_blocks_b, g.num_kb,
-                                scratch, g.sf_b_off, cs, launch_overlap()) != cudaSuccess) {
+                                g.v->sf_atoms, scratch, g.sf_b_off, cs, launch_overlap()) != cudaSuccess) {
       cudaGetLastError();
       release();
       return TKG_ERR_CUDA;

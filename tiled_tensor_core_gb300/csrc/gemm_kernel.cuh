@@ -158,12 +158,20 @@ struct GemmCfg {
   static constexpr int SF_ROW_BYTES = 16;
   static constexpr int SFA_STAGE = SCALED ? BM * SF_ROW_BYTES : 0;
   static constexpr int SFB_STAGE = SCALED ? BN * SF_ROW_BYTES : 0;
-  static constexpr int SF_GROUPS = SCALED ? SF_GROUPS_ : 0;
+  // SF_GROUPS_ = 0: the scales are copied from shared into tensor memory with tcgen05.cp, one lane of
+  // each of the four scale warps of the leader CTA issuing the copies of one MMA of every stage (a
+  // thread issues a copy about every 60-80 cycles; copies from several threads overlap the MMAs)
+  static constexpr bool SF_CP = SCALED && SF_GROUPS_ == 0;
+  static constexpr int SF_GROUPS = SCALED ? (SF_CP ? 1 : SF_GROUPS_) : 0;
   static constexpr int SF_WARPS = 4 * SF_GROUPS;
-  // operand bytes landing per CTA per stage on the (leader's) full barrier; the scales land on the
-  // CTA's own sf_full barrier
-  static constexpr int STAGE_TX = A_STAGE + B_BOX;
   static constexpr int SF_TX = SFA_STAGE + SFB_STAGE;
+  // operand bytes landing per CTA per stage on the (leader's) full barrier; the scales land on the
+  // CTA's own sf_full barrier (scale warps) or, copied, on the leader's
+  static constexpr int STAGE_TX = A_STAGE + B_BOX;
+  // one 512-byte shared-memory atom per MMA and 128 rows: the 4 scales of rows r, r + 32, r + 64,
+  // r + 96 at byte 16 r (r < 32), which tcgen05.cp.32x128b.warpx4 puts at lane r of every TMEM lane
+  // quarter, columns c .. c + 3 -- row m's scales at lane m, column c + m / 32
+  static constexpr int SF_ATOM = 512;
   static constexpr int ACC_STRIDE = BN <= 128 ? 128 : BN <= 256 ? 256 : BN;  // accumulators start on aligned columns
   static constexpr int ACC_COLS = NUM_ACC * ACC_STRIDE;
   // TMEM columns of one stage's scales: A: 4 per MMA (row m at column m/32);
@@ -196,7 +204,7 @@ struct GemmCfg {
   static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_BUFS * EPI_BUF;
   // full / empty per stage, tensor-memory full / empty per accumulator, drain, and (NVFP4) the
   // per-stage sf_full barriers
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1 + (SCALED ? STAGES : 0);
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1 + (SCALED ? STAGES : 0) + (SF_CP ? 1 : 0);
   // dynamic schedule: ring of cancellation answers (16 bytes each) with a full
   // barrier per slot in every CTA and an empty barrier per slot in the leader,
   // after the barriers above
@@ -284,6 +292,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
   const uint32_t drain_bar = bar0 + 8u * (2 * C::STAGES + 2 * C::NUM_ACC);
   // NVFP4: stage s's block scales landed in this CTA's shared memory
   auto sf_full_bar = [&](int st) { return bar0 + 8u * (2 * C::STAGES + 2 * C::NUM_ACC + 1 + st); };
+  // NVFP4, copied scales: the four copy issuers' last copies are done
+  const uint32_t cp_drain_bar = bar0 + 8u * (3 * C::STAGES + 2 * C::NUM_ACC + 1);
   auto sched_full_bar = [&](int j) { return bar0 + 8u * (C::SCHED_BAR0 + j); };
   auto sched_empty_bar = [&](int j) { return bar0 + 8u * (C::SCHED_BAR0 + C::SCHED_SLOTS + j); };
   const uint32_t sResp = sbase + C::OFF_SCHED;
@@ -308,7 +318,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(full_bar(s), C::SCALED ? 1 + C::CG * 4 : 1);  // + one arrival per scale warp of the group
+      // + one arrival per scale warp of the group (writing the scales: every CTA's; copying them: the
+      // leader's, by tcgen05.commit once its copies are done)
+      mbar_init(full_bar(s), C::SCALED ? 1 + (C::SF_CP ? 4 : C::CG * 4) : 1);
       mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < C::NUM_ACC; ++a) {
@@ -319,6 +331,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
     if constexpr (C::SCALED) {
       for (int st = 0; st < C::STAGES; ++st) mbar_init(sf_full_bar(st), 1);
     }
+    if constexpr (C::SF_CP) mbar_init(cp_drain_bar, 4);
     for (int j = 0; j < C::SCHED_SLOTS; ++j) {
       mbar_init(sched_full_bar(j), 1);  // the leader's expect_tx arrival + the 16-byte answer
       mbar_init(sched_empty_bar(j), C::SCHED_READERS);
@@ -440,13 +453,23 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
                                  kb * C::K_TMAP, b_row + sub * C::MMA_N);
             if constexpr (C::SCALED) {
               // staged scales: 2 KB (16 rows of 128 B) per (K stage, 128-row block), the blocks of
-              // one K stage contiguous; they land on this CTA's own sf_full barrier
+              // one K stage contiguous; with scale warps they land on this CTA's own sf_full
+              // barrier, else with the operands on the leader's full barrier
               const int ya = (kb * p.sf_blocks_a + a_row / 128) * 16;
               const int yb = (kb * p.sf_blocks_b + (tn * C::BN) / 128) * 16;
-              const uint32_t sfb_bar = sf_full_bar(stage);
-              mbar_arrive_expect_tx(sfb_bar, C::SF_TX);
-              tma_load_2d<1>(sSFA + stage * C::SFA_STAGE, &p.tmap_sfa, sfb_bar, 0, ya);
-              tma_load_2d<1>(sSFB + stage * C::SFB_STAGE, &p.tmap_sfb, sfb_bar, 0, yb);
+              if constexpr (C::SF_CP) {
+                // both CTAs' scales land on the leader's sf_full barrier: the leader's copies read
+                // them from both CTAs' shared memory
+                const uint32_t sfb_bar = (C::CG == 2) ? mapa_shared(sf_full_bar(stage), leader) : sf_full_bar(stage);
+                if (prank == 0) mbar_arrive_expect_tx(sf_full_bar(stage), C::SF_TX * C::CG);
+                tma_load_2d<C::CG>(sSFA + stage * C::SFA_STAGE, &p.tmap_sfa, sfb_bar, 0, ya);
+                tma_load_2d<C::CG>(sSFB + stage * C::SFB_STAGE, &p.tmap_sfb, sfb_bar, 0, yb);
+              } else {
+                const uint32_t sfb_bar = sf_full_bar(stage);
+                mbar_arrive_expect_tx(sfb_bar, C::SF_TX);
+                tma_load_2d<1>(sSFA + stage * C::SFA_STAGE, &p.tmap_sfa, sfb_bar, 0, ya);
+                tma_load_2d<1>(sSFB + stage * C::SFB_STAGE, &p.tmap_sfb, sfb_bar, 0, yb);
+              }
             }
           }
           first = false;
@@ -490,7 +513,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
           const uint32_t a0 = sA + stage * C::A_STAGE;
           const uint32_t b0 = sB + stage * C::B_STAGE;
           // this stage's TMEM scale slot (NVFP4): the stage's full barrier also counts the scale
-          // warps that wrote it
+          // warps that filled it
           const uint32_t sf_tmem = tmem_base + static_cast<uint32_t>(C::ACC_COLS + stage * C::SF_COLS_STAGE);
 #pragma unroll
           for (int kk = 0; kk < C::KSTEPS; ++kk) {
@@ -771,7 +794,55 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
     if (!seq_ok && lane == 0) record_timeout(p.status, kRoleEpilogue, abort_flag);
     if (lane == 0) bulk_wait_group<0>();
     __syncwarp();
-  } else if (warp < 2 + C::EPI_WARPS + C::SF_WARPS) {
+  } else if (C::SF_CP && warp < 2 + C::EPI_WARPS + C::SF_WARPS) {
+    // ------------------------------------------------------------ SCALES (NVFP4), copied
+    // Lane 0 of scale warp q of the leader CTA copies, for every K stage of the CTA pair's tile
+    // sequence, the scales of MMA q of the stage (one 512-byte atom of A's rows, BN / 128 of B's)
+    // from both CTAs' shared memory into the stage's TMEM scale slot of both CTAs, once the scales
+    // have landed (the leader's sf_full barrier counts both CTAs' copies), and then commits to the
+    // stage's full barrier: its arrival comes when the copies are done.  The slot is free by then:
+    // the producer refilled the stage only after the MMAs that last read it had completed.  The
+    // other warps, and the peer CTA's, only follow the tile sequence.
+    if constexpr (C::SF_CP) {
+      const int q = warp & 3;
+      const bool issuer = prank == 0 && lane == 0;
+      bool ok = true;
+      int k = 0;
+      int step = 0;
+      for (int t = first_tile; t >= 0 && ok; t = next_tile_warp(t, k, ok), ++k) {
+        const WorkItem wk = work_of(t);
+        if (issuer) {
+          for (int kb = wk.kb0; kb < wk.kb1 && ok; ++kb, ++step) {
+            const int j = step % C::STAGES;
+            const uint32_t ph = static_cast<uint32_t>(step / C::STAGES) & 1u;
+            if (!mbar_wait(sf_full_bar(j), ph, tmo, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t slot = tmem_base + static_cast<uint32_t>(C::ACC_COLS + j * C::SF_COLS_STAGE);
+            const uint32_t sfa_s = sSFA + j * C::SFA_STAGE + q * C::SF_ATOM;
+            const uint32_t sfb_s = sSFB + j * C::SFB_STAGE + q * C::SF_ATOM;
+            tmem_cp_32x128b_warpx4<C::CG>(slot + 4u * q, sdesc_rows16(sfa_s));
+#pragma unroll
+            for (int g = 0; g < C::BN / 128; ++g)
+              tmem_cp_32x128b_warpx4<C::CG>(slot + C::SF_COLS_A + (C::BN / 32) * q + 4u * g,
+                                            sdesc_rows16(sfb_s + g * C::KSTEPS * C::SF_ATOM));
+            mma_commit<C::CG>(full_bar(j), 0x1u);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      }
+      if (issuer) {
+        // no copy may still be writing tensor memory when it is released (a stage whose MMAs never
+        // ran, after a timeout elsewhere)
+        mma_commit<C::CG>(cp_drain_bar, 0x1u);
+        mbar_wait(cp_drain_bar, 0, tmo, never_abort);
+      }
+      if (!ok && lane == 0) record_timeout(p.status, kRoleProducer, abort_flag);
+      __syncwarp();
+    }
+  } else if (C::SF_WARPS > 0 && warp < 2 + C::EPI_WARPS + C::SF_WARPS) {
     // ------------------------------------------------------------ SCALES (NVFP4)
     // One warp per TMEM lane quarter q.  For each K stage of the CTA's tile
     // sequence (this group's share of them) it reads the stage's block scales
@@ -784,7 +855,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
     // stage's full barrier in the leader CTA.  The slot is free when the
     // scales land: the producer refilled the stage only after the MMAs that
     // last read the slot had completed.
-    if constexpr (C::SCALED) {
+    if constexpr (C::SF_WARPS > 0 && !C::SF_CP) {
       constexpr int G = C::BN / 32;  // B rows per lane this warp loads and stores
       const int quad = warp & 3;
       const int sgroup = (warp - 2 - C::EPI_WARPS) / 4;  // this warp takes steps sgroup, sgroup + SF_GROUPS, ...
@@ -865,6 +936,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
 
 struct KernelVariant {
   int kind;
+  int sf_atoms;  // NVFP4: staged scales as per-MMA 512-byte atoms (tcgen05.cp) instead of [row][16] runs
   int cg;
   int bn;
   int tile_m;    // output-tile rows (whole CTA pair)
@@ -879,7 +951,7 @@ struct KernelVariant {
 
 template <class C>
 KernelVariant make_variant(const char* name) {
-  return KernelVariant{static_cast<int>(C::KIND), C::CG,        C::BN,      C::TILE_M,    C::EPI_COLS,
+  return KernelVariant{static_cast<int>(C::KIND), C::SF_CP ? 1 : 0, C::CG, C::BN, C::TILE_M, C::EPI_COLS,
                        C::STAGES,                 C::EPI_WARPS, C::THREADS, C::SMEM_BYTES, name,
                        reinterpret_cast<const void*>(&tkg_gemm_kernel<C>)};
 }

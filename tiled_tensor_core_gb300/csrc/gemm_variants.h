@@ -18,7 +18,9 @@ enum VariantId : int {
                                   // four scale warps into tensor memory, eight epilogue warps (NVFP4)
   kVariant2Sm256x512 = 13,        // cta_group::2, 256 x 512 tile per CTA pair: two N = 256 MMAs per K step, the
                                   // second taking A from the tensor core's collector buffer (bf16 / FP8)
-  kNumVariants = 14
+  kVariant2Sm256x256SfCopy = 14,  // cta_group::2, 256 x 256, block scales through shared memory, copied into
+                                  // tensor memory (tcgen05.cp) by four issuing threads (NVFP4)
+  kNumVariants = 15
 };
 
 // Each returns the variant for `id`, or nullptr if that kind has no such variant.
@@ -27,12 +29,13 @@ const KernelVariant* fp8_variant(int id);
 const KernelVariant* nvfp4_variant(int id);
 
 // NVFP4: rewrite row-major [rows][K/16] block scales of A and B into the
-// 2 KB per (K stage, 128-row block) runs, [row][16 scales] inside a run, that
-// the GEMM stages (A's at scratch, B's at scratch + b_offset).  One kernel
-// launch on `stream`, as a programmatic dependent of the previous kernel if
-// `overlap` (it waits for that kernel before touching memory either way).
+// 2 KB per (K stage, 128-row block) runs that the GEMM stages (A's at scratch,
+// B's at scratch + b_offset): [row][16 scales] inside a run, or with `atoms`
+// four 512-byte per-MMA atoms (see gemm_nvfp4.cu).  One kernel launch on
+// `stream`, as a programmatic dependent of the previous kernel if `overlap`
+// (it waits for that kernel before touching memory either way).
 cudaError_t nvfp4_interleave_scales(const uint8_t* sfa, const uint8_t* sfb, int M, int N, int K, int blocks_a,
-                                    int blocks_b, int kstages, uint8_t* scratch, size_t b_offset,
+                                    int blocks_b, int kstages, int atoms, uint8_t* scratch, size_t b_offset,
                                     cudaStream_t stream, bool overlap);
 size_t nvfp4_scratch_bytes(int blocks_a, int blocks_b, int kstages);
 

@@ -328,6 +328,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   return d;
 }
 
+// Shared-memory descriptor for 32 (or more) rows of 16 bytes stored one after
+// another with no swizzle: 8-row groups of 128 bytes at a 128-byte stride (the
+// source of a tcgen05.cp of 32 rows x 128 bits).
+__device__ __forceinline__ uint64_t sdesc_rows16(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(128u >> 4) << 16;
+  d |= static_cast<uint64_t>(128u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  return d;
+}
+
 // Shared-memory descriptor for an MN-major operand tile with the 128-byte
 // swizzle: each row of 128 bytes holds 64 consecutive M (or N) elements of one
 // K index, 8 rows (8 K indices) form a 1024-byte atom.  `mn_stride` = bytes
@@ -444,6 +456,20 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask) {
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
       "h"(mask)
       : "memory");
+}
+
+// Shared -> tensor memory copy of 32 rows x 128 bits into lanes taddr.lane + r
+// of every 32-lane quarter (row r of the source to lane r of each quarter),
+// four consecutive columns from taddr.col; with cta_group::2, issued by the
+// leader, each CTA of the pair copies from its own shared memory into its own
+// tensor memory.  Runs on the tensor pipe in issue order with this thread's
+// MMAs.
+template <int CG>
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+  if constexpr (CG == 1)
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+  else
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // 32 lanes x 32 consecutive fp32 columns: thread i of the warp receives lane
