@@ -61,12 +61,12 @@ DTYPE = {"bf16": "bf16", "fp8": "e4m3", "nvfp4": "e2m1+e4m3"}
 # (profiles/gemm_*_ncu.md, profiles/attention_fwd_4096_d128_ncu.md), valid only while the sources of
 # that kernel hash to the value recorded with it.
 TRAFFIC = {
-    "bf16_4096": {"bytes": 93_894_656, "src": "08c2b4e0fac8c8d3"},
-    "bf16_8192": {"bytes": 831_954_176, "src": "08c2b4e0fac8c8d3"},
-    "bf16_skinny": {"bytes": 431_350_272, "src": "08c2b4e0fac8c8d3"},
-    "fp8_8192": {"bytes": 395_776_768, "src": "debcfee094d747c7"},
-    "nvfp4_16384": {"bytes": 1_621_055_232, "src": "5a47adf3141762d3"},
-    "attn_n4096_d128": {"bytes": 1_062_417_152, "src": "55fd825c5402713b"},
+    "bf16_4096": {"bytes": 94_393_088, "src": "d1e101cd173f3b69"},
+    "bf16_8192": {"bytes": 830_366_976, "src": "d1e101cd173f3b69"},
+    "bf16_skinny": {"bytes": 430_362_624, "src": "d1e101cd173f3b69"},
+    "fp8_8192": {"bytes": 393_982_720, "src": "37174705cfb83bd3"},
+    "nvfp4_16384": {"bytes": 1_574_212_352, "src": "9bb36253d9de5a7a"},
+    "attn_n4096_d128": {"bytes": 1_058_660_352, "src": "b961c627d127cc4f"},
 }
 KERNEL_SOURCES = {
     "bf16": ("tkg_device.cuh", "gemm_kernel.cuh", "gemm_bf16.cu"),

@@ -205,15 +205,16 @@ TKG_API void tkg_shutdown(void);
  *                      "Block Launch Order and L2 Cache Reuse", Table 3,
  *                      where the paper takes G = 8; 16 reads the least
  *                      from HBM on GB300 with 256-row pair tiles)
- *  TKG_OPT_VARIANT     force a kernel variant: 0 = the default (8 for
+ *  TKG_OPT_VARIANT     force a kernel variant: 0 = the default (14 for
  *                      NVFP4; for bf16 and FP8 13 when K >= 4096 and the
  *                      256x512 tiles fill at least four rounds of the
  *                      device's CTA pairs, else 2); 2 = 2-SM (CTA pair)
  *                      256x256 tiles, two tensor-memory accumulators (bf16
- *                      and FP8); 8 = 2-SM 256x256 tiles, one accumulator,
+ *                      and FP8); 14 = 2-SM 256x256 tiles, one accumulator,
  *                      the block scales brought into shared memory by the
- *                      ring's TMA and written to tensor memory by eight
- *                      scale warps (NVFP4); 13 = 2-SM 256x512 tiles, two
+ *                      ring's TMA and copied into tensor memory
+ *                      (tcgen05.cp) by four issuing threads (NVFP4);
+ *                      13 = 2-SM 256x512 tiles, two
  *                      N = 256 MMAs per K step into all 512 tensor-memory
  *                      columns, the second reusing A from the tensor
  *                      core's collector buffer (bf16 and FP8; no split-K

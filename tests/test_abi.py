@@ -242,7 +242,7 @@ def test_swizzle_selection_matches_definition(tkg):
 
 
 def test_compiled_variants_fit_the_sm(tkg):
-    compiled = {0: (2, 13), 1: (2, 13), 2: (8, 14)}
+    compiled = {0: (2, 13), 1: (2, 13), 2: (14,)}
     for kind in (0, 1, 2):
         for v in range(1, 16):
             if v not in compiled[kind]:
@@ -251,7 +251,7 @@ def test_compiled_variants_fit_the_sm(tkg):
                 continue
             info = tkg.tkg_debug_variant_info(kind, v)
             assert info["smem_bytes"] <= 232448
-            assert info["threads"] in (192, 320, 448)
+            assert info["threads"] in (192, 448)
             assert info["cta_group"] == 2
             assert info["tile_m"] == 256
             assert info["tile_n"] == (512 if v == 13 else 256)

@@ -565,8 +565,8 @@ tkg_status gemm_launch(int kind, int64_t M, int64_t N, int64_t K, const void* A,
       return TKG_ERR_CUDA;
     }
     if (nvfp4_interleave_scales(scales->a_block_scale, scales->b_block_scale, static_cast<int>(M),
-                                static_cast<int>(N), static_cast<int>(K), g.sf_blocks_a, g.sf_blocks_b, g.num_kb,
-                                g.v->sf_atoms, scratch, g.sf_b_off, cs, launch_overlap()) != cudaSuccess) {
+                                static_cast<int>(N), static_cast<int>(K), g.sf_blocks_a, g.sf_blocks_b, g.num_kb, scratch,
+                                g.sf_b_off, cs, launch_overlap()) != cudaSuccess) {
       cudaGetLastError();
       release();
       return TKG_ERR_CUDA;

@@ -6,7 +6,7 @@
 namespace tkg {
 
 using Bf16_2Sm_256 = GemmCfg<Kind::BF16, 2, 256, 6, 4>;
-using Bf16_2Sm_512 = GemmCfg<Kind::BF16, 2, 512, 4, 4, 1, 2, true>;
+using Bf16_2Sm_512 = GemmCfg<Kind::BF16, 2, 512, 4, 4, 1, true>;
 
 const KernelVariant* bf16_variant(int id) {
   static const KernelVariant v2 = make_variant<Bf16_2Sm_256>("bf16_2sm_256x256_s6");

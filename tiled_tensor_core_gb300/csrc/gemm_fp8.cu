@@ -8,7 +8,7 @@
 namespace tkg {
 
 using Fp8_2Sm_256 = GemmCfg<Kind::FP8, 2, 256, 6, 4>;
-using Fp8_2Sm_512 = GemmCfg<Kind::FP8, 2, 512, 4, 4, 1, 2, true>;
+using Fp8_2Sm_512 = GemmCfg<Kind::FP8, 2, 512, 4, 4, 1, true>;
 
 const KernelVariant* fp8_variant(int id) {
   static const KernelVariant v2 = make_variant<Fp8_2Sm_256>("fp8_2sm_256x256_s6");

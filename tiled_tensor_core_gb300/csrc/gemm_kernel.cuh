@@ -113,18 +113,20 @@ __host__ __device__ inline WorkItem work_item(int w, int split_tiles, int split_
 
 // NVFP4 block scales.  The caller's row-major [rows][K/16] e4m3 scales are
 // first rewritten on the device into 2 KB runs, one per (256-deep K stage,
-// 128-row block), [row][16 scales] inside a run.  The producer's TMA brings
-// each stage's runs (A: this CTA's 128 rows; B: all BN rows of the tile, since
-// every CTA of a pair multiplies by all of B) into shared memory beside the
-// operands, on the CTA's own sf_full barrier.  SF_GROUPS groups of four scale
-// warps (one warp per TMEM lane quarter; group g takes every SF_GROUPS-th
-// stage) read them there and write them with tcgen05.st into the stage's TMEM
-// scale slot, then arrive on the stage's full barrier, so the MMA thread waits
-// once per stage and the tensor pipe only runs MMAs (copying the scales with
-// tcgen05.cp instead costs the tensor pipe about 60 cycles per copy, twelve
-// copies per stage of a 256 x 256 tile).
-template <Kind KIND_, int CG_, int BN_, int STAGES_, int EPI_WARPS_, int NUM_ACC_ = 2, int SF_GROUPS_ = 2,
-          bool COLL_A_ = false, int EPI_BUFS_ = 2>
+// 128-row block), each run four 512-byte atoms, one per MMA of the stage
+// (gemm_nvfp4.cu).  The producers' TMA brings each stage's runs (A: the CTA's
+// own 128 rows; B: all BN rows of the tile, since every CTA of a pair
+// multiplies by all of B, and each TMEM lane quarter reads all of B's scales
+// from its own lanes) into shared memory beside the operands, both CTAs' on
+// the leader's sf_full barrier.  One lane of each of four scale warps of the
+// leader then copies them into the stage's TMEM scale slot in both CTAs with
+// tcgen05.cp (three 32x128b.warpx4 copies per MMA: one atom of A, BN / 128 of
+// B) and commits to the stage's full barrier, so the MMA thread waits once per
+// stage.  A thread issues a copy about every 60-80 cycles, so copies from one
+// thread cannot keep up with the MMAs; from four warps, each taking one MMA
+// of every stage, they run beside them.
+template <Kind KIND_, int CG_, int BN_, int STAGES_, int EPI_WARPS_, int NUM_ACC_ = 2, bool COLL_A_ = false,
+          int EPI_BUFS_ = 2>
 struct GemmCfg {
   static constexpr Kind KIND = KIND_;
   static constexpr int CG = CG_;                // CTAs per MMA (1, or 2 for the CTA pair) = CTAs per cluster
@@ -154,19 +156,15 @@ struct GemmCfg {
   static constexpr int B_BOX = B_ROWS * ROW_BYTES;             // bytes of one B tile load
   static constexpr int B_STAGE = (B_BOX + 1023) / 1024 * 1024;  // keeps every stage 1024-byte aligned
   // NVFP4 block scales per stage in shared memory: 16 bytes (the 16 scales of 256 K elements) per row,
-  // this CTA's 128 rows of A and all BN rows of B
+  // this CTA's 128 rows of A and all BN rows of B, as per-MMA atoms
   static constexpr int SF_ROW_BYTES = 16;
   static constexpr int SFA_STAGE = SCALED ? BM * SF_ROW_BYTES : 0;
   static constexpr int SFB_STAGE = SCALED ? BN * SF_ROW_BYTES : 0;
-  // SF_GROUPS_ = 0: the scales are copied from shared into tensor memory with tcgen05.cp, one lane of
-  // each of the four scale warps of the leader CTA issuing the copies of one MMA of every stage (a
-  // thread issues a copy about every 60-80 cycles; copies from several threads overlap the MMAs)
-  static constexpr bool SF_CP = SCALED && SF_GROUPS_ == 0;
-  static constexpr int SF_GROUPS = SCALED ? (SF_CP ? 1 : SF_GROUPS_) : 0;
-  static constexpr int SF_WARPS = 4 * SF_GROUPS;
+  // four scale warps: lane 0 of scale warp q of the leader copies the scales of MMA q of every stage
+  static constexpr int SF_WARPS = SCALED ? 4 : 0;
   static constexpr int SF_TX = SFA_STAGE + SFB_STAGE;
-  // operand bytes landing per CTA per stage on the (leader's) full barrier; the scales land on the
-  // CTA's own sf_full barrier (scale warps) or, copied, on the leader's
+  // operand bytes landing per CTA per stage on the leader's full barrier (the scales land on its
+  // sf_full barrier)
   static constexpr int STAGE_TX = A_STAGE + B_BOX;
   // one 512-byte shared-memory atom per MMA and 128 rows: the 4 scales of rows r, r + 32, r + 64,
   // r + 96 at byte 16 r (r < 32), which tcgen05.cp.32x128b.warpx4 puts at lane r of every TMEM lane
@@ -204,7 +202,7 @@ struct GemmCfg {
   static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_BUFS * EPI_BUF;
   // full / empty per stage, tensor-memory full / empty per accumulator, drain, and (NVFP4) the
   // per-stage sf_full barriers
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1 + (SCALED ? STAGES : 0) + (SF_CP ? 1 : 0);
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1 + (SCALED ? STAGES : 0) + (SCALED ? 1 : 0);
   // dynamic schedule: ring of cancellation answers (16 bytes each) with a full
   // barrier per slot in every CTA and an empty barrier per slot in the leader,
   // after the barriers above
@@ -231,7 +229,6 @@ struct GemmCfg {
   static_assert(TMEM_USED <= 512, "tensor memory has 512 columns");
   static_assert(!SCALED || (ACC_COLS % 16 == 0 && SF_COLS_STAGE % 16 == 0 && SF_COLS_A == 16),
                 "scale columns are written 16 at a time at 16-column-aligned addresses");
-  static_assert(!SCALED || SF_GROUPS == 1 || SF_GROUPS == 2, "one or two groups of scale warps");
   static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB shared-memory limit");
 };
 
@@ -318,9 +315,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      // + one arrival per scale warp of the group (writing the scales: every CTA's; copying them: the
-      // leader's, by tcgen05.commit once its copies are done)
-      mbar_init(full_bar(s), C::SCALED ? 1 + (C::SF_CP ? 4 : C::CG * 4) : 1);
+      // + one arrival per copy issuer of the leader (NVFP4; its tcgen05.commit, once its copies are done)
+      mbar_init(full_bar(s), C::SCALED ? 1 + 4 : 1);
       mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < C::NUM_ACC; ++a) {
@@ -331,7 +327,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
     if constexpr (C::SCALED) {
       for (int st = 0; st < C::STAGES; ++st) mbar_init(sf_full_bar(st), 1);
     }
-    if constexpr (C::SF_CP) mbar_init(cp_drain_bar, 4);
+    if constexpr (C::SCALED) mbar_init(cp_drain_bar, 4);
     for (int j = 0; j < C::SCHED_SLOTS; ++j) {
       mbar_init(sched_full_bar(j), 1);  // the leader's expect_tx arrival + the 16-byte answer
       mbar_init(sched_empty_bar(j), C::SCHED_READERS);
@@ -453,23 +449,14 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
                                  kb * C::K_TMAP, b_row + sub * C::MMA_N);
             if constexpr (C::SCALED) {
               // staged scales: 2 KB (16 rows of 128 B) per (K stage, 128-row block), the blocks of
-              // one K stage contiguous; with scale warps they land on this CTA's own sf_full
-              // barrier, else with the operands on the leader's full barrier
+              // one K stage contiguous; both CTAs' land on the leader's sf_full barrier, since the
+              // leader's copies read them from both CTAs' shared memory
               const int ya = (kb * p.sf_blocks_a + a_row / 128) * 16;
               const int yb = (kb * p.sf_blocks_b + (tn * C::BN) / 128) * 16;
-              if constexpr (C::SF_CP) {
-                // both CTAs' scales land on the leader's sf_full barrier: the leader's copies read
-                // them from both CTAs' shared memory
-                const uint32_t sfb_bar = (C::CG == 2) ? mapa_shared(sf_full_bar(stage), leader) : sf_full_bar(stage);
-                if (prank == 0) mbar_arrive_expect_tx(sf_full_bar(stage), C::SF_TX * C::CG);
-                tma_load_2d<C::CG>(sSFA + stage * C::SFA_STAGE, &p.tmap_sfa, sfb_bar, 0, ya);
-                tma_load_2d<C::CG>(sSFB + stage * C::SFB_STAGE, &p.tmap_sfb, sfb_bar, 0, yb);
-              } else {
-                const uint32_t sfb_bar = sf_full_bar(stage);
-                mbar_arrive_expect_tx(sfb_bar, C::SF_TX);
-                tma_load_2d<1>(sSFA + stage * C::SFA_STAGE, &p.tmap_sfa, sfb_bar, 0, ya);
-                tma_load_2d<1>(sSFB + stage * C::SFB_STAGE, &p.tmap_sfb, sfb_bar, 0, yb);
-              }
+              const uint32_t sfb_bar = (C::CG == 2) ? mapa_shared(sf_full_bar(stage), leader) : sf_full_bar(stage);
+              if (prank == 0) mbar_arrive_expect_tx(sf_full_bar(stage), C::SF_TX * C::CG);
+              tma_load_2d<C::CG>(sSFA + stage * C::SFA_STAGE, &p.tmap_sfa, sfb_bar, 0, ya);
+              tma_load_2d<C::CG>(sSFB + stage * C::SFB_STAGE, &p.tmap_sfb, sfb_bar, 0, yb);
             }
           }
           first = false;
@@ -512,8 +499,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
           tc_fence_after();
           const uint32_t a0 = sA + stage * C::A_STAGE;
           const uint32_t b0 = sB + stage * C::B_STAGE;
-          // this stage's TMEM scale slot (NVFP4): the stage's full barrier also counts the scale
-          // warps that filled it
+          // this stage's TMEM scale slot (NVFP4): the stage's full barrier also counts the copy
+          // issuers that filled it
           const uint32_t sf_tmem = tmem_base + static_cast<uint32_t>(C::ACC_COLS + stage * C::SF_COLS_STAGE);
 #pragma unroll
           for (int kk = 0; kk < C::KSTEPS; ++kk) {
@@ -794,8 +781,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
     if (!seq_ok && lane == 0) record_timeout(p.status, kRoleEpilogue, abort_flag);
     if (lane == 0) bulk_wait_group<0>();
     __syncwarp();
-  } else if (C::SF_CP && warp < 2 + C::EPI_WARPS + C::SF_WARPS) {
-    // ------------------------------------------------------------ SCALES (NVFP4), copied
+  } else if (warp < 2 + C::EPI_WARPS + C::SF_WARPS) {
+    // ------------------------------------------------------------ SCALES (NVFP4)
     // Lane 0 of scale warp q of the leader CTA copies, for every K stage of the CTA pair's tile
     // sequence, the scales of MMA q of the stage (one 512-byte atom of A's rows, BN / 128 of B's)
     // from both CTAs' shared memory into the stage's TMEM scale slot of both CTAs, once the scales
@@ -803,7 +790,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
     // stage's full barrier: its arrival comes when the copies are done.  The slot is free by then:
     // the producer refilled the stage only after the MMAs that last read it had completed.  The
     // other warps, and the peer CTA's, only follow the tile sequence.
-    if constexpr (C::SF_CP) {
+    if constexpr (C::SCALED) {
       const int q = warp & 3;
       const bool issuer = prank == 0 && lane == 0;
       bool ok = true;
@@ -842,81 +829,6 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
       if (!ok && lane == 0) record_timeout(p.status, kRoleProducer, abort_flag);
       __syncwarp();
     }
-  } else if (C::SF_WARPS > 0 && warp < 2 + C::EPI_WARPS + C::SF_WARPS) {
-    // ------------------------------------------------------------ SCALES (NVFP4)
-    // One warp per TMEM lane quarter q.  For each K stage of the CTA's tile
-    // sequence (this group's share of them) it reads the stage's block scales
-    // from shared memory once the producer's TMA has put them there, and
-    // writes them into the stage's TMEM scale slot with tcgen05.st: A's row
-    // 32q+lane to lane 32q+lane, column 4t+q of the slot's A columns (one word
-    // = the 4 scales of MMA t); B's rows 32g+lane (g < BN/32) to lane
-    // 32q+lane, column (BN/32)t+g of the slot's B columns, in every quarter
-    // (each quarter's rows read all of B's scales).  Then it arrives on the
-    // stage's full barrier in the leader CTA.  The slot is free when the
-    // scales land: the producer refilled the stage only after the MMAs that
-    // last read the slot had completed.
-    if constexpr (C::SF_WARPS > 0 && !C::SF_CP) {
-      constexpr int G = C::BN / 32;  // B rows per lane this warp loads and stores
-      const int quad = warp & 3;
-      const int sgroup = (warp - 2 - C::EPI_WARPS) / 4;  // this warp takes steps sgroup, sgroup + SF_GROUPS, ...
-      const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
-      const uint32_t ready_leader0 = (C::CG == 2) ? mapa_shared(full_bar(0), leader) : full_bar(0);
-      bool ok = true;
-      // scales of step s: [0] = this lane's A row, [1 + g] = B row 32g + lane, from the stage's
-      // shared-memory copy once it has landed
-      auto fetch = [&](int s_, uint4 (&v)[1 + G]) -> bool {
-        const int j = s_ % C::STAGES;
-        const uint32_t ph = static_cast<uint32_t>(s_ / C::STAGES) & 1u;
-        if (!__all_sync(0xffffffffu, mbar_wait(sf_full_bar(j), ph, tmo, abort_flag))) return false;
-        v[0] = ld_shared_v4(sSFA + j * C::SFA_STAGE + static_cast<uint32_t>(quad * 32 + lane) * 16u);
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-          v[1 + g] = ld_shared_v4(sSFB + j * C::SFB_STAGE + static_cast<uint32_t>(g * 32 + lane) * 16u);
-        return true;
-      };
-      // step s into the TMEM slot of its ring stage
-      auto put = [&](int s_, const uint4 (&v)[1 + G]) {
-        const int j = s_ % C::STAGES;
-        tc_fence_after();
-        const uint32_t cols = lane_base + static_cast<uint32_t>(C::ACC_COLS + j * C::SF_COLS_STAGE);
-        // A: only column 4t + q of MMA t is read by this quarter's rows
-        tmem_st_32x32b_x1(cols + static_cast<uint32_t>(quad), v[0].x);
-        tmem_st_32x32b_x1(cols + 4u + static_cast<uint32_t>(quad), v[0].y);
-        tmem_st_32x32b_x1(cols + 8u + static_cast<uint32_t>(quad), v[0].z);
-        tmem_st_32x32b_x1(cols + 12u + static_cast<uint32_t>(quad), v[0].w);
-        uint32_t rbw[G * C::KSTEPS];
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          rbw[0 * G + g] = v[1 + g].x;
-          rbw[1 * G + g] = v[1 + g].y;
-          rbw[2 * G + g] = v[1 + g].z;
-          rbw[3 * G + g] = v[1 + g].w;
-        }
-#pragma unroll
-        for (int h = 0; h < (G * C::KSTEPS) / 16; ++h)
-          tmem_st_32x32b_x16(cols + C::SF_COLS_A + 16u * h, *reinterpret_cast<uint32_t(*)[16]>(rbw + 16 * h));
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(ready_leader0 + 8u * j);
-      };
-      // Step s is K stage kb of the k-th work item of the sequence; this group takes the steps
-      // with s % SF_GROUPS == sgroup.
-      uint4 v0[1 + G];
-      int k = 0;
-      int step = 0;  // K stages of the sequence so far: the ring position of the next one
-      for (int t = first_tile; t >= 0 && ok; t = next_tile_warp(t, k, ok), ++k) {
-        const WorkItem wk = work_of(t);
-        for (int kb = wk.kb0; kb < wk.kb1 && ok; ++kb) {
-          const int s_ = step++;
-          if (s_ % C::SF_GROUPS != sgroup) continue;
-          ok = fetch(s_, v0);
-          if (ok) put(s_, v0);
-        }
-      }
-      if (!ok && lane == 0) record_timeout(p.status, kRoleProducer, abort_flag);
-      __syncwarp();
-    }
   }
 
   // ------------------------------------------------------------ teardown
@@ -936,7 +848,6 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
 
 struct KernelVariant {
   int kind;
-  int sf_atoms;  // NVFP4: staged scales as per-MMA 512-byte atoms (tcgen05.cp) instead of [row][16] runs
   int cg;
   int bn;
   int tile_m;    // output-tile rows (whole CTA pair)
@@ -951,7 +862,7 @@ struct KernelVariant {
 
 template <class C>
 KernelVariant make_variant(const char* name) {
-  return KernelVariant{static_cast<int>(C::KIND), C::SF_CP ? 1 : 0, C::CG, C::BN, C::TILE_M, C::EPI_COLS,
+  return KernelVariant{static_cast<int>(C::KIND), C::CG,        C::BN,      C::TILE_M,    C::EPI_COLS,
                        C::STAGES,                 C::EPI_WARPS, C::THREADS, C::SMEM_BYTES, name,
                        reinterpret_cast<const void*>(&tkg_gemm_kernel<C>)};
 }

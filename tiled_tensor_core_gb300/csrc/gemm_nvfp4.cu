@@ -5,18 +5,17 @@
 // tiling paragraphs).
 //
 // The tensor core reads the scales of one MMA (64 K elements = 4 scales per
-// row) from tensor memory: row m of a 128-row block at lane m, column
-// (base + m/32), byte = 16-element slice.  The caller's row-major [rows][K/16]
-// scales are first rewritten by interleave_scales_kernel into 2 KB runs, one
-// per (256-deep K stage, 128-row block), [row][16 scales] inside a run, the
-// runs of one K stage contiguous, so that every ring stage loads one
-// contiguous run per 128 rows with a plain 2-D TMA box.  Two ways into tensor
-// memory (gemm_kernel.cuh): scale warps read a row's 16 bytes from the stage's
-// shared-memory copy and write them to the row's own TMEM lane with
-// tcgen05.st; or the run holds four 512-byte atoms, one per MMA of the stage,
-// the 4 scales of rows r, r + 32, r + 64, r + 96 at byte 16 r, which one
-// tcgen05.cp.32x128b.warpx4 turns into that layout (lane r of quarter q,
-// column base + q: row 32 q + r).
+// row) from tensor memory: row m of A's 128-row block at lane m, column
+// (base + m/32); row n of B at lane n % 32 of every lane quarter, column
+// (base + n/32); byte j = the j-th 16-element slice.  The caller's row-major
+// [rows][K/16] scales are first rewritten by interleave_scales_kernel into
+// 2 KB runs, one per (256-deep K stage, 128-row block), the runs of one K
+// stage contiguous, so that every ring stage loads one contiguous run per 128
+// rows with a plain 2-D TMA box.  A run is four 512-byte atoms, one per MMA of
+// the stage, holding the 4 scales of rows r, r + 32, r + 64, r + 96 at byte
+// 16 r (r < 32): one tcgen05.cp.32x128b.warpx4 puts row r's 16 bytes at lane
+// r of every lane quarter, columns c .. c + 3, which is both layouts above
+// (gemm_kernel.cuh issues the copies).
 #include <cuda_bf16.h>
 
 #include "gemm_variants.h"
@@ -24,16 +23,13 @@
 namespace tkg {
 
 // five 38 KB ring stages, one accumulator, eight epilogue warps (two per TMEM lane quarter, each
-// draining half of the columns, one staging tile each) and one group of four scale warps
-using Nvfp4_2Sm_256 = GemmCfg<Kind::NVFP4, 2, 256, 5, 8, 1, 1, false, 1>;
-// the same with the scales copied into tensor memory (tcgen05.cp) by one lane of each scale warp
-using Nvfp4_2Sm_256_Cp = GemmCfg<Kind::NVFP4, 2, 256, 5, 8, 1, 0, false, 1>;
+// draining half of the columns, one staging tile each), four scale warps whose leader lanes copy
+// the scales into tensor memory
+using Nvfp4_2Sm_256 = GemmCfg<Kind::NVFP4, 2, 256, 5, 8, 1, false, 1>;
 
 const KernelVariant* nvfp4_variant(int id) {
-  static const KernelVariant v8 = make_variant<Nvfp4_2Sm_256>("nvfp4_2sm_256x256_s5_epi8_sfw4_smem");
-  static const KernelVariant v14 = make_variant<Nvfp4_2Sm_256_Cp>("nvfp4_2sm_256x256_s5_epi8_sfcp");
+  static const KernelVariant v14 = make_variant<Nvfp4_2Sm_256>("nvfp4_2sm_256x256_s5_epi8_sfcp");
   switch (id) {
-    case kVariant2Sm256x256SfSmem: return &v8;
     case kVariant2Sm256x256SfCopy: return &v14;
     default: return nullptr;
   }
@@ -43,21 +39,19 @@ namespace {
 
 struct InterleaveArgs {
   const uint8_t* src;  // row-major [rows][k16] e4m3 scales
-  uint8_t* dst;        // runs [kstages][blocks][128 rows][16 scales], or [kstages][blocks][4 MMAs][512-byte atom]
+  uint8_t* dst;        // runs [kstages][blocks][4 MMAs][512-byte atom]
   int rows;            // valid rows
   int k16;             // scales per row (K / 16)
   int blocks;          // 128-row blocks in dst (rows padded with zero scales)
   int kstages;         // 256-element K stages in dst (padded with zero scales)
-  int atoms;           // per-MMA atoms instead of [row][16 scales]
 };
 
-// One CTA rewrites one 128-row block for two consecutive K stages: thread t moves the 16 scales of
-// row t % 128 for stage kb0 + t / 128 (one 16-byte load from the row-major source, one 16-byte store
-// into the stage's run), so a warp writes 512 contiguous bytes and the two halves of the CTA read
-// each source row's 32 bytes (one sector) together.  Scales of rows or K positions past the matrix
-// are written as 0; a stage that runs past the last K position, or a row pitch that is not a
-// multiple of 16 bytes, takes byte loads.  For the atom layout the 128 rows of a stage pass through
-// shared memory so that the atoms, too, are written 512 contiguous bytes per warp.
+// One CTA rewrites one 128-row block for two consecutive K stages: thread t loads the 16 scales of
+// row t % 128 for stage kb0 + t / 128 (one 16-byte load from the row-major source; the two halves of
+// the CTA read each source row's 32 bytes, one sector, together) into shared memory, then writes
+// the 16 bytes of atom (t % 128) / 32 at row t % 32, so a warp writes 512 contiguous bytes.  Scales
+// of rows or K positions past the matrix are written as 0; a stage that runs past the last K
+// position, or a row pitch that is not a multiple of 16 bytes, takes byte loads.
 __global__ void __launch_bounds__(256) interleave_scales_kernel(InterleaveArgs a, InterleaveArgs b, int blocks_a) {
   // launched as a programmatic dependent: the previous GEMM may still read the
   // scratch this kernel rewrites, or a previous kernel still write the scales
@@ -87,12 +81,8 @@ __global__ void __launch_bounds__(256) interleave_scales_kernel(InterleaveArgs a
     }
   }
   const size_t run = static_cast<size_t>(kb) * s.blocks + rb;
-  if (!s.atoms) {
-    if (live) *reinterpret_cast<uint4*>(s.dst + run * 2048 + static_cast<size_t>(r_in) * 16) = v;
-    return;
-  }
-  // atoms: through shared memory, thread t then writes the 16 bytes of atom t / 32 (the stage's MMA)
-  // at row r = t % 32: that MMA's 4 scales of rows r, r + 32, r + 64, r + 96
+  // thread t then writes the 16 bytes of atom t / 32 (the stage's MMA) at row r = t % 32: that MMA's 4
+  // scales of rows r, r + 32, r + 64, r + 96
   __shared__ uint4 rows16[2][128];
   rows16[half][r_in] = v;
   __syncthreads();
@@ -111,10 +101,10 @@ __global__ void __launch_bounds__(256) interleave_scales_kernel(InterleaveArgs a
 // Rewrites both operands' scales into `scratch` (see the layout above), B's
 // runs at byte offset `b_offset`.
 cudaError_t nvfp4_interleave_scales(const uint8_t* sfa, const uint8_t* sfb, int M, int N, int K, int blocks_a,
-                                    int blocks_b, int kstages, int atoms, uint8_t* scratch, size_t b_offset,
+                                    int blocks_b, int kstages, uint8_t* scratch, size_t b_offset,
                                     cudaStream_t stream, bool overlap) {
-  InterleaveArgs a{sfa, scratch, M, K / 16, blocks_a, kstages, atoms};
-  InterleaveArgs b{sfb, scratch + b_offset, N, K / 16, blocks_b, kstages, atoms};
+  InterleaveArgs a{sfa, scratch, M, K / 16, blocks_a, kstages};
+  InterleaveArgs b{sfb, scratch + b_offset, N, K / 16, blocks_b, kstages};
   const int kpairs = (kstages + 1) / 2;
   const int grid_a = blocks_a * kpairs;
   const int grid_b = blocks_b * kpairs;

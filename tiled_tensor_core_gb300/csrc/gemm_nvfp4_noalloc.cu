@@ -76,8 +76,8 @@ extern "C" tkg_status tkg_gemm_nvfp4_noalloc(int64_t M, int64_t N, int64_t K, co
   // kernel (zeros for padding), so no clearing is needed between calls.
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (nvfp4_interleave_scales(scales->a_block_scale, scales->b_block_scale, static_cast<int>(M), static_cast<int>(N),
-                              static_cast<int>(K), g.sf_blocks_a, g.sf_blocks_b, g.num_kb, g.v->sf_atoms, scratch,
-                              g.sf_b_off, cs, launch_overlap()) != cudaSuccess) {
+                              static_cast<int>(K), g.sf_blocks_a, g.sf_blocks_b, g.num_kb, scratch, g.sf_b_off, cs,
+                              launch_overlap()) != cudaSuccess) {
     cudaGetLastError();
     return TKG_ERR_CUDA;
   }

@@ -9,17 +9,17 @@ namespace tkg {
 // Variant ids (also the values of TKG_OPT_VARIANT).  The ids are those of the
 // kernel forms measured while the tile shape was chosen; the forms that lost
 // (1-SM 128 x 256, 256 x 128 / 192 / 224 pair tiles, A multicast between two
-// pairs, a 512 x 256 pair tile whose two MMAs share B, NVFP4 scale staging by
-// tensor-pipe copies or from global memory) are no longer compiled.
+// pairs, a 512 x 256 pair tile whose two MMAs share B, NVFP4 scales read from
+// global memory, copied by the MMA-issuing thread or written into tensor
+// memory with tcgen05.st by scale warps) are no longer compiled.
 enum VariantId : int {
   kVariantAuto = 0,
   kVariant2Sm256x256 = 2,         // cta_group::2, 256 x 256 tile per CTA pair (bf16 / FP8)
-  kVariant2Sm256x256SfSmem = 8,   // cta_group::2, 256 x 256, block scales through shared memory and
-                                  // four scale warps into tensor memory, eight epilogue warps (NVFP4)
   kVariant2Sm256x512 = 13,        // cta_group::2, 256 x 512 tile per CTA pair: two N = 256 MMAs per K step, the
                                   // second taking A from the tensor core's collector buffer (bf16 / FP8)
   kVariant2Sm256x256SfCopy = 14,  // cta_group::2, 256 x 256, block scales through shared memory, copied into
-                                  // tensor memory (tcgen05.cp) by four issuing threads (NVFP4)
+                                  // tensor memory (tcgen05.cp) by four issuing threads, eight epilogue warps
+                                  // (NVFP4)
   kNumVariants = 15
 };
 
@@ -30,12 +30,12 @@ const KernelVariant* nvfp4_variant(int id);
 
 // NVFP4: rewrite row-major [rows][K/16] block scales of A and B into the
 // 2 KB per (K stage, 128-row block) runs that the GEMM stages (A's at scratch,
-// B's at scratch + b_offset): [row][16 scales] inside a run, or with `atoms`
-// four 512-byte per-MMA atoms (see gemm_nvfp4.cu).  One kernel launch on
-// `stream`, as a programmatic dependent of the previous kernel if `overlap`
-// (it waits for that kernel before touching memory either way).
+// B's at scratch + b_offset), four 512-byte per-MMA atoms inside a run (see
+// gemm_nvfp4.cu).  One kernel launch on `stream`, as a programmatic dependent
+// of the previous kernel if `overlap` (it waits for that kernel before
+// touching memory either way).
 cudaError_t nvfp4_interleave_scales(const uint8_t* sfa, const uint8_t* sfb, int M, int N, int K, int blocks_a,
-                                    int blocks_b, int kstages, int atoms, uint8_t* scratch, size_t b_offset,
+                                    int blocks_b, int kstages, uint8_t* scratch, size_t b_offset,
                                     cudaStream_t stream, bool overlap);
 size_t nvfp4_scratch_bytes(int blocks_a, int blocks_b, int kstages);
 
