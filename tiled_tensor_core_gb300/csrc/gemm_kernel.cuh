@@ -442,15 +442,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
           const uint32_t fb = (C::CG == 2) ? mapa_shared(full_bar(stage), leader) : full_bar(stage);
           if (prank == 0) mbar_arrive_expect_tx(full_bar(stage), C::STAGE_TX * C::CG);
           if (!(first && p.fault_mode == 1)) {
-            tma_load_2d<C::CG>(sA + stage * C::A_STAGE, &p.tmap_a, fb, kb * C::K_TMAP, a_row);
-#pragma unroll
-            for (int sub = 0; sub < C::NSUB; ++sub)
-              tma_load_2d<C::CG>(sB + stage * C::B_STAGE + sub * C::B_SUB_ROWS * C::ROW_BYTES, &p.tmap_b, fb,
-                                 kb * C::K_TMAP, b_row + sub * C::MMA_N);
             if constexpr (C::SCALED) {
               // staged scales: 2 KB (16 rows of 128 B) per (K stage, 128-row block), the blocks of
               // one K stage contiguous; both CTAs' land on the leader's sf_full barrier, since the
-              // leader's copies read them from both CTAs' shared memory
+              // leader's copies read them from both CTAs' shared memory.  Requested before the
+              // operands, so that the copies into tensor memory run while the operands arrive.
               const int ya = (kb * p.sf_blocks_a + a_row / 128) * 16;
               const int yb = (kb * p.sf_blocks_b + (tn * C::BN) / 128) * 16;
               const uint32_t sfb_bar = (C::CG == 2) ? mapa_shared(sf_full_bar(stage), leader) : sf_full_bar(stage);
@@ -458,6 +454,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
               tma_load_2d<C::CG>(sSFA + stage * C::SFA_STAGE, &p.tmap_sfa, sfb_bar, 0, ya);
               tma_load_2d<C::CG>(sSFB + stage * C::SFB_STAGE, &p.tmap_sfb, sfb_bar, 0, yb);
             }
+            tma_load_2d<C::CG>(sA + stage * C::A_STAGE, &p.tmap_a, fb, kb * C::K_TMAP, a_row);
+#pragma unroll
+            for (int sub = 0; sub < C::NSUB; ++sub)
+              tma_load_2d<C::CG>(sB + stage * C::B_STAGE + sub * C::B_SUB_ROWS * C::ROW_BYTES, &p.tmap_b, fb,
+                                 kb * C::K_TMAP, b_row + sub * C::MMA_N);
           }
           first = false;
           if (++stage == C::STAGES) {
