@@ -126,7 +126,7 @@ __host__ __device__ inline WorkItem work_item(int w, int split_tiles, int split_
 // thread cannot keep up with the MMAs; from four warps, each taking one MMA
 // of every stage, they run beside them.
 template <Kind KIND_, int CG_, int BN_, int STAGES_, int EPI_WARPS_, int NUM_ACC_ = 2, bool COLL_A_ = false,
-          int EPI_BUFS_ = 2>
+          int EPI_BUFS_ = 2, bool REG_SPLIT_ = false>
 struct GemmCfg {
   static constexpr Kind KIND = KIND_;
   static constexpr int CG = CG_;                // CTAs per MMA (1, or 2 for the CTA pair) = CTAs per cluster
@@ -189,7 +189,17 @@ struct GemmCfg {
   // staging tiles per epilogue warp: 2 lets a chunk's shared-memory writes overlap the previous
   // chunk's TMA store; 1 halves the staging memory (eight epilogue warps then fit beside the ring)
   static constexpr int EPI_BUFS = EPI_BUFS_;
-  static constexpr int THREADS = 64 + 32 * (EPI_WARPS + SF_WARPS);
+  // Register split (NVFP4): 16 warps in four warpgroups -- the copy issuers (warps 0-3), the
+  // epilogue (4-11), the producer, the MMA issuer and two idle warps (12-15) -- launched at 128
+  // registers each; the epilogue warpgroups take 192 (setmaxnreg), enough to read their whole share
+  // of the accumulator before storing any of it, the other two give theirs down to 64.
+  static constexpr bool REG_SPLIT = REG_SPLIT_;
+  static constexpr int THREADS = REG_SPLIT ? 512 : 64 + 32 * (EPI_WARPS + SF_WARPS);
+  static constexpr int PRODUCER_WARP = REG_SPLIT ? 12 : 0;
+  static constexpr int MMA_WARP = REG_SPLIT ? 13 : 1;
+  static constexpr int EPI_WARP0 = REG_SPLIT ? 4 : 2;
+  static constexpr int SF_WARP0 = REG_SPLIT ? 0 : 2 + EPI_WARPS;
+  static constexpr int EPI_REGS = 192, OTHER_REGS = 64;
   static constexpr uint32_t IDESC = (KIND == Kind::BF16)   ? idesc_dense(kFmtBF16, BM * CG, MMA_N)
                                     : (KIND == Kind::FP8) ? idesc_dense(kFmtE4M3, BM * CG, MMA_N)
                                                           : idesc_mxf4nvf4(BM * CG, MMA_N);
@@ -230,6 +240,10 @@ struct GemmCfg {
   static_assert(!SCALED || (ACC_COLS % 16 == 0 && SF_COLS_STAGE % 16 == 0 && SF_COLS_A == 16),
                 "scale columns are written 16 at a time at 16-column-aligned addresses");
   static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB shared-memory limit");
+  static_assert(!REG_SPLIT || (EPI_WARPS == 8 && SF_WARPS == 4 && CG == 2 && (BN / EPI_COLS) % 2 == 0),
+                "register split: eight epilogue warps, four copy issuers, CTA pairs");
+  // the warpgroups' shares may not exceed what the block was launched with (512 threads x 128)
+  static_assert(!REG_SPLIT || 2 * 128 * EPI_REGS + 2 * 128 * OTHER_REGS <= 512 * 128, "register split over budget");
 };
 
 __device__ __forceinline__ void record_timeout(unsigned int* status, int role, volatile int* abort_flag) {
@@ -343,7 +357,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
     }
     if (p.c_via_tma) tma_prefetch_desc(&p.tmap_c);
   }
-  if (warp == 1) {
+  if (warp == C::MMA_WARP) {
     tmem_alloc<C::CG>(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish<C::CG>();
   }
@@ -411,144 +425,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
     return n;
   };
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ LOAD
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      bool first = true;
-      int k = 0;
-      for (int t = first_tile; t >= 0 && ok; t = next_tile(t, k, ok), ++k) {
-        if (p.sched == kSchedDynamic && prank == 0 && !request_tile(k)) {
-          ok = false;
-          break;
-        }
-        const WorkItem wk = work_of(t);
-        int tm, tn;
-        tile_coord(wk.tile, tm, tn);
-        const int a_row = tm * C::TILE_M + static_cast<int>(prank) * C::BM;
-        // this CTA's rows of B for each MMA of the K step (one MMA unless the tile is 512 wide)
-        const int b_row = tn * C::BN + static_cast<int>(prank) * C::B_SUB_ROWS;
-        // serpentine K: odd items start where the previous item's K walk ended, on the
-        // operand panels' tails that are still in L2
-        const bool rev = p.k_serpentine && (k & 1);
-        for (int i = 0; i < wk.kb1 - wk.kb0; ++i) {
-          const int kb = rev ? wk.kb1 - 1 - i : wk.kb0 + i;
-          if (!mbar_wait(empty_bar(stage), phase ^ 1u, tmo, abort_flag)) {
-            ok = false;
-            break;
-          }
-          const uint32_t fb = (C::CG == 2) ? mapa_shared(full_bar(stage), leader) : full_bar(stage);
-          if (prank == 0) mbar_arrive_expect_tx(full_bar(stage), C::STAGE_TX * C::CG);
-          if (!(first && p.fault_mode == 1)) {
-            if constexpr (C::SCALED) {
-              // staged scales: 2 KB (16 rows of 128 B) per (K stage, 128-row block), the blocks of
-              // one K stage contiguous; both CTAs' land on the leader's sf_full barrier, since the
-              // leader's copies read them from both CTAs' shared memory.  Requested before the
-              // operands, so that the copies into tensor memory run while the operands arrive.
-              const int ya = (kb * p.sf_blocks_a + a_row / 128) * 16;
-              const int yb = (kb * p.sf_blocks_b + (tn * C::BN) / 128) * 16;
-              const uint32_t sfb_bar = (C::CG == 2) ? mapa_shared(sf_full_bar(stage), leader) : sf_full_bar(stage);
-              if (prank == 0) mbar_arrive_expect_tx(sf_full_bar(stage), C::SF_TX * C::CG);
-              tma_load_2d<C::CG>(sSFA + stage * C::SFA_STAGE, &p.tmap_sfa, sfb_bar, 0, ya);
-              tma_load_2d<C::CG>(sSFB + stage * C::SFB_STAGE, &p.tmap_sfb, sfb_bar, 0, yb);
-            }
-            tma_load_2d<C::CG>(sA + stage * C::A_STAGE, &p.tmap_a, fb, kb * C::K_TMAP, a_row);
-#pragma unroll
-            for (int sub = 0; sub < C::NSUB; ++sub)
-              tma_load_2d<C::CG>(sB + stage * C::B_STAGE + sub * C::B_SUB_ROWS * C::ROW_BYTES, &p.tmap_b, fb,
-                                 kb * C::K_TMAP, b_row + sub * C::MMA_N);
-          }
-          first = false;
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      if (!ok) {
-        record_timeout(p.status, kRoleProducer, abort_flag);
-        settle_inflight_copies();
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ COMPUTE
-    if (lane == 0 && prank == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      int it = 0;
-      for (int t = first_tile; t >= 0 && ok; t = next_tile(t, it, ok), ++it) {
-        const int acc = it % C::NUM_ACC;
-        const uint32_t acc_phase = (it / C::NUM_ACC) & 1;
-        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, tmo, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::ACC_STRIDE);
-        const WorkItem wk = work_of(t);
-        // K blocks in the producer's order (see the LOAD role); only the first MMA of the item
-        // overwrites the accumulator
-        for (int i = 0; i < wk.kb1 - wk.kb0; ++i) {
-          if (!mbar_wait(full_bar(stage), phase, tmo, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a0 = sA + stage * C::A_STAGE;
-          const uint32_t b0 = sB + stage * C::B_STAGE;
-          // this stage's TMEM scale slot (NVFP4): the stage's full barrier also counts the copy
-          // issuers that filled it
-          const uint32_t sf_tmem = tmem_base + static_cast<uint32_t>(C::ACC_COLS + stage * C::SF_COLS_STAGE);
-#pragma unroll
-          for (int kk = 0; kk < C::KSTEPS; ++kk) {
-            const uint64_t ad = sdesc_sw128(a0 + 32u * kk);
-            const uint64_t bd = sdesc_sw128(b0 + 32u * kk);
-            const uint32_t accum = (i != 0 || kk != 0) ? 1u : 0u;
-            if constexpr (C::NSUB > 1) {
-              // the two N = 256 halves of the tile, into adjacent accumulator column ranges
-              constexpr int C0 = C::COLL_A ? kCollFill : kCollNone;
-              constexpr int C1 = C::COLL_A ? kCollLastUse : kCollNone;
-              const uint64_t bd1 = sdesc_sw128(b0 + static_cast<uint32_t>(C::B_SUB_ROWS * C::ROW_BYTES) + 32u * kk);
-              const uint32_t d1 = d_tmem + static_cast<uint32_t>(C::MMA_N);
-              if constexpr (C::KIND == Kind::BF16) {
-                mma_bf16<C::CG, C0>(d_tmem, ad, bd, C::IDESC, accum);
-                mma_bf16<C::CG, C1>(d1, ad, bd1, C::IDESC, accum);
-              } else {
-                mma_f8f6f4<C::CG, C0>(d_tmem, ad, bd, C::IDESC, accum);
-                mma_f8f6f4<C::CG, C1>(d1, ad, bd1, C::IDESC, accum);
-              }
-            } else if constexpr (C::KIND == Kind::BF16)
-              mma_bf16<C::CG>(d_tmem, ad, bd, C::IDESC, accum);
-            else if constexpr (C::KIND == Kind::FP8)
-              mma_f8f6f4<C::CG>(d_tmem, ad, bd, C::IDESC, accum);
-            else
-              mma_mxf4nvf4<C::CG>(d_tmem, ad, bd, C::IDESC, sf_tmem + 4u * kk,
-                                  sf_tmem + C::SF_COLS_A + (C::BN / 32) * kk, accum);
-          }
-          // the stage (operands and, NVFP4, scale slot) is free for both CTAs of the pair
-          mma_commit<C::CG>(empty_bar(stage), (1u << C::CG) - 1u);
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (!ok) break;
-        mma_commit<C::CG>(tfull_bar(acc), static_cast<uint16_t>((1u << C::CG) - 1u));
-      }
-      // No MMA may still be writing TMEM when it is released.
-      mma_commit<C::CG>(drain_bar, 0x1u);
-      mbar_wait(drain_bar, 0, tmo, never_abort);
-      if (!ok) record_timeout(p.status, kRoleMma, abort_flag);
-    }
-    __syncwarp();
-  } else if (warp < 2 + C::EPI_WARPS) {
+  if (warp >= C::EPI_WARP0 && warp < C::EPI_WARP0 + C::EPI_WARPS) {
+    if constexpr (C::REG_SPLIT) setmaxnreg_inc<C::EPI_REGS>();
     // ------------------------------------------------------------ STORE / FINISH
     constexpr int SUBS = C::EPI_WARPS / 4;
-    const int ew = warp - 2;
+    const int ew = warp - C::EPI_WARP0;
     const int quad = warp & 3;  // the TMEM lane quarter this warp may read
     const int sub = ew / 4;
     const uint32_t stage0 = sEpi + static_cast<uint32_t>(ew * C::EPI_BUFS * C::EPI_BUF);
@@ -662,16 +543,35 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
       };
       if (!CAN_SPLIT || wk.piece < 0) {
         count_visit();
-        for (int c = sub; c < NCH; c += SUBS) {
-          uint32_t r[NLD][32];
-          load_chunk(c, r, true);
-          uint32_t pk[NPK];
+        if constexpr (C::REG_SPLIT) {
+          // the warp's whole share of the accumulator first (handed back after the last read), then
+          // scaled, packed and stored chunk by chunk while the next tile's MMAs run
+          constexpr int NL = NCH / SUBS;
+          uint32_t r[NL][NLD][32];
 #pragma unroll
-          for (int l = 0; l < NLD; ++l)
+          for (int j = 0; j < NL; ++j) load_chunk(sub + SUBS * j, r[j], true);
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              pk[16 * l + j] = scale_pack(__uint_as_float(r[l][2 * j]), __uint_as_float(r[l][2 * j + 1]));
-          store_chunk(c, pk);
+          for (int j = 0; j < NL; ++j) {
+            uint32_t pk[NPK];
+#pragma unroll
+            for (int l = 0; l < NLD; ++l)
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                pk[16 * l + i] = scale_pack(__uint_as_float(r[j][l][2 * i]), __uint_as_float(r[j][l][2 * i + 1]));
+            store_chunk(sub + SUBS * j, pk);
+          }
+        } else {
+          for (int c = sub; c < NCH; c += SUBS) {
+            uint32_t r[NLD][32];
+            load_chunk(c, r, true);
+            uint32_t pk[NPK];
+#pragma unroll
+            for (int l = 0; l < NLD; ++l)
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                pk[16 * l + j] = scale_pack(__uint_as_float(r[l][2 * j]), __uint_as_float(r[l][2 * j + 1]));
+            store_chunk(c, pk);
+          }
         }
       } else {
         const int S = p.split_s;
@@ -782,53 +682,190 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
     if (!seq_ok && lane == 0) record_timeout(p.status, kRoleEpilogue, abort_flag);
     if (lane == 0) bulk_wait_group<0>();
     __syncwarp();
-  } else if (warp < 2 + C::EPI_WARPS + C::SF_WARPS) {
-    // ------------------------------------------------------------ SCALES (NVFP4)
-    // Lane 0 of scale warp q of the leader CTA copies, for every K stage of the CTA pair's tile
-    // sequence, the scales of MMA q of the stage (one 512-byte atom of A's rows, BN / 128 of B's)
-    // from both CTAs' shared memory into the stage's TMEM scale slot of both CTAs, once the scales
-    // have landed (the leader's sf_full barrier counts both CTAs' copies), and then commits to the
-    // stage's full barrier: its arrival comes when the copies are done.  The slot is free by then:
-    // the producer refilled the stage only after the MMAs that last read it had completed.  The
-    // other warps, and the peer CTA's, only follow the tile sequence.
-    if constexpr (C::SCALED) {
-      const int q = warp & 3;
-      const bool issuer = prank == 0 && lane == 0;
-      bool ok = true;
-      int k = 0;
-      int step = 0;
-      for (int t = first_tile; t >= 0 && ok; t = next_tile_warp(t, k, ok), ++k) {
-        const WorkItem wk = work_of(t);
-        if (issuer) {
-          for (int kb = wk.kb0; kb < wk.kb1 && ok; ++kb, ++step) {
-            const int j = step % C::STAGES;
-            const uint32_t ph = static_cast<uint32_t>(step / C::STAGES) & 1u;
-            if (!mbar_wait(sf_full_bar(j), ph, tmo, abort_flag)) {
+  } else {
+    if constexpr (C::REG_SPLIT) setmaxnreg_dec<C::OTHER_REGS>();
+    if (warp == C::PRODUCER_WARP) {
+      // ------------------------------------------------------------ LOAD
+      if (lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        bool first = true;
+        int k = 0;
+        for (int t = first_tile; t >= 0 && ok; t = next_tile(t, k, ok), ++k) {
+          if (p.sched == kSchedDynamic && prank == 0 && !request_tile(k)) {
+            ok = false;
+            break;
+          }
+          const WorkItem wk = work_of(t);
+          int tm, tn;
+          tile_coord(wk.tile, tm, tn);
+          const int a_row = tm * C::TILE_M + static_cast<int>(prank) * C::BM;
+          // this CTA's rows of B for each MMA of the K step (one MMA unless the tile is 512 wide)
+          const int b_row = tn * C::BN + static_cast<int>(prank) * C::B_SUB_ROWS;
+          // serpentine K: odd items start where the previous item's K walk ended, on the
+          // operand panels' tails that are still in L2
+          const bool rev = p.k_serpentine && (k & 1);
+          for (int i = 0; i < wk.kb1 - wk.kb0; ++i) {
+            const int kb = rev ? wk.kb1 - 1 - i : wk.kb0 + i;
+            if (!mbar_wait(empty_bar(stage), phase ^ 1u, tmo, abort_flag)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = (C::CG == 2) ? mapa_shared(full_bar(stage), leader) : full_bar(stage);
+            if (prank == 0) mbar_arrive_expect_tx(full_bar(stage), C::STAGE_TX * C::CG);
+            if (!(first && p.fault_mode == 1)) {
+              if constexpr (C::SCALED) {
+                // staged scales: 2 KB (16 rows of 128 B) per (K stage, 128-row block), the blocks of
+                // one K stage contiguous; both CTAs' land on the leader's sf_full barrier, since the
+                // leader's copies read them from both CTAs' shared memory.  Requested before the
+                // operands, so that the copies into tensor memory run while the operands arrive.
+                const int ya = (kb * p.sf_blocks_a + a_row / 128) * 16;
+                const int yb = (kb * p.sf_blocks_b + (tn * C::BN) / 128) * 16;
+                const uint32_t sfb_bar = (C::CG == 2) ? mapa_shared(sf_full_bar(stage), leader) : sf_full_bar(stage);
+                if (prank == 0) mbar_arrive_expect_tx(sf_full_bar(stage), C::SF_TX * C::CG);
+                tma_load_2d<C::CG>(sSFA + stage * C::SFA_STAGE, &p.tmap_sfa, sfb_bar, 0, ya);
+                tma_load_2d<C::CG>(sSFB + stage * C::SFB_STAGE, &p.tmap_sfb, sfb_bar, 0, yb);
+              }
+              tma_load_2d<C::CG>(sA + stage * C::A_STAGE, &p.tmap_a, fb, kb * C::K_TMAP, a_row);
+  #pragma unroll
+              for (int sub = 0; sub < C::NSUB; ++sub)
+                tma_load_2d<C::CG>(sB + stage * C::B_STAGE + sub * C::B_SUB_ROWS * C::ROW_BYTES, &p.tmap_b, fb,
+                                   kb * C::K_TMAP, b_row + sub * C::MMA_N);
+            }
+            first = false;
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        if (!ok) {
+          record_timeout(p.status, kRoleProducer, abort_flag);
+          settle_inflight_copies();
+        }
+      }
+      __syncwarp();
+    } else if (warp == C::MMA_WARP) {
+      // ------------------------------------------------------------ COMPUTE
+      if (lane == 0 && prank == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        int it = 0;
+        for (int t = first_tile; t >= 0 && ok; t = next_tile(t, it, ok), ++it) {
+          const int acc = it % C::NUM_ACC;
+          const uint32_t acc_phase = (it / C::NUM_ACC) & 1;
+          if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, tmo, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::ACC_STRIDE);
+          const WorkItem wk = work_of(t);
+          // K blocks in the producer's order (see the LOAD role); only the first MMA of the item
+          // overwrites the accumulator
+          for (int i = 0; i < wk.kb1 - wk.kb0; ++i) {
+            if (!mbar_wait(full_bar(stage), phase, tmo, abort_flag)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t slot = tmem_base + static_cast<uint32_t>(C::ACC_COLS + j * C::SF_COLS_STAGE);
-            const uint32_t sfa_s = sSFA + j * C::SFA_STAGE + q * C::SF_ATOM;
-            const uint32_t sfb_s = sSFB + j * C::SFB_STAGE + q * C::SF_ATOM;
-            tmem_cp_32x128b_warpx4<C::CG>(slot + 4u * q, sdesc_rows16(sfa_s));
-#pragma unroll
-            for (int g = 0; g < C::BN / 128; ++g)
-              tmem_cp_32x128b_warpx4<C::CG>(slot + C::SF_COLS_A + (C::BN / 32) * q + 4u * g,
-                                            sdesc_rows16(sfb_s + g * C::KSTEPS * C::SF_ATOM));
-            mma_commit<C::CG>(full_bar(j), 0x1u);
+            const uint32_t a0 = sA + stage * C::A_STAGE;
+            const uint32_t b0 = sB + stage * C::B_STAGE;
+            // this stage's TMEM scale slot (NVFP4): the stage's full barrier also counts the copy
+            // issuers that filled it
+            const uint32_t sf_tmem = tmem_base + static_cast<uint32_t>(C::ACC_COLS + stage * C::SF_COLS_STAGE);
+  #pragma unroll
+            for (int kk = 0; kk < C::KSTEPS; ++kk) {
+              const uint64_t ad = sdesc_sw128(a0 + 32u * kk);
+              const uint64_t bd = sdesc_sw128(b0 + 32u * kk);
+              const uint32_t accum = (i != 0 || kk != 0) ? 1u : 0u;
+              if constexpr (C::NSUB > 1) {
+                // the two N = 256 halves of the tile, into adjacent accumulator column ranges
+                constexpr int C0 = C::COLL_A ? kCollFill : kCollNone;
+                constexpr int C1 = C::COLL_A ? kCollLastUse : kCollNone;
+                const uint64_t bd1 = sdesc_sw128(b0 + static_cast<uint32_t>(C::B_SUB_ROWS * C::ROW_BYTES) + 32u * kk);
+                const uint32_t d1 = d_tmem + static_cast<uint32_t>(C::MMA_N);
+                if constexpr (C::KIND == Kind::BF16) {
+                  mma_bf16<C::CG, C0>(d_tmem, ad, bd, C::IDESC, accum);
+                  mma_bf16<C::CG, C1>(d1, ad, bd1, C::IDESC, accum);
+                } else {
+                  mma_f8f6f4<C::CG, C0>(d_tmem, ad, bd, C::IDESC, accum);
+                  mma_f8f6f4<C::CG, C1>(d1, ad, bd1, C::IDESC, accum);
+                }
+              } else if constexpr (C::KIND == Kind::BF16)
+                mma_bf16<C::CG>(d_tmem, ad, bd, C::IDESC, accum);
+              else if constexpr (C::KIND == Kind::FP8)
+                mma_f8f6f4<C::CG>(d_tmem, ad, bd, C::IDESC, accum);
+              else
+                mma_mxf4nvf4<C::CG>(d_tmem, ad, bd, C::IDESC, sf_tmem + 4u * kk,
+                                    sf_tmem + C::SF_COLS_A + (C::BN / 32) * kk, accum);
+            }
+            // the stage (operands and, NVFP4, scale slot) is free for both CTAs of the pair
+            mma_commit<C::CG>(empty_bar(stage), (1u << C::CG) - 1u);
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
+          if (!ok) break;
+          mma_commit<C::CG>(tfull_bar(acc), static_cast<uint16_t>((1u << C::CG) - 1u));
         }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        // No MMA may still be writing TMEM when it is released.
+        mma_commit<C::CG>(drain_bar, 0x1u);
+        mbar_wait(drain_bar, 0, tmo, never_abort);
+        if (!ok) record_timeout(p.status, kRoleMma, abort_flag);
       }
-      if (issuer) {
-        // no copy may still be writing tensor memory when it is released (a stage whose MMAs never
-        // ran, after a timeout elsewhere)
-        mma_commit<C::CG>(cp_drain_bar, 0x1u);
-        mbar_wait(cp_drain_bar, 0, tmo, never_abort);
-      }
-      if (!ok && lane == 0) record_timeout(p.status, kRoleProducer, abort_flag);
       __syncwarp();
+    } else if (warp >= C::SF_WARP0 && warp < C::SF_WARP0 + C::SF_WARPS) {
+      // ------------------------------------------------------------ SCALES (NVFP4)
+      // Lane 0 of scale warp q of the leader CTA copies, for every K stage of the CTA pair's tile
+      // sequence, the scales of MMA q of the stage (one 512-byte atom of A's rows, BN / 128 of B's)
+      // from both CTAs' shared memory into the stage's TMEM scale slot of both CTAs, once the scales
+      // have landed (the leader's sf_full barrier counts both CTAs' copies), and then commits to the
+      // stage's full barrier: its arrival comes when the copies are done.  The slot is free by then:
+      // the producer refilled the stage only after the MMAs that last read it had completed.  The
+      // other warps, and the peer CTA's, only follow the tile sequence.
+      if constexpr (C::SCALED) {
+        const int q = warp & 3;
+        const bool issuer = prank == 0 && lane == 0;
+        bool ok = true;
+        int k = 0;
+        int step = 0;
+        for (int t = first_tile; t >= 0 && ok; t = next_tile_warp(t, k, ok), ++k) {
+          const WorkItem wk = work_of(t);
+          if (issuer) {
+            for (int kb = wk.kb0; kb < wk.kb1 && ok; ++kb, ++step) {
+              const int j = step % C::STAGES;
+              const uint32_t ph = static_cast<uint32_t>(step / C::STAGES) & 1u;
+              if (!mbar_wait(sf_full_bar(j), ph, tmo, abort_flag)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t slot = tmem_base + static_cast<uint32_t>(C::ACC_COLS + j * C::SF_COLS_STAGE);
+              const uint32_t sfa_s = sSFA + j * C::SFA_STAGE + q * C::SF_ATOM;
+              const uint32_t sfb_s = sSFB + j * C::SFB_STAGE + q * C::SF_ATOM;
+              tmem_cp_32x128b_warpx4<C::CG>(slot + 4u * q, sdesc_rows16(sfa_s));
+  #pragma unroll
+              for (int g = 0; g < C::BN / 128; ++g)
+                tmem_cp_32x128b_warpx4<C::CG>(slot + C::SF_COLS_A + (C::BN / 32) * q + 4u * g,
+                                              sdesc_rows16(sfb_s + g * C::KSTEPS * C::SF_ATOM));
+              mma_commit<C::CG>(full_bar(j), 0x1u);
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        }
+        if (issuer) {
+          // no copy may still be writing tensor memory when it is released (a stage whose MMAs never
+          // ran, after a timeout elsewhere)
+          mma_commit<C::CG>(cp_drain_bar, 0x1u);
+          mbar_wait(cp_drain_bar, 0, tmo, never_abort);
+        }
+        if (!ok && lane == 0) record_timeout(p.status, kRoleProducer, abort_flag);
+        __syncwarp();
+      }
     }
   }
 
@@ -839,7 +876,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
     cluster_arrive();
     cluster_wait();
   }
-  if (warp == 1) {
+  if (warp == C::MMA_WARP) {
     tc_fence_after();
     tmem_dealloc<C::CG>(tmem_base, C::TMEM_COLS);
   }

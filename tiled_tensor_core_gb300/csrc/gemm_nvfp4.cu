@@ -20,12 +20,16 @@
 
 #include "gemm_variants.h"
 
+#ifndef TKG_NVFP4_REG_SPLIT
+#define TKG_NVFP4_REG_SPLIT true
+#endif
+
 namespace tkg {
 
 // five 38 KB ring stages, one accumulator, eight epilogue warps (two per TMEM lane quarter, each
 // draining half of the columns, one staging tile each), four scale warps whose leader lanes copy
 // the scales into tensor memory
-using Nvfp4_2Sm_256 = GemmCfg<Kind::NVFP4, 2, 256, 5, 8, 1, false, 1>;
+using Nvfp4_2Sm_256 = GemmCfg<Kind::NVFP4, 2, 256, 5, 8, 1, false, 1, TKG_NVFP4_REG_SPLIT>;
 
 const KernelVariant* nvfp4_variant(int id) {
   static const KernelVariant v14 = make_variant<Nvfp4_2Sm_256>("nvfp4_2sm_256x256_s5_epi8_sfcp");
