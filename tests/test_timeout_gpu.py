@@ -5,9 +5,10 @@ runs out; the kernel records the timeout in the status word, every role stops,
 tensor memory is released, and the context stays usable for the next call.
 Every compiled GEMM variant is stalled this way: the 256x256 pair tile with its
 two accumulators, the 256x512 pair tile with a single accumulator and four
-48 KB stages, and the NVFP4 kernel, whose four scale warps also wait
-(for the stage's scales in shared memory) and must give up in turn, as must its
-eight epilogue warps."""
+48 KB stages, and the NVFP4 kernel, whose four scale-copy issuers also wait
+(for the stage's scales in shared memory) and must give up in turn, and then
+wait for their own copies, as must its eight epilogue warps (in their own
+warpgroups, with a register split)."""
 import numpy as np
 import pytest
 
