@@ -61,12 +61,12 @@ DTYPE = {"bf16": "bf16", "fp8": "e4m3", "nvfp4": "e2m1+e4m3"}
 # (profiles/gemm_*_ncu.md, profiles/attention_fwd_4096_d128_ncu.md), valid only while the sources of
 # that kernel hash to the value recorded with it.
 TRAFFIC = {
-    "bf16_4096": {"bytes": 94_393_088, "src": "d1e101cd173f3b69"},
-    "bf16_8192": {"bytes": 830_366_976, "src": "d1e101cd173f3b69"},
-    "bf16_skinny": {"bytes": 430_362_624, "src": "d1e101cd173f3b69"},
-    "fp8_8192": {"bytes": 393_982_720, "src": "37174705cfb83bd3"},
-    "nvfp4_16384": {"bytes": 1_574_212_352, "src": "9bb36253d9de5a7a"},
-    "attn_n4096_d128": {"bytes": 1_058_660_352, "src": "b961c627d127cc4f"},
+    "bf16_4096": {"bytes": 94_157_056, "src": "7eeb1b55ab7ecb0c"},
+    "bf16_8192": {"bytes": 836_847_872, "src": "7eeb1b55ab7ecb0c"},
+    "bf16_skinny": {"bytes": 431_096_320, "src": "7eeb1b55ab7ecb0c"},
+    "fp8_8192": {"bytes": 396_873_984, "src": "cb7fad1af803b15e"},
+    "nvfp4_16384": {"bytes": 1_582_764_288, "src": "751cc00dfc25b4ac"},
+    "attn_n4096_d128": {"bytes": 1_061_352_448, "src": "efbddb9120c04b5d"},
 }
 KERNEL_SOURCES = {
     "bf16": ("tkg_device.cuh", "gemm_kernel.cuh", "gemm_bf16.cu"),
