@@ -40,3 +40,11 @@ def test_every_gemm_variant_is_spill_free(usage):
     assert n >= 5, f"expected every compiled GEMM variant, found {n}"
     assert not bad, f"GEMM kernels spilling registers: {bad}"
 
+
+
+def test_register_split_kernel_uses_its_launch_registers(usage):
+    # the NVFP4 kernel's warpgroups trade registers with setmaxnreg out of what the block was
+    # launched with: 512 threads x 128; fewer at launch would leave setmaxnreg.inc waiting (the
+    # library refuses such a build at run time as well)
+    nv = [e for e in usage["gemm_nvfp4.cu"] if "tkg_gemm_kernel" in e["name"]]
+    assert nv and all(e["registers"] == 128 for e in nv), nv

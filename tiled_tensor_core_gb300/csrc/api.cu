@@ -270,6 +270,16 @@ tkg_status max_clusters(DevState& d, int kind, int id, const KernelVariant& v, i
     cudaGetLastError();
     return TKG_ERR_CUDA;
   }
+  // a register split hands registers between warpgroups out of what the block was launched with;
+  // launched with fewer than it was written for, its setmaxnreg.inc would wait forever
+  if (v.launch_regs > 0) {
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, v.func) != cudaSuccess) {
+      cudaGetLastError();
+      return TKG_ERR_CUDA;
+    }
+    if (fa.numRegs != v.launch_regs) return TKG_ERR_UNSUPPORTED_DEVICE;
+  }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(v.cg * d.sm_count), 1, 1);
   cfg.blockDim = dim3(static_cast<unsigned>(v.threads), 1, 1);

@@ -212,7 +212,10 @@ struct GemmCfg {
   static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_BUFS * EPI_BUF;
   // full / empty per stage, tensor-memory full / empty per accumulator, drain, and (NVFP4) the
   // per-stage sf_full barriers
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1 + (SCALED ? STAGES : 0) + (SCALED ? 1 : 0);
+  // (+1 for tiles of two MMAs per K step: the accumulator's upper half is handed back on its own
+  // barrier, so the next tile's first MMAs into the lower half need not wait for the whole drain)
+  static constexpr int NUM_BARS =
+      2 * STAGES + 2 * NUM_ACC + 1 + (SCALED ? STAGES : 0) + (SCALED ? 1 : 0) + (NSUB > 1 ? 1 : 0);
   // dynamic schedule: ring of cancellation answers (16 bytes each) with a full
   // barrier per slot in every CTA and an empty barrier per slot in the leader,
   // after the barriers above
@@ -301,6 +304,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + C::NUM_ACC + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * C::STAGES + 2 * C::NUM_ACC);
+  // two MMAs per K step (one accumulator): the epilogue has read the accumulator's upper half
+  const uint32_t tempty_hi_bar = bar0 + 8u * (C::NUM_BARS - 1);
   // NVFP4: stage s's block scales landed in this CTA's shared memory
   auto sf_full_bar = [&](int st) { return bar0 + 8u * (2 * C::STAGES + 2 * C::NUM_ACC + 1 + st); };
   // NVFP4, copied scales: the four copy issuers' last copies are done
@@ -338,6 +343,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
       mbar_init(tempty_bar(a), C::CG * C::EPI_WARPS);
     }
     mbar_init(drain_bar, 1);
+    if constexpr (C::NSUB > 1) mbar_init(tempty_hi_bar, C::CG * C::EPI_WARPS);
     if constexpr (C::SCALED) {
       for (int st = 0; st < C::STAGES; ++st) mbar_init(sf_full_bar(st), 1);
     }
@@ -439,6 +445,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
       sb = *p.b_scale;
     }
     const uint32_t tempty_leader0 = (C::CG == 2) ? mapa_shared(tempty_bar(0), leader) : tempty_bar(0);
+    const uint32_t tempty_hi_leader = (C::CG == 2) ? mapa_shared(tempty_hi_bar, leader) : tempty_hi_bar;
     int it = 0;
     int chunk_ctr = 0;
     bool seq_ok = true;
@@ -482,7 +489,19 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
         tmem_wait_ld();
 #pragma unroll
         for (int l = 0; l < NLD; ++l) reg_fence(r[l]);
-        if (may_release && c + SUBS >= NCH) {
+        if constexpr (C::NSUB > 1) {
+          // the two MMAs' halves of the accumulator are handed back one after the other
+          if (may_release && c < NCH / 2 && c + SUBS >= NCH / 2) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty_leader0 + 8u * acc);
+          }
+          if (may_release && c + SUBS >= NCH) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty_hi_leader);
+          }
+        } else if (may_release && c + SUBS >= NCH) {
           // last TMEM read of this accumulator by this warp: hand it back
           tc_fence_before();
           __syncwarp();
@@ -787,13 +806,22 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
                 constexpr int C1 = C::COLL_A ? kCollLastUse : kCollNone;
                 const uint64_t bd1 = sdesc_sw128(b0 + static_cast<uint32_t>(C::B_SUB_ROWS * C::ROW_BYTES) + 32u * kk);
                 const uint32_t d1 = d_tmem + static_cast<uint32_t>(C::MMA_N);
-                if constexpr (C::KIND == Kind::BF16) {
+                if constexpr (C::KIND == Kind::BF16)
                   mma_bf16<C::CG, C0>(d_tmem, ad, bd, C::IDESC, accum);
-                  mma_bf16<C::CG, C1>(d1, ad, bd1, C::IDESC, accum);
-                } else {
+                else
                   mma_f8f6f4<C::CG, C0>(d_tmem, ad, bd, C::IDESC, accum);
-                  mma_f8f6f4<C::CG, C1>(d1, ad, bd1, C::IDESC, accum);
+                if (kk == 0 && i == 0) {
+                  // the tile's first MMA into the upper half: the epilogue has read it
+                  if (!mbar_wait(tempty_hi_bar, acc_phase ^ 1u, tmo, abort_flag)) {
+                    ok = false;
+                    break;
+                  }
+                  tc_fence_after();
                 }
+                if constexpr (C::KIND == Kind::BF16)
+                  mma_bf16<C::CG, C1>(d1, ad, bd1, C::IDESC, accum);
+                else
+                  mma_f8f6f4<C::CG, C1>(d1, ad, bd1, C::IDESC, accum);
               } else if constexpr (C::KIND == Kind::BF16)
                 mma_bf16<C::CG>(d_tmem, ad, bd, C::IDESC, accum);
               else if constexpr (C::KIND == Kind::FP8)
@@ -802,6 +830,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
                 mma_mxf4nvf4<C::CG>(d_tmem, ad, bd, C::IDESC, sf_tmem + 4u * kk,
                                     sf_tmem + C::SF_COLS_A + (C::BN / 32) * kk, accum);
             }
+            if (!ok) break;  // (the wait for the accumulator's upper half ran out)
             // the stage (operands and, NVFP4, scale slot) is free for both CTAs of the pair
             mma_commit<C::CG>(empty_bar(stage), (1u << C::CG) - 1u);
             if (++stage == C::STAGES) {
@@ -894,6 +923,7 @@ struct KernelVariant {
   int epi_warps;
   int threads;
   int smem_bytes;
+  int launch_regs;  // registers a thread the kernel must be launched with (register split), else 0
   const char* name;
   const void* func;
 };
@@ -901,7 +931,7 @@ struct KernelVariant {
 template <class C>
 KernelVariant make_variant(const char* name) {
   return KernelVariant{static_cast<int>(C::KIND), C::CG,        C::BN,      C::TILE_M,    C::EPI_COLS,
-                       C::STAGES,                 C::EPI_WARPS, C::THREADS, C::SMEM_BYTES, name,
+                       C::STAGES,                 C::EPI_WARPS, C::THREADS, C::SMEM_BYTES, C::REG_SPLIT ? 128 : 0, name,
                        reinterpret_cast<const void*>(&tkg_gemm_kernel<C>)};
 }
 
