@@ -4,19 +4,24 @@
 // Structure (the LCSF template of "ThunderKittens: Simple, Fast, and Adorable
 // AI Kernels", "The Four Functions: Load, Compute, Store, Finish", re-cast for
 // tcgen05):
-//   warp 0, one lane   LOAD     TMA 2-D tile loads of A and B (and the NVFP4
+//   producer, one lane LOAD     TMA 2-D tile loads of A and B (and the NVFP4
 //                               block scales) into a STAGES-deep shared ring,
 //                               guarded by full/empty mbarriers
 //                               ("Multi-Stage Buffer", Table 1).
-//   warp 1, one lane   COMPUTE  tcgen05.mma into a double-buffered fp32
+//   MMA warp, one lane COMPUTE  tcgen05.mma into a double-buffered fp32
 //                               accumulator in tensor memory; each stage is
 //                               released by tcgen05.commit on its empty barrier.
-//   warps 2.., all     STORE /  TMEM -> registers (tcgen05.ld), per-tensor
+//   epilogue warps     STORE /  TMEM -> registers (tcgen05.ld), per-tensor
 //                      FINISH   scales, round to bf16, 128-byte-swizzled
 //                               staging tile, TMA store.  The accumulator is
 //                               handed back early so the next tile's MMAs
 //                               overlap this tile's store ("overlapping one
 //                               chunk's load with the previous chunk's finish").
+//   scale warps        (NVFP4)  copy the stage's block scales into tensor
+//                               memory (tcgen05.cp), one lane of each.
+// Warps: producer 0, MMA 1, epilogue 2.., scale warps after them; or, with the
+// NVFP4 kernel's register split, four warpgroups: scale warps 0-3, epilogue
+// 4-11, producer 12, MMA 13 (14-15 idle).
 // Grid: persistent, one CTA (or CTA pair for the 2-SM MMA) per SM, walking the
 // output tiles in the L2-aware grouped order ("Persistent Grid Launch",
 // "Block Launch Order and L2 Cache Reuse").
