@@ -490,6 +490,7 @@ def measure_gemm(name, args, world, rank, local, cpu_s):
         "l2": (f"{n_sets} rotating operand sets, {n_sets * footprint / 2**20:.0f} MiB > 129 MiB L2"
                if n_sets > 1 else f"operands {footprint / 2**20:.0f} MiB > 129 MiB L2"),
         "cuda_graph": graph is not None,
+        "inputs_sha256": ops.digest()[:16],
     }
     del sets, base
     torch.cuda.empty_cache()
@@ -520,7 +521,17 @@ def line_from_entry(e, args, world, extra_config=None):
         "gpu_launches": e["gpu_launches"], "clocks": e["clocks"], "parity": e["parity"],
         "median_gemm_ms": e["median_gemm_ms"], "step_ms": e["step_ms"],
         "host_enqueue_ms_per_step": e["host_enqueue_ms_per_step"], "cublas": e["cublas"],
+        "inputs_sha256": e["inputs_sha256"], "device": device_record(),
     }
+
+
+def device_record() -> dict:
+    """The GPU the line was measured on, from its device properties (the SM clocks under load
+    and their maximum are in `clocks`)."""
+    import torch
+    p = torch.cuda.get_device_properties(torch.cuda.current_device())
+    return {"name": p.name, "sm_count": p.multi_processor_count, "cc": f"{p.major}.{p.minor}",
+            "memory_gib": round(p.total_memory / 2**30, 1)}
 
 
 def run_tkg(args, world, rank, local):
