@@ -337,7 +337,9 @@ def measure_gemm(name, args, world, rank, local, cpu_s):
     ops = synth.workload_operands(name)
     base = DeviceGemm(ops, dev)
     footprint = base.input_bytes() + base.output_bytes()
-    n_sets = 1 if footprint >= 2 * L2_BYTES else min(16, math.ceil(4 * L2_BYTES / footprint))
+    # enough copies that a GEMM never finds its operands in L2 from the last time they were used
+    # (the 256^3 workload needs ~1400 of its 0.4 MB sets)
+    n_sets = 1 if footprint >= 2 * L2_BYTES else math.ceil(4 * L2_BYTES / footprint)
     sets = [base]
     for _ in range(n_sets - 1):
         g = DeviceGemm.__new__(DeviceGemm)
