@@ -8,9 +8,11 @@
 //                               block scales) into a STAGES-deep shared ring,
 //                               guarded by full/empty mbarriers
 //                               ("Multi-Stage Buffer", Table 1).
-//   MMA warp, one lane COMPUTE  tcgen05.mma into a double-buffered fp32
-//                               accumulator in tensor memory; each stage is
-//                               released by tcgen05.commit on its empty barrier.
+//   MMA warp, one lane COMPUTE  tcgen05.mma into fp32 accumulators in tensor
+//                               memory (two for 256-wide bf16 / FP8 tiles, one
+//                               when a 512-wide tile or the NVFP4 scales fill
+//                               the rest); each stage is released by
+//                               tcgen05.commit on its empty barrier.
 //   epilogue warps     STORE /  TMEM -> registers (tcgen05.ld), per-tensor
 //                      FINISH   scales, round to bf16, 128-byte-swizzled
 //                               staging tile, TMA store.  The accumulator is
