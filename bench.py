@@ -61,11 +61,11 @@ DTYPE = {"bf16": "bf16", "fp8": "e4m3", "nvfp4": "e2m1+e4m3"}
 # (profiles/gemm_*_ncu.md, profiles/attention_fwd_4096_d128_ncu.md), valid only while the sources of
 # that kernel hash to the value recorded with it.
 TRAFFIC = {
-    "bf16_4096": {"bytes": 93_570_816, "src": "883ed6da6583b46e"},
-    "bf16_8192": {"bytes": 828_623_872, "src": "883ed6da6583b46e"},
-    "bf16_skinny": {"bytes": 430_167_808, "src": "883ed6da6583b46e"},
-    "fp8_8192": {"bytes": 395_346_944, "src": "96fe946399d62b6b"},
-    "nvfp4_16384": {"bytes": 1_594_272_512, "src": "14051776c8fe5345"},
+    "bf16_4096": {"bytes": 93_633_792, "src": "89791659a5ea7ede"},
+    "bf16_8192": {"bytes": 834_269_952, "src": "89791659a5ea7ede"},
+    "bf16_skinny": {"bytes": 430_373_632, "src": "89791659a5ea7ede"},
+    "fp8_8192": {"bytes": 393_207_552, "src": "4c62e20fc0e24d30"},
+    "nvfp4_16384": {"bytes": 1_604_999_936, "src": "e8483128e1b39ae3"},
     "attn_n4096_d128": {"bytes": 1_061_352_448, "src": "efbddb9120c04b5d"},
 }
 KERNEL_SOURCES = {

@@ -206,7 +206,7 @@ TKG_API void tkg_shutdown(void);
  *                      where the paper takes G = 8; 16 reads the least
  *                      from HBM on GB300 with 256-row pair tiles)
  *  TKG_OPT_VARIANT     force a kernel variant: 0 = the default (14 for
- *                      NVFP4; for bf16 and FP8 13 when K >= 4096 and the
+ *                      NVFP4; for bf16 and FP8 15 when K >= 4096 and the
  *                      256x512 tiles fill at least four rounds of the
  *                      device's CTA pairs, else 2); 2 = 2-SM (CTA pair)
  *                      256x256 tiles, two tensor-memory accumulators (bf16
@@ -214,11 +214,11 @@ TKG_API void tkg_shutdown(void);
  *                      the block scales brought into shared memory by the
  *                      ring's TMA and copied into tensor memory
  *                      (tcgen05.cp) by four issuing threads (NVFP4);
- *                      13 = 2-SM 256x512 tiles, two
+ *                      15 = 2-SM 256x512 tiles, two
  *                      N = 256 MMAs per K step into all 512 tensor-memory
  *                      columns, the second reusing A from the tensor
- *                      core's collector buffer (bf16 and FP8; no split-K
- *                      head).  A variant
+ *                      core's collector buffer, eight epilogue warps
+ *                      (bf16 and FP8; no split-K head).  A variant
  *                      the kind lacks falls back to the default.
  *  TKG_OPT_MAX_CTAS    cap the persistent grid size (0 = all SMs)
  *  TKG_OPT_LAUNCH_OVERLAP

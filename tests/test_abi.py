@@ -242,9 +242,9 @@ def test_swizzle_selection_matches_definition(tkg):
 
 
 def test_compiled_variants_fit_the_sm(tkg):
-    compiled = {0: (2, 13), 1: (2, 13), 2: (14,)}
+    compiled = {0: (2, 15), 1: (2, 15), 2: (14,)}
     for kind in (0, 1, 2):
-        for v in range(1, 16):
+        for v in range(1, 17):
             if v not in compiled[kind]:
                 with pytest.raises(tkg.TkgError):
                     tkg.tkg_debug_variant_info(kind, v)
@@ -254,7 +254,7 @@ def test_compiled_variants_fit_the_sm(tkg):
             assert info["threads"] in (192, 512)
             assert info["cta_group"] == 2
             assert info["tile_m"] == 256
-            assert info["tile_n"] == (512 if v == 13 else 256)
+            assert info["tile_n"] == (512 if v == 15 else 256)
 
 
 @pytest.mark.parametrize("sms", [152, 148, 132, 76])
@@ -265,7 +265,7 @@ def test_default_tile_follows_the_device_sm_count(tkg, sms):
     for kind in (0, 1):
         for M, N in [(8192, 8192), (4096, 4096), (16384, 8192)]:
             wide = -(-M // 256) * -(-N // 512)
-            want = 13 if wide >= need else 2
+            want = 15 if wide >= need else 2
             assert tkg.tkg_debug_pick_variant(kind, M, N, 8192, sms) == want, (kind, M, N, sms)
             assert tkg.tkg_debug_pick_variant(kind, M, N, 2048, sms) == 2
     assert tkg.tkg_debug_pick_variant(2, 16384, 16384, 16384, sms) == 14

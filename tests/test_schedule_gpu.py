@@ -138,7 +138,7 @@ WIDE_SHAPES = [(300, 520, 200), (256, 1024, 128), (1000, 1000, 512), (77, 100, 4
                (512, 2100, 128)]
 
 
-@pytest.mark.parametrize("variant", [13], indirect=True)
+@pytest.mark.parametrize("variant", [15], indirect=True)
 @pytest.mark.parametrize("schedule", list(SCHEDULES), indirect=True)
 @pytest.mark.parametrize("kind", ["bf16", "fp8"])
 def test_wide_tile_matches_oracle_and_visits_each_tile_once(tkg, variant, schedule, kind):
@@ -152,7 +152,7 @@ def test_wide_tile_matches_oracle_and_visits_each_tile_once(tkg, variant, schedu
         check_against_oracle(kind, g.c_bits(), acc, c_ref, ops.scale_a, ops.scale_b)
 
 
-@pytest.mark.parametrize("variant", [13], indirect=True)
+@pytest.mark.parametrize("variant", [15], indirect=True)
 def test_wide_tile_one_cluster_walks_every_tile(tkg, variant):
     ops = synth.small_int_operands("bf16", 1280, 1600, 256, seed=11)
     tkg.tkg_set_option(tkg.TKG_OPT_MAX_CTAS, 2)

@@ -8,14 +8,16 @@
 namespace tkg {
 
 using Fp8_2Sm_256 = GemmCfg<Kind::FP8, 2, 256, 6, 4>;
-using Fp8_2Sm_512 = GemmCfg<Kind::FP8, 2, 512, 4, 4, 1, true>;
+// 256x512: two N = 256 MMAs per K step sharing A through the collector buffer; eight epilogue warps
+// given 192 registers by a warpgroup register split
+using Fp8_2Sm_512 = GemmCfg<Kind::FP8, 2, 512, 4, 8, 1, true, 1, true>;
 
 const KernelVariant* fp8_variant(int id) {
   static const KernelVariant v2 = make_variant<Fp8_2Sm_256>("fp8_2sm_256x256_s6");
-  static const KernelVariant v13 = make_variant<Fp8_2Sm_512>("fp8_2sm_256x512_s4_colla");
+  static const KernelVariant v15 = make_variant<Fp8_2Sm_512>("fp8_2sm_256x512_s4_epi8_regsplit");
   switch (id) {
     case kVariant2Sm256x256: return &v2;
-    case kVariant2Sm256x512: return &v13;
+    case kVariant2Sm256x512: return &v15;
     default: return nullptr;
   }
 }

@@ -196,10 +196,10 @@ struct GemmCfg {
   // staging tiles per epilogue warp: 2 lets a chunk's shared-memory writes overlap the previous
   // chunk's TMA store; 1 halves the staging memory (eight epilogue warps then fit beside the ring)
   static constexpr int EPI_BUFS = EPI_BUFS_;
-  // Register split (NVFP4): 16 warps in four warpgroups -- the copy issuers (warps 0-3), the
-  // epilogue (4-11), the producer, the MMA issuer and two idle warps (12-15) -- launched at 128
-  // registers each; the epilogue warpgroups take 192 (setmaxnreg), enough to read their whole share
-  // of the accumulator before storing any of it, the other two give theirs down to 64.
+  // Register split: 16 warps in four warpgroups -- the copy issuers (warps 0-3; idle without block
+  // scales), the epilogue (4-11), the producer, the MMA issuer and two idle warps (12-15) -- launched
+  // at 128 registers each; the epilogue warpgroups take 192 (setmaxnreg), enough to read their whole
+  // share of the accumulator before storing any of it, the other two give theirs down to 64.
   static constexpr bool REG_SPLIT = REG_SPLIT_;
   static constexpr int THREADS = REG_SPLIT ? 512 : 64 + 32 * (EPI_WARPS + SF_WARPS);
   static constexpr int PRODUCER_WARP = REG_SPLIT ? 12 : 0;
@@ -250,8 +250,8 @@ struct GemmCfg {
   static_assert(!SCALED || (ACC_COLS % 16 == 0 && SF_COLS_STAGE % 16 == 0 && SF_COLS_A == 16),
                 "scale columns are written 16 at a time at 16-column-aligned addresses");
   static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB shared-memory limit");
-  static_assert(!REG_SPLIT || (EPI_WARPS == 8 && SF_WARPS == 4 && CG == 2 && (BN / EPI_COLS) % 2 == 0),
-                "register split: eight epilogue warps, four copy issuers, CTA pairs");
+  static_assert(!REG_SPLIT || (EPI_WARPS == 8 && (SF_WARPS == 4 || !SCALED) && CG == 2 && (BN / EPI_COLS) % 2 == 0),
+                "register split: eight epilogue warps, four copy issuers (NVFP4), CTA pairs");
   // the warpgroups' shares may not exceed what the block was launched with (512 threads x 128)
   static_assert(!REG_SPLIT || 2 * 128 * EPI_REGS + 2 * 128 * OTHER_REGS <= 512 * 128, "register split over budget");
 };
@@ -489,13 +489,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
 
       const uint32_t t_row =
           tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * C::ACC_STRIDE);
-      auto load_chunk = [&](int c, uint32_t (&r)[NLD][32], bool may_release) {
-        __syncwarp();
-#pragma unroll
-        for (int l = 0; l < NLD; ++l) tmem_ld_32x32b_x32(t_row + c * C::EPI_COLS + 32 * l, r[l]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int l = 0; l < NLD; ++l) reg_fence(r[l]);
+      // after this warp's last read of chunk c: hand back what it no longer needs
+      auto release_after = [&](int c, bool may_release) {
         if constexpr (C::NSUB > 1) {
           // the two MMAs' halves of the accumulator are handed back one after the other
           if (may_release && c < NCH / 2 && c + SUBS >= NCH / 2) {
@@ -515,6 +510,15 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
           if (lane == 0) mbar_arrive_cluster(tempty_leader0 + 8u * acc);
         }
       };
+      auto load_chunk = [&](int c, uint32_t (&r)[NLD][32], bool may_release) {
+        __syncwarp();
+#pragma unroll
+        for (int l = 0; l < NLD; ++l) tmem_ld_32x32b_x32(t_row + c * C::EPI_COLS + 32 * l, r[l]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int l = 0; l < NLD; ++l) reg_fence(r[l]);
+        release_after(c, may_release);
+      };
       // two fp32 values, scaled (FP8 / NVFP4: by scale_a, then scale_b) and rounded to a bf16 pair
       auto scale_pack = [&](float x0, float x1) -> uint32_t {
         if constexpr (C::KIND != Kind::BF16) {
@@ -525,9 +529,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
         }
         return pack_bf16x2(x0, x1);
       };
-      // store chunk c of this warp's rows, given as packed bf16 pairs
-      auto store_chunk = [&](int c, const uint32_t (&pk)[NPK]) {
-        if (p.c_via_tma) {
+      // store chunk c of this warp's rows, given as packed bf16 pairs: through a staging tile and
+      // a TMA store, or (an output whose row pitch TMA cannot take) with generic stores
+      auto store_chunk_tma = [&](int c, const uint32_t (&pk)[NPK]) {
+        {
           uint32_t buf = stage0 + static_cast<uint32_t>(chunk_ctr % C::EPI_BUFS) * C::EPI_BUF;
           // one staging tile: its row addresses are loop-invariant, and the 128-register kernels
           // cannot keep them live across the tile loop; make the base opaque so they are
@@ -547,8 +552,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
             tma_store_2d(&p.tmap_c, buf, col0 + c * C::EPI_COLS, row0);
             bulk_commit_group();
           }
-        } else {
-          // generic path for an output whose row pitch TMA cannot take
+        }
+        ++chunk_ctr;
+      };
+      auto store_chunk_generic = [&](int c, const uint32_t (&pk)[NPK]) {
+        {
           const int row = row0 + lane;
           if (row < p.M) {
             uint16_t* out = static_cast<uint16_t*>(p.c_ptr) + static_cast<size_t>(row) * p.N;
@@ -563,16 +571,71 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
         }
         ++chunk_ctr;
       };
+      auto store_chunk = [&](int c, const uint32_t (&pk)[NPK]) {
+        if (p.c_via_tma)
+          store_chunk_tma(c, pk);
+        else
+          store_chunk_generic(c, pk);
+      };
       auto count_visit = [&]() {
         if (p.visits != nullptr && ew == 0 && lane == 0 && prank == 0)
           atomicAdd(p.visits + tm * p.tiles_n + tn, 1u);
       };
       if (!CAN_SPLIT || wk.piece < 0) {
         count_visit();
-        if constexpr (C::REG_SPLIT) {
+        constexpr int NL = NCH / SUBS;
+        if constexpr (C::REG_SPLIT && NL * NLD * 32 > 128) {
+          // the warp's whole share of the accumulator first, each chunk scaled and packed to bf16 as it
+          // is read (its fp32 values do not fit the registers at once; each half is handed back after
+          // its last read), then stored chunk by chunk while the next tile's MMAs run
+          if (!p.c_via_tma) {
+            // generic stores (an output row pitch TMA cannot take): 32 columns at a time, straight
+            // from the registers they were read into; this rare path need not hand back early
+            const int row = row0 + lane;
+            for (int c = sub; c < NCH; c += SUBS) {
+              for (int l = 0; l < NLD; ++l) {
+                uint32_t r[32];
+                __syncwarp();
+                tmem_ld_32x32b_x32(t_row + c * C::EPI_COLS + 32 * l, r);
+                tmem_wait_ld();
+                reg_fence(r);
+                if (row < p.M) {
+                  uint16_t* out = static_cast<uint16_t*>(p.c_ptr) + static_cast<size_t>(row) * p.N;
+#pragma unroll
+                  for (int i = 0; i < 16; ++i) {
+                    const uint32_t v = scale_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+                    const int col = col0 + c * C::EPI_COLS + 32 * l + 2 * i;
+                    if (col < p.N) out[col] = static_cast<uint16_t>(v & 0xFFFFu);
+                    if (col + 1 < p.N) out[col + 1] = static_cast<uint16_t>(v >> 16);
+                  }
+                }
+              }
+              release_after(c, true);
+            }
+          } else {
+          uint32_t pk[NL][NPK];
+#pragma unroll
+          for (int j = 0; j < NL; ++j) {
+            const int c = sub + SUBS * j;
+#pragma unroll
+            for (int l = 0; l < NLD; ++l) {
+              uint32_t r[32];
+              __syncwarp();
+              tmem_ld_32x32b_x32(t_row + c * C::EPI_COLS + 32 * l, r);
+              tmem_wait_ld();
+              reg_fence(r);
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                pk[j][16 * l + i] = scale_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+            }
+            release_after(c, true);
+          }
+#pragma unroll
+          for (int j = 0; j < NL; ++j) store_chunk_tma(sub + SUBS * j, pk[j]);
+          }
+        } else if constexpr (C::REG_SPLIT) {
           // the warp's whole share of the accumulator first (handed back after the last read), then
           // scaled, packed and stored chunk by chunk while the next tile's MMAs run
-          constexpr int NL = NCH / SUBS;
           uint32_t r[NL][NLD][32];
 #pragma unroll
           for (int j = 0; j < NL; ++j) load_chunk(sub + SUBS * j, r[j], true);

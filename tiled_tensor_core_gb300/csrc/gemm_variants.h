@@ -15,12 +15,13 @@ namespace tkg {
 enum VariantId : int {
   kVariantAuto = 0,
   kVariant2Sm256x256 = 2,         // cta_group::2, 256 x 256 tile per CTA pair (bf16 / FP8)
-  kVariant2Sm256x512 = 13,        // cta_group::2, 256 x 512 tile per CTA pair: two N = 256 MMAs per K step, the
-                                  // second taking A from the tensor core's collector buffer (bf16 / FP8)
   kVariant2Sm256x256SfCopy = 14,  // cta_group::2, 256 x 256, block scales through shared memory, copied into
                                   // tensor memory (tcgen05.cp) by four issuing threads, eight epilogue warps
                                   // (NVFP4)
-  kNumVariants = 15
+  kVariant2Sm256x512 = 15,        // cta_group::2, 256 x 512 tile per CTA pair: two N = 256 MMAs per K step, the
+                                  // second taking A from the tensor core's collector buffer; eight epilogue
+                                  // warps given 192 registers by a warpgroup register split (bf16 / FP8)
+  kNumVariants = 16
 };
 
 // Each returns the variant for `id`, or nullptr if that kind has no such variant.
