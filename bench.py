@@ -63,7 +63,7 @@ DTYPE = {"bf16": "bf16", "fp8": "e4m3", "nvfp4": "e2m1+e4m3"}
 TRAFFIC = {
     "bf16_4096": {"bytes": 93_633_792, "src": "89791659a5ea7ede"},
     "bf16_8192": {"bytes": 834_269_952, "src": "89791659a5ea7ede"},
-    "bf16_skinny": {"bytes": 430_373_632, "src": "89791659a5ea7ede"},
+    "bf16_skinny": {"bytes": 448_839_936, "src": "89791659a5ea7ede"},
     "fp8_8192": {"bytes": 393_207_552, "src": "4c62e20fc0e24d30"},
     "nvfp4_16384": {"bytes": 1_604_999_936, "src": "e8483128e1b39ae3"},
     "attn_n4096_d128": {"bytes": 1_061_352_448, "src": "efbddb9120c04b5d"},

@@ -206,7 +206,7 @@ TKG_API void tkg_shutdown(void);
  *                      where the paper takes G = 8; 16 reads the least
  *                      from HBM on GB300 with 256-row pair tiles)
  *  TKG_OPT_VARIANT     force a kernel variant: 0 = the default (14 for
- *                      NVFP4; for bf16 and FP8 15 when K >= 4096 and the
+ *                      NVFP4; for bf16 and FP8 15 when K >= 2048 and the
  *                      256x512 tiles fill at least four rounds of the
  *                      device's CTA pairs, else 2); 2 = 2-SM (CTA pair)
  *                      256x256 tiles, two tensor-memory accumulators (bf16

@@ -259,7 +259,7 @@ def test_compiled_variants_fit_the_sm(tkg):
 
 @pytest.mark.parametrize("sms", [152, 148, 132, 76])
 def test_default_tile_follows_the_device_sm_count(tkg, sms):
-    # bf16 / FP8 take the 256x512 tile for K >= 4096 once its tiles fill four rounds of the
+    # bf16 / FP8 take the 256x512 tile for K >= 2048 once its tiles fill four rounds of the
     # device's CTA pairs (SMs / 2), else the 256x256 tile; NVFP4 always its one variant
     need = 4 * (sms // 2)
     for kind in (0, 1):
@@ -267,7 +267,8 @@ def test_default_tile_follows_the_device_sm_count(tkg, sms):
             wide = -(-M // 256) * -(-N // 512)
             want = 15 if wide >= need else 2
             assert tkg.tkg_debug_pick_variant(kind, M, N, 8192, sms) == want, (kind, M, N, sms)
-            assert tkg.tkg_debug_pick_variant(kind, M, N, 2048, sms) == 2
+            assert tkg.tkg_debug_pick_variant(kind, M, N, 2048, sms) == want, (kind, M, N, sms)
+            assert tkg.tkg_debug_pick_variant(kind, M, N, 1024, sms) == 2
     assert tkg.tkg_debug_pick_variant(2, 16384, 16384, 16384, sms) == 14
 
 

@@ -238,15 +238,16 @@ const KernelVariant* variant_of(int kind, int id) {
 // ring's TMA put them stages ahead, keeps global-load latency off the scale
 // warps' critical path.
 //
-// bf16 / FP8 with long K and many tiles take the 256 x 512 pair tile instead: it
-// moves a third fewer operand bytes per flop, which draws less power, and under
-// the power cap that buys clock (8192^3 bf16: 1779 against 1710 TFLOP/s, at
-// 1601 against 1507 MHz); it keeps a single accumulator (a tile's store does not
-// overlap the next tile) and coarser rounds of tiles, so it loses with short K
-// (16384 x 8192 x 2048: 1674 against 1706) or few tiles (4096^3: 1609 against
+// bf16 / FP8 with K of 2048 or more and many tiles take the 256 x 512 pair tile
+// instead: it moves a third fewer operand bytes per flop, which draws less power,
+// and under the power cap that buys clock (8192^3 bf16: 1779 against 1710
+// TFLOP/s, at 1601 against 1507 MHz); it keeps a single accumulator, which its
+// eight register-split epilogue warps read whole and hand back before storing
+// (16384 x 8192 x 2048: 1787 / 1778 against 1758 / 1747 for the 256 x 256 tile),
+// and coarser rounds of tiles, so it loses with few tiles (4096^3: 1609 against
 // 1639, where the split-K head of the 256 x 256 tile helps more).  "Many" is
 // four rounds of 256 x 512 tiles over the device's CTA pairs (SMs / 2).
-constexpr int64_t kWideMinK = 4096;
+constexpr int64_t kWideMinK = 2048;
 constexpr int64_t kWideMinRounds = 4;
 int pick_variant(int kind, int64_t M, int64_t N, int64_t K, int sm_count) {
   const int forced = static_cast<int>(g_opt_variant.load(std::memory_order_relaxed));
