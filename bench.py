@@ -61,12 +61,12 @@ DTYPE = {"bf16": "bf16", "fp8": "e4m3", "nvfp4": "e2m1+e4m3"}
 # (profiles/gemm_*_ncu.md, profiles/attention_fwd_4096_d128_ncu.md), valid only while the sources of
 # that kernel hash to the value recorded with it.
 TRAFFIC = {
-    "bf16_4096": {"bytes": 93_633_792, "src": "89791659a5ea7ede"},
-    "bf16_8192": {"bytes": 834_269_952, "src": "89791659a5ea7ede"},
-    "bf16_skinny": {"bytes": 448_839_936, "src": "89791659a5ea7ede"},
-    "fp8_8192": {"bytes": 393_207_552, "src": "4c62e20fc0e24d30"},
-    "nvfp4_16384": {"bytes": 1_604_999_936, "src": "e8483128e1b39ae3"},
-    "attn_n4096_d128": {"bytes": 1_061_352_448, "src": "efbddb9120c04b5d"},
+    "bf16_4096": {"bytes": 93_633_792, "src": "4bed562ab90fb120"},
+    "bf16_8192": {"bytes": 834_269_952, "src": "4bed562ab90fb120"},
+    "bf16_skinny": {"bytes": 448_839_936, "src": "4bed562ab90fb120"},
+    "fp8_8192": {"bytes": 393_207_552, "src": "0ee1790daf721892"},
+    "nvfp4_16384": {"bytes": 1_604_999_936, "src": "0ef3cf4e1cc09e5e"},
+    "attn_n4096_d128": {"bytes": 1_061_352_448, "src": "83fdd4522b9cd05c"},
 }
 KERNEL_SOURCES = {
     "bf16": ("tkg_device.cuh", "gemm_kernel.cuh", "gemm_bf16.cu"),
@@ -77,8 +77,8 @@ KERNEL_SOURCES = {
 
 
 def kernel_source_hash(files) -> str:
-    """Hash of kernel sources with comments and blank lines removed, so that a
-    comment edit does not invalidate a recorded capture but any code change does."""
+    """Hash of kernel sources with comments, blank lines and indentation removed, so that a
+    comment or layout edit does not invalidate a recorded capture but any code change does."""
     import hashlib
     import re
     h = hashlib.sha256()
@@ -87,7 +87,7 @@ def kernel_source_hash(files) -> str:
         with open(os.path.join(csrc, f)) as fh:
             text = re.sub(r"/\*.*?\*/", "", fh.read(), flags=re.S)
         for line in text.splitlines():
-            line = re.sub(r"//.*$", "", line).rstrip()
+            line = re.sub(r"//.*$", "", line).strip()
             if line:
                 h.update(line.encode() + b"\n")
     return h.hexdigest()[:16]

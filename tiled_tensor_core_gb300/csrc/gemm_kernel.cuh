@@ -613,25 +613,25 @@ __global__ void __launch_bounds__(C::THREADS, 1) tkg_gemm_kernel(const __grid_co
               release_after(c, true);
             }
           } else {
-          uint32_t pk[NL][NPK];
+            uint32_t pk[NL][NPK];
 #pragma unroll
-          for (int j = 0; j < NL; ++j) {
-            const int c = sub + SUBS * j;
+            for (int j = 0; j < NL; ++j) {
+              const int c = sub + SUBS * j;
 #pragma unroll
-            for (int l = 0; l < NLD; ++l) {
-              uint32_t r[32];
-              __syncwarp();
-              tmem_ld_32x32b_x32(t_row + c * C::EPI_COLS + 32 * l, r);
-              tmem_wait_ld();
-              reg_fence(r);
+              for (int l = 0; l < NLD; ++l) {
+                uint32_t r[32];
+                __syncwarp();
+                tmem_ld_32x32b_x32(t_row + c * C::EPI_COLS + 32 * l, r);
+                tmem_wait_ld();
+                reg_fence(r);
 #pragma unroll
-              for (int i = 0; i < 16; ++i)
-                pk[j][16 * l + i] = scale_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+                for (int i = 0; i < 16; ++i)
+                  pk[j][16 * l + i] = scale_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+              }
+              release_after(c, true);
             }
-            release_after(c, true);
-          }
 #pragma unroll
-          for (int j = 0; j < NL; ++j) store_chunk_tma(sub + SUBS * j, pk[j]);
+            for (int j = 0; j < NL; ++j) store_chunk_tma(sub + SUBS * j, pk[j]);
           }
         } else if constexpr (C::REG_SPLIT) {
           // the warp's whole share of the accumulator first (handed back after the last read), then
