@@ -324,6 +324,13 @@ def set_options(tkg, args):
                        tkg.TKG_K_ORDER_SERPENTINE if args.k_order == "serpentine" else tkg.TKG_K_ORDER_FORWARD)
 
 
+def operand_sets(footprint: int) -> int:
+    """Copies of a workload's operands (and output) that the timed launches rotate over: enough
+    that a GEMM never finds its operands in L2 from the last time they were used (a footprint of
+    twice the 129 MB L2 needs one; the 256^3 workload ~1400 of its 0.4 MB sets)."""
+    return 1 if footprint >= 2 * L2_BYTES else math.ceil(4 * L2_BYTES / footprint)
+
+
 def measure_gemm(name, args, world, rank, local, cpu_s):
     """Warm-up, timed steps, parity gate, e2e, cuBLAS context and oracle timing of one
     GEMM workload.  Returns its entry (a dict); entry["parity"]["pass"] is False on a
@@ -337,9 +344,7 @@ def measure_gemm(name, args, world, rank, local, cpu_s):
     ops = synth.workload_operands(name)
     base = DeviceGemm(ops, dev)
     footprint = base.input_bytes() + base.output_bytes()
-    # enough copies that a GEMM never finds its operands in L2 from the last time they were used
-    # (the 256^3 workload needs ~1400 of its 0.4 MB sets)
-    n_sets = 1 if footprint >= 2 * L2_BYTES else math.ceil(4 * L2_BYTES / footprint)
+    n_sets = operand_sets(footprint)
     sets = [base]
     for _ in range(n_sets - 1):
         g = DeviceGemm.__new__(DeviceGemm)

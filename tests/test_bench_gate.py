@@ -53,3 +53,14 @@ def test_gate_rejects_a_dropped_tensor_scale():
     u = x.view(np.uint32)
     wrong = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
     assert not bench.parity_check(ops, wrong, rows)["pass"]
+
+
+@pytest.mark.parametrize("name", bench.SUITE + ["bf16_4096_k64", "bf16_4096_k1024"])
+def test_timed_launches_never_find_their_operands_in_l2(name):
+    # the launches of a step rotate over copies whose combined footprint (operands in, C out) is at
+    # least twice the 129 MB L2, so no launch reads what the previous use of its copy left there
+    w = synth.WORKLOADS[name]
+    a_b = {"bf16": 2 * (w.M + w.N) * w.K, "fp8": (w.M + w.N) * w.K + 8,
+           "nvfp4": (w.M + w.N) * w.K // 2 + (w.M + w.N) * w.K // 16 + 8}[w.kind]
+    footprint = a_b + 2 * w.M * w.N
+    assert bench.operand_sets(footprint) * footprint >= 2 * bench.L2_BYTES
