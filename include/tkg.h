@@ -23,7 +23,8 @@
  *    kernel launch and returns; it never synchronises.
  *  - Accumulation is fp32.  The output is rounded to bf16 with
  *    round-to-nearest-even.  There is no alpha/beta and no accumulate-into-C;
- *    C is overwritten.
+ *    C is overwritten.  C must not overlap A, B or the scales: tiles of C are
+ *    stored while other tiles still read the operands.
  *  - M and N are arbitrary (>= 1).  Tiles that run past M, N or K are handled
  *    by the hardware copy engine (zero fill on load, clipping on store), which
  *    is exact for a sum.
